@@ -1,0 +1,397 @@
+#!/usr/bin/env python
+"""Retention throughput on one GB300 (or N, one process per GPU).
+
+Headline: chunkwise retention forward, B=1 per GPU, H=16, N=8192, d_k=256,
+d_v=512, bf16 inputs, fp32 state, all three normalisations and GroupNorm
+(the long-sequence workload with 6.7B-scale heads).  One step = one full
+pass of the hot path through the C ABI (rotate-and-scale prologue, chunk
+kernel with state carry, GroupNorm epilogue).  Inputs (256 MiB) exceed the
+129 MB L2, so no flush is needed between steps.
+
+The same JSON line also carries the decode sweep (H=16, d_k=256, d_v=512,
+fp32 state from a 1024-token prefill, 2048 one-token steps captured in a
+CUDA graph, B = 1/8/32/128) and the gated MSR layer (B=2, N=4096, d=2048).
+
+``--impl reference`` times the float64 CPU oracle instead (a bounded sample
+of the same workload on the host cores).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "retention tokens/s (chunkwise fwd N=8192; decode steps/s) and % of roofline"
+H, N, DK, DV = 16, 8192, 256, 512
+BYTES_PER_TOKEN_HEAD = 2 * 2 * DK + 2 * DV + 2 * DV  # q,k,v read + o written (bf16)
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return d["hbm_gbs"], d["bf16_tflops"], "measured"
+    except Exception:
+        return 6800.0, 1900.0, "fallback"
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index, self.rows, self.proc = index, [], None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append([c.strip() for c in line.split(",")])
+
+    def __exit__(self, *exc):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+        return False
+
+    def summary(self):
+        if not self.rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        sm = sorted(float(r[0]) for r in self.rows if r[0].replace(".", "").isdigit())
+        mx = max(float(r[1]) for r in self.rows if r[1].replace(".", "").isdigit())
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in self.rows for i in range(4)
+                          if len(r) > 2 + i and r[2 + i].lower() == "active"})
+        return {"sm_mhz": sm[len(sm) // 2] if sm else None, "sm_max_mhz": mx,
+                "reasons": reasons, "samples": len(self.rows)}
+
+
+# ------------------------------------------------------------------ helpers
+def gen_bf16(shape, seed, device):
+    import torch
+    g = torch.Generator(device=device).manual_seed(seed)
+    return torch.randn(shape, generator=g, device=device, dtype=torch.float32).to(torch.bfloat16)
+
+
+def oracle_tokens_per_s(budget_s, threads):
+    """Float64 oracle (chunkwise form) on a bounded sample of the workload:
+    all 16 heads, the first n tokens; n doubles until one run takes >= budget/4."""
+    import numpy as np
+
+    import oracle
+    from linear_recurrent_sequence_gb300 import synth
+    oracle.build()
+    gam = synth.head_gammas(H)
+    n, t = 64, 0.0
+    while True:
+        _, q = synth.tensor(1003, "q", (1, H, n, DK), "bf16")
+        _, k = synth.tensor(1003, "k", (1, H, n, DK), "bf16")
+        _, v = synth.tensor(1003, "v", (1, H, n, DV), "bf16")
+        p = oracle.Problem(1, H, n, DK, DV, gam, norm_flags=oracle.NORM_ALL, gn_eps=1e-6,
+                           threads=threads)
+        t0 = time.perf_counter()
+        oracle.chunkwise(p, 64, q, k, v)
+        t = time.perf_counter() - t0
+        if t >= budget_s / 4 or n >= N:
+            return n / t, n, t
+        n *= 2
+
+
+# ------------------------------------------------------------------ arms
+def run_reference(args):
+    """The oracle as it stands, timed on the host cores (rank 0 only)."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    threads = os.cpu_count() or 1
+    rate, n, t = oracle_tokens_per_s(2.0, threads)
+    # steps: each one re-times the same bounded sample
+    import oracle
+    from linear_recurrent_sequence_gb300 import synth
+    gam = synth.head_gammas(H)
+    _, q = synth.tensor(1003, "q", (1, H, n, DK), "bf16")
+    _, k = synth.tensor(1003, "k", (1, H, n, DK), "bf16")
+    _, v = synth.tensor(1003, "v", (1, H, n, DV), "bf16")
+    p = oracle.Problem(1, H, n, DK, DV, gam, norm_flags=oracle.NORM_ALL, gn_eps=1e-6,
+                       threads=threads)
+    for _ in range(args.warmup):
+        oracle.chunkwise(p, 64, q, k, v)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.chunkwise(p, 64, q, k, v)
+    el = time.perf_counter() - t0
+    value = n * args.steps / el
+    sample = f"16 heads x first {n} tokens of the B=1 H=16 N=8192 workload per step"
+    line = {"metric": METRIC, "impl": "reference", "value": value, "unit": "tokens/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * el / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": workload_config(args, 1),
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads,
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def workload_config(args, world):
+    return {"workload": f"chunkwise retention fwd B=1/GPU H={H} N={N} d_k={DK} d_v={DV} "
+                        f"chunk={args.chunk} bf16 in/out, fp32 state, norms 1+2+3, GroupNorm",
+            "global_batch": world, "seq_len": N, "parallelism": f"dp{world}",
+            "l2": "inputs (256 MiB) larger than L2 (129 MB); no flush"}
+
+
+def run_ours(args):
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    from linear_recurrent_sequence_gb300 import retention as R
+    from linear_recurrent_sequence_gb300 import synth
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    def max_over_ranks(x):
+        if world == 1:
+            return x
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    gam = synth.head_gammas(H)
+    q = gen_bf16((1, H, N, DK), 1003 + 7 * rank, dev)
+    k = gen_bf16((1, H, N, DK), 1103 + 7 * rank, dev)
+    v = gen_bf16((1, H, N, DV), 1203 + 7 * rank, dev)
+    o = torch.empty(1, H, N, DV, dtype=torch.bfloat16, device=dev)
+    S = torch.empty(1, H, DK, DV, dtype=torch.float32, device=dev)
+    d, _g = R.make_desc(q, k, v, o, gam, chunk=args.chunk, norm_flags=R.NORM_ALL)
+    ws = R.new_workspace(R.workspace_size(d), dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        R.chunkwise_fwd(q, k, v, gam, chunk=args.chunk, norm_flags=R.NORM_ALL, out=o,
+                        S_out=S, workspace=ws, stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    barrier()
+    R.lib.retention_kernel_timer_reset()
+    R.lib.retention_kernel_timer_enable(1)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        barrier()
+        e0.record(stream)
+        for _ in range(args.steps):
+            step()
+        e1.record(stream)
+        barrier()
+    R.lib.retention_kernel_timer_enable(0)
+    ms = max_over_ranks(e0.elapsed_time(e1))
+    launches = int(R.lib.retention_launch_count())
+    ktimes = R.kernel_times()
+    tokens = world * N * args.steps
+    value = tokens / (ms * 1e-3)
+
+    # dominant kernel and its roofline
+    hbm, tflops, src = peaks()
+    top = max(ktimes.items(), key=lambda kv: kv[1][0])
+    top_name, (top_ms, top_n, top_timed) = top
+    avg_s = top_ms / max(top_timed, 1) * 1e-3
+    alg_bytes = BYTES_PER_TOKEN_HEAD * H * N  # per launch of the chunk kernel
+    achieved = alg_bytes / avg_s / 1e9
+    roofline = {"kernel": top_name, "bound": "hbm", "achieved": achieved, "peak": hbm,
+                "unit": "GB/s", "frac": achieved / hbm, "traffic": None,
+                "peak_source": f"{src} (MEASURED_PEAKS.json hbm_gbs)" if src == "measured"
+                else "fallback 6.8 TB/s",
+                "alg_bytes_per_launch": alg_bytes, "avg_launch_us": avg_s * 1e6,
+                "kernels": {k2: {"ms_total": v2[0], "launches": v2[1]}
+                            for k2, v2 in ktimes.items()}}
+
+    # end to end through the C ABI from pinned host buffers
+    hq = torch.empty(q.shape, dtype=q.dtype, pin_memory=True)
+    hk = torch.empty(k.shape, dtype=k.dtype, pin_memory=True)
+    hv = torch.empty(v.shape, dtype=v.dtype, pin_memory=True)
+    ho = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
+    hq.copy_(q.cpu()), hk.copy_(k.cpu()), hv.copy_(v.cpu())
+    dq, dk_, dv_ = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+
+    def e2e_step():
+        dq.copy_(hq, non_blocking=True)
+        dk_.copy_(hk, non_blocking=True)
+        dv_.copy_(hv, non_blocking=True)
+        R.chunkwise_fwd(dq, dk_, dv_, gam, chunk=args.chunk, norm_flags=R.NORM_ALL, out=o,
+                        S_out=S, workspace=ws, stream=stream)
+        ho.copy_(o, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    barrier()
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    barrier()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1))
+    h2d = (q.numel() + k.numel() + v.numel()) * 2
+    d2h = o.numel() * 2
+    e2e = {"value": tokens / (e2e_ms * 1e-3), "unit": "tokens/s",
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+    del hq, hk, hv, ho, dq, dk_, dv_
+
+    extra = {}
+    if not args.skip_extra:
+        extra["decode"] = bench_decode(args, R, dev, stream, hbm, world, max_over_ranks)
+        extra["msr_layer"] = bench_msr(args, R, dev, stream, tflops, world, max_over_ranks)
+
+    cpu = None
+    if rank == 0 and not args.skip_cpu:
+        rate, n, t = oracle_tokens_per_s(args.cpu_budget, os.cpu_count() or 1)
+        cpu = {"value": rate, "unit": "tokens/s", "cores": os.cpu_count() or 1,
+               "kind": "oracle",
+               "sample": f"float64 chunkwise oracle, 16 heads x {n} tokens ({t:.1f} s)"}
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                "dtype": "bf16", "data": "synthetic", "config": workload_config(args, world),
+                "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+                "gpu_launches": launches, "clocks": clk.summary()}
+        line.update(extra)
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def bench_decode(args, R, dev, stream, hbm, world, max_over_ranks):
+    import torch
+    from linear_recurrent_sequence_gb300 import synth
+    gam = synth.head_gammas(H)
+    P, STEPS = 1024, args.decode_steps
+    out = {}
+    for B in args.decode_batches:
+        q = gen_bf16((B, H, P + STEPS, DK), 2001 + B, dev)
+        k = gen_bf16((B, H, P + STEPS, DK), 2101 + B, dev)
+        v = gen_bf16((B, H, P + STEPS, DV), 2201 + B, dev)
+        S = torch.empty(B, H, DK, DV, dtype=torch.float32, device=dev)
+        R.chunkwise_fwd(q[:, :, :P], k[:, :, :P], v[:, :, :P], gam, chunk=64, S_out=S)
+        o = torch.empty(B, H, STEPS, DV, dtype=torch.bfloat16, device=dev)
+        ws = R.new_workspace(256, dev)
+        S0 = S.clone()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for t in range(STEPS):
+                R.recurrent_step(q[:, :, P + t], k[:, :, P + t], v[:, :, P + t], S, gam,
+                                 pos=P + t, out=o[:, :, t:t + 1], workspace=ws)
+        for _ in range(max(1, args.warmup // 3)):
+            S.copy_(S0)
+            g.replay()
+        S.copy_(S0)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        g.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        ms = max_over_ranks(e0.elapsed_time(e1))
+        state_bytes = B * H * DK * DV * 4 * 2  # read + write per step
+        gbs = state_bytes * STEPS / (ms * 1e-3) / 1e9
+        out[f"B{B}"] = {"steps_per_s": STEPS / (ms * 1e-3),
+                        "tokens_per_s": world * B * STEPS / (ms * 1e-3),
+                        "us_per_step": 1e3 * ms / STEPS, "state_GBps": gbs,
+                        "frac_hbm": gbs / hbm,
+                        "note": "state fits in L2" if state_bytes / 2 < 100e6 else "HBM-bound"}
+        del q, k, v, S, S0, o, g
+        torch.cuda.empty_cache()
+    return out
+
+
+def bench_msr(args, R, dev, stream, tflops, world, max_over_ranks):
+    import torch
+    from linear_recurrent_sequence_gb300 import synth
+    B, Nm, dm, Hm, dk, dv = 2, 4096, 2048, 8, 256, 512
+    X = gen_bf16((B, Nm, dm), 3001, dev)
+    W = [gen_bf16(s, 3002 + i, dev) * 0.02 for i, s in enumerate(
+        [(dm, Hm * dk), (dm, Hm * dk), (dm, Hm * dv), (dm, Hm * dv), (Hm * dv, dm)])]
+    gam = synth.head_gammas(Hm)
+    m, _g = R.msr_desc(B, Nm, dm, Hm, dk, dv, gam, chunk=128, norm_flags=R.NORM_ALL)
+    ws = R.new_workspace(int(R.lib.msr_workspace_size(m)), dev)
+    Y = torch.empty(B, Nm, dm, dtype=torch.bfloat16, device=dev)
+
+    def f():
+        R.msr_layer_fwd(X, *W, H=Hm, d_k=dk, d_v=dv, gamma=gam, chunk=128,
+                        norm_flags=R.NORM_ALL, out=Y, workspace=ws)
+    for _ in range(2):
+        f()
+    torch.cuda.synchronize()
+    reps = 3
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        f()
+    e1.record()
+    torch.cuda.synchronize()
+    ms = max_over_ranks(e0.elapsed_time(e1)) / reps
+    gemm_flops = 2.0 * B * Nm * dm * (2 * Hm * dk + 2 * Hm * dv) + 2.0 * B * Nm * Hm * dv * dm
+    return {"tokens_per_s": world * B * Nm / (ms * 1e-3), "ms": ms,
+            "gemm_TFLOPs": gemm_flops / (ms * 1e-3) / 1e12,
+            "frac_bf16_peak_if_all_gemm": gemm_flops / (ms * 1e-3) / 1e12 / tflops}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--chunk", type=int, default=64)
+    ap.add_argument("--decode-steps", type=int, default=2048)
+    ap.add_argument("--decode-batches", type=int, nargs="*", default=[1, 8, 32, 128])
+    ap.add_argument("--cpu-budget", type=float, default=12.0)
+    ap.add_argument("--skip-extra", action="store_true")
+    ap.add_argument("--skip-cpu", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

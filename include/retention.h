@@ -1,0 +1,217 @@
+/*
+ * retention.h -- C ABI of the GB300 (sm_103a) multi-scale retention library.
+ *
+ * The operation is RetNet's retention ("Retentive Network: A Successor to
+ * Transformer for Large Language Models", arXiv:2307.08621), as stated on
+ * the pages this library follows:
+ *   [hwhale]  hwhale.com/article/285883 -- RetNet explained: recurrence,
+ *             diagonalised closed form, parallel / recurrent / chunkwise
+ *             equations and pseudocode, the three normalisations, GroupNorm.
+ *   [sdkjxy]  m.sdkjxy.cn RetNet architecture walkthrough: pairs as complex
+ *             numbers (RoPE), zero initial state, gated MSR layer.
+ *   [m0nads]  m0nads.wordpress.com "A dubious successor to Transformer":
+ *             xPos rotation, recurrent pseudocode, chunkwise representation,
+ *             gated multi-scale retention.
+ *
+ * Per head with decay gamma:
+ *   Q = (X W_Q) (.) Theta,  K = (X W_K) (.) conj(Theta),  V = X W_V,
+ *   Theta_t = e^{i t theta},  theta_j = theta_base^(-2j/d_k)   [hwhale, eq. of Q,K,V]
+ *   D_nm = gamma^(n-m) (n >= m), else 0                          [hwhale, D]
+ *   Retention(X) = (Q K^T (.) D) V                               [hwhale, parallel]
+ *   S_n = gamma S_{n-1} + K_n^T V_n,  O_n = Q_n S_n              [hwhale, recurrent]
+ *   chunk i: (Q_[i] K_[i]^T (.) D) V_[i] + (Q_[i] S_i) (.) xi,
+ *            xi_row = gamma^(row+1)                              [hwhale, chunkwise]
+ * then the optional normalisations (1/sqrt(d_k); D row-normalised by
+ * sqrt(sum_{i<=n} D_ni); R row-normalised by max(|sum_i R_ni|, 1))
+ * [hwhale, the three normalisations] and a GroupNorm per (token, head) over
+ * d_v with no affine [hwhale, multi-head GroupNorm].
+ *
+ * Readings where the pages are silent (each one is listed in the design doc):
+ *   - the phase pairs element (2j, 2j+1) as x_2j + i x_2j+1 and multiplies
+ *     by e^{+i t theta_j}; the key's conjugate is carried by the dot product,
+ *     so score(t, m) = Re(q~_t conj(k~_m) e^{i (t-m) theta}) [hwhale closed form];
+ *   - token index tau in [0, N) sits at absolute position t = pos0 + tau; the
+ *     decay-row sum uses the 1-based n = t + 1;
+ *   - the state S is unnormalised (sum gamma^(t-m) K'_m^T V_m); the
+ *     normalisations touch outputs only.  The third normalisation's row sum
+ *     covers the whole causal prefix, carried across calls by
+ *     z = sum gamma^(t-m) K'_m (d_k floats per head);
+ *   - the state entering a chunk of L tokens is carried by
+ *     S <- gamma^L S + sum_j gamma^(L-1-j) K_j^T V_j.
+ *
+ * Conventions (every entry point):
+ *   - All tensor pointers are DEVICE pointers owned by the caller.  The
+ *     library never allocates device memory and never synchronises the
+ *     stream (except retention_poll_status, which says so).
+ *   - Calls are asynchronous on `stream` and return RET_OK once the work is
+ *     enqueued.  Invalid descriptors, shapes, strides, pointers or workspace
+ *     sizes return RET_EINVAL / RET_EWORKSPACE before anything is launched.
+ *     A launch failure returns RET_ECUDA; the cudaError_t is kept per thread
+ *     for retention_last_cuda_error().
+ *   - Errors found on the device (a bounded wait that ran out) are written
+ *     to a status word at the start of the workspace; read it with
+ *     retention_poll_status().
+ *   - Inputs are never modified, except S / z of retention_recurrent_step
+ *     (documented in/out) and when the caller aliases S_out/z_out to S_in/z_in.
+ */
+#ifndef RETENTION_H
+#define RETENTION_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t; NULL is the legacy default stream. */
+struct CUstream_st;
+typedef struct CUstream_st *ret_stream_t;
+
+typedef enum {
+  RET_OK = 0,
+  RET_EINVAL = 1,       /* bad shape, dtype, stride, pointer or option       */
+  RET_EUNSUPPORTED = 2, /* valid request that this build cannot run          */
+  RET_EWORKSPACE = 3,   /* ws NULL or ws_bytes < the size query's answer     */
+  RET_ECUDA = 4,        /* a CUDA call failed; see retention_last_cuda_error */
+  RET_ETIMEOUT = 5      /* a device-side bounded wait ran out                */
+} ret_status;
+
+typedef enum { RET_F32 = 0, RET_BF16 = 1 } ret_dtype;
+
+/* Normalisation flags [hwhale, the three normalisations]. */
+enum {
+  RET_NORM_SCALE = 1, /* Q K^T / sqrt(d_k)                       */
+  RET_NORM_DROW = 2,  /* D_nm / sqrt(sum_{i<=n} D_ni)             */
+  RET_NORM_RSUM = 4   /* R_nm / max(|sum_{i<=n} R_ni|, 1)         */
+};
+
+/* Largest head count one call accepts (per-head constants travel in the
+ * kernel parameters). */
+#define RET_MAX_HEADS 256
+
+typedef struct {
+  int B, H, N;     /* batch, heads, tokens in this call (N >= 0)             */
+  int d_k, d_v;    /* key/query and value widths per head                    */
+  int chunk;       /* chunk length of the chunkwise form, 1..256             */
+  ret_dtype in_dtype, out_dtype; /* q,k,v element type; o element type      */
+  const double *gamma; /* HOST pointer, H decays, each in [0, 1]             */
+  double theta_base;   /* theta_j = theta_base^(-2j/d_k); 10000 on the pages */
+  int norm_flags;      /* RET_NORM_* bitmask; 0 = the plain equations         */
+  float gn_eps;        /* GroupNorm epsilon (1e-6); negative = no GroupNorm  */
+  int64_t pos0;        /* absolute position of token 0 (>= 0)                */
+  int rotate;          /* 1 = apply Theta to q and k; 0 = inputs pre-rotated */
+  /* Element strides of (b, h, n) for q, k, v, o.  The feature dimension is
+   * contiguous (stride 1).  Contiguous [B,H,N,d] is {H*N*d, N*d, d}; a
+   * [B,N,H,d] view is {N*H*d, d, H*d}. */
+  int64_t sq[3], sk[3], sv[3], so[3];
+} ret_desc;
+
+/* Fill `d` with defaults for contiguous [B,H,N,d] bf16 in/out, chunk 64,
+ * theta_base 10000, gn_eps 1e-6, rotate on, no normalisations, pos0 0. */
+void retention_desc_init(ret_desc *d, int B, int H, int N, int d_k, int d_v,
+                         const double *gamma);
+
+/* Workspace bytes every retention_* call below needs for this descriptor
+ * (the largest of the three forms).  0 for an invalid descriptor. */
+size_t retention_workspace_size(const ret_desc *d);
+
+/*
+ * Rotate-and-scale prologue [hwhale, Q=(XW_Q)(.)Theta, K=(XW_K)(.)conj(Theta);
+ * m0nads, xPos].  x: [B,H,N,d] through strides sx (d = d_k, even); out:
+ * contiguous [B,H,N,d] of out_dtype.  Pair (2j, 2j+1) of token tau is turned
+ * by (pos0 + tau) theta_j and multiplied by scale[tau] when `scale` (a
+ * DEVICE array of N floats) is not NULL.
+ */
+ret_status retention_rotate(const ret_desc *d, const void *x, const int64_t sx[3],
+                            int dim, void *out, ret_dtype out_dtype,
+                            const float *scale, ret_stream_t stream);
+
+/*
+ * Parallel form [hwhale, Retention(X) = (Q K^T (.) D) V; ParallelRetention].
+ * q,k: [B,H,N,d_k]; v, o: [B,H,N,d_v] via the descriptor's strides.
+ * The call's tokens only (zero prior state); positions start at pos0.
+ */
+ret_status retention_parallel_fwd(const ret_desc *d, const void *q,
+                                  const void *k, const void *v, void *o,
+                                  void *ws, size_t ws_bytes, ret_stream_t stream);
+
+/*
+ * Chunkwise recurrent form [hwhale, chunkwise equation; ChunkwiseRetention;
+ * m0nads, chunkwise representation].  Starts from S_in/z_in (NULL = zeros,
+ * [sdkjxy] zero initial state) and writes the state after the last token to
+ * S_out/z_out (NULL = not wanted).  S: fp32 [B,H,d_k,d_v] contiguous,
+ * z: fp32 [B,H,d_k] contiguous.  S_out may alias S_in and z_out z_in.
+ * The result is the same function for every chunk length (up to rounding).
+ */
+ret_status retention_chunkwise_fwd(const ret_desc *d, const void *q,
+                                   const void *k, const void *v,
+                                   const float *S_in, const float *z_in,
+                                   float *S_out, float *z_out, void *o,
+                                   void *ws, size_t ws_bytes, ret_stream_t stream);
+
+/*
+ * One recurrent decode step [hwhale, S_n = gamma S_{n-1} + K_n^T V_n,
+ * O_n = Q_n S_n; RecurrentRetention: output read after the update, summed
+ * over d_k].  Requires N == 1; the token sits at position pos0.  S (fp32
+ * [B,H,d_k,d_v]) is read and overwritten in place; z (fp32 [B,H,d_k]) is
+ * read and overwritten when RET_NORM_RSUM is set (may be NULL otherwise).
+ */
+ret_status retention_recurrent_step(const ret_desc *d, const void *q,
+                                    const void *k, const void *v, float *S,
+                                    float *z, void *o, void *ws, size_t ws_bytes,
+                                    ret_stream_t stream);
+
+/* Gated multi-scale retention layer [m0nads, "Gated Multi-Scale Retention";
+ * sdkjxy, MSR layer]: MSR(X) = (swish(X W_G) (.) GroupNorm_h(Retention_h)) W_O,
+ * swish(x) = x sigmoid(x), heads with their own gamma. */
+typedef struct {
+  int B, N, d_model;   /* X: [B, N, d_model] bf16 contiguous                */
+  int H, d_k, d_v;     /* W_Q,W_K: [d_model, H d_k]; W_V,W_G: [d_model, H d_v];
+                          W_O: [H d_v, d_model]; all bf16 row-major (X W)    */
+  int chunk;           /* chunk length of the retention step                 */
+  const double *gamma; /* HOST pointer, H decays                             */
+  double theta_base;
+  int norm_flags;
+  float gn_eps;
+  int64_t pos0;
+} msr_desc;
+
+size_t msr_workspace_size(const msr_desc *d);
+
+/* Y: [B, N, d_model] bf16. */
+ret_status msr_layer_fwd(const msr_desc *d, const void *X, const void *WQ,
+                         const void *WK, const void *WV, const void *WG,
+                         const void *WO, void *Y, void *ws, size_t ws_bytes,
+                         ret_stream_t stream);
+
+/* Human-readable text of a status code (static storage). */
+const char *retention_status_string(ret_status s);
+
+/* cudaError_t of the calling thread's last RET_ECUDA (0 if none). */
+int retention_last_cuda_error(void);
+
+/* Reads and clears the device status word at the start of `ws`.  This call
+ * SYNCHRONISES `stream`.  Returns RET_OK or the first device-side error. */
+ret_status retention_poll_status(void *ws, ret_stream_t stream);
+
+/* ---- Instrumentation (no counterpart on the pages; a measuring aid). ----
+ * The library counts every kernel it launches.  With the timer enabled it
+ * also records a CUDA event pair on the launch stream around each launch,
+ * so the device time of each kernel can be read back after the stream has
+ * been synchronised.  Do not enable the timer while capturing a CUDA graph.
+ * Kernel ids run from 0 to retention_kernel_count()-1. */
+void retention_kernel_timer_enable(int on);
+void retention_kernel_timer_reset(void);
+int retention_kernel_count(void);
+const char *retention_kernel_name(int id);
+long long retention_launch_count(void);
+/* Sum of the timed launches of kernel `id` (milliseconds), its launch count
+ * since the last reset and how many of those were timed.  Returns a
+ * ret_status value. */
+int retention_kernel_timer_read(int id, double *total_ms, long long *launches, int *timed);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* RETENTION_H */

@@ -1,0 +1,354 @@
+// C ABI of the retention library: argument checks, per-head constants,
+// workspace layout and dispatch to the kernels.  Nothing here allocates
+// device memory or synchronises a stream (retention_poll_status excepted).
+#include <math.h>
+#include <string.h>
+
+#include "common.cuh"
+#include "ktimer.h"
+#include "launch.h"
+
+using namespace ret;
+
+namespace {
+
+thread_local int g_last_cuda_error = 0;
+
+ret_status cuda_fail(cudaError_t e) {
+  g_last_cuda_error = (int)e;
+  return RET_ECUDA;
+}
+
+#define RET_CUDA(call)                        \
+  do {                                        \
+    cudaError_t e_ = (call);                  \
+    if (e_ != cudaSuccess) return cuda_fail(e_); \
+  } while (0)
+
+size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+bool finite_pos(double x) { return isfinite(x) && x > 0.0; }
+
+// Checks shared by every retention_* entry point.
+bool desc_ok(const ret_desc *d) {
+  if (!d) return false;
+  if (d->B < 0 || d->H < 0 || d->N < 0) return false;
+  if (d->H > RET_MAX_HEADS) return false;
+  if ((long long)d->B * d->H > 65535) return false;
+  if (d->d_k < 2 || d->d_k > 2 * kMaxPairs || (d->d_k % 2)) return false;
+  if (d->d_v < 1 || d->d_v > 1024) return false;
+  if (d->chunk < 1 || d->chunk > 256) return false;
+  if (d->in_dtype != RET_F32 && d->in_dtype != RET_BF16) return false;
+  if (d->out_dtype != RET_F32 && d->out_dtype != RET_BF16) return false;
+  if (d->norm_flags & ~(RET_NORM_SCALE | RET_NORM_DROW | RET_NORM_RSUM)) return false;
+  if (!(d->gn_eps == d->gn_eps)) return false;  // NaN
+  if (d->pos0 < 0 || d->pos0 + (int64_t)d->N >= ((int64_t)1 << 24)) return false;
+  if (d->rotate != 0 && d->rotate != 1) return false;
+  if (d->rotate && !finite_pos(d->theta_base)) return false;
+  if (d->H > 0 && !d->gamma) return false;
+  for (int h = 0; h < d->H; ++h)
+    if (!(d->gamma[h] >= 0.0 && d->gamma[h] <= 1.0)) return false;
+  for (int i = 0; i < 3; ++i)
+    if (d->sq[i] < 0 || d->sk[i] < 0 || d->sv[i] < 0 || d->so[i] < 0) return false;
+  return true;
+}
+
+void make_params(const ret_desc *d, void *ws, KParams &p) {
+  memset(&p, 0, sizeof(p));
+  p.B = d->B; p.H = d->H; p.N = d->N; p.dk = d->d_k; p.dv = d->d_v; p.chunk = d->chunk;
+  for (int i = 0; i < 3; ++i) {
+    p.sq[i] = d->sq[i]; p.sk[i] = d->sk[i]; p.sv[i] = d->sv[i]; p.so[i] = d->so[i];
+  }
+  p.pos0 = d->pos0;
+  p.norm_flags = d->norm_flags;
+  p.rotate = d->rotate;
+  p.in_bf16 = d->in_dtype == RET_BF16;
+  p.out_bf16 = d->out_dtype == RET_BF16;
+  p.gn_eps = d->gn_eps;
+  p.inv_sqrt_dk = (float)(1.0 / sqrt((double)d->d_k));
+  for (int h = 0; h < d->H; ++h) {
+    const double g = d->gamma[h];
+    p.gam[h] = (float)g;
+    p.lng[h] = g == 0.0 ? -INFINITY : (float)log(g);
+    p.omg[h] = (float)(1.0 - g);
+  }
+  for (int j = 0; j < d->d_k / 2; ++j) {
+    const double th = d->rotate ? pow(d->theta_base, -2.0 * j / d->d_k) : 0.0;
+    p.th_hi[j] = (float)th;
+    p.th_lo[j] = (float)(th - (double)p.th_hi[j]);
+  }
+  p.status = reinterpret_cast<unsigned *>(ws);
+}
+
+// Workspace of the CUDA-core forms: status | Qr | Kr | Oraw | F | z copy.
+struct SimtWs {
+  size_t qr, kr, oraw, f, zc, total;
+};
+
+SimtWs simt_ws(const ret_desc *d) {
+  SimtWs w;
+  const size_t rows = (size_t)d->B * d->H * d->N;
+  size_t off = kStatusBytes;
+  w.qr = off; off = align256(off + rows * d->d_k * sizeof(float));
+  w.kr = off; off = align256(off + rows * d->d_k * sizeof(float));
+  w.oraw = off; off = align256(off + rows * d->d_v * sizeof(float));
+  w.f = off; off = align256(off + rows * sizeof(float));
+  w.zc = off; off = align256(off + (size_t)d->B * d->H * d->d_k * sizeof(float));
+  w.total = off;
+  return w;
+}
+
+template <typename T>
+T *at(void *ws, size_t off) {
+  return reinterpret_cast<T *>(reinterpret_cast<char *>(ws) + off);
+}
+
+ret_status check_ws(void *ws, size_t have, size_t need) {
+  if (need > 0 && (!ws || have < need)) return RET_EWORKSPACE;
+  if (ws && (reinterpret_cast<uintptr_t>(ws) & 255)) return RET_EWORKSPACE;
+  return RET_OK;
+}
+
+// Chunkwise form with an optional swish gate on the GroupNorm output.
+ret_status chunkwise_impl(const ret_desc *d, const void *q, const void *k, const void *v,
+                          const float *S_in, const float *z_in, float *S_out, float *z_out,
+                          void *o, Gate gate, void *ws, size_t ws_bytes, cudaStream_t st) {
+  if (!desc_ok(d)) return RET_EINVAL;
+  const bool empty = d->B == 0 || d->H == 0;
+  if (!empty && d->N > 0 && (!q || !k || !v || !o)) return RET_EINVAL;
+  const SimtWs w = simt_ws(d);
+  ret_status rs = check_ws(ws, ws_bytes, w.total);
+  if (rs != RET_OK) return rs;
+  if (empty) return RET_OK;
+  const size_t sbytes = (size_t)d->B * d->H * d->d_k * d->d_v * sizeof(float);
+  const size_t zbytes = (size_t)d->B * d->H * d->d_k * sizeof(float);
+  if (d->N == 0) {  // no tokens: the state passes through unchanged
+    if (S_out && S_out != S_in)
+      RET_CUDA(S_in ? cudaMemcpyAsync(S_out, S_in, sbytes, cudaMemcpyDeviceToDevice, st)
+                    : cudaMemsetAsync(S_out, 0, sbytes, st));
+    if (z_out && z_out != z_in)
+      RET_CUDA(z_in ? cudaMemcpyAsync(z_out, z_in, zbytes, cudaMemcpyDeviceToDevice, st)
+                    : cudaMemsetAsync(z_out, 0, zbytes, st));
+    return RET_OK;
+  }
+  KParams p;
+  make_params(d, ws, p);
+  float *Qr = at<float>(ws, w.qr), *Kr = at<float>(ws, w.kr);
+  float *Oraw = at<float>(ws, w.oraw), *F = at<float>(ws, w.f);
+  RET_CUDA(RET_TIMED_LAUNCH(kKRotate, st, launch_rotate(p, q, p.sq, d->d_k, Qr, 0, nullptr, kScaleNone, st)));
+  RET_CUDA(RET_TIMED_LAUNCH(kKRotate, st, launch_rotate(p, k, p.sk, d->d_k, Kr, 0, nullptr, kScaleNone, st)));
+  if (z_in && z_out == z_in) {  // every CTA of a head reads z_in; one writes z_out
+    RET_CUDA(cudaMemcpyAsync(at<float>(ws, w.zc), z_in, zbytes, cudaMemcpyDeviceToDevice, st));
+    z_in = at<float>(ws, w.zc);
+  }
+  RET_CUDA(RET_TIMED_LAUNCH(kKChunkSimt, st, launch_chunk_simt(p, Qr, Kr, v, S_in, z_in, S_out, z_out, Oraw, F, st)));
+  RET_CUDA(RET_TIMED_LAUNCH(kKGroupNorm, st, launch_groupnorm(p, Oraw, F, o, gate, st)));
+  return RET_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+void retention_desc_init(ret_desc *d, int B, int H, int N, int d_k, int d_v,
+                         const double *gamma) {
+  if (!d) return;
+  memset(d, 0, sizeof(*d));
+  d->B = B; d->H = H; d->N = N; d->d_k = d_k; d->d_v = d_v;
+  d->chunk = 64;
+  d->in_dtype = RET_BF16;
+  d->out_dtype = RET_BF16;
+  d->gamma = gamma;
+  d->theta_base = 10000.0;
+  d->norm_flags = 0;
+  d->gn_eps = 1e-6f;
+  d->pos0 = 0;
+  d->rotate = 1;
+  d->sq[0] = d->sk[0] = (int64_t)H * N * d_k;
+  d->sq[1] = d->sk[1] = (int64_t)N * d_k;
+  d->sq[2] = d->sk[2] = d_k;
+  d->sv[0] = d->so[0] = (int64_t)H * N * d_v;
+  d->sv[1] = d->so[1] = (int64_t)N * d_v;
+  d->sv[2] = d->so[2] = d_v;
+}
+
+size_t retention_workspace_size(const ret_desc *d) {
+  if (!desc_ok(d)) return 0;
+  return simt_ws(d).total;
+}
+
+ret_status retention_rotate(const ret_desc *d, const void *x, const int64_t sx[3], int dim,
+                            void *out, ret_dtype out_dtype, const float *scale,
+                            ret_stream_t stream) {
+  if (!desc_ok(d) || !sx || dim != d->d_k) return RET_EINVAL;
+  if (out_dtype != RET_F32 && out_dtype != RET_BF16) return RET_EINVAL;
+  if ((long long)d->B * d->H * d->N == 0) return RET_OK;
+  if (!x || !out) return RET_EINVAL;
+  for (int i = 0; i < 3; ++i)
+    if (sx[i] < 0) return RET_EINVAL;
+  KParams p;
+  make_params(d, nullptr, p);
+  const long long s[3] = {sx[0], sx[1], sx[2]};
+  RET_CUDA(RET_TIMED_LAUNCH(kKRotate, (cudaStream_t)stream,
+                            launch_rotate(p, x, s, dim, out, out_dtype == RET_BF16, scale,
+                                          scale ? kScaleArray : kScaleNone,
+                                          (cudaStream_t)stream)));
+  return RET_OK;
+}
+
+ret_status retention_parallel_fwd(const ret_desc *d, const void *q, const void *k,
+                                  const void *v, void *o, void *ws, size_t ws_bytes,
+                                  ret_stream_t stream) {
+  if (!desc_ok(d)) return RET_EINVAL;
+  const bool empty = (long long)d->B * d->H * d->N == 0;
+  if (!empty && (!q || !k || !v || !o)) return RET_EINVAL;
+  const SimtWs w = simt_ws(d);
+  ret_status rs = check_ws(ws, ws_bytes, w.total);
+  if (rs != RET_OK) return rs;
+  if (empty) return RET_OK;
+  cudaStream_t st = (cudaStream_t)stream;
+  KParams p;
+  make_params(d, ws, p);
+  float *Qr = at<float>(ws, w.qr), *Kr = at<float>(ws, w.kr);
+  float *Oraw = at<float>(ws, w.oraw), *F = at<float>(ws, w.f);
+  RET_CUDA(RET_TIMED_LAUNCH(kKRotate, st, launch_rotate(p, q, p.sq, d->d_k, Qr, 0, nullptr, kScaleNone, st)));
+  RET_CUDA(RET_TIMED_LAUNCH(kKRotate, st, launch_rotate(p, k, p.sk, d->d_k, Kr, 0, nullptr, kScaleNone, st)));
+  RET_CUDA(RET_TIMED_LAUNCH(kKParallelSimt, st, launch_parallel_simt(p, Qr, Kr, v, Oraw, F, st)));
+  RET_CUDA(RET_TIMED_LAUNCH(kKGroupNorm, st, launch_groupnorm(p, Oraw, F, o, Gate{nullptr, {0, 0, 0}}, st)));
+  return RET_OK;
+}
+
+ret_status retention_chunkwise_fwd(const ret_desc *d, const void *q, const void *k,
+                                   const void *v, const float *S_in, const float *z_in,
+                                   float *S_out, float *z_out, void *o, void *ws,
+                                   size_t ws_bytes, ret_stream_t stream) {
+  return chunkwise_impl(d, q, k, v, S_in, z_in, S_out, z_out, o, Gate{nullptr, {0, 0, 0}},
+                        ws, ws_bytes, (cudaStream_t)stream);
+}
+
+ret_status retention_recurrent_step(const ret_desc *d, const void *q, const void *k,
+                                    const void *v, float *S, float *z, void *o, void *ws,
+                                    size_t ws_bytes, ret_stream_t stream) {
+  if (!desc_ok(d) || d->N != 1) return RET_EINVAL;
+  if (d->d_v % 4) return RET_EINVAL;
+  const bool empty = (long long)d->B * d->H == 0;
+  if (!empty && (!q || !k || !v || !S || !o)) return RET_EINVAL;
+  if (!empty && (d->norm_flags & RET_NORM_RSUM) && !z) return RET_EINVAL;
+  if (reinterpret_cast<uintptr_t>(S) & 15) return RET_EINVAL;
+  ret_status rs = check_ws(ws, ws_bytes, kStatusBytes);
+  if (rs != RET_OK) return rs;
+  if (empty) return RET_OK;
+  KParams p;
+  make_params(d, ws, p);
+  RET_CUDA(RET_TIMED_LAUNCH(kKRecurrent, (cudaStream_t)stream, launch_recurrent_step(p, q, k, v, S, z, o, (cudaStream_t)stream)));
+  return RET_OK;
+}
+
+// ------------------------------------------------------------------ MSR
+static bool msr_ok(const msr_desc *d) {
+  if (!d) return false;
+  if (d->B < 0 || d->N < 0 || d->d_model < 1 || d->H < 1 || d->H > RET_MAX_HEADS) return false;
+  if (!d->gamma) return false;
+  return true;
+}
+
+static void msr_inner_desc(const msr_desc *m, ret_desc *d) {
+  retention_desc_init(d, m->B, m->H, m->N, m->d_k, m->d_v, m->gamma);
+  d->chunk = m->chunk;
+  d->theta_base = m->theta_base;
+  d->norm_flags = m->norm_flags;
+  d->gn_eps = m->gn_eps;
+  d->pos0 = m->pos0;
+  d->rotate = 1;
+  const int64_t HK = (int64_t)m->H * m->d_k, HV = (int64_t)m->H * m->d_v;
+  d->sq[0] = d->sk[0] = (int64_t)m->N * HK;
+  d->sq[1] = d->sk[1] = m->d_k;
+  d->sq[2] = d->sk[2] = HK;
+  d->sv[0] = d->so[0] = (int64_t)m->N * HV;
+  d->sv[1] = d->so[1] = m->d_v;
+  d->sv[2] = d->so[2] = HV;
+}
+
+struct MsrWs {
+  size_t q, k, v, g, y, inner, total;
+};
+
+static MsrWs msr_ws(const msr_desc *m, const ret_desc *inner) {
+  MsrWs w;
+  const size_t T = (size_t)m->B * m->N;
+  const size_t HK = (size_t)m->H * m->d_k, HV = (size_t)m->H * m->d_v;
+  size_t off = kStatusBytes;
+  w.q = off; off = align256(off + T * HK * 2);
+  w.k = off; off = align256(off + T * HK * 2);
+  w.v = off; off = align256(off + T * HV * 2);
+  w.g = off; off = align256(off + T * HV * 2);
+  w.y = off; off = align256(off + T * HV * 2);
+  w.inner = off; off = align256(off + retention_workspace_size(inner));
+  w.total = off;
+  return w;
+}
+
+size_t msr_workspace_size(const msr_desc *m) {
+  if (!msr_ok(m)) return 0;
+  ret_desc inner;
+  msr_inner_desc(m, &inner);
+  if (!desc_ok(&inner)) return 0;
+  return msr_ws(m, &inner).total;
+}
+
+ret_status msr_layer_fwd(const msr_desc *m, const void *X, const void *WQ, const void *WK,
+                         const void *WV, const void *WG, const void *WO, void *Y, void *ws,
+                         size_t ws_bytes, ret_stream_t stream) {
+  if (!msr_ok(m)) return RET_EINVAL;
+  ret_desc inner;
+  msr_inner_desc(m, &inner);
+  if (!desc_ok(&inner)) return RET_EINVAL;
+  const MsrWs w = msr_ws(m, &inner);
+  ret_status rs = check_ws(ws, ws_bytes, w.total);
+  if (rs != RET_OK) return rs;
+  const int T = m->B * m->N;
+  if (T == 0) return RET_OK;
+  if (!X || !WQ || !WK || !WV || !WG || !WO || !Y) return RET_EINVAL;
+  cudaStream_t st = (cudaStream_t)stream;
+  const int HK = m->H * m->d_k, HV = m->H * m->d_v;
+  void *Q = at<char>(ws, w.q), *K = at<char>(ws, w.k), *V = at<char>(ws, w.v);
+  void *G = at<char>(ws, w.g), *Yg = at<char>(ws, w.y);
+  RET_CUDA(RET_TIMED_LAUNCH(kKGemmSimt, st, launch_gemm_bf16(X, WQ, Q, T, HK, m->d_model, 1, st)));
+  RET_CUDA(RET_TIMED_LAUNCH(kKGemmSimt, st, launch_gemm_bf16(X, WK, K, T, HK, m->d_model, 1, st)));
+  RET_CUDA(RET_TIMED_LAUNCH(kKGemmSimt, st, launch_gemm_bf16(X, WV, V, T, HV, m->d_model, 1, st)));
+  RET_CUDA(RET_TIMED_LAUNCH(kKGemmSimt, st, launch_gemm_bf16(X, WG, G, T, HV, m->d_model, 1, st)));
+  Gate gate{G, {inner.sv[0], inner.sv[1], inner.sv[2]}};
+  rs = chunkwise_impl(&inner, Q, K, V, nullptr, nullptr, nullptr, nullptr, Yg, gate,
+                      at<char>(ws, w.inner), ws_bytes - w.inner, st);
+  if (rs != RET_OK) return rs;
+  RET_CUDA(RET_TIMED_LAUNCH(kKGemmSimt, st, launch_gemm_bf16(Yg, WO, Y, T, m->d_model, HV, 1, st)));
+  return RET_OK;
+}
+
+const char *retention_status_string(ret_status s) {
+  switch (s) {
+    case RET_OK: return "ok";
+    case RET_EINVAL: return "invalid argument";
+    case RET_EUNSUPPORTED: return "unsupported configuration";
+    case RET_EWORKSPACE: return "workspace missing, too small or not 256-byte aligned";
+    case RET_ECUDA: return "CUDA error";
+    case RET_ETIMEOUT: return "device-side wait timed out";
+  }
+  return "unknown status";
+}
+
+int retention_last_cuda_error(void) { return g_last_cuda_error; }
+
+ret_status retention_poll_status(void *ws, ret_stream_t stream) {
+  if (!ws) return RET_EINVAL;
+  cudaStream_t st = (cudaStream_t)stream;
+  unsigned word = 0;
+  RET_CUDA(cudaMemcpyAsync(&word, ws, sizeof(word), cudaMemcpyDeviceToHost, st));
+  RET_CUDA(cudaStreamSynchronize(st));
+  if (word == kDevOk) return RET_OK;
+  RET_CUDA(cudaMemsetAsync(ws, 0, sizeof(word), st));
+  RET_CUDA(cudaStreamSynchronize(st));
+  return word == kDevTimeout ? RET_ETIMEOUT : RET_EINVAL;
+}
+
+}  // extern "C"

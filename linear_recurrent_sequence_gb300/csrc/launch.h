@@ -1,0 +1,42 @@
+// Internal launchers shared between the kernel files and the C ABI layer.
+#pragma once
+
+#include "common.cuh"
+
+namespace ret {
+
+enum ScaleMode { kScaleNone = 0, kScaleArray = 1, kScaleXi = 2, kScaleZeta = 3 };
+
+// rotate.cu
+cudaError_t launch_rotate(const KParams &p, const void *x, const long long s[3], int d,
+                          void *out, int out_bf16, const float *scale, int mode,
+                          cudaStream_t st);
+
+// chunk_simt.cu: fp32 CUDA-core forms writing unnormalised rows + row factors.
+// Qr, Kr: rotated contiguous fp32 [B,H,N,dk]; Oraw: fp32 [B,H,N,dv];
+// F: fp32 [B,H,N] (row factor f = s(n) r(n)).
+cudaError_t launch_chunk_simt(const KParams &p, const float *Qr, const float *Kr,
+                              const void *v, const float *S_in, const float *z_in,
+                              float *S_out, float *z_out, float *Oraw, float *F,
+                              cudaStream_t st);
+cudaError_t launch_parallel_simt(const KParams &p, const float *Qr, const float *Kr,
+                                 const void *v, float *Oraw, float *F, cudaStream_t st);
+
+// groupnorm.cu: o = GroupNorm(F * Oraw) (* swish(gate)), written through so[].
+struct Gate {
+  const void *ptr;      // bf16, NULL = no gate
+  long long s[3];       // element strides of (b, h, n); feature contiguous
+};
+cudaError_t launch_groupnorm(const KParams &p, const float *Oraw, const float *F,
+                             void *o, Gate gate, cudaStream_t st);
+
+// recurrent.cu: one decode step, state in place.
+cudaError_t launch_recurrent_step(const KParams &p, const void *q, const void *k,
+                                  const void *v, float *S, float *z, void *o,
+                                  cudaStream_t st);
+
+// gemm_simt.cu: C[M,N] = A[M,K] B[K,N], bf16 in (row-major), fp32 accumulate.
+cudaError_t launch_gemm_bf16(const void *A, const void *Bm, void *C, int M, int N,
+                             int K, int out_bf16, cudaStream_t st);
+
+}  // namespace ret

@@ -1,0 +1,142 @@
+"""Host-side checks of the C ABI; no GPU needed (nothing here launches)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def R():
+    import __graft_entry__
+    __graft_entry__.build()
+    from linear_recurrent_sequence_gb300 import retention
+    return retention
+
+
+def declared_functions():
+    names = set()
+    for hdr in os.listdir(os.path.join(ROOT, "include")):
+        if not hdr.endswith(".h"):
+            continue
+        text = open(os.path.join(ROOT, "include", hdr)).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        for m in re.finditer(r"^\s*(?:const\s+)?[A-Za-z_][\w\s\*]*?\b([a-z_][a-z0-9_]*)\s*\(",
+                             text, flags=re.M):
+            if m.group(1) not in ("if", "sizeof"):
+                names.add(m.group(1))
+    return sorted(names)
+
+
+def test_header_declares_the_four_operations():
+    names = declared_functions()
+    for op in ("retention_chunkwise_fwd", "retention_recurrent_step",
+               "retention_parallel_fwd", "msr_layer_fwd"):
+        assert op in names
+
+
+def test_library_exports_every_declared_symbol(R):
+    names = declared_functions()
+    assert len(names) >= 10
+    for n in names:
+        assert hasattr(R.lib, n), f"{n} declared in include/ but not exported"
+        assert n in R._SIGS, f"{n} has no binding"
+
+
+def test_struct_layout_matches_header(R):
+    # ret_desc: 6 ints, 2 enums, pointer, double, int, float, int64, int, 4 x int64[3]
+    assert ctypes.sizeof(R.RetDesc) == 168
+    assert R.RetDesc.sq.offset == 72
+    assert ctypes.sizeof(R.MsrDesc) == 64
+
+
+def _desc(R, **kw):
+    g = (ctypes.c_double * 4)(0.9, 0.9, 0.9, 0.9)
+    d = R.RetDesc()
+    R.lib.retention_desc_init(ctypes.byref(d), 1, 2, 8, 4, 4, g)
+    for k, v in kw.items():
+        setattr(d, k, v)
+    return d, g
+
+
+def test_desc_init_defaults(R):
+    d, _ = _desc(R)
+    assert (d.chunk, d.in_dtype, d.out_dtype, d.rotate) == (64, 1, 1, 1)
+    assert abs(d.theta_base - 10000.0) < 1e-12 and abs(d.gn_eps - 1e-6) < 1e-12
+    assert list(d.sq) == [2 * 8 * 4, 8 * 4, 4]
+
+
+@pytest.mark.parametrize("field,value", [
+    ("B", -1), ("d_k", 3), ("d_k", 0), ("d_k", 512), ("d_v", 0), ("d_v", 2048),
+    ("chunk", 0), ("chunk", 300), ("in_dtype", 7), ("norm_flags", 8), ("pos0", -1),
+    ("pos0", 1 << 24), ("rotate", 2), ("theta_base", 0.0), ("H", 300)])
+def test_invalid_descriptors_rejected(R, field, value):
+    d, g = _desc(R, **{field: value})
+    assert R.lib.retention_workspace_size(ctypes.byref(d)) == 0
+    dummy = ctypes.c_void_p(256)
+    st = R.lib.retention_chunkwise_fwd(ctypes.byref(d), dummy, dummy, dummy, None, None, None,
+                                       None, dummy, dummy, 1 << 30, None)
+    assert st == 1  # RET_EINVAL, before any launch
+
+
+def test_gamma_out_of_range_rejected(R):
+    g = (ctypes.c_double * 2)(0.9, 1.5)
+    d = R.RetDesc()
+    R.lib.retention_desc_init(ctypes.byref(d), 1, 2, 8, 4, 4, g)
+    assert R.lib.retention_workspace_size(ctypes.byref(d)) == 0
+
+
+def test_null_pointers_and_workspace(R):
+    d, g = _desc(R)
+    need = R.lib.retention_workspace_size(ctypes.byref(d))
+    assert need >= 256
+    dummy = ctypes.c_void_p(256)
+    # null q
+    assert R.lib.retention_chunkwise_fwd(ctypes.byref(d), None, dummy, dummy, None, None, None,
+                                         None, dummy, dummy, need, None) == 1
+    # workspace too small, missing, misaligned
+    assert R.lib.retention_chunkwise_fwd(ctypes.byref(d), dummy, dummy, dummy, None, None, None,
+                                         None, dummy, dummy, need - 1, None) == 3
+    assert R.lib.retention_chunkwise_fwd(ctypes.byref(d), dummy, dummy, dummy, None, None, None,
+                                         None, dummy, None, need, None) == 3
+    assert R.lib.retention_chunkwise_fwd(ctypes.byref(d), dummy, dummy, dummy, None, None, None,
+                                         None, dummy, ctypes.c_void_p(260), need, None) == 3
+
+
+def test_recurrent_step_checks(R):
+    d, g = _desc(R, N=1)
+    dummy = ctypes.c_void_p(256)
+    # N must be 1
+    d2, g2 = _desc(R, N=2)
+    assert R.lib.retention_recurrent_step(ctypes.byref(d2), dummy, dummy, dummy, dummy, None,
+                                          dummy, dummy, 256, None) == 1
+    # S must be 16-byte aligned
+    assert R.lib.retention_recurrent_step(ctypes.byref(d), dummy, dummy, dummy,
+                                          ctypes.c_void_p(260), None, dummy, dummy, 256,
+                                          None) == 1
+    # the third normalisation needs z
+    d3, g3 = _desc(R, N=1, norm_flags=4)
+    assert R.lib.retention_recurrent_step(ctypes.byref(d3), dummy, dummy, dummy, dummy, None,
+                                          dummy, dummy, 256, None) == 1
+
+
+def test_empty_batch_is_a_no_op(R):
+    d, g = _desc(R, B=0)
+    assert R.lib.retention_chunkwise_fwd(ctypes.byref(d), None, None, None, None, None, None,
+                                         None, None, ctypes.c_void_p(256), 256, None) == 0
+
+
+def test_status_strings(R):
+    for code in range(6):
+        assert R.lib.retention_status_string(code)
+    assert R.lib.retention_last_cuda_error() == 0
+
+
+def test_msr_workspace_and_checks(R):
+    m, g = R.msr_desc(2, 4096, 2048, 8, 256, 512, [0.9] * 8, chunk=128)
+    ws = R.lib.msr_workspace_size(ctypes.byref(m))
+    assert ws >= 2 * 4096 * (2 * 8 * 256 + 3 * 8 * 512) * 2
+    m2, g2 = R.msr_desc(2, 4096, 2048, 8, 3, 512, [0.9] * 8)  # odd d_k
+    assert R.lib.msr_workspace_size(ctypes.byref(m2)) == 0

@@ -1,0 +1,202 @@
+"""GPU parity: the CUDA library (through its C ABI) against the float64 oracle
+on the same seeded inputs, for every workload shape and the edge cases.
+
+Workloads (seed = 1000 + index):
+  1. fp32, B=1 H=1 N=64 d_k=d_v=32, gamma=0.9, chunk 16: parallel, recurrent
+     and chunkwise forms.
+  2. bf16, B=4 H=8 N=2048 d_k=128 d_v=256, gamma_h = 1-2^(-5-h), chunk 64,
+     all three normalisations, GroupNorm.
+  3. bf16, B=1 H=16 N=8192 d_k=256 d_v=512, chunks 64/128/256 (heads
+     0, 5, 10, 15 compared in full).
+  4. decode: H=16 d_k=256 d_v=512, state from a 1024-token chunkwise prefill,
+     then one-token steps.
+  5. MSR layer: B=2 N=4096 d=2048 H=8 d_k=256 d_v=512, chunk 128.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from linear_recurrent_sequence_gb300 import synth
+from tests.helpers import check_bf16, check_f32, host, seeded
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def R():
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    from linear_recurrent_sequence_gb300 import retention
+    oracle.build()
+    return retention
+
+
+def inputs(seed, B, H, N, dk, dv, dtype):
+    q, q64 = seeded(seed, "q", (B, H, N, dk), dtype)
+    k, k64 = seeded(seed, "k", (B, H, N, dk), dtype)
+    v, v64 = seeded(seed, "v", (B, H, N, dv), dtype)
+    return (q, k, v), (q64, k64, v64)
+
+
+# ------------------------------------------------------------------ config 1
+@pytest.mark.parametrize("flags", [0, oracle.NORM_ALL])
+def test_config1_fp32_three_forms(R, flags):
+    B, H, N, dk, dv, C = 1, 1, 64, 32, 32, 16
+    (q, k, v), (q64, k64, v64) = inputs(1001, B, H, N, dk, dv, "f32")
+    p = oracle.Problem(B, H, N, dk, dv, 0.9, norm_flags=flags, gn_eps=1e-6)
+    ref = oracle.parallel(p, q64, k64, v64)
+    o_par = R.parallel_fwd(q, k, v, [0.9], norm_flags=flags)
+    check_f32(host(o_par), ref, "parallel")
+    o_ch = R.chunkwise_fwd(q, k, v, [0.9], chunk=C, norm_flags=flags)
+    check_f32(host(o_ch), ref, "chunkwise")
+    S = torch.zeros(B, H, dk, dv, device="cuda")
+    z = torch.zeros(B, H, dk, device="cuda")
+    outs = [R.recurrent_step(q[:, :, t], k[:, :, t], v[:, :, t], S, [0.9], z=z, pos=t,
+                             norm_flags=flags) for t in range(N)]
+    check_f32(host(torch.cat(outs, dim=2)), ref, "recurrent")
+    _, S_ref, _ = oracle.recurrent(p, q64, k64, v64)
+    check_f32(host(S), S_ref, "state")
+
+
+# ------------------------------------------------------------------ config 2
+def test_config2_training_shape(R):
+    B, H, N, dk, dv, C = 4, 8, 2048, 128, 256, 64
+    (q, k, v), (q64, k64, v64) = inputs(1002, B, H, N, dk, dv, "bf16")
+    gam = synth.head_gammas(H)
+    S_out = torch.empty(B, H, dk, dv, device="cuda")
+    o = R.chunkwise_fwd(q, k, v, gam, chunk=C, norm_flags=R.NORM_ALL, S_out=S_out)
+    p = oracle.Problem(B, H, N, dk, dv, gam, norm_flags=oracle.NORM_ALL, gn_eps=1e-6)
+    ref, S_ref, _ = oracle.chunkwise(p, C, q64, k64, v64)
+    check_bf16(host(o), ref, "config2 output")
+    rel = np.max(np.abs(host(S_out) - S_ref)) / np.max(np.abs(S_ref))
+    assert rel < 1e-2, rel
+
+
+# ------------------------------------------------------------------ config 3
+HEADS3 = [0, 5, 10, 15]
+
+
+@pytest.fixture(scope="module")
+def config3(R):
+    B, H, N, dk, dv = 1, 16, 8192, 256, 512
+    (q, k, v), (q64, k64, v64) = inputs(1003, B, H, N, dk, dv, "bf16")
+    gam = synth.head_gammas(H)
+    sel = HEADS3
+    p = oracle.Problem(B, len(sel), N, dk, dv, gam[sel], norm_flags=oracle.NORM_ALL,
+                       gn_eps=1e-6)
+    ref, S_ref, _ = oracle.chunkwise(p, 256, q64[:, sel], k64[:, sel], v64[:, sel])
+    return (q, k, v), gam, ref, S_ref
+
+
+@pytest.mark.parametrize("C", [64, 128, 256])
+def test_config3_long_sequence(R, config3, C):
+    (q, k, v), gam, ref, S_ref = config3
+    S_out = torch.empty(1, 16, 256, 512, device="cuda")
+    o = R.chunkwise_fwd(q, k, v, gam, chunk=C, norm_flags=R.NORM_ALL, S_out=S_out)
+    check_bf16(host(o[:, HEADS3]), ref, f"config3 C={C}")
+    rel = np.max(np.abs(host(S_out[:, HEADS3]) - S_ref)) / np.max(np.abs(S_ref))
+    assert rel < 1e-2, rel
+
+
+# ------------------------------------------------------------------ config 4
+@pytest.mark.parametrize("B,steps", [(1, 64), (8, 16)])
+def test_config4_decode_after_prefill(R, B, steps):
+    H, dk, dv, P = 16, 256, 512, 1024
+    N = P + steps
+    (q, k, v), (q64, k64, v64) = inputs(1004, B, H, N, dk, dv, "bf16")
+    gam = synth.head_gammas(H)
+    S = torch.empty(B, H, dk, dv, device="cuda")
+    o_pre = R.chunkwise_fwd(q[:, :, :P], k[:, :, :P], v[:, :, :P], gam, chunk=64, S_out=S)
+    outs = [R.recurrent_step(q[:, :, t], k[:, :, t], v[:, :, t], S, gam, pos=t)
+            for t in range(P, N)]
+    got = torch.cat([o_pre] + outs, dim=2)
+    p = oracle.Problem(B, H, N, dk, dv, gam, gn_eps=1e-6)
+    ref, S_ref, _ = oracle.chunkwise(p, 64, q64, k64, v64)
+    check_bf16(host(got), ref, f"decode B={B}")
+    rel = np.max(np.abs(host(S) - S_ref)) / np.max(np.abs(S_ref))
+    assert rel < 1e-2, rel
+
+
+# ------------------------------------------------------------------ config 5
+def test_config5_msr_layer(R):
+    from oracle.msr import msr_layer
+    B, N, dm, H, dk, dv, C = 2, 4096, 2048, 8, 256, 512, 128
+    X, X64 = seeded(1005, "x", (B, N, dm), "bf16")
+    W = {}
+    for name, shp in (("wq", (dm, H * dk)), ("wk", (dm, H * dk)), ("wv", (dm, H * dv)),
+                      ("wg", (dm, H * dv)), ("wo", (H * dv, dm))):
+        W[name] = seeded(1005, name, shp, "bf16", std=0.02)
+    gam = synth.head_gammas(H)
+    Y = R.msr_layer_fwd(X, W["wq"][0], W["wk"][0], W["wv"][0], W["wg"][0], W["wo"][0], H=H,
+                        d_k=dk, d_v=dv, gamma=gam, chunk=C, norm_flags=R.NORM_ALL)
+    ref = msr_layer(X64, W["wq"][1], W["wk"][1], W["wv"][1], W["wg"][1], W["wo"][1], H=H,
+                    dk=dk, dv=dv, gamma=gam, chunk=C, norm_flags=oracle.NORM_ALL, gn_eps=1e-6)
+    check_bf16(host(Y), ref, "msr layer")
+
+
+# ------------------------------------------------------------------ edges
+def test_ragged_tail_gamma_extremes_and_strides(R):
+    """N not a multiple of the chunk, gamma 0 and 1 among the heads, pos0 > 0,
+    [B,N,H,d] strided views, fp32 output from bf16 input."""
+    B, H, N, dk, dv = 2, 3, 203, 64, 96
+    qb, q64 = seeded(77, "q", (B, N, H, dk), "bf16")
+    kb, k64 = seeded(77, "k", (B, N, H, dk), "bf16")
+    vb, v64 = seeded(77, "v", (B, N, H, dv), "bf16")
+    q, k, v = (t.permute(0, 2, 1, 3) for t in (qb, kb, vb))
+    gam = [0.0, 0.97, 1.0]
+    p = oracle.Problem(B, H, N, dk, dv, gam, pos0=11, norm_flags=oracle.NORM_ALL, gn_eps=1e-6)
+    ref = oracle.parallel(p, q64.transpose(0, 2, 1, 3), k64.transpose(0, 2, 1, 3),
+                          v64.transpose(0, 2, 1, 3))
+    out = torch.empty(B, N, H, dv, device="cuda").permute(0, 2, 1, 3)
+    for C in (16, 64, 128):
+        R.chunkwise_fwd(q, k, v, gam, chunk=C, pos0=11, norm_flags=R.NORM_ALL, out=out)
+        check_bf16(host(out), ref, f"ragged C={C}")
+    o = R.parallel_fwd(q, k, v, gam, pos0=11, norm_flags=R.NORM_ALL, out_dtype=torch.float32)
+    check_bf16(host(o), ref, "parallel strided")
+
+
+def test_state_passing_and_aliasing(R):
+    """Two chunkwise calls with the carried (S, z), S_out aliasing S_in, equal
+    one call over the whole sequence; N = 0 passes the state through."""
+    B, H, N, dk, dv = 1, 2, 300, 32, 64
+    (q, k, v), (q64, k64, v64) = inputs(91, B, H, N, dk, dv, "f32")
+    gam = [0.9, 0.999]
+    p = oracle.Problem(B, H, N, dk, dv, gam, norm_flags=oracle.NORM_ALL, gn_eps=1e-6)
+    ref, S_ref, z_ref = oracle.chunkwise(p, 64, q64, k64, v64)
+    S = torch.zeros(B, H, dk, dv, device="cuda")
+    z = torch.zeros(B, H, dk, device="cuda")
+    a = 137
+    o1 = R.chunkwise_fwd(q[:, :, :a], k[:, :, :a], v[:, :, :a], gam, chunk=32,
+                         norm_flags=R.NORM_ALL, S_in=S, z_in=z, S_out=S, z_out=z)
+    o2 = R.chunkwise_fwd(q[:, :, a:], k[:, :, a:], v[:, :, a:], gam, chunk=64, pos0=a,
+                         norm_flags=R.NORM_ALL, S_in=S, z_in=z, S_out=S, z_out=z)
+    check_f32(host(torch.cat([o1, o2], dim=2)), ref, "split")
+    check_f32(host(S), S_ref, "S")
+    check_f32(host(z), z_ref, "z")
+    S2, z2 = torch.empty_like(S), torch.empty_like(z)
+    R.chunkwise_fwd(q[:, :, :0], k[:, :, :0], v[:, :, :0], gam, S_in=S, z_in=z, S_out=S2,
+                    z_out=z2, pos0=N)
+    assert torch.equal(S2, S) and torch.equal(z2, z)
+
+
+def test_single_token_and_no_groupnorm(R):
+    B, H, N, dk, dv = 2, 2, 1, 16, 8
+    (q, k, v), (q64, k64, v64) = inputs(5, B, H, N, dk, dv, "f32")
+    p = oracle.Problem(B, H, N, dk, dv, [0.5, 0.8], gn_eps=-1.0)
+    ref = oracle.parallel(p, q64, k64, v64)
+    o = R.chunkwise_fwd(q, k, v, [0.5, 0.8], gn_eps=None)
+    check_f32(host(o), ref, "N=1 raw")
+
+
+def test_rotate_entry_point(R):
+    x, x64 = seeded(3, "q", (1, 2, 50, 64), "f32")
+    got = R.rotate(x, pos0=4000, theta_base=10000.0)
+    p = oracle.Problem(1, 2, 50, 64, 1, [0.9, 0.9], pos0=4000)
+    ref = oracle.rotate(p, x64, 64)
+    assert np.max(np.abs(host(got) - ref)) < 5e-6
+
+
+def test_workspace_status_is_clean(R):
+    ws = R.new_workspace(1 << 20, "cuda")
+    assert R.poll_status(ws) == 0
