@@ -1,0 +1,34 @@
+/*
+ * retention_selftest.h -- tensor-core self-test of libretention.so.
+ *
+ * No counterpart on the pages: this checks the sm_103a tensor-core
+ * building blocks (shared-memory operand layouts, TMEM operands and the
+ * accumulator's lane layout) that the retention kernels rely on.
+ */
+#ifndef RETENTION_SELFTEST_H
+#define RETENTION_SELFTEST_H
+
+#include "retention.h"
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/*
+ * One CTA computes D = A * B^T with a chain of tcgen05 MMAs (bf16 inputs,
+ * fp32 accumulation).  A: [M][K] bf16, B: [N][K] bf16 (device, row-major).
+ * a_mode: 0 = A in shared memory K-major, 1 = MN-major, 2 = A in TMEM.
+ * b_mode: 0 = K-major, 1 = MN-major.  M in {64,128}, N in 32..256 (multiple
+ * of 32), K in {64,128}.  a_lbo/a_sbo/b_lbo/b_sbo: byte strides used in the
+ * MN-major descriptors.  D: [128][N] fp32 device buffer receiving all 128
+ * TMEM lanes of the accumulator.  status: device word, set non-zero if the
+ * MMA completion wait ran out.  Returns a ret_status value.
+ */
+int retention_tc_probe(int a_mode, int b_mode, int M, int N, int K, int a_lbo, int a_sbo,
+                       int b_lbo, int b_sbo, const void *A, const void *B, float *D,
+                       unsigned *status, ret_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif

@@ -1,0 +1,139 @@
+// Tensor-core self-test: one CTA computes D = A * B^T (bf16 in, fp32
+// accumulate) with one tcgen05 MMA chain, with A and B laid out in shared
+// memory in the 128-byte-swizzled K-major or MN-major forms (or A in TMEM)
+// that the retention kernels use.  All 128 TMEM lanes of D are written out,
+// so the accumulator layout of M=64 can be checked as well as the values.
+// The descriptor strides come from the caller, which lets one run check
+// layout hypotheses side by side.
+#include "tc.cuh"
+
+namespace ret {
+
+namespace {
+constexpr int kProbeSmem = 200 * 1024;
+}
+
+__global__ void __launch_bounds__(128)
+tc_probe_kernel(int a_mode, int b_mode, int M, int N, int K, int a_lbo, int a_sbo, int b_lbo,
+                int b_sbo, const __nv_bfloat16 *__restrict__ A,
+                const __nv_bfloat16 *__restrict__ B, float *__restrict__ D,
+                unsigned *status) {
+  extern __shared__ __align__(1024) uint8_t smraw[];
+  __shared__ uint64_t bar;
+  __shared__ uint32_t tbase;
+  uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~(uintptr_t)1023);
+  uint8_t *sA = sm;                 // up to 64 KB
+  uint8_t *sB = sm + 64 * 1024;     // up to 64 KB
+  const int tid = threadIdx.x, warp = tid >> 5;
+
+  if (tid == 0) {
+    tc::mbar_init(&bar, 1);
+    tc::fence_mbar_init();
+  }
+  if (warp == 0) {
+    tc::tmem_alloc(&tbase, 512);
+    tc::tmem_relinquish();
+  }
+  // Fill shared memory.  K-major: region per 64-wide K block, rows of 128 B.
+  // MN-major: region per 64-wide MN block, one 128-B row per k.
+  auto put = [&](uint8_t *base, int mode, int rows, int r, int k, __nv_bfloat16 x) {
+    uint32_t off;
+    if (mode == 0)
+      off = (uint32_t)(k / 64) * rows * 128 + tc::sw128_off(r, (k % 64) / 8) + (k % 8) * 2;
+    else
+      off = (uint32_t)(r / 64) * K * 128 + tc::sw128_off(k, (r % 64) / 8) + (r % 8) * 2;
+    *reinterpret_cast<__nv_bfloat16 *>(base + off) = x;
+  };
+  if (a_mode != 2)
+    for (int e = tid; e < M * K; e += 128) put(sA, a_mode, M, e / K, e % K, A[e]);
+  for (int e = tid; e < N * K; e += 128) put(sB, b_mode, N, e / K, e % K, B[e]);
+  tc::fence_proxy_async_smem();
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t t0 = tbase;
+  const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+  // Sentinel in every D column of this warp's lanes, then A into TMEM.
+  {
+    uint32_t r[32];
+    for (int i = 0; i < 32; ++i) r[i] = 0x7fc00000u;  // NaN
+    for (int c = 0; c < N; c += 32) tc::tmem_st32(t0 + lane_base + c, r);
+    if (a_mode == 2) {
+      const int m = tid;
+      for (int c0 = 0; c0 < K / 2; c0 += 32) {
+        for (int i = 0; i < 32; ++i) {
+          const int k = 2 * (c0 + i);
+          r[i] = (m < M && k + 1 < K + 1 && k < K)
+                     ? tc::pack_bf16(__bfloat162float(A[m * K + k]),
+                                     __bfloat162float(A[m * K + k + 1]))
+                     : 0u;
+        }
+        tc::tmem_st32(t0 + lane_base + 256 + c0, r);
+      }
+    }
+    tc::tmem_st_wait();
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  if (tid == 0) {
+    const uint32_t idesc = tc::idesc_bf16(M, N, a_mode == 1, b_mode == 1);
+    for (int s = 0; s < K / 16; ++s) {
+      const int k0 = s * 16;
+      uint64_t bdesc;
+      if (b_mode == 0)
+        bdesc = tc::smem_desc(tc::smem_u32(sB) + (k0 / 64) * N * 128 + (k0 % 64) * 2, 16, 1024,
+                              tc::kSw128);
+      else
+        bdesc = tc::smem_desc(tc::smem_u32(sB) + k0 * 128, b_lbo, b_sbo, tc::kSw128);
+      if (a_mode == 2) {
+        tc::mma_ts(t0, t0 + 256 + k0 / 2, bdesc, idesc, s > 0);
+      } else {
+        uint64_t adesc;
+        if (a_mode == 0)
+          adesc = tc::smem_desc(tc::smem_u32(sA) + (k0 / 64) * M * 128 + (k0 % 64) * 2, 16,
+                                1024, tc::kSw128);
+        else
+          adesc = tc::smem_desc(tc::smem_u32(sA) + k0 * 128, a_lbo, a_sbo, tc::kSw128);
+        tc::mma_ss(t0, adesc, bdesc, idesc, s > 0);
+      }
+    }
+    tc::mma_commit(&bar);
+  }
+  const bool ok = tc::mbar_wait(&bar, 0, status, 1u << 22);
+  tc::tc_fence_after();
+  if (ok) {
+    uint32_t r[32];
+    for (int c = 0; c < N; c += 32) {
+      tc::tmem_ld32(t0 + lane_base + c, r);
+      tc::tmem_ld_wait();
+      for (int i = 0; i < 32 && c + i < N; ++i)
+        D[(warp * 32 + (tid & 31)) * N + c + i] = __uint_as_float(r[i]);
+    }
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tc::tmem_dealloc(t0, 512);
+}
+
+}  // namespace ret
+
+extern "C" int retention_tc_probe(int a_mode, int b_mode, int M, int N, int K, int a_lbo,
+                                  int a_sbo, int b_lbo, int b_sbo, const void *A,
+                                  const void *B, float *D, unsigned *status,
+                                  ret_stream_t stream) {
+  using namespace ret;
+  if (a_mode < 0 || a_mode > 2 || b_mode < 0 || b_mode > 1) return RET_EINVAL;
+  if ((M != 64 && M != 128) || N < 16 || N > 256 || N % 32 || K < 16 || K > 128 || K % 64)
+    return RET_EINVAL;
+  if (a_mode == 2 && M != 128) return RET_EINVAL;
+  if (!A || !B || !D || !status) return RET_EINVAL;
+  cudaError_t e = cudaFuncSetAttribute(tc_probe_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kProbeSmem);
+  if (e != cudaSuccess) return RET_ECUDA;
+  tc_probe_kernel<<<1, 128, kProbeSmem, (cudaStream_t)stream>>>(
+      a_mode, b_mode, M, N, K, a_lbo, a_sbo, b_lbo, b_sbo,
+      reinterpret_cast<const __nv_bfloat16 *>(A), reinterpret_cast<const __nv_bfloat16 *>(B),
+      D, status);
+  return cudaGetLastError() == cudaSuccess ? RET_OK : RET_ECUDA;
+}
