@@ -162,6 +162,31 @@ ret_status retention_recurrent_step(const ret_desc *d, const void *q,
                                     float *z, void *o, void *ws, size_t ws_bytes,
                                     ret_stream_t stream);
 
+/*
+ * Chunkwise forward without a caller-supplied workspace.  No counterpart on
+ * the pages: it exists for callers that cannot allocate device memory, such
+ * as a plugin that an inference runtime hands only its input and output
+ * buffers, or a latency-critical loop where cudaMalloc (which can
+ * synchronise the device) is forbidden after start-up.  Same arguments and
+ * results as retention_chunkwise_fwd, minus ws/ws_bytes.
+ *   - The workspace is a fixed array of RET_NOALLOC_SCRATCH_BYTES inside the
+ *     library; every GPU that loads the library holds it until the process
+ *     exits.  A problem whose workspace (retention_workspace_size) exceeds
+ *     it returns RET_EUNSUPPORTED before anything is launched.
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress); make that first call before any stream capture.
+ *   - All calls share the one array: calls that may overlap on the GPU (on
+ *     different streams, or from several threads) race and must not be used.
+ *   - No memory is allocated or freed.  Device-side status words are cleared
+ *     at the start of each call and are not reported.
+ */
+#define RET_NOALLOC_SCRATCH_BYTES (32u << 20)
+ret_status retention_chunkwise_fwd_noalloc(const ret_desc *d, const void *q,
+                                           const void *k, const void *v,
+                                           const float *S_in, const float *z_in,
+                                           float *S_out, float *z_out, void *o,
+                                           ret_stream_t stream);
+
 /* Gated multi-scale retention layer [m0nads, "Gated Multi-Scale Retention";
  * sdkjxy, MSR layer]: MSR(X) = (swish(X W_G) (.) GroupNorm_h(Retention_h)) W_O,
  * swish(x) = x sigmoid(x), heads with their own gamma. */

@@ -59,6 +59,8 @@ _SIGS = {
                                                _P, _P, _P, _P, ctypes.c_size_t, _P]),
     "retention_recurrent_step": (ctypes.c_int, [ctypes.POINTER(RetDesc), _P, _P, _P, _P, _P,
                                                 _P, _P, ctypes.c_size_t, _P]),
+    "retention_chunkwise_fwd_noalloc": (ctypes.c_int, [ctypes.POINTER(RetDesc), _P, _P, _P, _P,
+                                                       _P, _P, _P, _P, _P]),
     "msr_workspace_size": (ctypes.c_size_t, [ctypes.POINTER(MsrDesc)]),
     "msr_layer_fwd": (ctypes.c_int, [ctypes.POINTER(MsrDesc), _P, _P, _P, _P, _P, _P, _P, _P,
                                      ctypes.c_size_t, _P]),
@@ -197,6 +199,21 @@ def chunkwise_fwd(q, k, v, gamma, *, chunk=64, norm_flags=0, gn_eps=1e-6, pos0=0
                                      _ptr(z_in), _ptr(S_out), _ptr(z_out), _ptr(out),
                                      _ptr(workspace), workspace.numel(), _stream(stream))
     _check(st, "retention_chunkwise_fwd")
+    return out
+
+
+def chunkwise_fwd_noalloc(q, k, v, gamma, *, chunk=64, norm_flags=0, gn_eps=1e-6, pos0=0,
+                          rotate=True, theta_base=10000.0, S_in=None, z_in=None, S_out=None,
+                          z_out=None, out=None, out_dtype=None, stream=None):
+    """Chunkwise forward whose workspace is the library's own fixed device
+    array (for callers that cannot allocate); see retention.h."""
+    out = _prep(q, k, v, out, out_dtype)
+    d, g = make_desc(q, k, v, out, gamma, chunk=chunk, norm_flags=norm_flags, gn_eps=gn_eps,
+                     pos0=pos0, rotate=rotate, theta_base=theta_base)
+    st = lib.retention_chunkwise_fwd_noalloc(ctypes.byref(d), _ptr(q), _ptr(k), _ptr(v),
+                                             _ptr(S_in), _ptr(z_in), _ptr(S_out), _ptr(z_out),
+                                             _ptr(out), _stream(stream))
+    _check(st, "retention_chunkwise_fwd_noalloc")
     return out
 
 
