@@ -98,6 +98,29 @@ SimtWs simt_ws(const ret_desc *d) {
   return w;
 }
 
+// Workspace of the tensor-core chunkwise path: status | Q' | K' | z copy.
+// Q'/K' are fp16 with per-(head, chunk) exponents and magnitudes.
+struct TcWs {
+  size_t qp, kp, zc, qe, ke, qm, km, total;
+};
+
+TcWs tc_ws(const ret_desc *d) {
+  TcWs w;
+  const size_t BH = (size_t)d->B * d->H;
+  const size_t rows = BH * d->N;
+  const size_t nch = ((size_t)d->N + d->chunk - 1) / d->chunk;
+  size_t off = kStatusBytes;
+  w.qp = off; off = align256(off + rows * d->d_k * 2);
+  w.kp = off; off = align256(off + rows * d->d_k * 2);
+  w.zc = off; off = align256(off + BH * d->d_k * sizeof(float));
+  w.qe = off; off = align256(off + BH * nch * sizeof(int));
+  w.ke = off; off = align256(off + BH * nch * sizeof(int));
+  w.qm = off; off = align256(off + BH * nch * sizeof(float));
+  w.km = off; off = align256(off + BH * nch * sizeof(float));
+  w.total = off;
+  return w;
+}
+
 template <typename T>
 T *at(void *ws, size_t off) {
   return reinterpret_cast<T *>(reinterpret_cast<char *>(ws) + off);
@@ -116,8 +139,12 @@ ret_status chunkwise_impl(const ret_desc *d, const void *q, const void *k, const
   if (!desc_ok(d)) return RET_EINVAL;
   const bool empty = d->B == 0 || d->H == 0;
   if (!empty && d->N > 0 && (!q || !k || !v || !o)) return RET_EINVAL;
+  KParams p;
+  make_params(d, ws, p);
+  const bool tc = !empty && d->N > 0 && chunk_tc_supported(p, v, p.sv);
   const SimtWs w = simt_ws(d);
-  ret_status rs = check_ws(ws, ws_bytes, w.total);
+  const TcWs tw = tc_ws(d);
+  ret_status rs = check_ws(ws, ws_bytes, tc ? tw.total : w.total);
   if (rs != RET_OK) return rs;
   if (empty) return RET_OK;
   const size_t sbytes = (size_t)d->B * d->H * d->d_k * d->d_v * sizeof(float);
@@ -131,8 +158,22 @@ ret_status chunkwise_impl(const ret_desc *d, const void *q, const void *k, const
                     : cudaMemsetAsync(z_out, 0, zbytes, st));
     return RET_OK;
   }
-  KParams p;
-  make_params(d, ws, p);
+  if (tc) {
+    // Tensor-core path: rotate-and-scale prologue (xi on queries, zeta on
+    // keys, bf16), then the fused chunk kernel with the GroupNorm epilogue.
+    void *Qp = at<char>(ws, tw.qp), *Kp = at<char>(ws, tw.kp);
+    int *qe = at<int>(ws, tw.qe), *ke = at<int>(ws, tw.ke);
+    float *qm = at<float>(ws, tw.qm), *km = at<float>(ws, tw.km);
+    RET_CUDA(RET_TIMED_LAUNCH(kKRotate, st, launch_rotate_chunk_f16(p, q, p.sq, Qp, qe, qm, kScaleXi, st)));
+    RET_CUDA(RET_TIMED_LAUNCH(kKRotate, st, launch_rotate_chunk_f16(p, k, p.sk, Kp, ke, km, kScaleZeta, st)));
+    if (z_in && z_out == z_in) {  // every CTA of a head reads z_in; one writes z_out
+      RET_CUDA(cudaMemcpyAsync(at<float>(ws, tw.zc), z_in, zbytes, cudaMemcpyDeviceToDevice, st));
+      z_in = at<float>(ws, tw.zc);
+    }
+    const int need_z = (d->norm_flags & RET_NORM_RSUM) || z_out != nullptr;
+    RET_CUDA(RET_TIMED_LAUNCH(kKChunkTc, st, launch_chunk_tc(p, Qp, Kp, v, qe, ke, qm, km, S_in, z_in, S_out, z_out, o, gate, need_z, st)));
+    return RET_OK;
+  }
   float *Qr = at<float>(ws, w.qr), *Kr = at<float>(ws, w.kr);
   float *Oraw = at<float>(ws, w.oraw), *F = at<float>(ws, w.f);
   RET_CUDA(RET_TIMED_LAUNCH(kKRotate, st, launch_rotate(p, q, p.sq, d->d_k, Qr, 0, nullptr, kScaleNone, st)));

@@ -1,0 +1,695 @@
+// Chunkwise retention on the sm_103a tensor cores (tcgen05 + TMEM + TMA).
+//
+// Computes, per head and chunk of 64 tokens (hwhale.com/article/285883,
+// chunkwise equation and ChunkwiseRetention; m0nads.wordpress.com,
+// chunkwise representation):
+//   O_[c] = (Q_[c] K_[c]^T (.) D) V_[c] + (Q_[c] S_c) (.) xi,  xi_i = gamma^(i+1)
+//   S_{c+1} = gamma^L S_c + K_[c]^T (V_[c] (.) zeta),          zeta_j = gamma^(L-1-j)
+// then the three normalisations and the per-head GroupNorm (+ swish gate).
+//
+// Operands.  The prologue writes Q' = xi (.) rot(q) and K' = zeta (.) rot(k)
+// per chunk as fp16 times a power of two.  Then Q'_i . K'_j =
+// gamma^(L+i-j) q_i . k_j, so the decay mask is the constant gamma^(-L) on
+// the causal triangle, the cross term is Q' S_c and the state update K'^T V.
+// Every MMA operand is fp16 (11-bit significand) with an exact power-of-two
+// block scale chosen from a rigorous upper bound of its magnitude, so no
+// operand can overflow: Q', K' per chunk (prologue), V per tile, and one
+// joint exponent per chunk for R and the 16-bit copy of the state (the two
+// share the O accumulator).  The fp32 state in TMEM carries its own power of
+// two, folded into the per-chunk rescale it needs anyway (gamma^L).
+//
+// Work split.  One CTA per (batch, head, 128-wide slice of d_v); the d_v/128
+// CTAs of a head form a cluster that exchanges GroupNorm statistics through
+// distributed shared memory.  Everything is transposed so the v-slice is
+// the MMA's M=128 dimension:
+//   T   = Q' K'^T            (M=64 i, N=64 j, K=d_k)       -> TMEM (M=64 layout)
+//   O^T = V^T R^T            (M=128 v, N=64 i, K=64 j)     -> TMEM
+//   O^T += S^T Q'^T          (A = fp16 copy of S^T in TMEM, K=d_k)
+//   S^T += V^T K'            (M=128 v, N=d_k, K=64 j)      -> TMEM fp32 state
+//
+// Warp roles (12 warps): warp 0 issues TMA loads (2-stage ring), warp 1
+// issues MMAs (one thread) and owns TMEM, warps 4-7 ("state" group) convert
+// V, refresh the state copy, build R and the row factors and carry z, warps
+// 8-11 ("output" group) drain O^T and run GroupNorm and the stores.  Every
+// wait is bounded; a wait that runs out sets the status word and an abort
+// flag, and every role leaves after draining its own asynchronous work.
+#include <cooperative_groups.h>
+#include <cudaTypedefs.h>
+
+#include "ktimer.h"
+#include "launch.h"
+#include "tc.cuh"
+
+namespace cg = cooperative_groups;
+
+namespace ret {
+
+namespace {
+
+constexpr int kC = 64;    // tokens per chunk
+constexpr int kW = 128;   // value columns per CTA
+constexpr int kNT = 384;  // threads per CTA
+
+// Shared-memory map (offsets from a 1024-byte aligned base).
+constexpr uint32_t kStage = 80 * 1024;  // Q' 32K | K' 32K | V 16K
+constexpr uint32_t kOffQ = 0, kOffK = 32 * 1024, kOffV = 64 * 1024;
+constexpr uint32_t kOffR = 2 * kStage;                  // 64 x 128 B, fp16
+constexpr uint32_t kOTPitch = 132;                      // floats per O^T row
+constexpr uint32_t kOffOT = kOffR + 8 * 1024;           // [64][132] fp32
+constexpr uint32_t kOffZ = kOffOT + 64 * kOTPitch * 4;  // [256] fp32
+constexpr uint32_t kOffF = kOffZ + 256 * 4;             // [2][64] fp32 row factors
+constexpr uint32_t kOffE = kOffF + 2 * 64 * 4;          // [2] int chunk exponents
+constexpr uint32_t kOffRed = kOffE + 16;                // [2 groups][8] fp32 scratch
+constexpr uint32_t kOffGN = kOffRed + 64;               // [2][8][64][2] fp32
+constexpr uint32_t kOffBar = kOffGN + 2 * 8 * 64 * 2 * 4;
+constexpr int kNumBars = 12;
+constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;
+constexpr uint32_t kSmemBytes = kOffMisc + 16 + 1024;   // + alignment slack
+
+enum Bar { FULL0 = 0, FULL1, EMPTY0, EMPTY1, QK, EPI, OFULL, SFULL, OFREE, GN0, GN1, DRAIN };
+
+// TMEM column map.
+constexpr uint32_t kTS = 0, kTSh = 256, kTO = 384, kTQK = 448;
+
+constexpr uint32_t kBudget = 1u << 24;
+
+struct TcArgs {
+  const float *S_in, *z_in;
+  float *S_out, *z_out;
+  void *o;
+  Gate gate;
+  const int *qexp, *kexp;      // per (bh, chunk) exponents of Q', K'
+  const float *qmax, *kmax;    // per (bh, chunk) max |rot q|, |rot k| before the decays
+  int NV;        // CTAs per head (d_v / 128)
+  int need_z;    // carry z (third normalisation or z_out)
+  int vec_out;   // o rows are 16-byte aligned: vector stores
+};
+
+// Named barrier among the 128 threads of group g (1 = state, 2 = output).
+__device__ __forceinline__ void grp_sync(int g) {
+  asm volatile("bar.sync %0, 128;" ::"r"(g) : "memory");
+}
+
+// AND of `v` over the 128 threads of group g; also a barrier among them.
+__device__ __forceinline__ bool grp_all(int g, bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.u32 p, %2, 0;\n"
+      " bar.red.and.pred q, %1, 128, p;\n selp.u32 %0, 1, 0, q;\n}"
+      : "=r"(r)
+      : "r"(g), "r"((uint32_t)v)
+      : "memory");
+  return r != 0;
+}
+
+// Max of `v` over the 128 threads of group g (red: 4 floats of scratch).
+__device__ __forceinline__ float grp_max(int g, float v, float *red, int et) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  if ((et & 31) == 0) red[et >> 5] = v;
+  grp_sync(g);
+  const float m = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
+  grp_sync(g);
+  return m;
+}
+
+// Bounded wait that also gives up when another role has aborted.
+__device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, volatile int *abort_p,
+                                         unsigned *status) {
+  for (uint32_t i = 0; i < kBudget; ++i) {
+    if (tc::mbar_try_wait(bar, parity)) return true;
+    if ((i & 255u) == 255u && *abort_p) return false;
+  }
+  report(status, kDevTimeout);
+  *abort_p = 1;
+  return false;
+}
+
+__device__ __forceinline__ bool wait_bar_cluster(uint64_t *bar, uint32_t parity,
+                                                 volatile int *abort_p, unsigned *status) {
+  for (uint32_t i = 0; i < kBudget; ++i) {
+    if (tc::mbar_try_wait_cluster(bar, parity)) return true;
+    if ((i & 255u) == 255u && *abort_p) return false;
+  }
+  report(status, kDevTimeout);
+  *abort_p = 1;
+  return false;
+}
+
+// Wait used only while draining: ignores the abort flag, still bounded.
+__device__ __forceinline__ void drain_wait(uint64_t *bar, uint32_t parity) {
+  for (uint32_t i = 0; i < kBudget; ++i)
+    if (tc::mbar_try_wait(bar, parity)) return;
+}
+
+// e such that m * 2^-e < 2^14 (0 for m = 0).
+__device__ __forceinline__ int expo14(float m) {
+  int e = 0;
+  if (m > 0.f && m < INFINITY) {
+    frexpf(m, &e);
+    e -= 14;
+  }
+  return e;
+}
+
+__device__ __forceinline__ float2 h2f(uint32_t w) {
+  return __half22float2(*reinterpret_cast<const __half2 *>(&w));
+}
+__device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+}  // namespace
+
+__global__ void __launch_bounds__(kNT, 1)
+chunk_tc_kernel(const __grid_constant__ KParams p, const __grid_constant__ CUtensorMap tmQ,
+                const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                const TcArgs a) {
+  extern __shared__ uint8_t smraw[];
+  uint8_t *sm = reinterpret_cast<uint8_t *>(
+      (reinterpret_cast<uintptr_t>(smraw) + 1023) & ~(uintptr_t)1023);
+  uint64_t *bars = reinterpret_cast<uint64_t *>(sm + kOffBar);
+  uint32_t *tbase_p = reinterpret_cast<uint32_t *>(sm + kOffMisc);
+  volatile int *abort_p = reinterpret_cast<volatile int *>(sm + kOffMisc + 4);
+  float *zsm = reinterpret_cast<float *>(sm + kOffZ);
+  float *fsm = reinterpret_cast<float *>(sm + kOffF);
+  int *Esm = reinterpret_cast<int *>(sm + kOffE);
+  float *red = reinterpret_cast<float *>(sm + kOffRed);
+  float *OT = reinterpret_cast<float *>(sm + kOffOT);
+  float *gns = reinterpret_cast<float *>(sm + kOffGN);
+
+  cg::cluster_group cluster = cg::this_cluster();
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int NV = a.NV;
+  const int rank = (int)cluster.block_rank();
+  const int bh = blockIdx.x / NV, b = bh / p.H, h = bh % p.H;
+  const int v0 = rank * kW;
+  const int DK = p.dk, NKB = DK / 64, N = p.N;
+  const int nch = (N + kC - 1) / kC;
+  const float lng = p.lng[h];
+
+  if (tid == 0) {
+    tc::mbar_init(&bars[FULL0], 1);
+    tc::mbar_init(&bars[FULL1], 1);
+    tc::mbar_init(&bars[EMPTY0], 2);
+    tc::mbar_init(&bars[EMPTY1], 2);
+    tc::mbar_init(&bars[QK], 1);
+    tc::mbar_init(&bars[EPI], 1);
+    tc::mbar_init(&bars[OFULL], 1);
+    tc::mbar_init(&bars[SFULL], 1);
+    tc::mbar_init(&bars[OFREE], 1);
+    tc::mbar_init(&bars[GN0], NV);
+    tc::mbar_init(&bars[GN1], NV);
+    tc::mbar_init(&bars[DRAIN], 1);
+    *abort_p = 0;
+    tc::fence_mbar_init();
+  }
+  if (warp == 1) {
+    tc::tmem_alloc(tbase_p, 512);
+    tc::tmem_relinquish();
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  cluster.sync();  // every CTA's barriers exist before any remote arrive
+  tc::tc_fence_after();
+  const uint32_t tb = *tbase_p;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA
+    if (lane == 0) {
+      tc::prefetch_tmap(&tmQ);
+      tc::prefetch_tmap(&tmK);
+      tc::prefetch_tmap(&tmV);
+      const uint32_t bytes = (uint32_t)NKB * 8192u * 2u + 16384u;
+      int issued = 0;
+      for (int c = 0; c < nch; ++c) {
+        const int s = c & 1;
+        if (c >= 2 && !wait_bar(&bars[EMPTY0 + s], ((c >> 1) - 1) & 1, abort_p, p.status)) break;
+        uint8_t *st = sm + s * kStage;
+        tc::mbar_arrive_expect_tx(&bars[FULL0 + s], bytes);
+        for (int kb = 0; kb < NKB; ++kb)
+          tc::tma_load_3d(st + kOffQ + kb * 8192, &tmQ, &bars[FULL0 + s], kb * 64, c * kC, bh);
+        for (int kb = 0; kb < NKB; ++kb)
+          tc::tma_load_3d(st + kOffK + kb * 8192, &tmK, &bars[FULL0 + s], kb * 64, c * kC, bh);
+        for (int vb = 0; vb < 2; ++vb)
+          tc::tma_load_4d(st + kOffV + vb * 8192, &tmV, &bars[FULL0 + s], v0 + vb * 64, c * kC,
+                          h, b);
+        ++issued;
+      }
+      // Let every issued copy land before the CTA can leave.
+      for (int c = issued > 2 ? issued - 2 : 0; c < issued; ++c)
+        drain_wait(&bars[FULL0 + (c & 1)], (c >> 1) & 1);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA
+    if (lane == 0) {
+      const uint32_t id_qk = tc::idesc_f16(64, 64, 0, 0);
+      const uint32_t id_o = tc::idesc_f16(128, 64, 1, 0);
+      const uint32_t id_x = tc::idesc_f16(128, 64, 0, 0);
+      const uint32_t id_s = tc::idesc_f16(128, DK, 1, 1);
+      const uint32_t sr = tc::smem_u32(sm + kOffR);
+      auto mma_qk = [&](int c) {  // T = Q' K'^T
+        const uint32_t sq = tc::smem_u32(sm + (c & 1) * kStage + kOffQ), sk = sq + kOffK;
+        for (int ks = 0; ks < DK / 16; ++ks) {
+          const uint32_t off = (ks >> 2) * 8192 + (ks & 3) * 32;
+          tc::mma_ss(tb + kTQK, tc::smem_desc(sq + off, 16, 1024, tc::kSw128),
+                     tc::smem_desc(sk + off, 16, 1024, tc::kSw128), id_qk, ks > 0);
+        }
+        tc::mma_commit(&bars[QK]);
+      };
+      bool go = nch > 0 && wait_bar(&bars[FULL0], 0, abort_p, p.status);
+      if (go) {
+        tc::tc_fence_after();
+        mma_qk(0);
+      }
+      for (int c = 0; go && c < nch; ++c) {
+        const int s = c & 1;
+        const uint32_t sq = tc::smem_u32(sm + s * kStage + kOffQ);
+        const uint32_t sk = sq + kOffK, sv = sq + kOffV;
+        if (!wait_bar(&bars[EPI], c & 1, abort_p, p.status)) break;
+        if (c > 0 && !wait_bar(&bars[OFREE], (c - 1) & 1, abort_p, p.status)) break;
+        tc::tc_fence_after();
+        for (int ks = 0; ks < 4; ++ks)  // O^T = V^T R^T
+          tc::mma_ss(tb + kTO, tc::smem_desc(sv + ks * 2048, 8192, 1024, tc::kSw128),
+                     tc::smem_desc(sr + ks * 32, 16, 1024, tc::kSw128), id_o, ks > 0);
+        for (int ks = 0; ks < DK / 16; ++ks)  // O^T += S^T Q'^T
+          tc::mma_ts(tb + kTO, tb + kTSh + ks * 8,
+                     tc::smem_desc(sq + (ks >> 2) * 8192 + (ks & 3) * 32, 16, 1024, tc::kSw128),
+                     id_x, 1);
+        tc::mma_commit(&bars[OFULL]);
+        for (int ks = 0; ks < 4; ++ks)  // S^T += V^T K'
+          tc::mma_ss(tb + kTS, tc::smem_desc(sv + ks * 2048, 8192, 1024, tc::kSw128),
+                     tc::smem_desc(sk + ks * 2048, 8192, 1024, tc::kSw128), id_s, 1);
+        tc::mma_commit(&bars[SFULL]);
+        tc::mma_commit(&bars[EMPTY0 + s]);
+        if (c + 1 < nch) {
+          if (!wait_bar(&bars[FULL0 + (s ^ 1)], ((c + 1) >> 1) & 1, abort_p, p.status)) break;
+          tc::tc_fence_after();
+          mma_qk(c + 1);
+        }
+      }
+      tc::mma_commit(&bars[DRAIN]);  // every MMA issued above is finished
+      drain_wait(&bars[DRAIN], 0);
+    }
+    __syncwarp();
+  } else if (warp >= 4 && warp < 8) {
+    // ------------------------------------------------------------ state group
+    const int G = 1;
+    const int q = warp & 3;                 // TMEM lane quarter
+    const int et = tid - 128;               // 0..127
+    const int vrow = q * 32 + lane;
+    const uint32_t lb = (uint32_t)(q * 32) << 16;
+    const long long vglob = v0 + vrow;
+    const bool rsum = (p.norm_flags & RET_NORM_RSUM) != 0;
+    float *rd = red;
+    bool ok = true;
+    if (a.need_z)
+      for (int k2 = et; k2 < DK; k2 += 128) zsm[k2] = a.z_in ? a.z_in[(long long)bh * DK + k2] : 0.f;
+    // Bound of |S| entering chunk 0.
+    float m0 = 0.f;
+    if (a.S_in)
+      for (int k2 = 0; k2 < DK; ++k2)
+        m0 = fmaxf(m0, fabsf(a.S_in[((long long)bh * DK + k2) * p.dv + vglob]));
+    float s_bound = grp_max(G, m0, rd, et);
+    int sigma = 0;  // TMEM state holds S * 2^-sigma
+    for (int c = 0; c < nch && ok; ++c) {
+      const int s = c & 1;
+      const int L = min(kC, N - c * kC);
+      const float gL = gpow(lng, L);
+      const float ginvL = expf(-(float)L * lng);
+      uint8_t *st = sm + s * kStage;
+      ok = grp_all(G, wait_bar(&bars[FULL0 + s], (c >> 1) & 1, abort_p, p.status));
+      if (!ok) break;
+      const int aq = a.qexp[bh * nch + c], bk = a.kexp[bh * nch + c];
+      const float qmx = a.qmax[bh * nch + c], kmx = a.kmax[bh * nch + c];
+      // (1) V tile: bf16 -> fp16 * 2^-vx in place.
+      uint4 vv[8];
+      float vm = 0.f;
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        vv[u] = reinterpret_cast<const uint4 *>(st + kOffV)[et + 128 * u];
+        const uint32_t w[4] = {vv[u].x, vv[u].y, vv[u].z, vv[u].w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) vm = fmaxf(vm, fmaxf(fabsf(bf_lo(w[e])), fabsf(bf_hi(w[e]))));
+      }
+      const float vmx = grp_max(G, vm, rd, et);
+      const int vx = expo14(vmx);
+      const float vsc = exp2f((float)-vx);
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const uint32_t w[4] = {vv[u].x, vv[u].y, vv[u].z, vv[u].w};
+        uint32_t o4[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) o4[e] = tc::pack_f16(bf_lo(w[e]) * vsc, bf_hi(w[e]) * vsc);
+        reinterpret_cast<uint4 *>(st + kOffV)[et + 128 * u] = make_uint4(o4[0], o4[1], o4[2], o4[3]);
+      }
+      // (2) exponents: R and the state copy share the O accumulator's scale.
+      // |R_ij| = gamma^(i-j) |q_i . k_j| <= d_k max|rot q| max|rot k| (j <= i).
+      const int rr_nat = expo14((float)DK * qmx * kmx);
+      int E = rr_nat + vx;
+      if (s_bound > 0.f) E = max(E, expo14(s_bound) + aq);
+      const int rr = E - vx, ss = E - aq;
+      const int sigma_next = vx + bk;
+      // (3) state pass: fp16 copy of S_c * 2^-ss; S_acc <- gamma^L S_c * 2^-sigma_next
+      if (c > 0) {
+        ok = grp_all(G, wait_bar(&bars[SFULL], (c - 1) & 1, abort_p, p.status));
+        if (!ok) break;
+        tc::tc_fence_after();
+      }
+      // Slot s is free again: the output group read chunk c-2's exponent and
+      // row factors before it released O^T (OFREE), which the MMA issue of
+      // chunk c-1 (hence SFULL above) waited for.
+      if (et == 0) Esm[s] = E;
+      {
+        const float f_cp = exp2f((float)(sigma - ss));
+        const float f_pre = gL * exp2f((float)(sigma - sigma_next));
+        float ml = 0.f;
+        for (int g = 0; g < DK / 32; ++g) {
+          uint32_t r[32], pk[16];
+          if (c == 0) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              r[i] = __float_as_uint(
+                  a.S_in ? a.S_in[((long long)bh * DK + g * 32 + i) * p.dv + vglob] : 0.f);
+          } else {
+            tc::tmem_ld32(tb + lb + kTS + g * 32, r);
+            tc::tmem_ld_wait();
+          }
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const float x0 = __uint_as_float(r[2 * i]), x1 = __uint_as_float(r[2 * i + 1]);
+            ml = fmaxf(ml, fmaxf(fabsf(x0), fabsf(x1)));
+            pk[i] = tc::pack_f16(x0 * f_cp, x1 * f_cp);
+          }
+          tc::tmem_st16(tb + lb + kTSh + g * 16, pk);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * f_pre);
+          tc::tmem_st32(tb + lb + kTS + g * 32, r);
+        }
+        tc::tmem_st_wait();
+        const float Mc = grp_max(G, ml, rd, et) * exp2f((float)sigma);  // max |S_c|
+        s_bound = gL * Mc + (float)L * kmx * vmx;  // bound of max |S_{c+1}| (zeta <= 1)
+        sigma = sigma_next;
+      }
+      // (4) R (fp16, * 2^-rr) as K-major rows; row factors.
+      ok = grp_all(G, wait_bar(&bars[QK], c & 1, abort_p, p.status));
+      if (!ok) break;
+      tc::tc_fence_after();
+      {
+        uint32_t t0[32], t1[32];
+        tc::tmem_ld32(tb + lb + kTQK, t0);
+        tc::tmem_ld32(tb + lb + kTQK + 32, t1);
+        tc::tmem_ld_wait();
+        if (lane < 16) {
+          const int i = q * 16 + lane;  // M=64 accumulator: row i in lane 32(i/16) + i%16
+          const float tsc = exp2f((float)(aq + bk)) * ginvL;
+          const float rsc = exp2f((float)-rr);
+          float rs = 0.f;
+#pragma unroll
+          for (int cc = 0; cc < 8; ++cc) {
+            uint32_t w[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int j = cc * 8 + 2 * e;
+              const float x0 = __uint_as_float(j < 32 ? t0[j] : t1[j - 32]);
+              const float x1 = __uint_as_float(j + 1 < 32 ? t0[j + 1] : t1[j + 1 - 32]);
+              const float r0 = (j <= i && i < L) ? x0 * tsc : 0.f;
+              const float r1 = (j + 1 <= i && i < L) ? x1 * tsc : 0.f;
+              rs += r0 + r1;
+              w[e] = tc::pack_f16(r0 * rsc, r1 * rsc);
+            }
+            *reinterpret_cast<uint4 *>(sm + kOffR + tc::sw128_off(i, cc)) =
+                make_uint4(w[0], w[1], w[2], w[3]);
+          }
+          float f = 0.f;
+          if (i < L) {
+            if (rsum) {
+              float qz = 0.f;
+              for (int kb = 0; kb < NKB; ++kb)
+#pragma unroll
+                for (int cc = 0; cc < 8; ++cc) {
+                  const uint4 u =
+                      *reinterpret_cast<const uint4 *>(st + kOffQ + kb * 8192 + tc::sw128_off(i, cc));
+                  const float *zz = zsm + kb * 64 + cc * 8;
+                  const float2 a0 = h2f(u.x), a1 = h2f(u.y), a2 = h2f(u.z), a3 = h2f(u.w);
+                  qz += a0.x * zz[0] + a0.y * zz[1] + a1.x * zz[2] + a1.y * zz[3] +
+                        a2.x * zz[4] + a2.y * zz[5] + a3.x * zz[6] + a3.y * zz[7];
+                }
+              rs += qz * exp2f((float)aq);
+            }
+            const float sn = row_scale(p, h, p.pos0 + (long long)c * kC + i + 1);
+            f = sn * rsum_scale(p, sn * rs);
+          }
+          fsm[s * 64 + i] = f;
+        }
+      }
+      tc::fence_proxy_async_smem();
+      tc::tc_fence_before();
+      grp_sync(G);
+      if (et == 0) tc::mbar_arrive(&bars[EPI]);
+      // (5) z_{c+1} = gamma^L z_c + sum_j K'_j
+      if (a.need_z) {
+        const int k2 = 2 * et;
+        if (k2 < DK) {
+          float z0 = 0.f, z1 = 0.f;
+          const uint8_t *kbase = st + kOffK + (k2 >> 6) * 8192;
+          const uint32_t cc = (k2 & 63) >> 3, within = (k2 & 7) * 2;
+          for (int j = 0; j < L; ++j) {
+            const float2 kv =
+                h2f(*reinterpret_cast<const uint32_t *>(kbase + tc::sw128_off(j, cc) + within));
+            z0 += kv.x;
+            z1 += kv.y;
+          }
+          const float ksc = exp2f((float)bk);
+          zsm[k2] = fmaf(gL, zsm[k2], z0 * ksc);
+          zsm[k2 + 1] = fmaf(gL, zsm[k2 + 1], z1 * ksc);
+        }
+      }
+      grp_sync(G);
+      if (et == 0) tc::mbar_arrive(&bars[EMPTY0 + s]);
+    }
+    if (ok && a.S_out) {
+      ok = grp_all(G, wait_bar(&bars[SFULL], (nch - 1) & 1, abort_p, p.status));
+      if (ok) {
+        tc::tc_fence_after();
+        const float back = exp2f((float)sigma);
+        for (int g = 0; g < DK / 32; ++g) {
+          uint32_t r[32];
+          tc::tmem_ld32(tb + lb + kTS + g * 32, r);
+          tc::tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            a.S_out[((long long)bh * DK + g * 32 + i) * p.dv + vglob] = __uint_as_float(r[i]) * back;
+        }
+      }
+    }
+    if (ok && a.z_out && rank == 0)
+      for (int k2 = et; k2 < DK; k2 += 128) a.z_out[(long long)bh * DK + k2] = zsm[k2];
+  } else if (warp >= 8) {
+    // ------------------------------------------------------------ output group
+    const int G = 2;
+    const int q = warp & 3;
+    const int et = tid - 256;  // 0..127
+    const int vrow = q * 32 + lane;
+    const uint32_t lb = (uint32_t)(q * 32) << 16;
+    const bool gn = p.gn_eps >= 0.f;
+    const int ti = et >> 1, hf = et & 1;
+    bool ok = true;
+    for (int c = 0; c < nch && ok; ++c) {
+      const int s = c & 1;
+      const int L = min(kC, N - c * kC);
+      ok = grp_all(G, wait_bar(&bars[OFULL], c & 1, abort_p, p.status));
+      if (!ok) break;
+      tc::tc_fence_after();
+      const float osc = exp2f((float)Esm[s]);
+      const float f = fsm[s * 64 + ti];
+      {
+        uint32_t t0[32], t1[32];
+        tc::tmem_ld32(tb + lb + kTO, t0);
+        tc::tmem_ld32(tb + lb + kTO + 32, t1);
+        tc::tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          OT[i * kOTPitch + vrow] = __uint_as_float(t0[i]) * osc;
+          OT[(32 + i) * kOTPitch + vrow] = __uint_as_float(t1[i]) * osc;
+        }
+      }
+      tc::tc_fence_before();
+      grp_sync(G);
+      if (et == 0) tc::mbar_arrive(&bars[OFREE]);
+      const float *row = OT + ti * kOTPitch + hf * 64;
+      float m = 0.f;
+#pragma unroll 16
+      for (int e = 0; e < 64; ++e) m += row[e];
+      m += __shfl_xor_sync(0xffffffffu, m, 1);
+      m *= (1.f / kW);
+      float M2 = 0.f;
+#pragma unroll 16
+      for (int e = 0; e < 64; ++e) {
+        const float d = row[e] - m;
+        M2 = fmaf(d, d, M2);
+      }
+      M2 += __shfl_xor_sync(0xffffffffu, M2, 1);
+      float mean = m, var = M2 * (1.f / kW);
+      if (gn && NV > 1) {
+        // Chan's merge of the per-slice (mean, M2) of every CTA of the head.
+        const int par = c & 1;
+        if (hf == 0)
+          for (int r2 = 0; r2 < NV; ++r2) {
+            float *dst = cluster.map_shared_rank(gns, r2) + ((par * 8 + rank) * 64 + ti) * 2;
+            dst[0] = m;
+            dst[1] = M2;
+          }
+        asm volatile("fence.acq_rel.cluster;" ::: "memory");
+        grp_sync(G);
+        if (et == 0)
+          for (int r2 = 0; r2 < NV; ++r2) tc::mbar_arrive_remote(&bars[GN0 + par], r2);
+        ok = grp_all(G, wait_bar_cluster(&bars[GN0 + par], (c >> 1) & 1, abort_p, p.status));
+        if (!ok) break;
+        float msum = 0.f;
+        for (int r2 = 0; r2 < NV; ++r2) msum += gns[((par * 8 + r2) * 64 + ti) * 2];
+        mean = msum / NV;
+        float M2t = 0.f;
+        for (int r2 = 0; r2 < NV; ++r2) {
+          const float *sl = gns + ((par * 8 + r2) * 64 + ti) * 2;
+          const float d = sl[0] - mean;
+          M2t += sl[1] + (float)kW * d * d;
+        }
+        var = M2t / (float)(kW * NV);
+      }
+      // GroupNorm of x = f o: y = (o - mean) f / sqrt(f^2 var + eps); no
+      // GroupNorm: y = f o.
+      const float scale = gn ? f * rsqrtf(f * f * var + p.gn_eps) : f;
+      const float shift = gn ? mean : 0.f;
+      if (ti < L) {
+        const long long n = (long long)c * kC + ti;
+        const long long ob = b * p.so[0] + h * p.so[1] + n * p.so[2] + v0 + hf * 64;
+        const long long gb = b * a.gate.s[0] + h * a.gate.s[1] + n * a.gate.s[2] + v0 + hf * 64;
+        if (a.vec_out && p.out_bf16 && !a.gate.ptr) {
+          uint4 *dst = reinterpret_cast<uint4 *>(reinterpret_cast<__nv_bfloat16 *>(a.o) + ob);
+#pragma unroll
+          for (int e8 = 0; e8 < 8; ++e8) {
+            uint32_t w[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              w[e] = tc::pack_bf16((row[e8 * 8 + 2 * e] - shift) * scale,
+                                   (row[e8 * 8 + 2 * e + 1] - shift) * scale);
+            dst[e8] = make_uint4(w[0], w[1], w[2], w[3]);
+          }
+        } else {
+          for (int e = 0; e < 64; ++e) {
+            float y = (row[e] - shift) * scale;
+            if (a.gate.ptr) {
+              const float g = ld_elem(a.gate.ptr, gb + e, 1);
+              y *= g / (1.f + expf(-g));
+            }
+            st_elem(a.o, ob + e, y, p.out_bf16);
+          }
+        }
+      }
+      grp_sync(G);
+    }
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  cluster.sync();  // no CTA leaves while a peer may still write to it
+  if (warp == 1) {
+    tc::tc_fence_after();
+    tc::tmem_dealloc(tb, 512);
+  }
+}
+
+// ------------------------------------------------------------------ host
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void *ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                         cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  }
+  return fn;
+}
+
+bool make_map(CUtensorMap *m, CUtensorMapDataType dt, const void *base, int rank,
+              const cuuint64_t *dims, const cuuint64_t *strides_bytes, const cuuint32_t *box) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint32_t es[5] = {1, 1, 1, 1, 1};
+  return fn(m, dt, rank, const_cast<void *>(base), dims, strides_bytes, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+bool chunk_tc_supported(const KParams &p, const void *v, const long long sv[3]) {
+  if (!p.in_bf16 || p.chunk != kC) return false;
+  if (p.dk % 64 || p.dk < 64 || p.dk > 256) return false;
+  if (p.dv % kW || p.dv / kW > 8) return false;
+  if (reinterpret_cast<uintptr_t>(v) & 15) return false;
+  for (int i = 0; i < 3; ++i)
+    if (sv[i] % 8) return false;
+  // Folding the decays into fp16 rows spans gamma^(L-1) inside one chunk:
+  // keep it within fp16's normal range (gamma^64 >= 2^-16, gamma >= 0.841).
+  for (int h = 0; h < p.H; ++h)
+    if (!(p.lng[h] * kC >= -16.f * 0.69314718f)) return false;
+  return encode_fn() != nullptr;
+}
+
+cudaError_t launch_chunk_tc(const KParams &p, const void *Qp, const void *Kp, const void *v,
+                            const int *qexp, const int *kexp, const float *qmax,
+                            const float *kmax, const float *S_in, const float *z_in,
+                            float *S_out, float *z_out, void *o, Gate gate, int need_z,
+                            cudaStream_t st) {
+  const int BH = p.B * p.H;
+  CUtensorMap tq, tk, tv;
+  const cuuint64_t dq[3] = {(cuuint64_t)p.dk, (cuuint64_t)p.N, (cuuint64_t)BH};
+  const cuuint64_t sq[2] = {(cuuint64_t)p.dk * 2, (cuuint64_t)p.N * p.dk * 2};
+  const cuuint32_t bq[3] = {64, (cuuint32_t)kC, 1};
+  const cuuint64_t dv4[4] = {(cuuint64_t)p.dv, (cuuint64_t)p.N, (cuuint64_t)p.H, (cuuint64_t)p.B};
+  const cuuint64_t sv4[3] = {(cuuint64_t)p.sv[2] * 2, (cuuint64_t)p.sv[1] * 2,
+                             (cuuint64_t)p.sv[0] * 2};
+  const cuuint32_t bv[4] = {64, (cuuint32_t)kC, 1, 1};
+  if (!make_map(&tq, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, Qp, 3, dq, sq, bq) ||
+      !make_map(&tk, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, Kp, 3, dq, sq, bq) ||
+      !make_map(&tv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, v, 4, dv4, sv4, bv))
+    return cudaErrorInvalidValue;
+  TcArgs a;
+  a.S_in = S_in;
+  a.z_in = z_in;
+  a.S_out = S_out;
+  a.z_out = z_out;
+  a.o = o;
+  a.gate = gate;
+  a.qexp = qexp;
+  a.kexp = kexp;
+  a.qmax = qmax;
+  a.kmax = kmax;
+  a.NV = p.dv / kW;
+  a.need_z = need_z;
+  a.vec_out = (reinterpret_cast<uintptr_t>(o) % 16 == 0) && p.so[0] % 8 == 0 &&
+              p.so[1] % 8 == 0 && p.so[2] % 8 == 0;
+  cudaError_t e = cudaFuncSetAttribute(chunk_tc_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(BH * a.NV));
+  cfg.blockDim = dim3(kNT);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = a.NV;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, chunk_tc_kernel, p, tq, tk, tv, a);
+}
+
+}  // namespace ret

@@ -12,6 +12,10 @@ cudaError_t launch_rotate(const KParams &p, const void *x, const long long s[3],
                           void *out, int out_bf16, const float *scale, int mode,
                           cudaStream_t st);
 
+cudaError_t launch_rotate_chunk_f16(const KParams &p, const void *x, const long long s[3],
+                                    void *out, int *exps, float *maxs, int mode,
+                                    cudaStream_t st);
+
 // chunk_simt.cu: fp32 CUDA-core forms writing unnormalised rows + row factors.
 // Qr, Kr: rotated contiguous fp32 [B,H,N,dk]; Oraw: fp32 [B,H,N,dv];
 // F: fp32 [B,H,N] (row factor f = s(n) r(n)).
@@ -22,6 +26,14 @@ cudaError_t launch_chunk_simt(const KParams &p, const float *Qr, const float *Kr
 cudaError_t launch_parallel_simt(const KParams &p, const float *Qr, const float *Kr,
                                  const void *v, float *Oraw, float *F, cudaStream_t st);
 
+// chunk_tc.cu: tensor-core chunkwise kernel (chunk 64, d_k in 64..256 step
+// 64, d_v multiple of 128 up to 1024, bf16 inputs, gamma^64 >= 2^-16).
+// Qp, Kp: contiguous bf16 [B,H,N,d_k] from the rotate-and-scale prologue
+// (xi-scaled queries, zeta-scaled keys), fp16 with per-chunk power-of-two
+// exponents qexp/kexp and magnitudes qmax/kmax ([B*H][chunks]).
+struct Gate;
+bool chunk_tc_supported(const KParams &p, const void *v, const long long sv[3]);
+
 // groupnorm.cu: o = GroupNorm(F * Oraw) (* swish(gate)), written through so[].
 struct Gate {
   const void *ptr;      // bf16, NULL = no gate
@@ -29,6 +41,12 @@ struct Gate {
 };
 cudaError_t launch_groupnorm(const KParams &p, const float *Oraw, const float *F,
                              void *o, Gate gate, cudaStream_t st);
+
+cudaError_t launch_chunk_tc(const KParams &p, const void *Qp, const void *Kp, const void *v,
+                            const int *qexp, const int *kexp, const float *qmax,
+                            const float *kmax, const float *S_in, const float *z_in,
+                            float *S_out, float *z_out, void *o, Gate gate, int need_z,
+                            cudaStream_t st);
 
 // recurrent.cu: one decode step, state in place.
 cudaError_t launch_recurrent_step(const KParams &p, const void *q, const void *k,

@@ -200,3 +200,105 @@ def test_rotate_entry_point(R):
 def test_workspace_status_is_clean(R):
     ws = R.new_workspace(1 << 20, "cuda")
     assert R.poll_status(ws) == 0
+
+
+# ------------------------------------------------------------------ tensor-core chunk kernel
+@pytest.mark.parametrize("B,H,N,dk,dv", [
+    (1, 2, 64, 64, 128),      # one chunk, cluster of 1
+    (2, 3, 333, 128, 256),    # ragged tail, cluster of 2
+    (1, 2, 200, 192, 384),    # d_k not a power of two, cluster of 3
+    (1, 1, 130, 256, 1024),   # cluster of 8
+])
+@pytest.mark.parametrize("flags", [0, oracle.NORM_ALL])
+def test_tc_chunk_shapes(R, B, H, N, dk, dv, flags):
+    (q, k, v), (q64, k64, v64) = inputs(2000 + dk + dv, B, H, N, dk, dv, "bf16")
+    gam = [0.85, 0.96875, 0.999, 1.0][:H] if H <= 4 else synth.head_gammas(H)
+    S = torch.empty(B, H, dk, dv, device="cuda")
+    z = torch.empty(B, H, dk, device="cuda")
+    o = R.chunkwise_fwd(q, k, v, gam, chunk=64, norm_flags=flags, S_out=S, z_out=z, pos0=5)
+    p = oracle.Problem(B, H, N, dk, dv, gam, pos0=5, norm_flags=flags, gn_eps=1e-6)
+    ref, S_ref, z_ref = oracle.chunkwise(p, 64, q64, k64, v64)
+    check_bf16(host(o), ref, f"tc {B}x{H}x{N} dk{dk} dv{dv}")
+    assert np.max(np.abs(host(S) - S_ref)) / np.max(np.abs(S_ref)) < 1e-2
+    assert np.max(np.abs(host(z) - z_ref)) / np.max(np.abs(z_ref)) < 1e-2
+
+
+def test_tc_chunk_state_in_strided_fp32_out(R):
+    """Carried (S, z) in, [B,N,H,d] strided q/k/v/o, fp32 output, two calls
+    that split the sequence (state passed through aliasing S_out = S_in)."""
+    B, H, N, dk, dv = 2, 2, 300, 128, 256
+    qb, q64 = seeded(31, "q", (B, N, H, dk), "bf16")
+    kb, k64 = seeded(31, "k", (B, N, H, dk), "bf16")
+    vb, v64 = seeded(31, "v", (B, N, H, dv), "bf16")
+    q, k, v = (t.permute(0, 2, 1, 3) for t in (qb, kb, vb))
+    gam = [0.97, 0.995]
+    S0 = torch.randn(B, H, dk, dv, device="cuda")
+    z0 = torch.randn(B, H, dk, device="cuda")
+    p = oracle.Problem(B, H, N, dk, dv, gam, pos0=40, norm_flags=oracle.NORM_ALL, gn_eps=1e-6)
+    ref, S_ref, _ = oracle.chunkwise(p, 64, q64.transpose(0, 2, 1, 3), k64.transpose(0, 2, 1, 3),
+                                     v64.transpose(0, 2, 1, 3), S0.double().cpu().numpy(),
+                                     z0.double().cpu().numpy())
+    out = torch.empty(B, N, H, dv, device="cuda", dtype=torch.float32).permute(0, 2, 1, 3)
+    S, z = S0.clone(), z0.clone()
+    a = 128
+    R.chunkwise_fwd(q[:, :, :a], k[:, :, :a], v[:, :, :a], gam, chunk=64, pos0=40,
+                    norm_flags=R.NORM_ALL, S_in=S, z_in=z, S_out=S, z_out=z, out=out[:, :, :a])
+    R.chunkwise_fwd(q[:, :, a:], k[:, :, a:], v[:, :, a:], gam, chunk=64, pos0=40 + a,
+                    norm_flags=R.NORM_ALL, S_in=S, z_in=z, S_out=S, z_out=z, out=out[:, :, a:])
+    check_bf16(host(out), ref, "tc strided split")
+    assert np.max(np.abs(host(S) - S_ref)) / np.max(np.abs(S_ref)) < 1e-2
+
+
+def test_tc_msr_layer_chunk64(R):
+    """The gated MSR layer with chunk 64 runs the tensor-core kernel's swish
+    gate epilogue."""
+    from oracle.msr import msr_layer
+    B, N, dm, H, dk, dv = 1, 256, 256, 2, 64, 128
+    X, X64 = seeded(77, "x", (B, N, dm), "bf16")
+    W = {}
+    for name, shp in (("wq", (dm, H * dk)), ("wk", (dm, H * dk)), ("wv", (dm, H * dv)),
+                      ("wg", (dm, H * dv)), ("wo", (H * dv, dm))):
+        W[name] = seeded(77, name, shp, "bf16", std=0.05)
+    gam = synth.head_gammas(H)
+    Y = R.msr_layer_fwd(X, W["wq"][0], W["wk"][0], W["wv"][0], W["wg"][0], W["wo"][0], H=H,
+                        d_k=dk, d_v=dv, gamma=gam, chunk=64, norm_flags=R.NORM_ALL)
+    ref = msr_layer(X64, W["wq"][1], W["wk"][1], W["wv"][1], W["wg"][1], W["wo"][1], H=H,
+                    dk=dk, dv=dv, gamma=gam, chunk=64, norm_flags=oracle.NORM_ALL, gn_eps=1e-6)
+    check_bf16(host(Y), ref, "msr chunk 64")
+
+
+def test_small_gamma_takes_the_cuda_core_kernel(R):
+    """gamma^64 < 2^-16 (here 0.6) is outside the tensor-core kernel's fp16
+    range; the CUDA-core kernel serves it and matches the oracle."""
+    (q, k, v), (q64, k64, v64) = inputs(9, 1, 2, 130, 64, 128, "bf16")
+    R.lib.retention_kernel_timer_reset()
+    o = R.chunkwise_fwd(q, k, v, [0.6, 0.97], chunk=64, norm_flags=R.NORM_ALL)
+    torch.cuda.synchronize()
+    assert "chunk_simt" in R.kernel_times()
+    p = oracle.Problem(1, 2, 130, 64, 128, [0.6, 0.97], norm_flags=oracle.NORM_ALL, gn_eps=1e-6)
+    check_bf16(host(o), oracle.chunkwise(p, 64, q64, k64, v64)[0], "gamma 0.6")
+
+
+def test_tc_kernel_is_used(R):
+    """The tensor-core kernel (not the CUDA-core fallback) serves bf16,
+    chunk 64, d_v % 128 == 0."""
+    (q, k, v), _ = inputs(5, 1, 2, 256, 128, 256, "bf16")
+    R.lib.retention_kernel_timer_reset()
+    R.chunkwise_fwd(q, k, v, [0.9, 0.99], chunk=64)
+    torch.cuda.synchronize()
+    names = R.kernel_times()
+    assert "chunk_tc" in names and "chunk_simt" not in names, names
+
+
+@pytest.mark.parametrize("scale", [2.0 ** -10, 2.0 ** 10])
+def test_tc_chunk_extreme_magnitudes(R, scale):
+    """The fp16 operands carry power-of-two block scales: inputs 2^+-10 times
+    larger or smaller (exact in bf16) must still match the oracle."""
+    B, H, N, dk, dv = 1, 2, 256, 128, 256
+    (q, k, v), (q64, k64, v64) = inputs(61, B, H, N, dk, dv, "bf16")
+    q, k, v = q * scale, k * scale, v * scale
+    gam = [0.9, 0.999]
+    o = R.chunkwise_fwd(q, k, v, gam, chunk=64, gn_eps=0.0)
+    p = oracle.Problem(B, H, N, dk, dv, gam, gn_eps=0.0)
+    ref, _, _ = oracle.chunkwise(p, 64, q64 * scale, k64 * scale, v64 * scale)
+    check_bf16(host(o), ref, f"scale {scale}")
