@@ -101,7 +101,7 @@ SimtWs simt_ws(const ret_desc *d) {
 // Workspace of the tensor-core chunkwise path: status | Q' | K' | z copy.
 // Q'/K' are fp16 with per-(head, chunk) exponents and magnitudes.
 struct TcWs {
-  size_t qp, kp, zc, qe, ke, qm, km, total;
+  size_t qp, kp, zc, qe, ke, qm, km, ks, total;
 };
 
 TcWs tc_ws(const ret_desc *d) {
@@ -117,6 +117,7 @@ TcWs tc_ws(const ret_desc *d) {
   w.ke = off; off = align256(off + BH * nch * sizeof(int));
   w.qm = off; off = align256(off + BH * nch * sizeof(float));
   w.km = off; off = align256(off + BH * nch * sizeof(float));
+  w.ks = off; off = align256(off + BH * nch * d->d_k * sizeof(float));
   w.total = off;
   return w;
 }
@@ -163,15 +164,15 @@ ret_status chunkwise_impl(const ret_desc *d, const void *q, const void *k, const
     // keys, bf16), then the fused chunk kernel with the GroupNorm epilogue.
     void *Qp = at<char>(ws, tw.qp), *Kp = at<char>(ws, tw.kp);
     int *qe = at<int>(ws, tw.qe), *ke = at<int>(ws, tw.ke);
-    float *qm = at<float>(ws, tw.qm), *km = at<float>(ws, tw.km);
-    RET_CUDA(RET_TIMED_LAUNCH(kKRotate, st, launch_rotate_chunk_f16(p, q, p.sq, Qp, qe, qm, kScaleXi, st)));
-    RET_CUDA(RET_TIMED_LAUNCH(kKRotate, st, launch_rotate_chunk_f16(p, k, p.sk, Kp, ke, km, kScaleZeta, st)));
+    float *qm = at<float>(ws, tw.qm), *km = at<float>(ws, tw.km), *ks = at<float>(ws, tw.ks);
+    const int need_z = (d->norm_flags & RET_NORM_RSUM) || z_out != nullptr;
+    RET_CUDA(RET_TIMED_LAUNCH(kKRotate, st, launch_rotate_chunk_f16(p, q, p.sq, Qp, qe, qm, nullptr, kScaleXi, st)));
+    RET_CUDA(RET_TIMED_LAUNCH(kKRotate, st, launch_rotate_chunk_f16(p, k, p.sk, Kp, ke, km, need_z ? ks : nullptr, kScaleZeta, st)));
     if (z_in && z_out == z_in) {  // every CTA of a head reads z_in; one writes z_out
       RET_CUDA(cudaMemcpyAsync(at<float>(ws, tw.zc), z_in, zbytes, cudaMemcpyDeviceToDevice, st));
       z_in = at<float>(ws, tw.zc);
     }
-    const int need_z = (d->norm_flags & RET_NORM_RSUM) || z_out != nullptr;
-    RET_CUDA(RET_TIMED_LAUNCH(kKChunkTc, st, launch_chunk_tc(p, Qp, Kp, v, qe, ke, qm, km, S_in, z_in, S_out, z_out, o, gate, need_z, st)));
+    RET_CUDA(RET_TIMED_LAUNCH(kKChunkTc, st, launch_chunk_tc(p, Qp, Kp, v, qe, ke, qm, km, ks, S_in, z_in, S_out, z_out, o, gate, need_z, st)));
     return RET_OK;
   }
   float *Qr = at<float>(ws, w.qr), *Kr = at<float>(ws, w.kr);

@@ -28,9 +28,11 @@
 //   S^T += V^T K'            (M=128 v, N=d_k, K=64 j)      -> TMEM fp32 state
 //
 // Warp roles (12 warps): warp 0 issues TMA loads (2-stage ring), warp 1
-// issues MMAs (one thread) and owns TMEM, warps 4-7 ("state" group) convert
-// V, refresh the state copy, build R and the row factors and carry z, warps
-// 8-11 ("output" group) drain O^T and run GroupNorm and the stores.  Every
+// issues MMAs (one thread) and owns TMEM, warps 2-3 ("helper" group)
+// convert V to fp16, compute Q'.z for the third normalisation and carry z,
+// warps 4-7 ("state" group) refresh the state copy, build R and the row
+// factors, warps 8-11 ("output" group) drain O^T and run GroupNorm and the
+// stores.  Every
 // wait is bounded; a wait that runs out sets the status word and an abort
 // flag, and every role leaves after draining its own asynchronous work.
 #include <cooperative_groups.h>
@@ -61,12 +63,19 @@ constexpr uint32_t kOffF = kOffZ + 256 * 4;             // [2][64] fp32 row fact
 constexpr uint32_t kOffE = kOffF + 2 * 64 * 4;          // [2] int chunk exponents
 constexpr uint32_t kOffRed = kOffE + 16;                // [2 groups][8] fp32 scratch
 constexpr uint32_t kOffGN = kOffRed + 64;               // [2][8][64][2] fp32
-constexpr uint32_t kOffBar = kOffGN + 2 * 8 * 64 * 2 * 4;
-constexpr int kNumBars = 12;
+constexpr uint32_t kOffNrm = kOffGN + 2 * 8 * 64 * 2 * 4;  // [64][2] fp32 shift, scale
+constexpr uint32_t kOffVX = kOffNrm + 64 * 2 * 4;          // [2] int vx, [2] float max|V|
+constexpr uint32_t kOffQZ = kOffVX + 16;                   // [2][64] fp32 Q'_i . z
+constexpr uint32_t kOffHRed = kOffQZ + 2 * 64 * 4;         // [2][2] fp32 helper scratch
+constexpr uint32_t kOffBar = kOffHRed + 16;
+constexpr int kNumBars = 16;
 constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;
 constexpr uint32_t kSmemBytes = kOffMisc + 16 + 1024;   // + alignment slack
 
-enum Bar { FULL0 = 0, FULL1, EMPTY0, EMPTY1, QK, EPI, OFULL, SFULL, OFREE, GN0, GN1, DRAIN };
+enum Bar {
+  FULL0 = 0, FULL1, EMPTY0, EMPTY1, QK, EPI, OFULL, SFULL, OFREE, GN0, GN1, DRAIN,
+  VRDY0, VRDY1, QZRDY0, QZRDY1  // per parity: the helper may run one chunk ahead
+};
 
 // TMEM column map.
 constexpr uint32_t kTS = 0, kTSh = 256, kTO = 384, kTQK = 448;
@@ -80,37 +89,42 @@ struct TcArgs {
   Gate gate;
   const int *qexp, *kexp;      // per (bh, chunk) exponents of Q', K'
   const float *qmax, *kmax;    // per (bh, chunk) max |rot q|, |rot k| before the decays
+  const float *ksum;           // per (bh, chunk) column sums of K' (d_k floats)
   int NV;        // CTAs per head (d_v / 128)
   int need_z;    // carry z (third normalisation or z_out)
   int vec_out;   // o rows are 16-byte aligned: vector stores
 };
 
-// Named barrier among the 128 threads of group g (1 = state, 2 = output).
-__device__ __forceinline__ void grp_sync(int g) {
-  asm volatile("bar.sync %0, 128;" ::"r"(g) : "memory");
+// Named barrier among the n threads of group g (1 = state, 2 = output,
+// 3 = helper).
+__device__ __forceinline__ void grp_sync(int g, int n = 128) {
+  asm volatile("bar.sync %0, %1;" ::"r"(g), "r"(n) : "memory");
 }
 
-// AND of `v` over the 128 threads of group g; also a barrier among them.
-__device__ __forceinline__ bool grp_all(int g, bool v) {
+// AND of `v` over the n threads of group g; also a barrier among them.
+__device__ __forceinline__ bool grp_all(int g, bool v, int n = 128) {
   uint32_t r;
   asm volatile(
       "{\n .reg .pred p, q;\n setp.ne.u32 p, %2, 0;\n"
-      " bar.red.and.pred q, %1, 128, p;\n selp.u32 %0, 1, 0, q;\n}"
+      " bar.red.and.pred q, %1, %3, p;\n selp.u32 %0, 1, 0, q;\n}"
       : "=r"(r)
-      : "r"(g), "r"((uint32_t)v)
+      : "r"(g), "r"((uint32_t)v), "r"(n)
       : "memory");
   return r != 0;
 }
 
-// Max of `v` over the 128 threads of group g (red: 4 floats of scratch).
-__device__ __forceinline__ float grp_max(int g, float v, float *red, int et) {
+// Max of `v` over the 128 threads of group g.  `red` holds two 4-float
+// slots used alternately (`slot` flips every call), so one barrier suffices:
+// a slot is rewritten only after the next call's barrier, which every
+// thread passes after reading it.
+__device__ __forceinline__ float grp_max(int g, float v, float *red, int &slot, int et) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-  if ((et & 31) == 0) red[et >> 5] = v;
+  float *r = red + 4 * slot;
+  slot ^= 1;
+  if ((et & 31) == 0) r[et >> 5] = v;
   grp_sync(g);
-  const float m = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
-  grp_sync(g);
-  return m;
+  return fmaxf(fmaxf(r[0], r[1]), fmaxf(r[2], r[3]));
 }
 
 // Bounded wait that also gives up when another role has aborted.
@@ -176,6 +190,11 @@ chunk_tc_kernel(const __grid_constant__ KParams p, const __grid_constant__ CUten
   float *red = reinterpret_cast<float *>(sm + kOffRed);
   float *OT = reinterpret_cast<float *>(sm + kOffOT);
   float *gns = reinterpret_cast<float *>(sm + kOffGN);
+  float *nrm = reinterpret_cast<float *>(sm + kOffNrm);
+  int *vxs = reinterpret_cast<int *>(sm + kOffVX);
+  float *vmxs = reinterpret_cast<float *>(sm + kOffVX + 8);
+  float *qzs = reinterpret_cast<float *>(sm + kOffQZ);
+  float *hred = reinterpret_cast<float *>(sm + kOffHRed);
 
   cg::cluster_group cluster = cg::this_cluster();
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -197,9 +216,13 @@ chunk_tc_kernel(const __grid_constant__ KParams p, const __grid_constant__ CUten
     tc::mbar_init(&bars[OFULL], 1);
     tc::mbar_init(&bars[SFULL], 1);
     tc::mbar_init(&bars[OFREE], 1);
-    tc::mbar_init(&bars[GN0], NV);
-    tc::mbar_init(&bars[GN1], NV);
+    tc::mbar_init(&bars[GN0], 1);
+    tc::mbar_init(&bars[GN1], 1);
     tc::mbar_init(&bars[DRAIN], 1);
+    tc::mbar_init(&bars[VRDY0], 1);
+    tc::mbar_init(&bars[VRDY1], 1);
+    tc::mbar_init(&bars[QZRDY0], 1);
+    tc::mbar_init(&bars[QZRDY1], 1);
     *abort_p = 0;
     tc::fence_mbar_init();
   }
@@ -292,6 +315,89 @@ chunk_tc_kernel(const __grid_constant__ KParams p, const __grid_constant__ CUten
       drain_wait(&bars[DRAIN], 0);
     }
     __syncwarp();
+  } else if (warp == 2 || warp == 3) {
+    // ------------------------------------------------------------ helper group
+    const int G = 3, NT = 64;
+    const int ht = tid - 64;  // 0..63
+    const bool rsum = (p.norm_flags & RET_NORM_RSUM) != 0;
+    int hslot = 0;
+    bool ok = true;
+    if (a.need_z)
+      for (int k2 = ht; k2 < DK; k2 += NT) zsm[k2] = a.z_in ? a.z_in[(long long)bh * DK + k2] : 0.f;
+    grp_sync(G, NT);
+    for (int c = 0; c < nch && ok; ++c) {
+      const int s = c & 1;
+      uint8_t *st = sm + s * kStage;
+      ok = grp_all(G, wait_bar(&bars[FULL0 + s], (c >> 1) & 1, abort_p, p.status), NT);
+      if (!ok) break;
+      // (1) V tile: bf16 -> fp16 * 2^-vx in place (1024 16-byte words).
+      uint4 vv[16];
+      float vm = 0.f;
+#pragma unroll
+      for (int u = 0; u < 16; ++u) {
+        vv[u] = reinterpret_cast<const uint4 *>(st + kOffV)[ht + NT * u];
+        const uint32_t w[4] = {vv[u].x, vv[u].y, vv[u].z, vv[u].w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) vm = fmaxf(vm, fmaxf(fabsf(bf_lo(w[e])), fabsf(bf_hi(w[e]))));
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) vm = fmaxf(vm, __shfl_xor_sync(0xffffffffu, vm, o));
+      float *hr = hred + 2 * hslot;
+      hslot ^= 1;
+      if ((ht & 31) == 0) hr[ht >> 5] = vm;
+      grp_sync(G, NT);
+      const float vmx = fmaxf(hr[0], hr[1]);
+      const int vx = expo14(vmx);
+      const float vsc = exp2f((float)-vx);
+#pragma unroll
+      for (int u = 0; u < 16; ++u) {
+        const uint32_t w[4] = {vv[u].x, vv[u].y, vv[u].z, vv[u].w};
+        uint32_t o4[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) o4[e] = tc::pack_f16(bf_lo(w[e]) * vsc, bf_hi(w[e]) * vsc);
+        reinterpret_cast<uint4 *>(st + kOffV)[ht + NT * u] = make_uint4(o4[0], o4[1], o4[2], o4[3]);
+      }
+      if (ht == 0) {
+        vxs[s] = vx;
+        vmxs[s] = vmx;
+      }
+      tc::fence_proxy_async_smem();
+      grp_sync(G, NT);
+      if (ht == 0) tc::mbar_arrive(&bars[VRDY0 + s]);
+      // (2) Q'_i . z_c for the row sums of the third normalisation.
+      if (rsum) {
+        const int i = ht;
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int kb = 0; kb < NKB; ++kb)
+#pragma unroll
+          for (int cc = 0; cc < 8; ++cc) {
+            const uint4 u =
+                *reinterpret_cast<const uint4 *>(st + kOffQ + kb * 8192 + tc::sw128_off(i, cc));
+            const float4 z0 = *reinterpret_cast<const float4 *>(zsm + kb * 64 + cc * 8);
+            const float4 z1 = *reinterpret_cast<const float4 *>(zsm + kb * 64 + cc * 8 + 4);
+            const float2 a0 = h2f(u.x), a1 = h2f(u.y), a2 = h2f(u.z), a3 = h2f(u.w);
+            acc[0] = fmaf(a0.x, z0.x, fmaf(a0.y, z0.y, acc[0]));
+            acc[1] = fmaf(a1.x, z0.z, fmaf(a1.y, z0.w, acc[1]));
+            acc[2] = fmaf(a2.x, z1.x, fmaf(a2.y, z1.y, acc[2]));
+            acc[3] = fmaf(a3.x, z1.z, fmaf(a3.y, z1.w, acc[3]));
+          }
+        qzs[s * 64 + i] = ((acc[0] + acc[1]) + (acc[2] + acc[3])) *
+                          exp2f((float)a.qexp[bh * nch + c]);
+        grp_sync(G, NT);
+        if (ht == 0) tc::mbar_arrive(&bars[QZRDY0 + s]);
+      }
+      // (3) z_{c+1} = gamma^L z_c + sum_j K'_j (column sums from the prologue).
+      if (a.need_z) {
+        const int L = min(kC, N - c * kC);
+        const float gL = gpow(lng, L);
+        const float *ks = a.ksum + ((long long)bh * nch + c) * DK;
+        for (int k2 = ht; k2 < DK; k2 += NT) zsm[k2] = fmaf(gL, zsm[k2], ks[k2]);
+      }
+      grp_sync(G, NT);
+      if (ht == 0) tc::mbar_arrive(&bars[EMPTY0 + s]);
+    }
+    if (ok && a.z_out && rank == 0)
+      for (int k2 = ht; k2 < DK; k2 += NT) a.z_out[(long long)bh * DK + k2] = zsm[k2];
   } else if (warp >= 4 && warp < 8) {
     // ------------------------------------------------------------ state group
     const int G = 1;
@@ -302,47 +408,26 @@ chunk_tc_kernel(const __grid_constant__ KParams p, const __grid_constant__ CUten
     const long long vglob = v0 + vrow;
     const bool rsum = (p.norm_flags & RET_NORM_RSUM) != 0;
     float *rd = red;
+    int rslot = 0;
     bool ok = true;
-    if (a.need_z)
-      for (int k2 = et; k2 < DK; k2 += 128) zsm[k2] = a.z_in ? a.z_in[(long long)bh * DK + k2] : 0.f;
     // Bound of |S| entering chunk 0.
     float m0 = 0.f;
     if (a.S_in)
       for (int k2 = 0; k2 < DK; ++k2)
         m0 = fmaxf(m0, fabsf(a.S_in[((long long)bh * DK + k2) * p.dv + vglob]));
-    float s_bound = grp_max(G, m0, rd, et);
+    float s_bound = grp_max(G, m0, rd, rslot, et);
     int sigma = 0;  // TMEM state holds S * 2^-sigma
     for (int c = 0; c < nch && ok; ++c) {
       const int s = c & 1;
       const int L = min(kC, N - c * kC);
       const float gL = gpow(lng, L);
       const float ginvL = expf(-(float)L * lng);
-      uint8_t *st = sm + s * kStage;
-      ok = grp_all(G, wait_bar(&bars[FULL0 + s], (c >> 1) & 1, abort_p, p.status));
-      if (!ok) break;
       const int aq = a.qexp[bh * nch + c], bk = a.kexp[bh * nch + c];
       const float qmx = a.qmax[bh * nch + c], kmx = a.kmax[bh * nch + c];
-      // (1) V tile: bf16 -> fp16 * 2^-vx in place.
-      uint4 vv[8];
-      float vm = 0.f;
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        vv[u] = reinterpret_cast<const uint4 *>(st + kOffV)[et + 128 * u];
-        const uint32_t w[4] = {vv[u].x, vv[u].y, vv[u].z, vv[u].w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) vm = fmaxf(vm, fmaxf(fabsf(bf_lo(w[e])), fabsf(bf_hi(w[e]))));
-      }
-      const float vmx = grp_max(G, vm, rd, et);
-      const int vx = expo14(vmx);
-      const float vsc = exp2f((float)-vx);
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const uint32_t w[4] = {vv[u].x, vv[u].y, vv[u].z, vv[u].w};
-        uint32_t o4[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) o4[e] = tc::pack_f16(bf_lo(w[e]) * vsc, bf_hi(w[e]) * vsc);
-        reinterpret_cast<uint4 *>(st + kOffV)[et + 128 * u] = make_uint4(o4[0], o4[1], o4[2], o4[3]);
-      }
+      ok = grp_all(G, wait_bar(&bars[VRDY0 + s], (c >> 1) & 1, abort_p, p.status));
+      if (!ok) break;
+      const int vx = vxs[s];
+      const float vmx = vmxs[s];
       // (2) exponents: R and the state copy share the O accumulator's scale.
       // |R_ij| = gamma^(i-j) |q_i . k_j| <= d_k max|rot q| max|rot k| (j <= i).
       const int rr_nat = expo14((float)DK * qmx * kmx);
@@ -363,36 +448,44 @@ chunk_tc_kernel(const __grid_constant__ KParams p, const __grid_constant__ CUten
       {
         const float f_cp = exp2f((float)(sigma - ss));
         const float f_pre = gL * exp2f((float)(sigma - sigma_next));
-        float ml = 0.f;
-        for (int g = 0; g < DK / 32; ++g) {
-          uint32_t r[32], pk[16];
+        for (int g0 = 0; g0 < DK / 32; g0 += 2) {
+          uint32_t r[2][32];
           if (c == 0) {
 #pragma unroll
-            for (int i = 0; i < 32; ++i)
-              r[i] = __float_as_uint(
-                  a.S_in ? a.S_in[((long long)bh * DK + g * 32 + i) * p.dv + vglob] : 0.f);
+            for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+              for (int i = 0; i < 32; ++i)
+                r[hh][i] = __float_as_uint(
+                    a.S_in ? a.S_in[((long long)bh * DK + (g0 + hh) * 32 + i) * p.dv + vglob] : 0.f);
           } else {
-            tc::tmem_ld32(tb + lb + kTS + g * 32, r);
+            tc::tmem_ld32(tb + lb + kTS + g0 * 32, r[0]);
+            tc::tmem_ld32(tb + lb + kTS + g0 * 32 + 32, r[1]);
             tc::tmem_ld_wait();
           }
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const float x0 = __uint_as_float(r[2 * i]), x1 = __uint_as_float(r[2 * i + 1]);
-            ml = fmaxf(ml, fmaxf(fabsf(x0), fabsf(x1)));
-            pk[i] = tc::pack_f16(x0 * f_cp, x1 * f_cp);
-          }
-          tc::tmem_st16(tb + lb + kTSh + g * 16, pk);
+          for (int hh = 0; hh < 2; ++hh) {
+            uint32_t pk[16];
 #pragma unroll
-          for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * f_pre);
-          tc::tmem_st32(tb + lb + kTS + g * 32, r);
+            for (int i = 0; i < 16; ++i) {
+              const float x0 = __uint_as_float(r[hh][2 * i]), x1 = __uint_as_float(r[hh][2 * i + 1]);
+              pk[i] = tc::pack_f16(x0 * f_cp, x1 * f_cp);
+            }
+            tc::tmem_st16(tb + lb + kTSh + (g0 + hh) * 16, pk);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) r[hh][i] = __float_as_uint(__uint_as_float(r[hh][i]) * f_pre);
+            tc::tmem_st32(tb + lb + kTS + (g0 + hh) * 32, r[hh]);
+          }
         }
         tc::tmem_st_wait();
-        const float Mc = grp_max(G, ml, rd, et) * exp2f((float)sigma);  // max |S_c|
-        s_bound = gL * Mc + (float)L * kmx * vmx;  // bound of max |S_{c+1}| (zeta <= 1)
+        // Upper bound of max |S_{c+1}|: |S_{c+1}| <= gamma^L |S_c| + sum_j |K'_j||V_j|
+        // with zeta <= 1.  It is loose by the ratio of a sum of L terms to
+        // their random-sign size, which costs nothing in floating point.
+        s_bound = gL * s_bound + (float)L * kmx * vmx;
         sigma = sigma_next;
       }
       // (4) R (fp16, * 2^-rr) as K-major rows; row factors.
-      ok = grp_all(G, wait_bar(&bars[QK], c & 1, abort_p, p.status));
+      ok = grp_all(G, wait_bar(&bars[QK], c & 1, abort_p, p.status) &&
+                          (!rsum || wait_bar(&bars[QZRDY0 + s], (c >> 1) & 1, abort_p, p.status)));
       if (!ok) break;
       tc::tc_fence_after();
       {
@@ -423,20 +516,7 @@ chunk_tc_kernel(const __grid_constant__ KParams p, const __grid_constant__ CUten
           }
           float f = 0.f;
           if (i < L) {
-            if (rsum) {
-              float qz = 0.f;
-              for (int kb = 0; kb < NKB; ++kb)
-#pragma unroll
-                for (int cc = 0; cc < 8; ++cc) {
-                  const uint4 u =
-                      *reinterpret_cast<const uint4 *>(st + kOffQ + kb * 8192 + tc::sw128_off(i, cc));
-                  const float *zz = zsm + kb * 64 + cc * 8;
-                  const float2 a0 = h2f(u.x), a1 = h2f(u.y), a2 = h2f(u.z), a3 = h2f(u.w);
-                  qz += a0.x * zz[0] + a0.y * zz[1] + a1.x * zz[2] + a1.y * zz[3] +
-                        a2.x * zz[4] + a2.y * zz[5] + a3.x * zz[6] + a3.y * zz[7];
-                }
-              rs += qz * exp2f((float)aq);
-            }
+            if (rsum) rs += qzs[s * 64 + i];
             const float sn = row_scale(p, h, p.pos0 + (long long)c * kC + i + 1);
             f = sn * rsum_scale(p, sn * rs);
           }
@@ -447,26 +527,6 @@ chunk_tc_kernel(const __grid_constant__ KParams p, const __grid_constant__ CUten
       tc::tc_fence_before();
       grp_sync(G);
       if (et == 0) tc::mbar_arrive(&bars[EPI]);
-      // (5) z_{c+1} = gamma^L z_c + sum_j K'_j
-      if (a.need_z) {
-        const int k2 = 2 * et;
-        if (k2 < DK) {
-          float z0 = 0.f, z1 = 0.f;
-          const uint8_t *kbase = st + kOffK + (k2 >> 6) * 8192;
-          const uint32_t cc = (k2 & 63) >> 3, within = (k2 & 7) * 2;
-          for (int j = 0; j < L; ++j) {
-            const float2 kv =
-                h2f(*reinterpret_cast<const uint32_t *>(kbase + tc::sw128_off(j, cc) + within));
-            z0 += kv.x;
-            z1 += kv.y;
-          }
-          const float ksc = exp2f((float)bk);
-          zsm[k2] = fmaf(gL, zsm[k2], z0 * ksc);
-          zsm[k2 + 1] = fmaf(gL, zsm[k2 + 1], z1 * ksc);
-        }
-      }
-      grp_sync(G);
-      if (et == 0) tc::mbar_arrive(&bars[EMPTY0 + s]);
     }
     if (ok && a.S_out) {
       ok = grp_all(G, wait_bar(&bars[SFULL], (nch - 1) & 1, abort_p, p.status));
@@ -483,8 +543,6 @@ chunk_tc_kernel(const __grid_constant__ KParams p, const __grid_constant__ CUten
         }
       }
     }
-    if (ok && a.z_out && rank == 0)
-      for (int k2 = et; k2 < DK; k2 += 128) a.z_out[(long long)bh * DK + k2] = zsm[k2];
   } else if (warp >= 8) {
     // ------------------------------------------------------------ output group
     const int G = 2;
@@ -493,7 +551,9 @@ chunk_tc_kernel(const __grid_constant__ KParams p, const __grid_constant__ CUten
     const int vrow = q * 32 + lane;
     const uint32_t lb = (uint32_t)(q * 32) << 16;
     const bool gn = p.gn_eps >= 0.f;
-    const int ti = et >> 1, hf = et & 1;
+    // Statistics: 4 threads per token, interleaved columns (conflict-free
+    // with a row pitch of 132 floats); 32 tokens per pass, two passes.
+    const int sq4 = et & 3, st0 = et >> 2;
     bool ok = true;
     for (int c = 0; c < nch && ok; ++c) {
       const int s = c & 1;
@@ -502,7 +562,9 @@ chunk_tc_kernel(const __grid_constant__ KParams p, const __grid_constant__ CUten
       if (!ok) break;
       tc::tc_fence_after();
       const float osc = exp2f((float)Esm[s]);
-      const float f = fsm[s * 64 + ti];
+      float fr[2];
+      fr[0] = fsm[s * 64 + st0];
+      fr[1] = fsm[s * 64 + st0 + 32];
       {
         uint32_t t0[32], t1[32];
         tc::tmem_ld32(tb + lb + kTO, t0);
@@ -510,80 +572,123 @@ chunk_tc_kernel(const __grid_constant__ KParams p, const __grid_constant__ CUten
         tc::tmem_ld_wait();
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
-          OT[i * kOTPitch + vrow] = __uint_as_float(t0[i]) * osc;
-          OT[(32 + i) * kOTPitch + vrow] = __uint_as_float(t1[i]) * osc;
+          OT[i * kOTPitch + vrow] = __uint_as_float(t0[i]);
+          OT[(32 + i) * kOTPitch + vrow] = __uint_as_float(t1[i]);
         }
       }
       tc::tc_fence_before();
       grp_sync(G);
       if (et == 0) tc::mbar_arrive(&bars[OFREE]);
-      const float *row = OT + ti * kOTPitch + hf * 64;
-      float m = 0.f;
-#pragma unroll 16
-      for (int e = 0; e < 64; ++e) m += row[e];
-      m += __shfl_xor_sync(0xffffffffu, m, 1);
-      m *= (1.f / kW);
-      float M2 = 0.f;
-#pragma unroll 16
-      for (int e = 0; e < 64; ++e) {
-        const float d = row[e] - m;
-        M2 = fmaf(d, d, M2);
+      float mloc[2], M2loc[2];
+#pragma unroll
+      for (int pass = 0; pass < 2; ++pass) {
+        const float *row = OT + (st0 + 32 * pass) * kOTPitch + sq4;
+        float sm0 = 0.f, sm1 = 0.f;
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+          sm0 += row[4 * e];
+          sm1 += row[4 * e + 4];
+        }
+        float m = sm0 + sm1;
+        m += __shfl_xor_sync(0xffffffffu, m, 1);
+        m += __shfl_xor_sync(0xffffffffu, m, 2);
+        m *= (1.f / kW);
+        float q0 = 0.f, q1 = 0.f;
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+          const float d0 = row[4 * e] - m, d1 = row[4 * e + 4] - m;
+          q0 = fmaf(d0, d0, q0);
+          q1 = fmaf(d1, d1, q1);
+        }
+        float M2 = q0 + q1;
+        M2 += __shfl_xor_sync(0xffffffffu, M2, 1);
+        M2 += __shfl_xor_sync(0xffffffffu, M2, 2);
+        mloc[pass] = m * osc;  // O^T holds O * 2^-E; osc = 2^E
+        M2loc[pass] = M2 * osc * osc;
       }
-      M2 += __shfl_xor_sync(0xffffffffu, M2, 1);
-      float mean = m, var = M2 * (1.f / kW);
+      float mean[2] = {mloc[0], mloc[1]};
+      float var[2] = {M2loc[0] * (1.f / kW), M2loc[1] * (1.f / kW)};
       if (gn && NV > 1) {
-        // Chan's merge of the per-slice (mean, M2) of every CTA of the head.
+        // Every CTA of the head sends its per-token (mean, M2) to every CTA;
+        // each copy completes 8 bytes on the receiver's barrier, which
+        // expects NV*64*8 bytes for this chunk.
         const int par = c & 1;
-        if (hf == 0)
-          for (int r2 = 0; r2 < NV; ++r2) {
-            float *dst = cluster.map_shared_rank(gns, r2) + ((par * 8 + rank) * 64 + ti) * 2;
-            dst[0] = m;
-            dst[1] = M2;
+        if (et == 0) tc::mbar_arrive_expect_tx(&bars[GN0 + par], (uint32_t)(NV * 64 * 8));
+        if (sq4 == 0)
+#pragma unroll
+          for (int pass = 0; pass < 2; ++pass) {
+            const float *slot = gns + ((par * 8 + rank) * 64 + st0 + 32 * pass) * 2;
+            for (int r2 = 0; r2 < NV; ++r2)
+              tc::st_async_v2(slot, &bars[GN0 + par], r2, mloc[pass], M2loc[pass]);
           }
-        asm volatile("fence.acq_rel.cluster;" ::: "memory");
-        grp_sync(G);
-        if (et == 0)
-          for (int r2 = 0; r2 < NV; ++r2) tc::mbar_arrive_remote(&bars[GN0 + par], r2);
         ok = grp_all(G, wait_bar_cluster(&bars[GN0 + par], (c >> 1) & 1, abort_p, p.status));
         if (!ok) break;
-        float msum = 0.f;
-        for (int r2 = 0; r2 < NV; ++r2) msum += gns[((par * 8 + r2) * 64 + ti) * 2];
-        mean = msum / NV;
-        float M2t = 0.f;
-        for (int r2 = 0; r2 < NV; ++r2) {
-          const float *sl = gns + ((par * 8 + r2) * 64 + ti) * 2;
-          const float d = sl[0] - mean;
-          M2t += sl[1] + (float)kW * d * d;
+#pragma unroll
+        for (int pass = 0; pass < 2; ++pass) {
+          const int ti = st0 + 32 * pass;
+          float msum = 0.f;
+          for (int r2 = 0; r2 < NV; ++r2) msum += gns[((par * 8 + r2) * 64 + ti) * 2];
+          const float mu = msum / NV;
+          float M2t = 0.f;
+          for (int r2 = 0; r2 < NV; ++r2) {
+            const float *sl = gns + ((par * 8 + r2) * 64 + ti) * 2;
+            const float d = sl[0] - mu;
+            M2t += sl[1] + (float)kW * d * d;
+          }
+          mean[pass] = mu;
+          var[pass] = M2t / (float)(kW * NV);
         }
-        var = M2t / (float)(kW * NV);
       }
       // GroupNorm of x = f o: y = (o - mean) f / sqrt(f^2 var + eps); no
       // GroupNorm: y = f o.
-      const float scale = gn ? f * rsqrtf(f * f * var + p.gn_eps) : f;
-      const float shift = gn ? mean : 0.f;
-      if (ti < L) {
-        const long long n = (long long)c * kC + ti;
-        const long long ob = b * p.so[0] + h * p.so[1] + n * p.so[2] + v0 + hf * 64;
-        const long long gb = b * a.gate.s[0] + h * a.gate.s[1] + n * a.gate.s[2] + v0 + hf * 64;
-        if (a.vec_out && p.out_bf16 && !a.gate.ptr) {
-          uint4 *dst = reinterpret_cast<uint4 *>(reinterpret_cast<__nv_bfloat16 *>(a.o) + ob);
+      // Stored O^T is O * 2^-E: fold 2^E into the per-token shift and scale.
+      if (sq4 == 0)
 #pragma unroll
-          for (int e8 = 0; e8 < 8; ++e8) {
-            uint32_t w[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e)
-              w[e] = tc::pack_bf16((row[e8 * 8 + 2 * e] - shift) * scale,
-                                   (row[e8 * 8 + 2 * e + 1] - shift) * scale);
-            dst[e8] = make_uint4(w[0], w[1], w[2], w[3]);
-          }
-        } else {
-          for (int e = 0; e < 64; ++e) {
-            float y = (row[e] - shift) * scale;
+        for (int pass = 0; pass < 2; ++pass) {
+          const float f = fr[pass];
+          nrm[(st0 + 32 * pass) * 2] = gn ? mean[pass] / osc : 0.f;
+          nrm[(st0 + 32 * pass) * 2 + 1] =
+              (gn ? f * rsqrtf(f * f * var[pass] + p.gn_eps) : f) * osc;
+        }
+      grp_sync(G);
+      // Stores: warp q writes token rows 2q + 8k and 2q + 8k + 1; half-warp
+      // per row, 8 columns per lane (one 16-byte bf16 store).
+      {
+        const int rsel = lane >> 4, col = 8 * (lane & 15);
+        const long long rstride = 8 * p.so[2];
+        long long ob = b * p.so[0] + h * p.so[1] + ((long long)c * kC + 2 * q + rsel) * p.so[2] +
+                       v0 + col;
+        long long gb = b * a.gate.s[0] + h * a.gate.s[1] +
+                       ((long long)c * kC + 2 * q + rsel) * a.gate.s[2] + v0 + col;
+#pragma unroll 2
+        for (int it = 0; it < 8; ++it, ob += rstride, gb += 8 * a.gate.s[2]) {
+          const int ti = 2 * q + 8 * it + rsel;
+          if (ti < L) {
+            const float shift = nrm[ti * 2], scale = nrm[ti * 2 + 1];
+            const float4 x0 = *reinterpret_cast<const float4 *>(OT + ti * kOTPitch + col);
+            const float4 x1 = *reinterpret_cast<const float4 *>(OT + ti * kOTPitch + col + 4);
+            float y[8] = {(x0.x - shift) * scale, (x0.y - shift) * scale, (x0.z - shift) * scale,
+                          (x0.w - shift) * scale, (x1.x - shift) * scale, (x1.y - shift) * scale,
+                          (x1.z - shift) * scale, (x1.w - shift) * scale};
             if (a.gate.ptr) {
-              const float g = ld_elem(a.gate.ptr, gb + e, 1);
-              y *= g / (1.f + expf(-g));
+#pragma unroll
+              for (int e = 0; e < 8; ++e) {
+                const float g = ld_elem(a.gate.ptr, gb + e, 1);
+                y[e] *= g / (1.f + expf(-g));
+              }
             }
-            st_elem(a.o, ob + e, y, p.out_bf16);
+            if (a.vec_out && p.out_bf16) {
+              *reinterpret_cast<uint4 *>(reinterpret_cast<__nv_bfloat16 *>(a.o) + ob) =
+                  make_uint4(tc::pack_bf16(y[0], y[1]), tc::pack_bf16(y[2], y[3]),
+                             tc::pack_bf16(y[4], y[5]), tc::pack_bf16(y[6], y[7]));
+            } else if (a.vec_out) {
+              float4 *dst = reinterpret_cast<float4 *>(reinterpret_cast<float *>(a.o) + ob);
+              dst[0] = make_float4(y[0], y[1], y[2], y[3]);
+              dst[1] = make_float4(y[4], y[5], y[6], y[7]);
+            } else {
+#pragma unroll
+              for (int e = 0; e < 8; ++e) st_elem(a.o, ob + e, y[e], p.out_bf16);
+            }
           }
         }
       }
@@ -643,9 +748,9 @@ bool chunk_tc_supported(const KParams &p, const void *v, const long long sv[3]) 
 
 cudaError_t launch_chunk_tc(const KParams &p, const void *Qp, const void *Kp, const void *v,
                             const int *qexp, const int *kexp, const float *qmax,
-                            const float *kmax, const float *S_in, const float *z_in,
-                            float *S_out, float *z_out, void *o, Gate gate, int need_z,
-                            cudaStream_t st) {
+                            const float *kmax, const float *ksum, const float *S_in,
+                            const float *z_in, float *S_out, float *z_out, void *o, Gate gate,
+                            int need_z, cudaStream_t st) {
   const int BH = p.B * p.H;
   CUtensorMap tq, tk, tv;
   const cuuint64_t dq[3] = {(cuuint64_t)p.dk, (cuuint64_t)p.N, (cuuint64_t)BH};
@@ -670,10 +775,14 @@ cudaError_t launch_chunk_tc(const KParams &p, const void *Qp, const void *Kp, co
   a.kexp = kexp;
   a.qmax = qmax;
   a.kmax = kmax;
+  a.ksum = ksum;
   a.NV = p.dv / kW;
   a.need_z = need_z;
-  a.vec_out = (reinterpret_cast<uintptr_t>(o) % 16 == 0) && p.so[0] % 8 == 0 &&
-              p.so[1] % 8 == 0 && p.so[2] % 8 == 0;
+  // Row-vector stores: 8 columns per lane (16 bytes bf16, 2 x 16 bytes fp32).
+  const int al = p.out_bf16 ? 8 : 4;  // elements per aligned vector
+  const uintptr_t abytes = 16;
+  a.vec_out = (reinterpret_cast<uintptr_t>(o) % abytes == 0) && p.so[0] % al == 0 &&
+              p.so[1] % al == 0 && p.so[2] % al == 0;
   cudaError_t e = cudaFuncSetAttribute(chunk_tc_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;

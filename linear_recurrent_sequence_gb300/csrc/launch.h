@@ -13,7 +13,7 @@ cudaError_t launch_rotate(const KParams &p, const void *x, const long long s[3],
                           cudaStream_t st);
 
 cudaError_t launch_rotate_chunk_f16(const KParams &p, const void *x, const long long s[3],
-                                    void *out, int *exps, float *maxs, int mode,
+                                    void *out, int *exps, float *maxs, float *colsum, int mode,
                                     cudaStream_t st);
 
 // chunk_simt.cu: fp32 CUDA-core forms writing unnormalised rows + row factors.
@@ -44,7 +44,8 @@ cudaError_t launch_groupnorm(const KParams &p, const float *Oraw, const float *F
 
 cudaError_t launch_chunk_tc(const KParams &p, const void *Qp, const void *Kp, const void *v,
                             const int *qexp, const int *kexp, const float *qmax,
-                            const float *kmax, const float *S_in, const float *z_in,
+                            const float *kmax, const float *ksum, const float *S_in,
+                            const float *z_in,
                             float *S_out, float *z_out, void *o, Gate gate, int need_z,
                             cudaStream_t st);
 

@@ -63,6 +63,12 @@ recurrent_step_kernel(KParams p, int KS, const void *__restrict__ q,
   float *vs = kr + R;         // [dv]
   float *opart = vs + dv;     // [dv] this CTA's partial q.S
   float *red = opart + dv;    // [8]: [0] partial q.z, [1] sum x, [2] sum (x-mu)^2, warp scratch
+  __shared__ float th[2][kMaxPairs];  // per-pair frequencies (indexed per thread)
+  for (int t = tid; t < R / 2; t += NT) {
+    th[0][t] = p.th_hi[k0 / 2 + t];
+    th[1][t] = p.th_lo[k0 / 2 + t];
+  }
+  __syncthreads();
 
   // Rotated q, k rows of this CTA (positions: the token sits at pos0).
   const long long qb = b * p.sq[0] + h * p.sq[1];
@@ -73,7 +79,7 @@ recurrent_step_kernel(KParams p, int KS, const void *__restrict__ q,
     float c0 = ld_elem(k, kb + 2 * j, p.in_bf16), c1 = ld_elem(k, kb + 2 * j + 1, p.in_bf16);
     if (p.rotate) {
       float cs, sn;
-      rot_cs(p.pos0, p.th_hi[j], p.th_lo[j], cs, sn);
+      rot_cs(p.pos0, th[0][t], th[1][t], cs, sn);
       const float a = q0 * cs - q1 * sn, bq = q0 * sn + q1 * cs;
       const float c = c0 * cs - c1 * sn, d = c0 * sn + c1 * cs;
       q0 = a; q1 = bq; c0 = c; c1 = d;

@@ -73,6 +73,20 @@ __device__ __forceinline__ void mbar_arrive_remote(uint64_t *bar, uint32_t rank)
                : "memory");
 }
 
+// 8-byte store into cluster CTA `rank`'s shared memory (same offset as
+// `local`) that completes 8 bytes of transaction count on that CTA's
+// mbarrier at the same offset as `bar`.
+__device__ __forceinline__ void st_async_v2(const float *local, uint64_t *bar, uint32_t rank,
+                                            float a, float b) {
+  uint32_t ra, rb;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(smem_u32(local)), "r"(rank));
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(rb) : "r"(smem_u32(bar)), "r"(rank));
+  asm volatile(
+      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.f32 [%0], {%1, %2}, [%3];" ::"r"(ra),
+      "f"(a), "f"(b), "r"(rb)
+      : "memory");
+}
+
 // Bounded wait with acquire at cluster scope (pairs with mbar_arrive_remote).
 __device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t *bar, uint32_t parity) {
   uint32_t ok;
