@@ -204,6 +204,15 @@ typedef struct {
 
 size_t msr_workspace_size(const msr_desc *d);
 
+/* The layer's projections as a plain GEMM [m0nads, "Gated Multi-Scale
+ * Retention": X W_Q, X W_K, X W_V, X W_G, Y W_O]: C[M,N] = A[M,K] B[K,N],
+ * bf16 row-major device buffers, fp32 accumulation, bf16 result.  Runs on
+ * the tensor cores when M % 128 == 0, N % 256 == 0, K % 64 == 0 and the
+ * pointers are 16-byte aligned, on CUDA cores otherwise.  ws: at least 256
+ * bytes (the device status word). */
+ret_status retention_gemm_bf16(const void *A, const void *B, void *C, int M, int N, int K,
+                               void *ws, size_t ws_bytes, ret_stream_t stream);
+
 /* Y: [B, N, d_model] bf16. */
 ret_status msr_layer_fwd(const msr_desc *d, const void *X, const void *WQ,
                          const void *WK, const void *WV, const void *WG,

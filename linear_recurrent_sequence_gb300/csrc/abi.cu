@@ -286,6 +286,15 @@ ret_status retention_recurrent_step(const ret_desc *d, const void *q, const void
   return RET_OK;
 }
 
+// bf16 GEMM used by the MSR layer: the tensor-core kernel where the shape
+// allows, the CUDA-core kernel otherwise.
+static cudaError_t gemm_any(const void *A, const void *Bm, void *C, int M, int N, int K,
+                            unsigned *status, cudaStream_t st) {
+  if (gemm_tc_supported(A, Bm, C, M, N, K))
+    return RET_TIMED_LAUNCH(kKGemmTc, st, launch_gemm_tc(A, Bm, C, M, N, K, status, st));
+  return RET_TIMED_LAUNCH(kKGemmSimt, st, launch_gemm_bf16(A, Bm, C, M, N, K, 1, st));
+}
+
 // ------------------------------------------------------------------ MSR
 static bool msr_ok(const msr_desc *d) {
   if (!d) return false;
@@ -355,15 +364,27 @@ ret_status msr_layer_fwd(const msr_desc *m, const void *X, const void *WQ, const
   const int HK = m->H * m->d_k, HV = m->H * m->d_v;
   void *Q = at<char>(ws, w.q), *K = at<char>(ws, w.k), *V = at<char>(ws, w.v);
   void *G = at<char>(ws, w.g), *Yg = at<char>(ws, w.y);
-  RET_CUDA(RET_TIMED_LAUNCH(kKGemmSimt, st, launch_gemm_bf16(X, WQ, Q, T, HK, m->d_model, 1, st)));
-  RET_CUDA(RET_TIMED_LAUNCH(kKGemmSimt, st, launch_gemm_bf16(X, WK, K, T, HK, m->d_model, 1, st)));
-  RET_CUDA(RET_TIMED_LAUNCH(kKGemmSimt, st, launch_gemm_bf16(X, WV, V, T, HV, m->d_model, 1, st)));
-  RET_CUDA(RET_TIMED_LAUNCH(kKGemmSimt, st, launch_gemm_bf16(X, WG, G, T, HV, m->d_model, 1, st)));
+  unsigned *status = reinterpret_cast<unsigned *>(ws);
+  RET_CUDA(gemm_any(X, WQ, Q, T, HK, m->d_model, status, st));
+  RET_CUDA(gemm_any(X, WK, K, T, HK, m->d_model, status, st));
+  RET_CUDA(gemm_any(X, WV, V, T, HV, m->d_model, status, st));
+  RET_CUDA(gemm_any(X, WG, G, T, HV, m->d_model, status, st));
   Gate gate{G, {inner.sv[0], inner.sv[1], inner.sv[2]}};
   rs = chunkwise_impl(&inner, Q, K, V, nullptr, nullptr, nullptr, nullptr, Yg, gate,
                       at<char>(ws, w.inner), ws_bytes - w.inner, st);
   if (rs != RET_OK) return rs;
-  RET_CUDA(RET_TIMED_LAUNCH(kKGemmSimt, st, launch_gemm_bf16(Yg, WO, Y, T, m->d_model, HV, 1, st)));
+  RET_CUDA(gemm_any(Yg, WO, Y, T, m->d_model, HV, status, st));
+  return RET_OK;
+}
+
+ret_status retention_gemm_bf16(const void *A, const void *Bm, void *C, int M, int N, int K,
+                               void *ws, size_t ws_bytes, ret_stream_t stream) {
+  if (M < 0 || N < 0 || K < 1) return RET_EINVAL;
+  if ((long long)M * N == 0) return RET_OK;
+  if (!A || !Bm || !C) return RET_EINVAL;
+  ret_status rs = check_ws(ws, ws_bytes, kStatusBytes);
+  if (rs != RET_OK) return rs;
+  RET_CUDA(gemm_any(A, Bm, C, M, N, K, reinterpret_cast<unsigned *>(ws), (cudaStream_t)stream));
   return RET_OK;
 }
 

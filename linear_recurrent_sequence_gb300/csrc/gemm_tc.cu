@@ -1,0 +1,251 @@
+// bf16 GEMM on the sm_103a tensor cores for the MSR layer's projections
+// (m0nads.wordpress.com, "Gated Multi-Scale Retention": Q = X W_Q,
+// K = X W_K, V = X W_V, G = X W_G and the output projection Y W_O).
+//
+// C[M,N] = A[M,K] B[K,N]; A, B, C row-major bf16, fp32 accumulation.
+// Persistent CTAs walk 128 x 256 output tiles.  Per CTA: warp 0 streams
+// A (K-major) and B (MN-major) 64-deep slabs through a 4-stage TMA ring,
+// warp 1 issues tcgen05 MMAs (M=128, N=256, K=16) into one of two TMEM
+// accumulators, warps 2-5 drain the other accumulator (TMEM -> registers ->
+// bf16 -> global) while the next tile is being computed.  Every wait is
+// bounded (a timeout sets the status word and all roles leave).
+#include <cudaTypedefs.h>
+
+#include "ktimer.h"
+#include "launch.h"
+#include "tc.cuh"
+
+namespace ret {
+
+namespace {
+
+constexpr int BM = 128, BN = 256, BK = 64, kStages = 4, kNT = 192;
+constexpr uint32_t kABytes = BM * BK * 2;   // 16 KB
+constexpr uint32_t kBBytes = BK * BN * 2;   // 32 KB
+constexpr uint32_t kStageBytes = kABytes + kBBytes;
+constexpr uint32_t kOffBar = kStages * kStageBytes;
+constexpr int kNumBars = 2 * kStages + 5;
+constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;
+constexpr uint32_t kSmem = kOffMisc + 16 + 1024;
+constexpr uint32_t kBudget = 1u << 24;
+
+__device__ __forceinline__ bool gwait(uint64_t *bar, uint32_t parity, volatile int *abort_p,
+                                      unsigned *status) {
+  for (uint32_t i = 0; i < kBudget; ++i) {
+    if (tc::mbar_try_wait(bar, parity)) return true;
+    if ((i & 255u) == 255u && *abort_p) return false;
+  }
+  report(status, kDevTimeout);
+  *abort_p = 1;
+  return false;
+}
+
+__device__ __forceinline__ void gdrain(uint64_t *bar, uint32_t parity) {
+  for (uint32_t i = 0; i < kBudget; ++i)
+    if (tc::mbar_try_wait(bar, parity)) return;
+}
+
+}  // namespace
+
+__global__ void __launch_bounds__(kNT, 1)
+gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+               __nv_bfloat16 *__restrict__ C, int M, int N, int K, unsigned *status) {
+  extern __shared__ uint8_t smraw[];
+  uint8_t *sm = reinterpret_cast<uint8_t *>(
+      (reinterpret_cast<uintptr_t>(smraw) + 1023) & ~(uintptr_t)1023);
+  uint64_t *full = reinterpret_cast<uint64_t *>(sm + kOffBar);
+  uint64_t *empty = full + kStages;
+  uint64_t *acc_full = empty + kStages;  // [2]
+  uint64_t *acc_empty = acc_full + 2;    // [2]
+  uint64_t *drain = acc_empty + 2;       // MMA completion marker
+  uint32_t *tbase_p = reinterpret_cast<uint32_t *>(sm + kOffMisc);
+  volatile int *abort_p = reinterpret_cast<volatile int *>(sm + kOffMisc + 4);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int tiles_n = N / BN, tiles = (M / BM) * tiles_n, nk = K / BK;
+
+  if (tid == 0) {
+    for (int i = 0; i < kStages; ++i) {
+      tc::mbar_init(&full[i], 1);
+      tc::mbar_init(&empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      tc::mbar_init(&acc_full[i], 1);
+      tc::mbar_init(&acc_empty[i], 1);
+    }
+    tc::mbar_init(drain, 1);
+    *abort_p = 0;
+    tc::fence_mbar_init();
+  }
+  if (warp == 1) {
+    tc::tmem_alloc(tbase_p, 512);
+    tc::tmem_relinquish();
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tb = *tbase_p;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      tc::prefetch_tmap(&tmA);
+      tc::prefetch_tmap(&tmB);
+      int it = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; ok && t < tiles; t += gridDim.x) {
+        const int m0 = (t / tiles_n) * BM, n0 = (t % tiles_n) * BN;
+        for (int kb = 0; kb < nk; ++kb, ++it) {
+          const int s = it % kStages;
+          if (it >= kStages && !gwait(&empty[s], ((it / kStages) - 1) & 1, abort_p, status)) {
+            ok = false;
+            break;
+          }
+          uint8_t *st = sm + s * kStageBytes;
+          tc::mbar_arrive_expect_tx(&full[s], kStageBytes);
+          tc::tma_load_2d(st, &tmA, &full[s], kb * BK, m0);
+#pragma unroll
+          for (int j = 0; j < BN / 64; ++j)
+            tc::tma_load_2d(st + kABytes + j * 8192, &tmB, &full[s], n0 + j * 64, kb * BK);
+        }
+      }
+      for (int i = it > kStages ? it - kStages : 0; i < it; ++i)
+        gdrain(&full[i % kStages], (i / kStages) & 1);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    if (lane == 0) {
+      const uint32_t idesc = tc::idesc_bf16(BM, BN, 0, 1);
+      int it = 0, lt = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; ok && t < tiles; t += gridDim.x, ++lt) {
+        const int buf = lt & 1;
+        if (lt >= 2 && !gwait(&acc_empty[buf], ((lt >> 1) - 1) & 1, abort_p, status)) break;
+        tc::tc_fence_after();
+        const uint32_t d = tb + buf * BN;
+        for (int kb = 0; kb < nk; ++kb, ++it) {
+          const int s = it % kStages;
+          if (!gwait(&full[s], (it / kStages) & 1, abort_p, status)) {
+            ok = false;
+            break;
+          }
+          tc::tc_fence_after();
+          const uint32_t sa = tc::smem_u32(sm + s * kStageBytes), sb = sa + kABytes;
+#pragma unroll
+          for (int k = 0; k < BK / 16; ++k)
+            tc::mma_ss(d, tc::smem_desc(sa + k * 32, 16, 1024, tc::kSw128),
+                       tc::smem_desc(sb + k * 2048, 8192, 1024, tc::kSw128), idesc,
+                       (kb | k) != 0);
+          tc::mma_commit(&empty[s]);
+        }
+        if (ok) tc::mma_commit(&acc_full[buf]);
+      }
+      tc::mma_commit(drain);  // arrives once every MMA issued above is done
+      gdrain(drain, 0);
+    }
+    __syncwarp();
+  } else {
+    // Epilogue: thread = one accumulator row (TMEM lane).
+    const int q = warp & 3, row = q * 32 + lane;
+    const uint32_t lb = (uint32_t)(q * 32) << 16;
+    int lt = 0;
+    for (int t = blockIdx.x; t < tiles; t += gridDim.x, ++lt) {
+      const int buf = lt & 1;
+      bool ok = gwait(&acc_full[buf], (lt >> 1) & 1, abort_p, status);
+      {  // all four epilogue warps leave together
+        uint32_t r;
+        asm volatile(
+            "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n"
+            " bar.red.and.pred q, 1, 128, p;\n selp.u32 %0, 1, 0, q;\n}"
+            : "=r"(r)
+            : "r"((uint32_t)ok)
+            : "memory");
+        ok = r != 0;
+      }
+      if (!ok) break;
+      tc::tc_fence_after();
+      const int m0 = (t / tiles_n) * BM, n0 = (t % tiles_n) * BN;
+      __nv_bfloat16 *crow = C + (long long)(m0 + row) * N + n0;
+      for (int g = 0; g < BN / 32; ++g) {
+        uint32_t r[32];
+        tc::tmem_ld32(tb + lb + buf * BN + g * 32, r);
+        tc::tmem_ld_wait();
+        uint4 *dst = reinterpret_cast<uint4 *>(crow + g * 32);
+#pragma unroll
+        for (int v = 0; v < 4; ++v)
+          dst[v] = make_uint4(
+              tc::pack_bf16(__uint_as_float(r[8 * v + 0]), __uint_as_float(r[8 * v + 1])),
+              tc::pack_bf16(__uint_as_float(r[8 * v + 2]), __uint_as_float(r[8 * v + 3])),
+              tc::pack_bf16(__uint_as_float(r[8 * v + 4]), __uint_as_float(r[8 * v + 5])),
+              tc::pack_bf16(__uint_as_float(r[8 * v + 6]), __uint_as_float(r[8 * v + 7])));
+      }
+      tc::tc_fence_before();
+      asm volatile("bar.sync 1, 128;" ::: "memory");
+      if (tid == 64) tc::mbar_arrive(&acc_empty[buf]);
+    }
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc::tc_fence_after();
+    tc::tmem_dealloc(tb, 512);
+  }
+}
+
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 gemm_encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void *ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                         cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  }
+  return fn;
+}
+
+}  // namespace
+
+bool gemm_tc_supported(const void *A, const void *Bm, const void *C, int M, int N, int K) {
+  if (M <= 0 || N <= 0 || K <= 0) return false;
+  if (M % BM || N % BN || K % BK) return false;
+  if ((reinterpret_cast<uintptr_t>(A) | reinterpret_cast<uintptr_t>(Bm) |
+       reinterpret_cast<uintptr_t>(C)) & 15)
+    return false;
+  return gemm_encode_fn() != nullptr;
+}
+
+cudaError_t launch_gemm_tc(const void *A, const void *Bm, void *C, int M, int N, int K,
+                           unsigned *status, cudaStream_t st) {
+  auto fn = gemm_encode_fn();
+  if (!fn) return cudaErrorNotSupported;
+  CUtensorMap ta, tbm;
+  cuuint32_t es[2] = {1, 1};
+  const cuuint64_t da[2] = {(cuuint64_t)K, (cuuint64_t)M};
+  const cuuint64_t sa[1] = {(cuuint64_t)K * 2};
+  const cuuint32_t ba[2] = {BK, BM};
+  const cuuint64_t db[2] = {(cuuint64_t)N, (cuuint64_t)K};
+  const cuuint64_t sb[1] = {(cuuint64_t)N * 2};
+  const cuuint32_t bb[2] = {64, BK};
+  if (fn(&ta, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(A), da, sa, ba, es,
+         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS ||
+      fn(&tbm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(Bm), db, sb, bb, es,
+         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return cudaErrorInvalidValue;
+  cudaError_t e =
+      cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+  if (e != cudaSuccess) return e;
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int tiles = (M / BM) * (N / BN);
+  const int grid = tiles < sms ? tiles : sms;
+  gemm_tc_kernel<<<grid, kNT, kSmem, st>>>(ta, tbm, reinterpret_cast<__nv_bfloat16 *>(C), M, N,
+                                            K, status);
+  return cudaGetLastError();
+}
+
+}  // namespace ret

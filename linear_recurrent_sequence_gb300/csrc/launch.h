@@ -54,6 +54,12 @@ cudaError_t launch_recurrent_step(const KParams &p, const void *q, const void *k
                                   const void *v, float *S, float *z, void *o,
                                   cudaStream_t st);
 
+// gemm_tc.cu: tensor-core C[M,N] = A[M,K] B[K,N] (bf16 row-major, fp32
+// accumulate); M % 128, N % 256, K % 64 == 0 and 16-byte aligned pointers.
+bool gemm_tc_supported(const void *A, const void *Bm, const void *C, int M, int N, int K);
+cudaError_t launch_gemm_tc(const void *A, const void *Bm, void *C, int M, int N, int K,
+                           unsigned *status, cudaStream_t st);
+
 // gemm_simt.cu: C[M,N] = A[M,K] B[K,N], bf16 in (row-major), fp32 accumulate.
 cudaError_t launch_gemm_bf16(const void *A, const void *Bm, void *C, int M, int N,
                              int K, int out_bf16, cudaStream_t st);

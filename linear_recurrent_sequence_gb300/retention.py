@@ -62,6 +62,8 @@ _SIGS = {
     "retention_chunkwise_fwd_noalloc": (ctypes.c_int, [ctypes.POINTER(RetDesc), _P, _P, _P, _P,
                                                        _P, _P, _P, _P, _P]),
     "msr_workspace_size": (ctypes.c_size_t, [ctypes.POINTER(MsrDesc)]),
+    "retention_gemm_bf16": (ctypes.c_int, [_P, _P, _P, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                           _P, ctypes.c_size_t, _P]),
     "msr_layer_fwd": (ctypes.c_int, [ctypes.POINTER(MsrDesc), _P, _P, _P, _P, _P, _P, _P, _P,
                                      ctypes.c_size_t, _P]),
     "retention_status_string": (ctypes.c_char_p, [ctypes.c_int]),
@@ -293,6 +295,19 @@ def msr_layer_fwd(X, WQ, WK, WV, WG, WO, *, H, d_k, d_v, gamma, chunk=128, norm_
                            _ptr(WO), _ptr(out), _ptr(workspace), workspace.numel(),
                            _stream(stream))
     _check(st, "msr_layer_fwd")
+    return out
+
+
+def gemm_bf16(A, B, out=None, workspace=None, stream=None):
+    """C = A @ B for bf16 row-major matrices (the MSR projections' GEMM)."""
+    M, K = A.shape
+    N = B.shape[1]
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=A.device)
+    if workspace is None:
+        workspace = new_workspace(256, A.device)
+    _check(lib.retention_gemm_bf16(_ptr(A), _ptr(B), _ptr(out), M, N, K, _ptr(workspace),
+                                   workspace.numel(), _stream(stream)), "retention_gemm_bf16")
     return out
 
 
