@@ -41,6 +41,7 @@
 #include "ktimer.h"
 #include "launch.h"
 #include "tc.cuh"
+#include "tmap.h"
 
 namespace cg = cooperative_groups;
 
@@ -705,33 +706,6 @@ chunk_tc_kernel(const __grid_constant__ KParams p, const __grid_constant__ CUten
 }
 
 // ------------------------------------------------------------------ host
-namespace {
-
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (!fn) {
-    void *ptr = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
-                                         cudaEnableDefault, &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-  }
-  return fn;
-}
-
-bool make_map(CUtensorMap *m, CUtensorMapDataType dt, const void *base, int rank,
-              const cuuint64_t *dims, const cuuint64_t *strides_bytes, const cuuint32_t *box) {
-  auto fn = encode_fn();
-  if (!fn) return false;
-  cuuint32_t es[5] = {1, 1, 1, 1, 1};
-  return fn(m, dt, rank, const_cast<void *>(base), dims, strides_bytes, box, es,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-}  // namespace
-
 bool chunk_tc_supported(const KParams &p, const void *v, const long long sv[3]) {
   if (!p.in_bf16 || p.chunk != kC) return false;
   if (p.dk % 64 || p.dk < 64 || p.dk > 256) return false;
@@ -743,7 +717,7 @@ bool chunk_tc_supported(const KParams &p, const void *v, const long long sv[3]) 
   // keep it within fp16's normal range (gamma^64 >= 2^-16, gamma >= 0.841).
   for (int h = 0; h < p.H; ++h)
     if (!(p.lng[h] * kC >= -16.f * 0.69314718f)) return false;
-  return encode_fn() != nullptr;
+  return tmap_available();
 }
 
 cudaError_t launch_chunk_tc(const KParams &p, const void *Qp, const void *Kp, const void *v,
@@ -760,9 +734,12 @@ cudaError_t launch_chunk_tc(const KParams &p, const void *Qp, const void *Kp, co
   const cuuint64_t sv4[3] = {(cuuint64_t)p.sv[2] * 2, (cuuint64_t)p.sv[1] * 2,
                              (cuuint64_t)p.sv[0] * 2};
   const cuuint32_t bv[4] = {64, (cuuint32_t)kC, 1, 1};
-  if (!make_map(&tq, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, Qp, 3, dq, sq, bq) ||
-      !make_map(&tk, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, Kp, 3, dq, sq, bq) ||
-      !make_map(&tv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, v, 4, dv4, sv4, bv))
+  if (!tmap_encode(&tq, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, Qp, dq, sq, bq,
+                   CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !tmap_encode(&tk, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, Kp, dq, sq, bq,
+                   CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !tmap_encode(&tv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, v, dv4, sv4, bv,
+                   CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
   TcArgs a;
   a.S_in = S_in;

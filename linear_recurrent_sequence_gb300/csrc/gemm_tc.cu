@@ -14,6 +14,7 @@
 #include "ktimer.h"
 #include "launch.h"
 #include "tc.cuh"
+#include "tmap.h"
 
 namespace ret {
 
@@ -190,50 +191,28 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   }
 }
 
-namespace {
-
-PFN_cuTensorMapEncodeTiled_v12000 gemm_encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (!fn) {
-    void *ptr = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
-                                         cudaEnableDefault, &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-  }
-  return fn;
-}
-
-}  // namespace
-
 bool gemm_tc_supported(const void *A, const void *Bm, const void *C, int M, int N, int K) {
   if (M <= 0 || N <= 0 || K <= 0) return false;
   if (M % BM || N % BN || K % BK) return false;
   if ((reinterpret_cast<uintptr_t>(A) | reinterpret_cast<uintptr_t>(Bm) |
        reinterpret_cast<uintptr_t>(C)) & 15)
     return false;
-  return gemm_encode_fn() != nullptr;
+  return tmap_available();
 }
 
 cudaError_t launch_gemm_tc(const void *A, const void *Bm, void *C, int M, int N, int K,
                            unsigned *status, cudaStream_t st) {
-  auto fn = gemm_encode_fn();
-  if (!fn) return cudaErrorNotSupported;
   CUtensorMap ta, tbm;
-  cuuint32_t es[2] = {1, 1};
   const cuuint64_t da[2] = {(cuuint64_t)K, (cuuint64_t)M};
   const cuuint64_t sa[1] = {(cuuint64_t)K * 2};
   const cuuint32_t ba[2] = {BK, BM};
   const cuuint64_t db[2] = {(cuuint64_t)N, (cuuint64_t)K};
   const cuuint64_t sb[1] = {(cuuint64_t)N * 2};
   const cuuint32_t bb[2] = {64, BK};
-  if (fn(&ta, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(A), da, sa, ba, es,
-         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS ||
-      fn(&tbm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(Bm), db, sb, bb, es,
-         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+  if (!tmap_encode(&ta, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, A, da, sa, ba,
+                   CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !tmap_encode(&tbm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, Bm, db, sb, bb,
+                   CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
   cudaError_t e =
       cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);

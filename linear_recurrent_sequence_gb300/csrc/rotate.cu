@@ -11,7 +11,10 @@
 //   kScaleZeta: row j of a chunk  * gamma^(L-1-j)      (keys; L = chunk length)
 #include "common.cuh"
 #include "launch.h"
+#include "tc.cuh"
+#include "tmap.h"
 #include <cuda_fp16.h>
+#include <string.h>
 
 namespace ret {
 
@@ -68,10 +71,16 @@ rotate_scale_kernel(KParams p, const void *__restrict__ x, long long s0, long lo
 // e^{i t theta_j} is advanced by the rotation e^{i s theta_j} and re-anchored
 // with the accurate reduction every 8 rows, so the angle error stays near
 // 1e-6 rad while most rows cost four FMAs instead of a sine and cosine.
+template <bool kTma>
 __global__ void __launch_bounds__(256)
 rotate_chunk_f16_kernel(KParams p, const void *__restrict__ x, long long s0, long long s1,
-                        long long s2, __half *__restrict__ out, int *__restrict__ exps,
+                        long long s2, const __grid_constant__ CUtensorMap tmx,
+                        __half *__restrict__ out, int *__restrict__ exps,
                         float *__restrict__ maxs, float *__restrict__ colsum, int mode) {
+  // kTma: the chunk's rows arrive in shared memory by one TMA copy (row-major
+  // [C][dk] bf16); otherwise each thread loads its pairs from global memory.
+  extern __shared__ __align__(128) uint8_t xtile[];
+  __shared__ __align__(8) uint64_t tbar;
   constexpr int kPer = 32;  // pairs per thread: 64 rows * 128 pairs / 256 threads
   __shared__ float wmax[8], wraw[8];
   __shared__ float th[2][kMaxPairs];  // per-pair frequencies (indexed per thread)
@@ -82,7 +91,20 @@ rotate_chunk_f16_kernel(KParams p, const void *__restrict__ x, long long s0, lon
     th[0][tid] = p.th_hi[tid];
     th[1][tid] = p.th_lo[tid];
   }
+  if (kTma && tid == 0) {
+    tc::mbar_init(&tbar, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
   __syncthreads();
+  if (kTma) {
+    if (tid == 0) {
+      tc::mbar_arrive_expect_tx(&tbar, (uint32_t)(C * p.dk * 2));
+      tc::tma_load_4d(xtile, &tmx, &tbar, 0, c * C, h, b);
+    }
+    // Bounded wait; if it ever ran out, wait (bounded) again for the copy
+    // to land before reading or leaving.
+    if (!tc::mbar_wait(&tbar, 0, p.status, 1u << 24)) tc::mbar_wait(&tbar, 0, nullptr, 1u << 24);
+  }
   const int t0 = c * C, L = min(C, p.N - t0);
   // Pair (i, j) of element e = tid + 256 u; when P divides 256 the thread
   // keeps column jp and walks rows ip + u*istep.
@@ -99,7 +121,10 @@ rotate_chunk_f16_kernel(KParams p, const void *__restrict__ x, long long s0, lon
     const int i = walk ? ip + u * istep : e / P, j = walk ? jp : e % P;
     if (u < U && i < L && (walk || e < L * P)) {
       const long long src = b * s0 + h * s1 + (long long)(t0 + i) * s2 + 2 * j;
-      if (pair_ld) {
+      if (kTma) {
+        const uint32_t w = *reinterpret_cast<const uint32_t *>(xtile + ((size_t)i * p.dk + 2 * j) * 2);
+        v[u] = make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+      } else if (pair_ld) {
         const uint32_t w = __ldg(reinterpret_cast<const uint32_t *>(
             reinterpret_cast<const __nv_bfloat16 *>(x) + src));
         v[u] = make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
@@ -217,9 +242,31 @@ cudaError_t launch_rotate_chunk_f16(const KParams &p, const void *x, const long 
   if (p.N == 0 || p.B == 0 || p.H == 0) return cudaSuccess;
   if (p.chunk * (p.dk / 2) > 256 * 32) return cudaErrorInvalidValue;
   dim3 grid((p.N + p.chunk - 1) / p.chunk, p.B * p.H);
-  rotate_chunk_f16_kernel<<<grid, 256, 0, st>>>(p, x, s[0], s[1], s[2],
-                                                reinterpret_cast<__half *>(out), exps, maxs,
-                                                colsum, mode);
+  // TMA source when the rows are 16-byte aligned bf16 with 16-byte strides.
+  CUtensorMap tm;
+  memset(&tm, 0, sizeof(tm));
+  bool tma = p.in_bf16 && (reinterpret_cast<uintptr_t>(x) % 16 == 0) && s[0] % 8 == 0 &&
+             s[1] % 8 == 0 && s[2] % 8 == 0 && p.dk <= 256 && p.chunk <= 256;
+  if (tma) {
+    const cuuint64_t dims[4] = {(cuuint64_t)p.dk, (cuuint64_t)p.N, (cuuint64_t)p.H,
+                                (cuuint64_t)p.B};
+    const cuuint64_t strides[3] = {(cuuint64_t)s[2] * 2, (cuuint64_t)s[1] * 2,
+                                   (cuuint64_t)s[0] * 2};
+    const cuuint32_t box[4] = {(cuuint32_t)p.dk, (cuuint32_t)p.chunk, 1, 1};
+    tma = tmap_encode(&tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, x, dims, strides, box,
+                      CU_TENSOR_MAP_SWIZZLE_NONE);
+  }
+  if (tma) {
+    const size_t smem = (size_t)p.chunk * p.dk * 2;
+    cudaError_t e = cudaFuncSetAttribute(rotate_chunk_f16_kernel<true>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    rotate_chunk_f16_kernel<true><<<grid, 256, smem, st>>>(
+        p, x, s[0], s[1], s[2], tm, reinterpret_cast<__half *>(out), exps, maxs, colsum, mode);
+  } else {
+    rotate_chunk_f16_kernel<false><<<grid, 256, 0, st>>>(
+        p, x, s[0], s[1], s[2], tm, reinterpret_cast<__half *>(out), exps, maxs, colsum, mode);
+  }
   return cudaGetLastError();
 }
 
