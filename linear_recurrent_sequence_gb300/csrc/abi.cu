@@ -98,10 +98,21 @@ SimtWs simt_ws(const ret_desc *d) {
   return w;
 }
 
-// Workspace of the tensor-core chunkwise path: status | Q' | K' | z copy.
+// Sequence segments of the tensor-core chunk kernel: at most kMaxSegments
+// segments of at least kMinSegChunks chunks, and at most kMaxPieces pieces
+// of partial state.
+constexpr int kMaxSegments = 8, kMinSegChunks = 4, kMaxPieces = 8;
+
+bool split_possible(const ret_desc *d) {
+  const long long nch = ((long long)d->N + 63) / 64;
+  return d->chunk == 64 && nch >= 2 * kMinSegChunks;
+}
+
+// Workspace of the tensor-core chunkwise path: status | Q' | K' | z copy |
+// exponents, magnitudes, key column sums | (segments) S copy, pieces.
 // Q'/K' are fp16 with per-(head, chunk) exponents and magnitudes.
 struct TcWs {
-  size_t qp, kp, zc, qe, ke, qm, km, ks, total;
+  size_t qp, kp, zc, qe, ke, qm, km, ks, sc, part, zpart, total;
 };
 
 TcWs tc_ws(const ret_desc *d) {
@@ -118,8 +129,43 @@ TcWs tc_ws(const ret_desc *d) {
   w.qm = off; off = align256(off + BH * nch * sizeof(float));
   w.km = off; off = align256(off + BH * nch * sizeof(float));
   w.ks = off; off = align256(off + BH * nch * d->d_k * sizeof(float));
+  const size_t sbytes = BH * d->d_k * d->d_v * sizeof(float);
+  const bool split = split_possible(d);
+  w.sc = off; off = align256(off + (split ? sbytes : 0));
+  w.part = off; off = align256(off + (split ? kMaxPieces * sbytes : 0));
+  w.zpart = off; off = align256(off + (split ? kMaxPieces * BH * d->d_k * sizeof(float) : 0));
   w.total = off;
   return w;
+}
+
+// How the tensor-core path splits the sequence: as many segments as keep
+// every segment's CTAs (one per SM) resident together, and enough pieces to
+// give the state kernel about two CTAs per SM.
+SegPlan plan_segments(const ret_desc *d, int NV) {
+  SegPlan pl;
+  if (!split_possible(d)) return pl;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return pl;
+  const int nch = (d->N + 63) / 64;
+  const long long per_seg = (long long)d->B * d->H * NV;
+  long long P = sms / per_seg;
+  P = P < kMaxSegments ? P : kMaxSegments;
+  P = P < nch / kMinSegChunks ? P : nch / kMinSegChunks;
+  if (P < 2) return pl;
+  const int seg_len = (int)((nch + P - 1) / P);
+  P = (nch + seg_len - 1) / seg_len;
+  if (P < 2) return pl;
+  int split = 1;  // pieces per segment length: a divisor of seg_len
+  for (int t = 1; t <= seg_len; ++t)
+    if (seg_len % t == 0 && (P - 1) * t <= kMaxPieces && (P - 1) * t * per_seg <= 2LL * sms)
+      split = t;
+  pl.P = (int)P;
+  pl.seg_len = seg_len;
+  pl.piece_len = seg_len / split;
+  pl.npieces = (int)(P - 1) * split;
+  return pl;
 }
 
 template <typename T>
@@ -145,7 +191,9 @@ ret_status chunkwise_impl(const ret_desc *d, const void *q, const void *k, const
   const bool tc = !empty && d->N > 0 && chunk_tc_supported(p, v, p.sv);
   const SimtWs w = simt_ws(d);
   const TcWs tw = tc_ws(d);
-  ret_status rs = check_ws(ws, ws_bytes, tc ? tw.total : w.total);
+  // The requirement is the one retention_workspace_size reports, whichever
+  // kernel runs.
+  ret_status rs = check_ws(ws, ws_bytes, w.total > tw.total ? w.total : tw.total);
   if (rs != RET_OK) return rs;
   if (empty) return RET_OK;
   const size_t sbytes = (size_t)d->B * d->H * d->d_k * d->d_v * sizeof(float);
@@ -172,7 +220,18 @@ ret_status chunkwise_impl(const ret_desc *d, const void *q, const void *k, const
       RET_CUDA(cudaMemcpyAsync(at<float>(ws, tw.zc), z_in, zbytes, cudaMemcpyDeviceToDevice, st));
       z_in = at<float>(ws, tw.zc);
     }
-    RET_CUDA(RET_TIMED_LAUNCH(kKChunkTc, st, launch_chunk_tc(p, Qp, Kp, v, qe, ke, qm, km, ks, S_in, z_in, S_out, z_out, o, gate, need_z, st)));
+    SegPlan seg = plan_segments(d, d->d_v / 128);
+    if (seg.P > 1) {
+      // Segments read S_in at their start while the last one writes S_out.
+      if (S_in && S_out == S_in) {
+        RET_CUDA(cudaMemcpyAsync(at<float>(ws, tw.sc), S_in, sbytes, cudaMemcpyDeviceToDevice, st));
+        S_in = at<float>(ws, tw.sc);
+      }
+      seg.Part = at<float>(ws, tw.part);
+      seg.zPart = at<float>(ws, tw.zpart);
+      RET_CUDA(RET_TIMED_LAUNCH(kKStatePass, st, launch_state_tc(p, Kp, v, ke, ks, seg.npieces, seg.piece_len, seg.Part, seg.zPart, need_z, st)));
+    }
+    RET_CUDA(RET_TIMED_LAUNCH(kKChunkTc, st, launch_chunk_tc(p, Qp, Kp, v, qe, ke, qm, km, ks, S_in, z_in, S_out, z_out, o, gate, need_z, seg, st)));
     return RET_OK;
   }
   float *Qr = at<float>(ws, w.qr), *Kr = at<float>(ws, w.kr);
@@ -216,7 +275,8 @@ void retention_desc_init(ret_desc *d, int B, int H, int N, int d_k, int d_v,
 
 size_t retention_workspace_size(const ret_desc *d) {
   if (!desc_ok(d)) return 0;
-  return simt_ws(d).total;
+  const size_t a = simt_ws(d).total, b = tc_ws(d).total;
+  return a > b ? a : b;
 }
 
 ret_status retention_rotate(const ret_desc *d, const void *x, const int64_t sx[3], int dim,

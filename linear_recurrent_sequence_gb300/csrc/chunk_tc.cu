@@ -91,6 +91,13 @@ struct TcArgs {
   const int *qexp, *kexp;      // per (bh, chunk) exponents of Q', K'
   const float *qmax, *kmax;    // per (bh, chunk) max |rot q|, |rot k| before the decays
   const float *ksum;           // per (bh, chunk) column sums of K' (d_k floats)
+  // Sequence segments: segment k (blockIdx.x / (B H NV)) runs chunks
+  // [k seg_len, (k+1) seg_len).  Its entry state is gamma^(64 c0) S_in plus
+  // the pieces (piece_len whole chunks each, [piece][bh][d_k][d_v] fp32 and
+  // [piece][bh][d_k]) that end at or before its first chunk, each decayed
+  // from its end to c0.
+  const float *Part, *zPart;
+  int seg_len, piece_len;
   int NV;        // CTAs per head (d_v / 128)
   int need_z;    // carry z (third normalisation or z_out)
   int vec_out;   // o rows are 16-byte aligned: vector stores
@@ -201,10 +208,17 @@ chunk_tc_kernel(const __grid_constant__ KParams p, const __grid_constant__ CUten
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int NV = a.NV;
   const int rank = (int)cluster.block_rank();
-  const int bh = blockIdx.x / NV, b = bh / p.H, h = bh % p.H;
+  const int BHNV = p.B * p.H * NV;
+  const int seg = blockIdx.x / BHNV;
+  const int bh = (blockIdx.x % BHNV) / NV, b = bh / p.H, h = bh % p.H;
   const int v0 = rank * kW;
   const int DK = p.dk, NKB = DK / 64, N = p.N;
   const int nch = (N + kC - 1) / kC;
+  // This CTA's chunks: global c = c0 + lc; barrier phases follow lc.
+  const int c0 = seg * a.seg_len;
+  const int ncl = min(nch, c0 + a.seg_len) - c0;
+  const bool last_seg = c0 + ncl >= nch;
+  const int npc = seg > 0 ? c0 / a.piece_len : 0;  // pieces before c0
   const float lng = p.lng[h];
 
   if (tid == 0) {
@@ -245,9 +259,9 @@ chunk_tc_kernel(const __grid_constant__ KParams p, const __grid_constant__ CUten
       tc::prefetch_tmap(&tmV);
       const uint32_t bytes = (uint32_t)NKB * 8192u * 2u + 16384u;
       int issued = 0;
-      for (int c = 0; c < nch; ++c) {
-        const int s = c & 1;
-        if (c >= 2 && !wait_bar(&bars[EMPTY0 + s], ((c >> 1) - 1) & 1, abort_p, p.status)) break;
+      for (int lc = 0; lc < ncl; ++lc) {
+        const int s = lc & 1, c = c0 + lc;
+        if (lc >= 2 && !wait_bar(&bars[EMPTY0 + s], ((lc >> 1) - 1) & 1, abort_p, p.status)) break;
         uint8_t *st = sm + s * kStage;
         tc::mbar_arrive_expect_tx(&bars[FULL0 + s], bytes);
         for (int kb = 0; kb < NKB; ++kb)
@@ -260,8 +274,8 @@ chunk_tc_kernel(const __grid_constant__ KParams p, const __grid_constant__ CUten
         ++issued;
       }
       // Let every issued copy land before the CTA can leave.
-      for (int c = issued > 2 ? issued - 2 : 0; c < issued; ++c)
-        drain_wait(&bars[FULL0 + (c & 1)], (c >> 1) & 1);
+      for (int lc = issued > 2 ? issued - 2 : 0; lc < issued; ++lc)
+        drain_wait(&bars[FULL0 + (lc & 1)], (lc >> 1) & 1);
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -272,8 +286,8 @@ chunk_tc_kernel(const __grid_constant__ KParams p, const __grid_constant__ CUten
       const uint32_t id_x = tc::idesc_f16(128, 64, 0, 0);
       const uint32_t id_s = tc::idesc_f16(128, DK, 1, 1);
       const uint32_t sr = tc::smem_u32(sm + kOffR);
-      auto mma_qk = [&](int c) {  // T = Q' K'^T
-        const uint32_t sq = tc::smem_u32(sm + (c & 1) * kStage + kOffQ), sk = sq + kOffK;
+      auto mma_qk = [&](int lc) {  // T = Q' K'^T
+        const uint32_t sq = tc::smem_u32(sm + (lc & 1) * kStage + kOffQ), sk = sq + kOffK;
         for (int ks = 0; ks < DK / 16; ++ks) {
           const uint32_t off = (ks >> 2) * 8192 + (ks & 3) * 32;
           tc::mma_ss(tb + kTQK, tc::smem_desc(sq + off, 16, 1024, tc::kSw128),
@@ -281,17 +295,17 @@ chunk_tc_kernel(const __grid_constant__ KParams p, const __grid_constant__ CUten
         }
         tc::mma_commit(&bars[QK]);
       };
-      bool go = nch > 0 && wait_bar(&bars[FULL0], 0, abort_p, p.status);
+      bool go = ncl > 0 && wait_bar(&bars[FULL0], 0, abort_p, p.status);
       if (go) {
         tc::tc_fence_after();
         mma_qk(0);
       }
-      for (int c = 0; go && c < nch; ++c) {
-        const int s = c & 1;
+      for (int lc = 0; go && lc < ncl; ++lc) {
+        const int s = lc & 1;
         const uint32_t sq = tc::smem_u32(sm + s * kStage + kOffQ);
         const uint32_t sk = sq + kOffK, sv = sq + kOffV;
-        if (!wait_bar(&bars[EPI], c & 1, abort_p, p.status)) break;
-        if (c > 0 && !wait_bar(&bars[OFREE], (c - 1) & 1, abort_p, p.status)) break;
+        if (!wait_bar(&bars[EPI], lc & 1, abort_p, p.status)) break;
+        if (lc > 0 && !wait_bar(&bars[OFREE], (lc - 1) & 1, abort_p, p.status)) break;
         tc::tc_fence_after();
         for (int ks = 0; ks < 4; ++ks)  // O^T = V^T R^T
           tc::mma_ss(tb + kTO, tc::smem_desc(sv + ks * 2048, 8192, 1024, tc::kSw128),
@@ -306,10 +320,10 @@ chunk_tc_kernel(const __grid_constant__ KParams p, const __grid_constant__ CUten
                      tc::smem_desc(sk + ks * 2048, 8192, 1024, tc::kSw128), id_s, 1);
         tc::mma_commit(&bars[SFULL]);
         tc::mma_commit(&bars[EMPTY0 + s]);
-        if (c + 1 < nch) {
-          if (!wait_bar(&bars[FULL0 + (s ^ 1)], ((c + 1) >> 1) & 1, abort_p, p.status)) break;
+        if (lc + 1 < ncl) {
+          if (!wait_bar(&bars[FULL0 + (s ^ 1)], ((lc + 1) >> 1) & 1, abort_p, p.status)) break;
           tc::tc_fence_after();
-          mma_qk(c + 1);
+          mma_qk(lc + 1);
         }
       }
       tc::mma_commit(&bars[DRAIN]);  // every MMA issued above is finished
@@ -324,12 +338,21 @@ chunk_tc_kernel(const __grid_constant__ KParams p, const __grid_constant__ CUten
     int hslot = 0;
     bool ok = true;
     if (a.need_z)
-      for (int k2 = ht; k2 < DK; k2 += NT) zsm[k2] = a.z_in ? a.z_in[(long long)bh * DK + k2] : 0.f;
+      for (int k2 = ht; k2 < DK; k2 += NT) {
+        float z = a.z_in ? a.z_in[(long long)bh * DK + k2] : 0.f;
+        if (seg > 0) {  // entry z of a later segment
+          z *= gpow(lng, kC * c0);
+          for (int i = 0; i < npc; ++i)
+            z = fmaf(gpow(lng, kC * (c0 - (i + 1) * a.piece_len)),
+                     a.zPart[((long long)i * p.B * p.H + bh) * DK + k2], z);
+        }
+        zsm[k2] = z;
+      }
     grp_sync(G, NT);
-    for (int c = 0; c < nch && ok; ++c) {
-      const int s = c & 1;
+    for (int lc = 0; lc < ncl && ok; ++lc) {
+      const int s = lc & 1, c = c0 + lc;
       uint8_t *st = sm + s * kStage;
-      ok = grp_all(G, wait_bar(&bars[FULL0 + s], (c >> 1) & 1, abort_p, p.status), NT);
+      ok = grp_all(G, wait_bar(&bars[FULL0 + s], (lc >> 1) & 1, abort_p, p.status), NT);
       if (!ok) break;
       // (1) V tile: bf16 -> fp16 * 2^-vx in place (1024 16-byte words).
       uint4 vv[16];
@@ -397,7 +420,7 @@ chunk_tc_kernel(const __grid_constant__ KParams p, const __grid_constant__ CUten
       grp_sync(G, NT);
       if (ht == 0) tc::mbar_arrive(&bars[EMPTY0 + s]);
     }
-    if (ok && a.z_out && rank == 0)
+    if (ok && a.z_out && rank == 0 && last_seg)
       for (int k2 = ht; k2 < DK; k2 += NT) a.z_out[(long long)bh * DK + k2] = zsm[k2];
   } else if (warp >= 4 && warp < 8) {
     // ------------------------------------------------------------ state group
@@ -411,21 +434,44 @@ chunk_tc_kernel(const __grid_constant__ KParams p, const __grid_constant__ CUten
     float *rd = red;
     int rslot = 0;
     bool ok = true;
-    // Bound of |S| entering chunk 0.
+    // Entry state (S_in, or for a later segment the decayed sum of S_in and
+    // the pieces before it) goes to the TMEM state columns; s_bound = max |S|.
+    const bool has_state = a.S_in != nullptr || npc > 0;
     float m0 = 0.f;
-    if (a.S_in)
-      for (int k2 = 0; k2 < DK; ++k2)
-        m0 = fmaxf(m0, fabsf(a.S_in[((long long)bh * DK + k2) * p.dv + vglob]));
+    if (has_state) {
+      const float w_in = seg > 0 ? gpow(lng, kC * c0) : 1.f;
+      for (int g = 0; g < DK / 32; ++g) {
+        uint32_t r[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const long long e = ((long long)bh * DK + g * 32 + i) * p.dv + vglob;
+          r[i] = __float_as_uint(a.S_in ? w_in * a.S_in[e] : 0.f);
+        }
+        for (int pi = 0; pi < npc; ++pi) {
+          const float w = gpow(lng, kC * (c0 - (pi + 1) * a.piece_len));
+          const float *src = a.Part + (long long)pi * p.B * p.H * DK * p.dv;
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const long long e = ((long long)bh * DK + g * 32 + i) * p.dv + vglob;
+            r[i] = __float_as_uint(fmaf(w, src[e], __uint_as_float(r[i])));
+          }
+        }
+#pragma unroll
+        for (int i = 0; i < 32; ++i) m0 = fmaxf(m0, fabsf(__uint_as_float(r[i])));
+        tc::tmem_st32(tb + lb + kTS + g * 32, r);
+      }
+      tc::tmem_st_wait();
+    }
     float s_bound = grp_max(G, m0, rd, rslot, et);
     int sigma = 0;  // TMEM state holds S * 2^-sigma
-    for (int c = 0; c < nch && ok; ++c) {
-      const int s = c & 1;
+    for (int lc = 0; lc < ncl && ok; ++lc) {
+      const int s = lc & 1, c = c0 + lc;
       const int L = min(kC, N - c * kC);
       const float gL = gpow(lng, L);
       const float ginvL = expf(-(float)L * lng);
       const int aq = a.qexp[bh * nch + c], bk = a.kexp[bh * nch + c];
       const float qmx = a.qmax[bh * nch + c], kmx = a.kmax[bh * nch + c];
-      ok = grp_all(G, wait_bar(&bars[VRDY0 + s], (c >> 1) & 1, abort_p, p.status));
+      ok = grp_all(G, wait_bar(&bars[VRDY0 + s], (lc >> 1) & 1, abort_p, p.status));
       if (!ok) break;
       const int vx = vxs[s];
       const float vmx = vmxs[s];
@@ -437,8 +483,8 @@ chunk_tc_kernel(const __grid_constant__ KParams p, const __grid_constant__ CUten
       const int rr = E - vx, ss = E - aq;
       const int sigma_next = vx + bk;
       // (3) state pass: fp16 copy of S_c * 2^-ss; S_acc <- gamma^L S_c * 2^-sigma_next
-      if (c > 0) {
-        ok = grp_all(G, wait_bar(&bars[SFULL], (c - 1) & 1, abort_p, p.status));
+      if (lc > 0) {
+        ok = grp_all(G, wait_bar(&bars[SFULL], (lc - 1) & 1, abort_p, p.status));
         if (!ok) break;
         tc::tc_fence_after();
       }
@@ -451,13 +497,11 @@ chunk_tc_kernel(const __grid_constant__ KParams p, const __grid_constant__ CUten
         const float f_pre = gL * exp2f((float)(sigma - sigma_next));
         for (int g0 = 0; g0 < DK / 32; g0 += 2) {
           uint32_t r[2][32];
-          if (c == 0) {
+          if (lc == 0 && !has_state) {
 #pragma unroll
             for (int hh = 0; hh < 2; ++hh)
 #pragma unroll
-              for (int i = 0; i < 32; ++i)
-                r[hh][i] = __float_as_uint(
-                    a.S_in ? a.S_in[((long long)bh * DK + (g0 + hh) * 32 + i) * p.dv + vglob] : 0.f);
+              for (int i = 0; i < 32; ++i) r[hh][i] = 0u;
           } else {
             tc::tmem_ld32(tb + lb + kTS + g0 * 32, r[0]);
             tc::tmem_ld32(tb + lb + kTS + g0 * 32 + 32, r[1]);
@@ -485,8 +529,8 @@ chunk_tc_kernel(const __grid_constant__ KParams p, const __grid_constant__ CUten
         sigma = sigma_next;
       }
       // (4) R (fp16, * 2^-rr) as K-major rows; row factors.
-      ok = grp_all(G, wait_bar(&bars[QK], c & 1, abort_p, p.status) &&
-                          (!rsum || wait_bar(&bars[QZRDY0 + s], (c >> 1) & 1, abort_p, p.status)));
+      ok = grp_all(G, wait_bar(&bars[QK], lc & 1, abort_p, p.status) &&
+                          (!rsum || wait_bar(&bars[QZRDY0 + s], (lc >> 1) & 1, abort_p, p.status)));
       if (!ok) break;
       tc::tc_fence_after();
       {
@@ -529,8 +573,8 @@ chunk_tc_kernel(const __grid_constant__ KParams p, const __grid_constant__ CUten
       grp_sync(G);
       if (et == 0) tc::mbar_arrive(&bars[EPI]);
     }
-    if (ok && a.S_out) {
-      ok = grp_all(G, wait_bar(&bars[SFULL], (nch - 1) & 1, abort_p, p.status));
+    if (ok && a.S_out && last_seg) {
+      ok = grp_all(G, wait_bar(&bars[SFULL], (ncl - 1) & 1, abort_p, p.status));
       if (ok) {
         tc::tc_fence_after();
         const float back = exp2f((float)sigma);
@@ -556,10 +600,10 @@ chunk_tc_kernel(const __grid_constant__ KParams p, const __grid_constant__ CUten
     // with a row pitch of 132 floats); 32 tokens per pass, two passes.
     const int sq4 = et & 3, st0 = et >> 2;
     bool ok = true;
-    for (int c = 0; c < nch && ok; ++c) {
-      const int s = c & 1;
+    for (int lc = 0; lc < ncl && ok; ++lc) {
+      const int s = lc & 1, c = c0 + lc;
       const int L = min(kC, N - c * kC);
-      ok = grp_all(G, wait_bar(&bars[OFULL], c & 1, abort_p, p.status));
+      ok = grp_all(G, wait_bar(&bars[OFULL], lc & 1, abort_p, p.status));
       if (!ok) break;
       tc::tc_fence_after();
       const float osc = exp2f((float)Esm[s]);
@@ -613,7 +657,7 @@ chunk_tc_kernel(const __grid_constant__ KParams p, const __grid_constant__ CUten
         // Every CTA of the head sends its per-token (mean, M2) to every CTA;
         // each copy completes 8 bytes on the receiver's barrier, which
         // expects NV*64*8 bytes for this chunk.
-        const int par = c & 1;
+        const int par = lc & 1;
         if (et == 0) tc::mbar_arrive_expect_tx(&bars[GN0 + par], (uint32_t)(NV * 64 * 8));
         if (sq4 == 0)
 #pragma unroll
@@ -622,7 +666,7 @@ chunk_tc_kernel(const __grid_constant__ KParams p, const __grid_constant__ CUten
             for (int r2 = 0; r2 < NV; ++r2)
               tc::st_async_v2(slot, &bars[GN0 + par], r2, mloc[pass], M2loc[pass]);
           }
-        ok = grp_all(G, wait_bar_cluster(&bars[GN0 + par], (c >> 1) & 1, abort_p, p.status));
+        ok = grp_all(G, wait_bar_cluster(&bars[GN0 + par], (lc >> 1) & 1, abort_p, p.status));
         if (!ok) break;
 #pragma unroll
         for (int pass = 0; pass < 2; ++pass) {
@@ -724,7 +768,7 @@ cudaError_t launch_chunk_tc(const KParams &p, const void *Qp, const void *Kp, co
                             const int *qexp, const int *kexp, const float *qmax,
                             const float *kmax, const float *ksum, const float *S_in,
                             const float *z_in, float *S_out, float *z_out, void *o, Gate gate,
-                            int need_z, cudaStream_t st) {
+                            int need_z, const SegPlan &seg, cudaStream_t st) {
   const int BH = p.B * p.H;
   CUtensorMap tq, tk, tv;
   const cuuint64_t dq[3] = {(cuuint64_t)p.dk, (cuuint64_t)p.N, (cuuint64_t)BH};
@@ -755,6 +799,12 @@ cudaError_t launch_chunk_tc(const KParams &p, const void *Qp, const void *Kp, co
   a.ksum = ksum;
   a.NV = p.dv / kW;
   a.need_z = need_z;
+  const int nch = (p.N + kC - 1) / kC;
+  a.seg_len = seg.P > 1 ? seg.seg_len : nch;
+  a.piece_len = seg.P > 1 ? seg.piece_len : 1;
+  a.Part = seg.Part;
+  a.zPart = seg.zPart;
+  const int P = seg.P > 1 ? seg.P : 1;
   // Row-vector stores: 8 columns per lane (16 bytes bf16, 2 x 16 bytes fp32).
   const int al = p.out_bf16 ? 8 : 4;  // elements per aligned vector
   const uintptr_t abytes = 16;
@@ -764,7 +814,7 @@ cudaError_t launch_chunk_tc(const KParams &p, const void *Qp, const void *Kp, co
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)(BH * a.NV));
+  cfg.gridDim = dim3((unsigned)(P * BH * a.NV));
   cfg.blockDim = dim3(kNT);
   cfg.dynamicSmemBytes = kSmemBytes;
   cfg.stream = st;

@@ -42,12 +42,26 @@ struct Gate {
 cudaError_t launch_groupnorm(const KParams &p, const float *Oraw, const float *F,
                              void *o, Gate gate, cudaStream_t st);
 
+// Sequence segments of the tensor-core chunk kernel.  P segments of seg_len
+// chunks run as separate CTA groups; the entry state of segment k > 0 is
+// assembled from the partial states of the npieces pieces (piece_len whole
+// chunks each, covering chunks [0, (P-1) seg_len)) that state_tc writes.
+struct SegPlan {
+  int P = 1, seg_len = 0, npieces = 0, piece_len = 1;
+  float *Part = nullptr, *zPart = nullptr;  // [piece][B*H][d_k][d_v], [piece][B*H][d_k]
+};
+
 cudaError_t launch_chunk_tc(const KParams &p, const void *Qp, const void *Kp, const void *v,
                             const int *qexp, const int *kexp, const float *qmax,
                             const float *kmax, const float *ksum, const float *S_in,
                             const float *z_in,
                             float *S_out, float *z_out, void *o, Gate gate, int need_z,
-                            cudaStream_t st);
+                            const SegPlan &seg, cudaStream_t st);
+
+// state_tc.cu: partial states of the pieces of a SegPlan (tensor cores).
+cudaError_t launch_state_tc(const KParams &p, const void *Kp, const void *v, const int *kexp,
+                            const float *ksum, int npieces, int piece_len, float *Part,
+                            float *zPart, int need_z, cudaStream_t st);
 
 // recurrent.cu: one decode step, state in place.
 cudaError_t launch_recurrent_step(const KParams &p, const void *q, const void *k,

@@ -302,3 +302,39 @@ def test_tc_chunk_extreme_magnitudes(R, scale):
     p = oracle.Problem(B, H, N, dk, dv, gam, gn_eps=0.0)
     ref, _, _ = oracle.chunkwise(p, 64, q64 * scale, k64 * scale, v64 * scale)
     check_bf16(host(o), ref, f"scale {scale}")
+
+
+@pytest.mark.parametrize("B,H,N,dk,dv", [
+    (1, 2, 64 * 40 + 17, 128, 128),  # 7 segments of 6 chunks, one piece each, ragged tail
+    (1, 1, 64 * 16, 64, 256),        # 4 segments, two pieces per segment
+    (2, 2, 64 * 9 + 1, 256, 512),    # 2 segments, one-chunk pieces, 1-token last chunk
+])
+@pytest.mark.parametrize("inplace", [False, True])
+def test_tc_sequence_segments(R, B, H, N, dk, dv, inplace):
+    """Few heads on a long sequence: the chunk kernel runs the sequence as
+    several segments whose entry states come from the state kernel's pieces.
+    Carried (S, z) in and out, in place or not, all three normalisations."""
+    (q, k, v), (q64, k64, v64) = inputs(3000 + N, B, H, N, dk, dv, "bf16")
+    gam = [0.9, 0.99][:H]
+    S0 = torch.randn(B, H, dk, dv, device="cuda")
+    z0 = torch.randn(B, H, dk, device="cuda")
+    p = oracle.Problem(B, H, N, dk, dv, gam, pos0=3, norm_flags=oracle.NORM_ALL, gn_eps=1e-6)
+    ref, S_ref, z_ref = oracle.chunkwise(p, 64, q64, k64, v64, S0.double().cpu().numpy(),
+                                         z0.double().cpu().numpy())
+    if inplace:
+        S, z = S0.clone(), z0.clone()
+        S_in, z_in, S_out, z_out = S, z, S, z
+    else:
+        S_in, z_in = S0, z0
+        S_out = torch.full_like(S0, float("nan"))
+        z_out = torch.full_like(z0, float("nan"))
+    R.lib.retention_kernel_timer_reset()
+    o = R.chunkwise_fwd(q, k, v, gam, chunk=64, pos0=3, norm_flags=R.NORM_ALL, S_in=S_in,
+                        z_in=z_in, S_out=S_out, z_out=z_out)
+    torch.cuda.synchronize()
+    assert "state_pass" in R.kernel_times()
+    check_bf16(host(o), ref, f"segments {B}x{H}x{N}")
+    assert np.max(np.abs(host(S_out) - S_ref)) / np.max(np.abs(S_ref)) < 1e-2
+    assert np.max(np.abs(host(z_out) - z_ref)) / np.max(np.abs(z_ref)) < 1e-2
+    if not inplace:
+        assert torch.equal(S_in, S0) and torch.equal(z_in, z0)
