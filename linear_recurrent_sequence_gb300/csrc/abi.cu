@@ -109,10 +109,10 @@ bool split_possible(const ret_desc *d) {
 }
 
 // Workspace of the tensor-core chunkwise path: status | Q' | K' | z copy |
-// exponents, magnitudes, key column sums | (segments) S copy, pieces.
+// per-chunk records, key column sums | (segments) S copy, pieces.
 // Q'/K' are fp16 with per-(head, chunk) exponents and magnitudes.
 struct TcWs {
-  size_t qp, kp, zc, qe, ke, qm, km, ks, sc, part, zpart, total;
+  size_t qp, kp, zc, meta, ks, sc, part, zpart, total;
 };
 
 TcWs tc_ws(const ret_desc *d) {
@@ -124,10 +124,7 @@ TcWs tc_ws(const ret_desc *d) {
   w.qp = off; off = align256(off + rows * d->d_k * 2);
   w.kp = off; off = align256(off + rows * d->d_k * 2);
   w.zc = off; off = align256(off + BH * d->d_k * sizeof(float));
-  w.qe = off; off = align256(off + BH * nch * sizeof(int));
-  w.ke = off; off = align256(off + BH * nch * sizeof(int));
-  w.qm = off; off = align256(off + BH * nch * sizeof(float));
-  w.km = off; off = align256(off + BH * nch * sizeof(float));
+  w.meta = off; off = align256(off + BH * nch * sizeof(ChunkMeta));
   w.ks = off; off = align256(off + BH * nch * d->d_k * sizeof(float));
   const size_t sbytes = BH * d->d_k * d->d_v * sizeof(float);
   const bool split = split_possible(d);
@@ -210,12 +207,11 @@ ret_status chunkwise_impl(const ret_desc *d, const void *q, const void *k, const
   if (tc) {
     // Tensor-core path: rotate-and-scale prologue (xi on queries, zeta on
     // keys, bf16), then the fused chunk kernel with the GroupNorm epilogue.
-    void *Qp = at<char>(ws, tw.qp), *Kp = at<char>(ws, tw.kp);
-    int *qe = at<int>(ws, tw.qe), *ke = at<int>(ws, tw.ke);
-    float *qm = at<float>(ws, tw.qm), *km = at<float>(ws, tw.km), *ks = at<float>(ws, tw.ks);
+    __half *Qp = at<__half>(ws, tw.qp), *Kp = at<__half>(ws, tw.kp);
+    ChunkMeta *meta = at<ChunkMeta>(ws, tw.meta);
+    float *ks = at<float>(ws, tw.ks);
     const int need_z = (d->norm_flags & RET_NORM_RSUM) || z_out != nullptr;
-    RET_CUDA(RET_TIMED_LAUNCH(kKRotate, st, launch_rotate_chunk_f16(p, q, p.sq, Qp, qe, qm, nullptr, kScaleXi, st)));
-    RET_CUDA(RET_TIMED_LAUNCH(kKRotate, st, launch_rotate_chunk_f16(p, k, p.sk, Kp, ke, km, need_z ? ks : nullptr, kScaleZeta, st)));
+    RET_CUDA(RET_TIMED_LAUNCH(kKRotate, st, launch_rotate_qk(p, q, k, Qp, Kp, meta, need_z ? ks : nullptr, st)));
     if (z_in && z_out == z_in) {  // every CTA of a head reads z_in; one writes z_out
       RET_CUDA(cudaMemcpyAsync(at<float>(ws, tw.zc), z_in, zbytes, cudaMemcpyDeviceToDevice, st));
       z_in = at<float>(ws, tw.zc);
@@ -229,9 +225,9 @@ ret_status chunkwise_impl(const ret_desc *d, const void *q, const void *k, const
       }
       seg.Part = at<float>(ws, tw.part);
       seg.zPart = at<float>(ws, tw.zpart);
-      RET_CUDA(RET_TIMED_LAUNCH(kKStatePass, st, launch_state_tc(p, Kp, v, ke, ks, seg.npieces, seg.piece_len, seg.Part, seg.zPart, need_z, st)));
+      RET_CUDA(RET_TIMED_LAUNCH(kKStatePass, st, launch_state_tc(p, Kp, v, meta, ks, seg.npieces, seg.piece_len, seg.Part, seg.zPart, need_z, st)));
     }
-    RET_CUDA(RET_TIMED_LAUNCH(kKChunkTc, st, launch_chunk_tc(p, Qp, Kp, v, qe, ke, qm, km, ks, S_in, z_in, S_out, z_out, o, gate, need_z, seg, st)));
+    RET_CUDA(RET_TIMED_LAUNCH(kKChunkTc, st, launch_chunk_tc(p, Qp, Kp, v, meta, ks, S_in, z_in, S_out, z_out, o, gate, need_z, seg, st)));
     return RET_OK;
   }
   float *Qr = at<float>(ws, w.qr), *Kr = at<float>(ws, w.kr);

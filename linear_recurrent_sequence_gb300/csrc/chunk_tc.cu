@@ -54,8 +54,10 @@ constexpr int kW = 128;   // value columns per CTA
 constexpr int kNT = 384;  // threads per CTA
 
 // Shared-memory map (offsets from a 1024-byte aligned base).
-constexpr uint32_t kStage = 80 * 1024;  // Q' 32K | K' 32K | V 16K
+// Stage: Q' 32K | K' 32K | V 16K | key column sums (d_k fp32) | ChunkMeta.
 constexpr uint32_t kOffQ = 0, kOffK = 32 * 1024, kOffV = 64 * 1024;
+constexpr uint32_t kOffKs = 80 * 1024, kOffMeta = kOffKs + 1024;
+constexpr uint32_t kStage = 82 * 1024;
 constexpr uint32_t kOffR = 2 * kStage;                  // 64 x 128 B, fp16
 constexpr uint32_t kOTPitch = 132;                      // floats per O^T row
 constexpr uint32_t kOffOT = kOffR + 8 * 1024;           // [64][132] fp32
@@ -72,6 +74,7 @@ constexpr uint32_t kOffBar = kOffHRed + 16;
 constexpr int kNumBars = 16;
 constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;
 constexpr uint32_t kSmemBytes = kOffMisc + 16 + 1024;   // + alignment slack
+static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 
 enum Bar {
   FULL0 = 0, FULL1, EMPTY0, EMPTY1, QK, EPI, OFULL, SFULL, OFREE, GN0, GN1, DRAIN,
@@ -88,8 +91,7 @@ struct TcArgs {
   float *S_out, *z_out;
   void *o;
   Gate gate;
-  const int *qexp, *kexp;      // per (bh, chunk) exponents of Q', K'
-  const float *qmax, *kmax;    // per (bh, chunk) max |rot q|, |rot k| before the decays
+  const ChunkMeta *meta;       // per (bh, chunk): exponents and magnitudes of Q', K'
   const float *ksum;           // per (bh, chunk) column sums of K' (d_k floats)
   // Sequence segments: segment k (blockIdx.x / (B H NV)) runs chunks
   // [k seg_len, (k+1) seg_len).  Its entry state is gamma^(64 c0) S_in plus
@@ -257,7 +259,8 @@ chunk_tc_kernel(const __grid_constant__ KParams p, const __grid_constant__ CUten
       tc::prefetch_tmap(&tmQ);
       tc::prefetch_tmap(&tmK);
       tc::prefetch_tmap(&tmV);
-      const uint32_t bytes = (uint32_t)NKB * 8192u * 2u + 16384u;
+      const uint32_t bytes = (uint32_t)NKB * 8192u * 2u + 16384u + 16u +
+                             (a.need_z ? (uint32_t)DK * 4u : 0u);
       int issued = 0;
       for (int lc = 0; lc < ncl; ++lc) {
         const int s = lc & 1, c = c0 + lc;
@@ -271,6 +274,10 @@ chunk_tc_kernel(const __grid_constant__ KParams p, const __grid_constant__ CUten
         for (int vb = 0; vb < 2; ++vb)
           tc::tma_load_4d(st + kOffV + vb * 8192, &tmV, &bars[FULL0 + s], v0 + vb * 64, c * kC,
                           h, b);
+        tc::bulk_load(st + kOffMeta, a.meta + (long long)bh * nch + c, 16u, &bars[FULL0 + s]);
+        if (a.need_z)
+          tc::bulk_load(st + kOffKs, a.ksum + ((long long)bh * nch + c) * DK, (uint32_t)DK * 4u,
+                        &bars[FULL0 + s]);
         ++issued;
       }
       // Let every issued copy land before the CTA can leave.
@@ -406,7 +413,7 @@ chunk_tc_kernel(const __grid_constant__ KParams p, const __grid_constant__ CUten
             acc[3] = fmaf(a3.x, z1.z, fmaf(a3.y, z1.w, acc[3]));
           }
         qzs[s * 64 + i] = ((acc[0] + acc[1]) + (acc[2] + acc[3])) *
-                          exp2f((float)a.qexp[bh * nch + c]);
+                          exp2f((float)reinterpret_cast<const ChunkMeta *>(st + kOffMeta)->qexp);
         grp_sync(G, NT);
         if (ht == 0) tc::mbar_arrive(&bars[QZRDY0 + s]);
       }
@@ -414,7 +421,7 @@ chunk_tc_kernel(const __grid_constant__ KParams p, const __grid_constant__ CUten
       if (a.need_z) {
         const int L = min(kC, N - c * kC);
         const float gL = gpow(lng, L);
-        const float *ks = a.ksum + ((long long)bh * nch + c) * DK;
+        const float *ks = reinterpret_cast<const float *>(st + kOffKs);
         for (int k2 = ht; k2 < DK; k2 += NT) zsm[k2] = fmaf(gL, zsm[k2], ks[k2]);
       }
       grp_sync(G, NT);
@@ -469,15 +476,17 @@ chunk_tc_kernel(const __grid_constant__ KParams p, const __grid_constant__ CUten
       const int L = min(kC, N - c * kC);
       const float gL = gpow(lng, L);
       const float ginvL = expf(-(float)L * lng);
-      const int aq = a.qexp[bh * nch + c], bk = a.kexp[bh * nch + c];
-      const float qmx = a.qmax[bh * nch + c], kmx = a.kmax[bh * nch + c];
       ok = grp_all(G, wait_bar(&bars[VRDY0 + s], (lc >> 1) & 1, abort_p, p.status));
       if (!ok) break;
+      const ChunkMeta mt = *reinterpret_cast<const ChunkMeta *>(sm + s * kStage + kOffMeta);
+      const int aq = mt.qexp, bk = mt.kexp;
+      const float qmx = mt.qmax, kmx = mt.kmax;
       const int vx = vxs[s];
       const float vmx = vmxs[s];
       // (2) exponents: R and the state copy share the O accumulator's scale.
-      // |R_ij| = gamma^(i-j) |q_i . k_j| <= d_k max|rot q| max|rot k| (j <= i).
-      const int rr_nat = expo14((float)DK * qmx * kmx);
+      // |R_ij| = gamma^(i-j) |q_i . k_j| <= (d_k/2) max|pair of rot q| max|pair of rot k|
+      // (j <= i; a dot product is a sum of d_k/2 pair products).
+      const int rr_nat = expo14((float)(DK / 2) * qmx * kmx);
       int E = rr_nat + vx;
       if (s_bound > 0.f) E = max(E, expo14(s_bound) + aq);
       const int rr = E - vx, ss = E - aq;
@@ -523,7 +532,7 @@ chunk_tc_kernel(const __grid_constant__ KParams p, const __grid_constant__ CUten
         }
         tc::tmem_st_wait();
         // Upper bound of max |S_{c+1}|: |S_{c+1}| <= gamma^L |S_c| + sum_j |K'_j||V_j|
-        // with zeta <= 1.  It is loose by the ratio of a sum of L terms to
+        // with zeta <= 1 (a pair norm bounds each component of its pair).  It is loose by the ratio of a sum of L terms to
         // their random-sign size, which costs nothing in floating point.
         s_bound = gL * s_bound + (float)L * kmx * vmx;
         sigma = sigma_next;
@@ -765,8 +774,7 @@ bool chunk_tc_supported(const KParams &p, const void *v, const long long sv[3]) 
 }
 
 cudaError_t launch_chunk_tc(const KParams &p, const void *Qp, const void *Kp, const void *v,
-                            const int *qexp, const int *kexp, const float *qmax,
-                            const float *kmax, const float *ksum, const float *S_in,
+                            const ChunkMeta *meta, const float *ksum, const float *S_in,
                             const float *z_in, float *S_out, float *z_out, void *o, Gate gate,
                             int need_z, const SegPlan &seg, cudaStream_t st) {
   const int BH = p.B * p.H;
@@ -792,10 +800,7 @@ cudaError_t launch_chunk_tc(const KParams &p, const void *Qp, const void *Kp, co
   a.z_out = z_out;
   a.o = o;
   a.gate = gate;
-  a.qexp = qexp;
-  a.kexp = kexp;
-  a.qmax = qmax;
-  a.kmax = kmax;
+  a.meta = meta;
   a.ksum = ksum;
   a.NV = p.dv / kW;
   a.need_z = need_z;

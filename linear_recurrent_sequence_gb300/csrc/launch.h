@@ -1,6 +1,8 @@
 // Internal launchers shared between the kernel files and the C ABI layer.
 #pragma once
 
+#include <cuda_fp16.h>
+
 #include "common.cuh"
 
 namespace ret {
@@ -12,9 +14,18 @@ cudaError_t launch_rotate(const KParams &p, const void *x, const long long s[3],
                           void *out, int out_bf16, const float *scale, int mode,
                           cudaStream_t st);
 
-cudaError_t launch_rotate_chunk_f16(const KParams &p, const void *x, const long long s[3],
-                                    void *out, int *exps, float *maxs, float *colsum, int mode,
-                                    cudaStream_t st);
+// Per-(batch*head, chunk) record of the tensor-core path's fp16 operands,
+// written by the prologue and copied into shared memory with each chunk.
+struct ChunkMeta {
+  int qexp, kexp;    // Q', K' are stored as fp16 * 2^-exp
+  float qmax, kmax;  // largest pair norm of the rotated q / k rows before the decays
+};
+
+// Rotate-and-scale prologue of the tensor-core path (bf16 q, k; chunk 64):
+// Q' = xi (.) rot(q), K' = zeta (.) rot(k) as contiguous fp16 [B*H][N][d_k]
+// with per-chunk exponents, magnitudes and (if colsum) key column sums.
+cudaError_t launch_rotate_qk(const KParams &p, const void *q, const void *k, __half *Qp,
+                             __half *Kp, ChunkMeta *meta, float *colsum, cudaStream_t st);
 
 // chunk_simt.cu: fp32 CUDA-core forms writing unnormalised rows + row factors.
 // Qr, Kr: rotated contiguous fp32 [B,H,N,dk]; Oraw: fp32 [B,H,N,dv];
@@ -28,9 +39,9 @@ cudaError_t launch_parallel_simt(const KParams &p, const float *Qr, const float 
 
 // chunk_tc.cu: tensor-core chunkwise kernel (chunk 64, d_k in 64..256 step
 // 64, d_v multiple of 128 up to 1024, bf16 inputs, gamma^64 >= 2^-16).
-// Qp, Kp: contiguous bf16 [B,H,N,d_k] from the rotate-and-scale prologue
-// (xi-scaled queries, zeta-scaled keys), fp16 with per-chunk power-of-two
-// exponents qexp/kexp and magnitudes qmax/kmax ([B*H][chunks]).
+// Qp, Kp: contiguous fp16 [B,H,N,d_k] from the rotate-and-scale prologue
+// (xi-scaled queries, zeta-scaled keys) with per-chunk records meta
+// ([B*H][chunks]) and key column sums ksum ([B*H][chunks][d_k]).
 struct Gate;
 bool chunk_tc_supported(const KParams &p, const void *v, const long long sv[3]);
 
@@ -52,16 +63,15 @@ struct SegPlan {
 };
 
 cudaError_t launch_chunk_tc(const KParams &p, const void *Qp, const void *Kp, const void *v,
-                            const int *qexp, const int *kexp, const float *qmax,
-                            const float *kmax, const float *ksum, const float *S_in,
-                            const float *z_in,
-                            float *S_out, float *z_out, void *o, Gate gate, int need_z,
-                            const SegPlan &seg, cudaStream_t st);
+                            const ChunkMeta *meta, const float *ksum, const float *S_in,
+                            const float *z_in, float *S_out, float *z_out, void *o, Gate gate,
+                            int need_z, const SegPlan &seg, cudaStream_t st);
 
 // state_tc.cu: partial states of the pieces of a SegPlan (tensor cores).
-cudaError_t launch_state_tc(const KParams &p, const void *Kp, const void *v, const int *kexp,
-                            const float *ksum, int npieces, int piece_len, float *Part,
-                            float *zPart, int need_z, cudaStream_t st);
+cudaError_t launch_state_tc(const KParams &p, const void *Kp, const void *v,
+                            const ChunkMeta *meta, const float *ksum, int npieces,
+                            int piece_len, float *Part, float *zPart, int need_z,
+                            cudaStream_t st);
 
 // recurrent.cu: one decode step, state in place.
 cudaError_t launch_recurrent_step(const KParams &p, const void *q, const void *k,

@@ -56,216 +56,237 @@ rotate_scale_kernel(KParams p, const void *__restrict__ x, long long s0, long lo
   st_elem(out, dst + 1, c2 * f, out_bf16);
 }
 
-// fp16 operand prologue of the tensor-core chunk kernel: one CTA per
-// (batch*head, chunk).  Each chunk's rows are rotated and scaled by xi
-// (queries) or zeta (keys) in fp32, then written as fp16 times a power of
-// two 2^-e chosen from the chunk's largest scaled magnitude m
-// (m 2^-e < 2^14), so no value can overflow and every value keeps fp16's
-// 11-bit precision.  e goes to exps[bh*nch + c]; the largest magnitude of
-// the rotated rows BEFORE the decay factor goes to maxs[bh*nch + c] (it
-// bounds the scores and the state update downstream).  For keys, the
-// column sums of the scaled rows (sum_j zeta_j rot(k_j), fp32) go to
-// colsum[(bh*nch + c)*dk + col]: the chunk's contribution to z.
+// fp16 operand prologue of the tensor-core chunk kernel, queries and keys in
+// one launch.  A tile is the 64 rows of one (batch*head, chunk) of q or k.
+// Its rows are rotated and scaled by xi (queries) or zeta (keys) in fp32,
+// then written as fp16 times a power of two 2^-e with m 2^-e < 2^14, m the
+// largest scaled pair norm of the tile: a rotation keeps each pair's norm, so
+// m bounds every rotated component and is known before any rotation, and no
+// value can overflow while each keeps fp16's 11-bit precision.  e and the
+// largest pair norm before the decay go to the tile's ChunkMeta record; for
+// keys the column sums of the scaled rows (sum_j zeta_j rot(k_j), fp32) go to
+// colsum[(bh*nch + c)*dk + col], the chunk's contribution to z.
 //
-// Angles: a thread keeps one pair column j and walks rows i0, i0+s, ...;
-// e^{i t theta_j} is advanced by the rotation e^{i s theta_j} and re-anchored
-// with the accurate reduction every 8 rows, so the angle error stays near
-// 1e-6 rad while most rows cost four FMAs instead of a sine and cosine.
+// Persistent CTAs walk the tiles; the next tile's rows arrive by TMA into the
+// second of two shared-memory buffers while the current one is processed.
+// A thread keeps one pair column j and walks rows i0, i0+s, ...; the angle
+// e^{i t theta_j} and the decay advance by constant factors and are
+// re-anchored from their closed forms every 8 rows (angle error near 1e-6
+// rad, decay error near 1e-6 relative).
+struct RotQK {
+  const void *x[2];         // q, k (bf16)
+  long long s[2][3];        // element strides (b, h, n)
+  __half *out[2];           // Q', K' contiguous [B*H][N][dk] fp16
+  ChunkMeta *meta;          // [B*H][nch]
+  float *colsum;            // [B*H][nch][dk] or null
+  int ntiles;               // 2 * B*H * nch
+};
+
 template <bool kTma>
 __global__ void __launch_bounds__(256)
-rotate_chunk_f16_kernel(KParams p, const void *__restrict__ x, long long s0, long long s1,
-                        long long s2, const __grid_constant__ CUtensorMap tmx,
-                        __half *__restrict__ out, int *__restrict__ exps,
-                        float *__restrict__ maxs, float *__restrict__ colsum, int mode) {
-  // kTma: the chunk's rows arrive in shared memory by one TMA copy (row-major
-  // [C][dk] bf16); otherwise each thread loads its pairs from global memory.
-  extern __shared__ __align__(128) uint8_t xtile[];
-  __shared__ __align__(8) uint64_t tbar;
-  constexpr int kPer = 32;  // pairs per thread: 64 rows * 128 pairs / 256 threads
-  __shared__ float wmax[8], wraw[8];
-  __shared__ float th[2][kMaxPairs];  // per-pair frequencies (indexed per thread)
+rotate_qk_kernel(const __grid_constant__ KParams p, const __grid_constant__ RotQK a,
+                 const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk) {
+  constexpr int C = 64;
+  extern __shared__ __align__(128) uint8_t xt[];  // [2][C][dk] bf16
+  __shared__ __align__(8) uint64_t tbar[2];
+  __shared__ float red[2][8];
+  __shared__ float th[2][kMaxPairs];
   __shared__ float2 csum[256];
-  const int c = blockIdx.x, bh = blockIdx.y, b = bh / p.H, h = bh % p.H;
-  const int C = p.chunk, P = p.dk / 2, tid = threadIdx.x;
+  const int tid = threadIdx.x, P = p.dk / 2;
+  const int istep = 256 / P, jp = tid % P, ip = tid / P;
+  const bool active = tid < P * istep;
+  const int nch = (p.N + C - 1) / C;
+  const uint32_t tile_bytes = (uint32_t)(C * p.dk * 2);
   if (tid < P) {
     th[0][tid] = p.th_hi[tid];
     th[1][tid] = p.th_lo[tid];
   }
   if (kTma && tid == 0) {
-    tc::mbar_init(&tbar, 1);
+    tc::mbar_init(&tbar[0], 1);
+    tc::mbar_init(&tbar[1], 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
-  if (kTma) {
-    if (tid == 0) {
-      tc::mbar_arrive_expect_tx(&tbar, (uint32_t)(C * p.dk * 2));
-      tc::tma_load_4d(xtile, &tmx, &tbar, 0, c * C, h, b);
+  auto issue = [&](int t, int buf) {
+    const int which = t & 1, r = t >> 1, bh = r / nch, c = r % nch;
+    tc::mbar_arrive_expect_tx(&tbar[buf], tile_bytes);
+    tc::tma_load_4d(xt + buf * tile_bytes, which ? &tmk : &tmq, &tbar[buf], 0, c * C,
+                    bh % p.H, bh / p.H);
+  };
+  if (kTma && tid == 0 && (int)blockIdx.x < a.ntiles) issue(blockIdx.x, 0);
+  int k = 0;
+  for (int t = blockIdx.x; t < a.ntiles; t += gridDim.x, ++k) {
+    const int which = t & 1, r = t >> 1, bh = r / nch, c = r % nch;
+    const int b = bh / p.H, h = bh % p.H;
+    const int buf = kTma ? (k & 1) : 0;
+    const uint8_t *tile = xt + buf * tile_bytes;
+    const int t0 = c * C, L = min(C, p.N - t0);
+    const float lng = p.lng[h];
+    if (kTma) {
+      if (tid == 0 && t + (int)gridDim.x < a.ntiles) issue(t + gridDim.x, buf ^ 1);
+      // Bounded wait; if it ever ran out, wait (bounded) again for the copy
+      // to land before reading or leaving.
+      if (!tc::mbar_wait(&tbar[buf], (k >> 1) & 1, p.status, 1u << 24))
+        tc::mbar_wait(&tbar[buf], (k >> 1) & 1, nullptr, 1u << 24);
+    } else {
+      const long long *sx = a.s[which];
+      const __nv_bfloat16 *x = reinterpret_cast<const __nv_bfloat16 *>(a.x[which]);
+      for (int e = tid; e < L * P; e += 256) {
+        const int i = e / P, j = e % P;
+        const long long src = b * sx[0] + h * sx[1] + (long long)(t0 + i) * sx[2] + 2 * j;
+        __nv_bfloat162 w;
+        w.x = x[src];
+        w.y = x[src + 1];
+        *reinterpret_cast<__nv_bfloat162 *>(xt + ((size_t)i * p.dk + 2 * j) * 2) = w;
+      }
+      __syncthreads();
     }
-    // Bounded wait; if it ever ran out, wait (bounded) again for the copy
-    // to land before reading or leaving.
-    if (!tc::mbar_wait(&tbar, 0, p.status, 1u << 24)) tc::mbar_wait(&tbar, 0, nullptr, 1u << 24);
-  }
-  const int t0 = c * C, L = min(C, p.N - t0);
-  // Pair (i, j) of element e = tid + 256 u; when P divides 256 the thread
-  // keeps column jp and walks rows ip + u*istep.
-  const bool walk = (256 % P) == 0;
-  const int jp = tid % P, ip = tid / P, istep = 256 / P;
-  const int U = walk ? (C + istep - 1) / istep : kPer;
-  const bool pair_ld = p.in_bf16 && ((reinterpret_cast<uintptr_t>(x) & 3) == 0) &&
-                       !(s0 & 1) && !(s1 & 1) && !(s2 & 1);
-  float2 v[kPer];
-#pragma unroll
-  for (int u = 0; u < kPer; ++u) {
-    v[u] = make_float2(0.f, 0.f);
-    const int e = tid + u * 256;
-    const int i = walk ? ip + u * istep : e / P, j = walk ? jp : e % P;
-    if (u < U && i < L && (walk || e < L * P)) {
-      const long long src = b * s0 + h * s1 + (long long)(t0 + i) * s2 + 2 * j;
-      if (kTma) {
-        const uint32_t w = *reinterpret_cast<const uint32_t *>(xtile + ((size_t)i * p.dk + 2 * j) * 2);
-        v[u] = make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
-      } else if (pair_ld) {
-        const uint32_t w = __ldg(reinterpret_cast<const uint32_t *>(
-            reinterpret_cast<const __nv_bfloat16 *>(x) + src));
-        v[u] = make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
-      } else {
-        v[u] = make_float2(ld_elem(x, src, p.in_bf16), ld_elem(x, src + 1, p.in_bf16));
+    // Decay of row i: xi = gamma^(i+1) (queries), zeta = gamma^(L-1-i) (keys).
+    const bool xi = which == 0;
+    const float fstep = xi ? gpow(lng, istep) : expf(-(float)istep * lng);
+    auto fexact = [&](int i) { return gpow(lng, xi ? i + 1 : L - 1 - i); };
+    // Pass 1: largest pair norm, before and after the decay.
+    float n2 = 0.f, n2f = 0.f;
+    if (active) {
+      float f = 1.f;
+      for (int u = 0, i = ip; i < L; ++u, i += istep) {
+        f = (u & 7) == 0 ? fexact(i) : f * fstep;
+        const uint32_t w = *reinterpret_cast<const uint32_t *>(tile + ((size_t)i * p.dk + 2 * jp) * 2);
+        const float a0 = __uint_as_float(w << 16), a1 = __uint_as_float(w & 0xffff0000u);
+        const float nn = fmaf(a0, a0, a1 * a1);
+        n2 = fmaxf(n2, nn);
+        n2f = fmaxf(n2f, nn * (f * f));
       }
     }
-  }
-  const float lng = p.lng[h];
-  float m = 0.f, mraw = 0.f;
-  float2 cs_acc = make_float2(0.f, 0.f);
-  // Angle and decay recurrences (walk mode).
-  float cs = 1.f, sn = 0.f, dcs = 1.f, dsn = 0.f;
-  if (walk && p.rotate) rot_cs(istep, th[0][jp], th[1][jp], dcs, dsn);
-  const float dstep = gpow(lng, istep);
 #pragma unroll
-  for (int u = 0; u < kPer; ++u) {
-    const int e = tid + u * 256;
-    const int i = walk ? ip + u * istep : e / P, j = walk ? jp : e % P;
-    if (u < U && i < L && (walk || e < L * P)) {
-      float a0 = v[u].x, a1 = v[u].y;
-      if (p.rotate) {
-        if (!walk || (u & 7) == 0) {
-          rot_cs(p.pos0 + t0 + i, th[0][j], th[1][j], cs, sn);
+    for (int o = 16; o > 0; o >>= 1) {
+      n2 = fmaxf(n2, __shfl_xor_sync(0xffffffffu, n2, o));
+      n2f = fmaxf(n2f, __shfl_xor_sync(0xffffffffu, n2f, o));
+    }
+    if ((tid & 31) == 0) {
+      red[0][tid >> 5] = n2;
+      red[1][tid >> 5] = n2f;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int w = 0; w < 8; ++w) {
+      n2 = fmaxf(n2, red[0][w]);
+      n2f = fmaxf(n2f, red[1][w]);
+    }
+    const float m = sqrtf(n2f);
+    int ex = 0;
+    if (m > 0.f && m < INFINITY) {
+      frexpf(m, &ex);
+      ex -= 14;
+    }
+    const float sc = exp2f((float)-ex);
+    // Pass 2: rotate, scale, round to fp16, store; key column sums.
+    float2 acc = make_float2(0.f, 0.f);
+    if (active) {
+      __half2 *o2 = reinterpret_cast<__half2 *>(a.out[which] + ((long long)bh * p.N + t0) * p.dk);
+      float cs = 1.f, sn = 0.f, dcs = 1.f, dsn = 0.f, f = 1.f;
+      if (p.rotate) rot_cs(istep, th[0][jp], th[1][jp], dcs, dsn);
+      for (int u = 0, i = ip; i < L; ++u, i += istep) {
+        if ((u & 7) == 0) {
+          f = fexact(i);
+          if (p.rotate) rot_cs(p.pos0 + t0 + i, th[0][jp], th[1][jp], cs, sn);
         } else {
+          f *= fstep;
           const float nc = cs * dcs - sn * dsn, ns = sn * dcs + cs * dsn;
           cs = nc;
           sn = ns;
         }
-        const float r0 = a0 * cs - a1 * sn, r1 = a0 * sn + a1 * cs;
-        a0 = r0;
-        a1 = r1;
-      }
-      mraw = fmaxf(mraw, fmaxf(fabsf(a0), fabsf(a1)));
-      const float f = gpow(lng, mode == kScaleXi ? i + 1 : L - 1 - i);
-      v[u] = make_float2(a0 * f, a1 * f);
-      m = fmaxf(m, fmaxf(fabsf(v[u].x), fabsf(v[u].y)));
-      cs_acc.x += v[u].x;
-      cs_acc.y += v[u].y;
-    }
-  }
-  (void)dstep;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-    mraw = fmaxf(mraw, __shfl_xor_sync(0xffffffffu, mraw, o));
-  }
-  if ((tid & 31) == 0) {
-    wmax[tid >> 5] = m;
-    wraw[tid >> 5] = mraw;
-  }
-  if (colsum && walk) csum[tid] = cs_acc;
-  __syncthreads();
-  m = wmax[0];
-  mraw = wraw[0];
-#pragma unroll
-  for (int w = 1; w < 8; ++w) {
-    m = fmaxf(m, wmax[w]);
-    mraw = fmaxf(mraw, wraw[w]);
-  }
-  int ex = 0;
-  if (m > 0.f && m < INFINITY) {
-    frexpf(m, &ex);
-    ex -= 14;
-  }
-  const float sc = exp2f((float)-ex);
-  __half2 *o2 = reinterpret_cast<__half2 *>(out + ((long long)bh * p.N + t0) * p.dk);
-#pragma unroll
-  for (int u = 0; u < kPer; ++u) {
-    const int e = tid + u * 256;
-    const int i = walk ? ip + u * istep : e / P, j = walk ? jp : e % P;
-    if (u < U && i < L && (walk || e < L * P))
-      o2[i * P + j] = __floats2half2_rn(v[u].x * sc, v[u].y * sc);
-  }
-  const int nch = (p.N + C - 1) / C;
-  if (colsum) {
-    float *cdst = colsum + ((long long)bh * nch + c) * p.dk;
-    if (walk) {
-      if (tid < P) {
-        float2 acc = csum[tid];
-        for (int r = 1; r < istep; ++r) {
-          acc.x += csum[tid + r * P].x;
-          acc.y += csum[tid + r * P].y;
+        const uint32_t w = *reinterpret_cast<const uint32_t *>(tile + ((size_t)i * p.dk + 2 * jp) * 2);
+        float a0 = __uint_as_float(w << 16), a1 = __uint_as_float(w & 0xffff0000u);
+        if (p.rotate) {
+          const float r0 = a0 * cs - a1 * sn, r1 = a0 * sn + a1 * cs;
+          a0 = r0;
+          a1 = r1;
         }
-        cdst[2 * tid] = acc.x;
-        cdst[2 * tid + 1] = acc.y;
+        a0 *= f;
+        a1 *= f;
+        acc.x += a0;
+        acc.y += a1;
+        o2[i * P + jp] = __floats2half2_rn(a0 * sc, a1 * sc);
       }
-    } else {
-      // General pair count: sum the columns from the fp32 values via shared
-      // memory atomics (this path is only taken for d_k = 192).
-      __shared__ float cacc[2 * kMaxPairs];
-      for (int t = tid; t < p.dk; t += 256) cacc[t] = 0.f;
-      __syncthreads();
-#pragma unroll
-      for (int u = 0; u < kPer; ++u) {
-        const int e = tid + u * 256;
-        if (e < L * P) {
-          atomicAdd(&cacc[2 * (e % P)], v[u].x);
-          atomicAdd(&cacc[2 * (e % P) + 1], v[u].y);
-        }
-      }
-      __syncthreads();
-      for (int t = tid; t < p.dk; t += 256) cdst[t] = cacc[t];
     }
-  }
-  if (tid == 0) {
-    exps[bh * nch + c] = ex;
-    maxs[bh * nch + c] = mraw;
+    if (!xi && a.colsum) csum[tid] = acc;
+    __syncthreads();
+    if (!xi && a.colsum && tid < P) {
+      float2 s2 = csum[tid];
+      for (int rr = 1; rr < istep; ++rr) {
+        s2.x += csum[tid + rr * P].x;
+        s2.y += csum[tid + rr * P].y;
+      }
+      float *cdst = a.colsum + ((long long)bh * nch + c) * p.dk;
+      cdst[2 * tid] = s2.x;
+      cdst[2 * tid + 1] = s2.y;
+    }
+    if (tid == 0) {
+      ChunkMeta *mt = a.meta + (long long)bh * nch + c;
+      if (xi) {
+        mt->qexp = ex;
+        mt->qmax = sqrtf(n2);
+      } else {
+        mt->kexp = ex;
+        mt->kmax = sqrtf(n2);
+      }
+    }
+    __syncthreads();  // buffer, csum and red are free for the next tile
   }
 }
 
-cudaError_t launch_rotate_chunk_f16(const KParams &p, const void *x, const long long s[3],
-                                    void *out, int *exps, float *maxs, float *colsum, int mode,
-                                    cudaStream_t st) {
+cudaError_t launch_rotate_qk(const KParams &p, const void *q, const void *k, __half *Qp,
+                             __half *Kp, ChunkMeta *meta, float *colsum, cudaStream_t st) {
   if (p.N == 0 || p.B == 0 || p.H == 0) return cudaSuccess;
-  if (p.chunk * (p.dk / 2) > 256 * 32) return cudaErrorInvalidValue;
-  dim3 grid((p.N + p.chunk - 1) / p.chunk, p.B * p.H);
-  // TMA source when the rows are 16-byte aligned bf16 with 16-byte strides.
-  CUtensorMap tm;
-  memset(&tm, 0, sizeof(tm));
-  bool tma = p.in_bf16 && (reinterpret_cast<uintptr_t>(x) % 16 == 0) && s[0] % 8 == 0 &&
-             s[1] % 8 == 0 && s[2] % 8 == 0 && p.dk <= 256 && p.chunk <= 256;
-  if (tma) {
+  if (p.chunk != 64 || p.dk < 2 || p.dk > 256 || !p.in_bf16) return cudaErrorInvalidValue;
+  RotQK a;
+  a.x[0] = q;
+  a.x[1] = k;
+  for (int i = 0; i < 3; ++i) {
+    a.s[0][i] = p.sq[i];
+    a.s[1][i] = p.sk[i];
+  }
+  a.out[0] = Qp;
+  a.out[1] = Kp;
+  a.meta = meta;
+  a.colsum = colsum;
+  const int nch = (p.N + 63) / 64;
+  a.ntiles = 2 * p.B * p.H * nch;
+  // TMA source when both inputs are 16-byte aligned with 16-byte strides.
+  CUtensorMap tm[2];
+  memset(tm, 0, sizeof(tm));
+  bool tma = p.dk % 8 == 0;
+  for (int w = 0; w < 2 && tma; ++w) {
+    const long long *s = a.s[w];
+    tma = (reinterpret_cast<uintptr_t>(a.x[w]) % 16 == 0) && s[0] % 8 == 0 && s[1] % 8 == 0 &&
+          s[2] % 8 == 0;
+    if (!tma) break;
     const cuuint64_t dims[4] = {(cuuint64_t)p.dk, (cuuint64_t)p.N, (cuuint64_t)p.H,
                                 (cuuint64_t)p.B};
     const cuuint64_t strides[3] = {(cuuint64_t)s[2] * 2, (cuuint64_t)s[1] * 2,
                                    (cuuint64_t)s[0] * 2};
-    const cuuint32_t box[4] = {(cuuint32_t)p.dk, (cuuint32_t)p.chunk, 1, 1};
-    tma = tmap_encode(&tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, x, dims, strides, box,
+    const cuuint32_t box[4] = {(cuuint32_t)p.dk, 64, 1, 1};
+    tma = tmap_encode(&tm[w], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, a.x[w], dims, strides, box,
                       CU_TENSOR_MAP_SWIZZLE_NONE);
   }
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const size_t tile = (size_t)64 * p.dk * 2;
   if (tma) {
-    const size_t smem = (size_t)p.chunk * p.dk * 2;
-    cudaError_t e = cudaFuncSetAttribute(rotate_chunk_f16_kernel<true>,
+    const size_t smem = 2 * tile;
+    cudaError_t e = cudaFuncSetAttribute(rotate_qk_kernel<true>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    rotate_chunk_f16_kernel<true><<<grid, 256, smem, st>>>(
-        p, x, s[0], s[1], s[2], tm, reinterpret_cast<__half *>(out), exps, maxs, colsum, mode);
+    const int grid = a.ntiles < 3 * sms ? a.ntiles : 3 * sms;
+    rotate_qk_kernel<true><<<grid, 256, smem, st>>>(p, a, tm[0], tm[1]);
   } else {
-    rotate_chunk_f16_kernel<false><<<grid, 256, 0, st>>>(
-        p, x, s[0], s[1], s[2], tm, reinterpret_cast<__half *>(out), exps, maxs, colsum, mode);
+    cudaError_t e = cudaFuncSetAttribute(rotate_qk_kernel<false>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tile);
+    if (e != cudaSuccess) return e;
+    const int grid = a.ntiles < 6 * sms ? a.ntiles : 6 * sms;
+    rotate_qk_kernel<false><<<grid, 256, tile, st>>>(p, a, tm[0], tm[1]);
   }
   return cudaGetLastError();
 }

@@ -26,8 +26,9 @@ namespace ret {
 namespace {
 
 constexpr int kC = 64, kW = 128, kNT = 192;
-constexpr uint32_t kStage = 48 * 1024;  // K' 32K | V 16K
-constexpr uint32_t kOffK = 0, kOffV = 32 * 1024;
+// Stage: K' 32K | V 16K | key column sums (d_k fp32) | ChunkMeta.
+constexpr uint32_t kOffK = 0, kOffV = 32 * 1024, kOffKs = 48 * 1024, kOffMeta = kOffKs + 1024;
+constexpr uint32_t kStage = 50 * 1024;
 constexpr uint32_t kOffRed = 2 * kStage;
 constexpr uint32_t kOffBar = kOffRed + 64;
 constexpr int kNumBars = 8;
@@ -81,7 +82,7 @@ __device__ __forceinline__ float bfh(uint32_t w) { return __uint_as_float(w & 0x
 
 __global__ void __launch_bounds__(kNT, 1)
 state_tc_kernel(const __grid_constant__ KParams p, const __grid_constant__ CUtensorMap tmK,
-                const __grid_constant__ CUtensorMap tmV, const int *__restrict__ kexp,
+                const __grid_constant__ CUtensorMap tmV, const ChunkMeta *__restrict__ meta,
                 const float *__restrict__ ksum, int piece_len, float *Part, float *zPart,
                 int need_z) {
   extern __shared__ uint8_t smraw[];
@@ -125,7 +126,8 @@ state_tc_kernel(const __grid_constant__ KParams p, const __grid_constant__ CUten
     if (lane == 0) {
       tc::prefetch_tmap(&tmK);
       tc::prefetch_tmap(&tmV);
-      const uint32_t bytes = (uint32_t)NKB * 8192u + 16384u;
+      const uint32_t bytes =
+          (uint32_t)NKB * 8192u + 16384u + 16u + (need_z ? (uint32_t)DK * 4u : 0u);
       int issued = 0;
       for (int lc = 0; lc < ncl; ++lc) {
         const int s = lc & 1, c = c0 + lc;
@@ -137,6 +139,10 @@ state_tc_kernel(const __grid_constant__ KParams p, const __grid_constant__ CUten
         for (int vb = 0; vb < 2; ++vb)
           tc::tma_load_4d(st + kOffV + vb * 8192, &tmV, &bars[FULL0 + s], v0 + vb * 64, c * kC,
                           h, b);
+        tc::bulk_load(st + kOffMeta, meta + (long long)bh * nch + c, 16u, &bars[FULL0 + s]);
+        if (need_z)
+          tc::bulk_load(st + kOffKs, ksum + ((long long)bh * nch + c) * DK, (uint32_t)DK * 4u,
+                        &bars[FULL0 + s]);
         ++issued;
       }
       for (int lc = issued > 2 ? issued - 2 : 0; lc < issued; ++lc)
@@ -177,10 +183,17 @@ state_tc_kernel(const __grid_constant__ KParams p, const __grid_constant__ CUten
       const int s = lc & 1, c = c0 + lc;
       const int L = min(kC, N - c * kC);
       const float gL = gpow(lng, L);
-      const int bk = kexp[bh * nch + c];
       uint8_t *st = sm + s * kStage;
       ok = grp_all4(swait(&bars[FULL0 + s], (lc >> 1) & 1, abort_p, p.status));
       if (!ok) break;
+      const int bk = reinterpret_cast<const ChunkMeta *>(st + kOffMeta)->kexp;
+      // (0) z over the piece: z <- gamma^L z + sum_j K'_j (read before the
+      // stage is released).
+      if (zown) {
+        const float *ks = reinterpret_cast<const float *>(st + kOffKs);
+        zr0 = fmaf(gL, zr0, ks[2 * et]);
+        zr1 = fmaf(gL, zr1, ks[2 * et + 1]);
+      }
       // (1) V tile: bf16 -> fp16 * 2^-vx in place (1024 16-byte words).
       uint4 vv[8];
       float vm = 0.f;
@@ -236,12 +249,6 @@ state_tc_kernel(const __grid_constant__ KParams p, const __grid_constant__ CUten
       tc::tc_fence_before();
       asm volatile("bar.sync 1, 128;" ::: "memory");
       if (et == 0) tc::mbar_arrive(&bars[EPI]);
-      // (3) z over the piece: z <- gamma^L z + sum_j K'_j.
-      if (zown) {
-        const float *ks = ksum + ((long long)bh * nch + c) * DK;
-        zr0 = fmaf(gL, zr0, ks[2 * et]);
-        zr1 = fmaf(gL, zr1, ks[2 * et + 1]);
-      }
     }
     if (ok && ncl > 0) {
       ok = grp_all4(swait(&bars[SFULL], (ncl - 1) & 1, abort_p, p.status));
@@ -273,9 +280,10 @@ state_tc_kernel(const __grid_constant__ KParams p, const __grid_constant__ CUten
   }
 }
 
-cudaError_t launch_state_tc(const KParams &p, const void *Kp, const void *v, const int *kexp,
-                            const float *ksum, int npieces, int piece_len, float *Part,
-                            float *zPart, int need_z, cudaStream_t st) {
+cudaError_t launch_state_tc(const KParams &p, const void *Kp, const void *v,
+                            const ChunkMeta *meta, const float *ksum, int npieces,
+                            int piece_len, float *Part, float *zPart, int need_z,
+                            cudaStream_t st) {
   const int BH = p.B * p.H;
   CUtensorMap tk, tv;
   const cuuint64_t dq[3] = {(cuuint64_t)p.dk, (cuuint64_t)p.N, (cuuint64_t)BH};
@@ -294,7 +302,7 @@ cudaError_t launch_state_tc(const KParams &p, const void *Kp, const void *v, con
       cudaFuncSetAttribute(state_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
   if (e != cudaSuccess) return e;
   const int grid = npieces * BH * (p.dv / kW);
-  state_tc_kernel<<<grid, kNT, kSmem, st>>>(p, tk, tv, kexp, ksum, piece_len, Part, zPart,
+  state_tc_kernel<<<grid, kNT, kSmem, st>>>(p, tk, tv, meta, ksum, piece_len, Part, zPart,
                                              need_z);
   return cudaGetLastError();
 }
