@@ -30,11 +30,14 @@
 // Warp roles (12 warps): warp 0 issues TMA loads (2-stage ring), warp 1
 // issues MMAs (one thread) and owns TMEM, warps 2-3 ("helper" group)
 // convert V to fp16, compute Q'.z for the third normalisation and carry z,
-// warps 4-7 ("state" group) refresh the state copy, build R and the row
-// factors, warps 8-11 ("output" group) drain O^T and run GroupNorm and the
-// stores.  Every
-// wait is bounded; a wait that runs out sets the status word and an abort
-// flag, and every role leaves after draining its own asynchronous work.
+// warps 4-7 ("state" group) build R and the row factors, then refresh the
+// state copy, warps 8-11 ("output" group) drain O^T and run GroupNorm and
+// the stores.  The MMA order per chunk c is O^T = V^T R^T (once R is built),
+// the scores of chunk c+1, then (once the state copy is refreshed) the cross
+// term and the state update, so R of chunk c+1 is built while the state MMAs
+// of chunk c run.  Every wait is bounded; a wait that runs out sets the
+// status word and an abort flag, and every role leaves after draining its
+// own asynchronous work.
 #include <cooperative_groups.h>
 #include <cudaTypedefs.h>
 
@@ -71,14 +74,15 @@ constexpr uint32_t kOffVX = kOffNrm + 64 * 2 * 4;          // [2] int vx, [2] fl
 constexpr uint32_t kOffQZ = kOffVX + 16;                   // [2][64] fp32 Q'_i . z
 constexpr uint32_t kOffHRed = kOffQZ + 2 * 64 * 4;         // [2][2] fp32 helper scratch
 constexpr uint32_t kOffBar = kOffHRed + 16;
-constexpr int kNumBars = 16;
+constexpr int kNumBars = 17;
 constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;
 constexpr uint32_t kSmemBytes = kOffMisc + 16 + 1024;   // + alignment slack
 static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 
 enum Bar {
-  FULL0 = 0, FULL1, EMPTY0, EMPTY1, QK, EPI, OFULL, SFULL, OFREE, GN0, GN1, DRAIN,
-  VRDY0, VRDY1, QZRDY0, QZRDY1  // per parity: the helper may run one chunk ahead
+  FULL0 = 0, FULL1, EMPTY0, EMPTY1, QK, RRDY, OFULL, SFULL, OFREE, GN0, GN1, DRAIN,
+  VRDY0, VRDY1, QZRDY0, QZRDY1,  // per parity: the helper may run one chunk ahead
+  SRDY
 };
 
 // TMEM column map.
@@ -229,7 +233,8 @@ chunk_tc_kernel(const __grid_constant__ KParams p, const __grid_constant__ CUten
     tc::mbar_init(&bars[EMPTY0], 2);
     tc::mbar_init(&bars[EMPTY1], 2);
     tc::mbar_init(&bars[QK], 1);
-    tc::mbar_init(&bars[EPI], 1);
+    tc::mbar_init(&bars[RRDY], 1);
+    tc::mbar_init(&bars[SRDY], 1);
     tc::mbar_init(&bars[OFULL], 1);
     tc::mbar_init(&bars[SFULL], 1);
     tc::mbar_init(&bars[OFREE], 1);
@@ -307,16 +312,27 @@ chunk_tc_kernel(const __grid_constant__ KParams p, const __grid_constant__ CUten
         tc::tc_fence_after();
         mma_qk(0);
       }
+      // Per chunk: O^T = V^T R^T once R is built and O^T of the previous
+      // chunk is drained; then the next chunk's scores, so the state group
+      // can build the next R while this chunk's state MMAs run; then, once
+      // the state copy is refreshed, the cross term and the state update.
       for (int lc = 0; go && lc < ncl; ++lc) {
         const int s = lc & 1;
         const uint32_t sq = tc::smem_u32(sm + s * kStage + kOffQ);
         const uint32_t sk = sq + kOffK, sv = sq + kOffV;
-        if (!wait_bar(&bars[EPI], lc & 1, abort_p, p.status)) break;
+        if (!wait_bar(&bars[RRDY], lc & 1, abort_p, p.status)) break;
         if (lc > 0 && !wait_bar(&bars[OFREE], (lc - 1) & 1, abort_p, p.status)) break;
         tc::tc_fence_after();
         for (int ks = 0; ks < 4; ++ks)  // O^T = V^T R^T
           tc::mma_ss(tb + kTO, tc::smem_desc(sv + ks * 2048, 8192, 1024, tc::kSw128),
                      tc::smem_desc(sr + ks * 32, 16, 1024, tc::kSw128), id_o, ks > 0);
+        if (lc + 1 < ncl) {
+          if (!wait_bar(&bars[FULL0 + (s ^ 1)], ((lc + 1) >> 1) & 1, abort_p, p.status)) break;
+          tc::tc_fence_after();
+          mma_qk(lc + 1);
+        }
+        if (!wait_bar(&bars[SRDY], lc & 1, abort_p, p.status)) break;
+        tc::tc_fence_after();
         for (int ks = 0; ks < DK / 16; ++ks)  // O^T += S^T Q'^T
           tc::mma_ts(tb + kTO, tb + kTSh + ks * 8,
                      tc::smem_desc(sq + (ks >> 2) * 8192 + (ks & 3) * 32, 16, 1024, tc::kSw128),
@@ -327,11 +343,6 @@ chunk_tc_kernel(const __grid_constant__ KParams p, const __grid_constant__ CUten
                      tc::smem_desc(sk + ks * 2048, 8192, 1024, tc::kSw128), id_s, 1);
         tc::mma_commit(&bars[SFULL]);
         tc::mma_commit(&bars[EMPTY0 + s]);
-        if (lc + 1 < ncl) {
-          if (!wait_bar(&bars[FULL0 + (s ^ 1)], ((lc + 1) >> 1) & 1, abort_p, p.status)) break;
-          tc::tc_fence_after();
-          mma_qk(lc + 1);
-        }
       }
       tc::mma_commit(&bars[DRAIN]);  // every MMA issued above is finished
       drain_wait(&bars[DRAIN], 0);
@@ -491,57 +502,15 @@ chunk_tc_kernel(const __grid_constant__ KParams p, const __grid_constant__ CUten
       if (s_bound > 0.f) E = max(E, expo14(s_bound) + aq);
       const int rr = E - vx, ss = E - aq;
       const int sigma_next = vx + bk;
-      // (3) state pass: fp16 copy of S_c * 2^-ss; S_acc <- gamma^L S_c * 2^-sigma_next
-      if (lc > 0) {
-        ok = grp_all(G, wait_bar(&bars[SFULL], (lc - 1) & 1, abort_p, p.status));
-        if (!ok) break;
-        tc::tc_fence_after();
-      }
-      // Slot s is free again: the output group read chunk c-2's exponent and
-      // row factors before it released O^T (OFREE), which the MMA issue of
-      // chunk c-1 (hence SFULL above) waited for.
-      if (et == 0) Esm[s] = E;
-      {
-        const float f_cp = exp2f((float)(sigma - ss));
-        const float f_pre = gL * exp2f((float)(sigma - sigma_next));
-        for (int g0 = 0; g0 < DK / 32; g0 += 2) {
-          uint32_t r[2][32];
-          if (lc == 0 && !has_state) {
-#pragma unroll
-            for (int hh = 0; hh < 2; ++hh)
-#pragma unroll
-              for (int i = 0; i < 32; ++i) r[hh][i] = 0u;
-          } else {
-            tc::tmem_ld32(tb + lb + kTS + g0 * 32, r[0]);
-            tc::tmem_ld32(tb + lb + kTS + g0 * 32 + 32, r[1]);
-            tc::tmem_ld_wait();
-          }
-#pragma unroll
-          for (int hh = 0; hh < 2; ++hh) {
-            uint32_t pk[16];
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              const float x0 = __uint_as_float(r[hh][2 * i]), x1 = __uint_as_float(r[hh][2 * i + 1]);
-              pk[i] = tc::pack_f16(x0 * f_cp, x1 * f_cp);
-            }
-            tc::tmem_st16(tb + lb + kTSh + (g0 + hh) * 16, pk);
-#pragma unroll
-            for (int i = 0; i < 32; ++i) r[hh][i] = __float_as_uint(__uint_as_float(r[hh][i]) * f_pre);
-            tc::tmem_st32(tb + lb + kTS + (g0 + hh) * 32, r[hh]);
-          }
-        }
-        tc::tmem_st_wait();
-        // Upper bound of max |S_{c+1}|: |S_{c+1}| <= gamma^L |S_c| + sum_j |K'_j||V_j|
-        // with zeta <= 1 (a pair norm bounds each component of its pair).  It is loose by the ratio of a sum of L terms to
-        // their random-sign size, which costs nothing in floating point.
-        s_bound = gL * s_bound + (float)L * kmx * vmx;
-        sigma = sigma_next;
-      }
-      // (4) R (fp16, * 2^-rr) as K-major rows; row factors.
+      // (3) R (fp16, * 2^-rr) as K-major rows; row factors.  The scores'
+      // completion (QK) means every earlier MMA is finished: MMA2 of the
+      // previous chunk, the last reader of R, and, through MMA2's wait on
+      // OFREE two chunks back, the output group's reads of slot s.
       ok = grp_all(G, wait_bar(&bars[QK], lc & 1, abort_p, p.status) &&
                           (!rsum || wait_bar(&bars[QZRDY0 + s], (lc >> 1) & 1, abort_p, p.status)));
       if (!ok) break;
       tc::tc_fence_after();
+      if (et == 0) Esm[s] = E;
       {
         uint32_t t0[32], t1[32];
         tc::tmem_ld32(tb + lb + kTQK, t0);
@@ -580,7 +549,53 @@ chunk_tc_kernel(const __grid_constant__ KParams p, const __grid_constant__ CUten
       tc::fence_proxy_async_smem();
       tc::tc_fence_before();
       grp_sync(G);
-      if (et == 0) tc::mbar_arrive(&bars[EPI]);
+      if (et == 0) tc::mbar_arrive(&bars[RRDY]);
+      // (4) state pass: fp16 copy of S_c * 2^-ss; S_acc <- gamma^L S_c * 2^-sigma_next
+      if (lc > 0) {
+        ok = grp_all(G, wait_bar(&bars[SFULL], (lc - 1) & 1, abort_p, p.status));
+        if (!ok) break;
+        tc::tc_fence_after();
+      }
+      {
+        const float f_cp = exp2f((float)(sigma - ss));
+        const float f_pre = gL * exp2f((float)(sigma - sigma_next));
+        for (int g0 = 0; g0 < DK / 32; g0 += 2) {
+          uint32_t r[2][32];
+          if (lc == 0 && !has_state) {
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+              for (int i = 0; i < 32; ++i) r[hh][i] = 0u;
+          } else {
+            tc::tmem_ld32(tb + lb + kTS + g0 * 32, r[0]);
+            tc::tmem_ld32(tb + lb + kTS + g0 * 32 + 32, r[1]);
+            tc::tmem_ld_wait();
+          }
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            uint32_t pk[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const float x0 = __uint_as_float(r[hh][2 * i]), x1 = __uint_as_float(r[hh][2 * i + 1]);
+              pk[i] = tc::pack_f16(x0 * f_cp, x1 * f_cp);
+            }
+            tc::tmem_st16(tb + lb + kTSh + (g0 + hh) * 16, pk);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) r[hh][i] = __float_as_uint(__uint_as_float(r[hh][i]) * f_pre);
+            tc::tmem_st32(tb + lb + kTS + (g0 + hh) * 32, r[hh]);
+          }
+        }
+        tc::tmem_st_wait();
+      }
+      tc::tc_fence_before();
+      grp_sync(G);
+      if (et == 0) tc::mbar_arrive(&bars[SRDY]);
+      // Upper bound of max |S_{c+1}|: |S_{c+1}| <= gamma^L |S_c| + sum_j |K'_j||V_j|
+      // with zeta <= 1 (a pair norm bounds each component of its pair).  It is
+      // loose by the ratio of a sum of L terms to their random-sign size,
+      // which costs nothing in floating point.
+      s_bound = gL * s_bound + (float)L * kmx * vmx;
+      sigma = sigma_next;
     }
     if (ok && a.S_out && last_seg) {
       ok = grp_all(G, wait_bar(&bars[SFULL], (ncl - 1) & 1, abort_p, p.status));

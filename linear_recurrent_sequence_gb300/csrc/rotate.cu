@@ -59,20 +59,22 @@ rotate_scale_kernel(KParams p, const void *__restrict__ x, long long s0, long lo
 // fp16 operand prologue of the tensor-core chunk kernel, queries and keys in
 // one launch.  A tile is the 64 rows of one (batch*head, chunk) of q or k.
 // Its rows are rotated and scaled by xi (queries) or zeta (keys) in fp32,
-// then written as fp16 times a power of two 2^-e with m 2^-e < 2^14, m the
-// largest scaled pair norm of the tile: a rotation keeps each pair's norm, so
-// m bounds every rotated component and is known before any rotation, and no
-// value can overflow while each keeps fp16's 11-bit precision.  e and the
-// largest pair norm before the decay go to the tile's ChunkMeta record; for
-// keys the column sums of the scaled rows (sum_j zeta_j rot(k_j), fp32) go to
-// colsum[(bh*nch + c)*dk + col], the chunk's contribution to z.
+// then written as fp16 times a power of two 2^-e, e chosen from a bound m of
+// the scaled values (m 2^-e < 2^14): a rotation keeps each pair's norm, which
+// is at most sqrt(2) max|x| over the tile's raw elements, and the decay is at
+// most gamma (xi) or 1 (zeta).  So no value can overflow and every normal
+// value keeps fp16's 11-bit precision.  e and the pair-norm bound before the
+// decay go to the tile's ChunkMeta record; for keys the column sums of the
+// scaled rows (sum_j zeta_j rot(k_j), fp32) go to colsum[(bh*nch + c)*dk + col],
+// the chunk's contribution to z.
 //
 // Persistent CTAs walk the tiles; the next tile's rows arrive by TMA into the
 // second of two shared-memory buffers while the current one is processed.
-// A thread keeps one pair column j and walks rows i0, i0+s, ...; the angle
-// e^{i t theta_j} and the decay advance by constant factors and are
-// re-anchored from their closed forms every 8 rows (angle error near 1e-6
-// rad, decay error near 1e-6 relative).
+// A thread keeps two adjacent pair columns and walks rows i0, i0+s, ...; the
+// angles start from e^{i (pos0+t0) theta_j} (one per column and tile, shared
+// through shared memory) times the thread's fixed offset e^{i i0 theta_j} and
+// advance by e^{i s theta_j}; the decay advances by gamma^(+-s).  A walk is at
+// most 16 steps, so the rounding it accumulates stays near 1e-6.
 struct RotQK {
   const void *x[2];         // q, k (bf16)
   long long s[2][3];        // element strides (b, h, n)
@@ -89,18 +91,23 @@ rotate_qk_kernel(const __grid_constant__ KParams p, const __grid_constant__ RotQ
   constexpr int C = 64;
   extern __shared__ __align__(128) uint8_t xt[];  // [2][C][dk] bf16
   __shared__ __align__(8) uint64_t tbar[2];
-  __shared__ float red[2][8];
-  __shared__ float th[2][kMaxPairs];
-  __shared__ float2 csum[256];
-  const int tid = threadIdx.x, P = p.dk / 2;
-  const int istep = 256 / P, jp = tid % P, ip = tid / P;
-  const bool active = tid < P * istep;
+  __shared__ unsigned red[8];
+  __shared__ __align__(16) float2 anc[kMaxPairs];  // e^{i (pos0+t0) theta_j}
+  __shared__ __align__(16) float4 csum[256];
+  const int tid = threadIdx.x, P = p.dk / 2, Q2 = p.dk / 4;
+  const int istep = 256 / Q2, jq = tid % Q2, ip = tid / Q2;
+  const bool active = tid < Q2 * istep;
   const int nch = (p.N + C - 1) / C;
   const uint32_t tile_bytes = (uint32_t)(C * p.dk * 2);
-  if (tid < P) {
-    th[0][tid] = p.th_hi[tid];
-    th[1][tid] = p.th_lo[tid];
-  }
+  // The thread's fixed angle offsets: e^{i ip theta} and e^{i istep theta}
+  // for its pair columns 2jq and 2jq+1.
+  float oc[2] = {1.f, 1.f}, os[2] = {0.f, 0.f}, dc[2] = {1.f, 1.f}, ds[2] = {0.f, 0.f};
+  if (p.rotate && active)
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      rot_cs(ip, p.th_hi[2 * jq + e], p.th_lo[2 * jq + e], oc[e], os[e]);
+      rot_cs(istep, p.th_hi[2 * jq + e], p.th_lo[2 * jq + e], dc[e], ds[e]);
+    }
   if (kTma && tid == 0) {
     tc::mbar_init(&tbar[0], 1);
     tc::mbar_init(&tbar[1], 1);
@@ -122,6 +129,7 @@ rotate_qk_kernel(const __grid_constant__ KParams p, const __grid_constant__ RotQ
     const uint8_t *tile = xt + buf * tile_bytes;
     const int t0 = c * C, L = min(C, p.N - t0);
     const float lng = p.lng[h];
+    const bool xi = which == 0;
     if (kTma) {
       if (tid == 0 && t + (int)gridDim.x < a.ntiles) issue(t + gridDim.x, buf ^ 1);
       // Bounded wait; if it ever ran out, wait (bounded) again for the copy
@@ -141,39 +149,33 @@ rotate_qk_kernel(const __grid_constant__ KParams p, const __grid_constant__ RotQ
       }
       __syncthreads();
     }
-    // Decay of row i: xi = gamma^(i+1) (queries), zeta = gamma^(L-1-i) (keys).
-    const bool xi = which == 0;
-    const float fstep = xi ? gpow(lng, istep) : expf(-(float)istep * lng);
-    auto fexact = [&](int i) { return gpow(lng, xi ? i + 1 : L - 1 - i); };
-    // Pass 1: largest pair norm, before and after the decay.
-    float n2 = 0.f, n2f = 0.f;
-    if (active) {
-      float f = 1.f;
-      for (int u = 0, i = ip; i < L; ++u, i += istep) {
-        f = (u & 7) == 0 ? fexact(i) : f * fstep;
-        const uint32_t w = *reinterpret_cast<const uint32_t *>(tile + ((size_t)i * p.dk + 2 * jp) * 2);
-        const float a0 = __uint_as_float(w << 16), a1 = __uint_as_float(w & 0xffff0000u);
-        const float nn = fmaf(a0, a0, a1 * a1);
-        n2 = fmaxf(n2, nn);
-        n2f = fmaxf(n2f, nn * (f * f));
+    // Pass 1: max |x| over the tile's rows (bf16 magnitudes compare as
+    // unsigned 16-bit integers); the tile's angle anchors.
+    unsigned mb = 0;
+    {
+      const uint4 *t4 = reinterpret_cast<const uint4 *>(tile);
+      const int n4 = L * p.dk / 8;
+      for (int e = tid; e < n4; e += 256) {
+        const uint4 u = t4[e];
+        mb = __vmaxu2(mb, __vmaxu2(__vmaxu2(u.x & 0x7fff7fffu, u.y & 0x7fff7fffu),
+                                   __vmaxu2(u.z & 0x7fff7fffu, u.w & 0x7fff7fffu)));
       }
     }
+    if (p.rotate && tid < P) {
+      float cs, sn;
+      rot_cs(p.pos0 + t0, p.th_hi[tid], p.th_lo[tid], cs, sn);
+      anc[tid] = make_float2(cs, sn);
+    }
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      n2 = fmaxf(n2, __shfl_xor_sync(0xffffffffu, n2, o));
-      n2f = fmaxf(n2f, __shfl_xor_sync(0xffffffffu, n2f, o));
-    }
-    if ((tid & 31) == 0) {
-      red[0][tid >> 5] = n2;
-      red[1][tid >> 5] = n2f;
-    }
+    for (int o = 16; o > 0; o >>= 1) mb = __vmaxu2(mb, __shfl_xor_sync(0xffffffffu, mb, o));
+    if ((tid & 31) == 0) red[tid >> 5] = mb;
     __syncthreads();
+    mb = red[0];
 #pragma unroll
-    for (int w = 0; w < 8; ++w) {
-      n2 = fmaxf(n2, red[0][w]);
-      n2f = fmaxf(n2f, red[1][w]);
-    }
-    const float m = sqrtf(n2f);
+    for (int w = 1; w < 8; ++w) mb = __vmaxu2(mb, red[w]);
+    const float xmax = fmaxf(__uint_as_float(mb << 16), __uint_as_float(mb & 0xffff0000u));
+    const float nb = xmax * 1.41421366f;  // >= sqrt(2) max|x|: bound of every pair norm
+    const float m = xi ? nb * p.gam[h] : nb;
     int ex = 0;
     if (m > 0.f && m < INFINITY) {
       frexpf(m, &ex);
@@ -181,65 +183,77 @@ rotate_qk_kernel(const __grid_constant__ KParams p, const __grid_constant__ RotQ
     }
     const float sc = exp2f((float)-ex);
     // Pass 2: rotate, scale, round to fp16, store; key column sums.
-    float2 acc = make_float2(0.f, 0.f);
-    if (active) {
-      __half2 *o2 = reinterpret_cast<__half2 *>(a.out[which] + ((long long)bh * p.N + t0) * p.dk);
-      float cs = 1.f, sn = 0.f, dcs = 1.f, dsn = 0.f, f = 1.f;
-      if (p.rotate) rot_cs(istep, th[0][jp], th[1][jp], dcs, dsn);
-      for (int u = 0, i = ip; i < L; ++u, i += istep) {
-        if ((u & 7) == 0) {
-          f = fexact(i);
-          if (p.rotate) rot_cs(p.pos0 + t0 + i, th[0][jp], th[1][jp], cs, sn);
-        } else {
-          f *= fstep;
-          const float nc = cs * dcs - sn * dsn, ns = sn * dcs + cs * dsn;
-          cs = nc;
-          sn = ns;
-        }
-        const uint32_t w = *reinterpret_cast<const uint32_t *>(tile + ((size_t)i * p.dk + 2 * jp) * 2);
-        float a0 = __uint_as_float(w << 16), a1 = __uint_as_float(w & 0xffff0000u);
-        if (p.rotate) {
-          const float r0 = a0 * cs - a1 * sn, r1 = a0 * sn + a1 * cs;
-          a0 = r0;
-          a1 = r1;
-        }
-        a0 *= f;
-        a1 *= f;
-        acc.x += a0;
-        acc.y += a1;
-        o2[i * P + jp] = __floats2half2_rn(a0 * sc, a1 * sc);
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (active && ip < L) {
+      // Decay of row i: xi = gamma^(i+1) (queries), zeta = gamma^(L-1-i) (keys).
+      const float fstep = xi ? gpow(lng, istep) : expf(-(float)istep * lng);
+      float fs = gpow(lng, xi ? ip + 1 : L - 1 - ip) * sc;
+      float c0 = 1.f, s0 = 0.f, c1 = 1.f, s1 = 0.f;
+      if (p.rotate) {
+        const float4 an = *reinterpret_cast<const float4 *>(&anc[2 * jq]);
+        c0 = an.x * oc[0] - an.y * os[0];
+        s0 = an.x * os[0] + an.y * oc[0];
+        c1 = an.z * oc[1] - an.w * os[1];
+        s1 = an.z * os[1] + an.w * oc[1];
+      }
+      const uint8_t *src = tile + ((size_t)ip * p.dk + 4 * jq) * 2;
+      uint2 *dst = reinterpret_cast<uint2 *>(a.out[which] + ((long long)bh * p.N + t0 + ip) * p.dk +
+                                             4 * jq);
+      const size_t sstep = (size_t)istep * p.dk * 2, dstep = (size_t)istep * p.dk / 4;
+      for (int i = ip; i < L; i += istep, src += sstep, dst += dstep) {
+        const uint2 w = *reinterpret_cast<const uint2 *>(src);
+        const float a0 = __uint_as_float(w.x << 16), a1 = __uint_as_float(w.x & 0xffff0000u);
+        const float a2 = __uint_as_float(w.y << 16), a3 = __uint_as_float(w.y & 0xffff0000u);
+        const float r0 = (a0 * c0 - a1 * s0) * fs, r1 = (a0 * s0 + a1 * c0) * fs;
+        const float r2 = (a2 * c1 - a3 * s1) * fs, r3 = (a2 * s1 + a3 * c1) * fs;
+        acc.x += r0;
+        acc.y += r1;
+        acc.z += r2;
+        acc.w += r3;
+        *dst = make_uint2(tc::pack_f16(r0, r1), tc::pack_f16(r2, r3));
+        fs *= fstep;
+        const float n0 = c0 * dc[0] - s0 * ds[0], m0 = s0 * dc[0] + c0 * ds[0];
+        const float n1 = c1 * dc[1] - s1 * ds[1], m1 = s1 * dc[1] + c1 * ds[1];
+        c0 = n0;
+        s0 = m0;
+        c1 = n1;
+        s1 = m1;
       }
     }
     if (!xi && a.colsum) csum[tid] = acc;
     __syncthreads();
-    if (!xi && a.colsum && tid < P) {
-      float2 s2 = csum[tid];
+    if (!xi && a.colsum && tid < Q2) {
+      float4 s4 = csum[tid];
       for (int rr = 1; rr < istep; ++rr) {
-        s2.x += csum[tid + rr * P].x;
-        s2.y += csum[tid + rr * P].y;
+        const float4 o4 = csum[tid + rr * Q2];
+        s4.x += o4.x;
+        s4.y += o4.y;
+        s4.z += o4.z;
+        s4.w += o4.w;
       }
-      float *cdst = a.colsum + ((long long)bh * nch + c) * p.dk;
-      cdst[2 * tid] = s2.x;
-      cdst[2 * tid + 1] = s2.y;
+      const float back = exp2f((float)ex);  // the sums were taken in units of 2^ex
+      float4 *cdst = reinterpret_cast<float4 *>(a.colsum + ((long long)bh * nch + c) * p.dk) + tid;
+      *cdst = make_float4(s4.x * back, s4.y * back, s4.z * back, s4.w * back);
     }
     if (tid == 0) {
       ChunkMeta *mt = a.meta + (long long)bh * nch + c;
       if (xi) {
         mt->qexp = ex;
-        mt->qmax = sqrtf(n2);
+        mt->qmax = nb;
       } else {
         mt->kexp = ex;
-        mt->kmax = sqrtf(n2);
+        mt->kmax = nb;
       }
     }
-    __syncthreads();  // buffer, csum and red are free for the next tile
+    __syncthreads();  // buffer, csum, anc and red are free for the next tile
   }
 }
 
 cudaError_t launch_rotate_qk(const KParams &p, const void *q, const void *k, __half *Qp,
                              __half *Kp, ChunkMeta *meta, float *colsum, cudaStream_t st) {
   if (p.N == 0 || p.B == 0 || p.H == 0) return cudaSuccess;
-  if (p.chunk != 64 || p.dk < 2 || p.dk > 256 || !p.in_bf16) return cudaErrorInvalidValue;
+  if (p.chunk != 64 || p.dk < 4 || p.dk > 256 || p.dk % 4 || !p.in_bf16)
+    return cudaErrorInvalidValue;
   RotQK a;
   a.x[0] = q;
   a.x[1] = k;
