@@ -193,8 +193,7 @@ chunk_tc_kernel(const __grid_constant__ KParams p, const __grid_constant__ CUten
                 const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                 const TcArgs a) {
   extern __shared__ uint8_t smraw[];
-  uint8_t *sm = reinterpret_cast<uint8_t *>(
-      (reinterpret_cast<uintptr_t>(smraw) + 1023) & ~(uintptr_t)1023);
+  uint8_t *sm = tc::smem_align1024(smraw);
   uint64_t *bars = reinterpret_cast<uint64_t *>(sm + kOffBar);
   uint32_t *tbase_p = reinterpret_cast<uint32_t *>(sm + kOffMisc);
   volatile int *abort_p = reinterpret_cast<volatile int *>(sm + kOffMisc + 4);

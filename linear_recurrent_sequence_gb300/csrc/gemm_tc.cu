@@ -52,8 +52,7 @@ __global__ void __launch_bounds__(kNT, 1)
 gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                __nv_bfloat16 *__restrict__ C, int M, int N, int K, unsigned *status) {
   extern __shared__ uint8_t smraw[];
-  uint8_t *sm = reinterpret_cast<uint8_t *>(
-      (reinterpret_cast<uintptr_t>(smraw) + 1023) & ~(uintptr_t)1023);
+  uint8_t *sm = tc::smem_align1024(smraw);
   uint64_t *full = reinterpret_cast<uint64_t *>(sm + kOffBar);
   uint64_t *empty = full + kStages;
   uint64_t *acc_full = empty + kStages;  // [2]

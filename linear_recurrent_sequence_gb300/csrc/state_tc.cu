@@ -86,8 +86,7 @@ state_tc_kernel(const __grid_constant__ KParams p, const __grid_constant__ CUten
                 const float *__restrict__ ksum, int piece_len, float *Part, float *zPart,
                 int need_z) {
   extern __shared__ uint8_t smraw[];
-  uint8_t *sm = reinterpret_cast<uint8_t *>(
-      (reinterpret_cast<uintptr_t>(smraw) + 1023) & ~(uintptr_t)1023);
+  uint8_t *sm = tc::smem_align1024(smraw);
   uint64_t *bars = reinterpret_cast<uint64_t *>(sm + kOffBar);
   float *red = reinterpret_cast<float *>(sm + kOffRed);
   uint32_t *tbase_p = reinterpret_cast<uint32_t *>(sm + kOffMisc);

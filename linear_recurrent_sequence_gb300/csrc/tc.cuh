@@ -20,6 +20,14 @@ __device__ __forceinline__ uint32_t smem_u32(const void *p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+// The first 1024-byte aligned byte at or after `base` (a __shared__ array).
+// The offset is added to the array itself so the compiler keeps shared-space
+// loads and stores for every pointer derived from the result; a round trip
+// through an integer address would turn them into generic accesses.
+__device__ __forceinline__ uint8_t *smem_align1024(uint8_t *base) {
+  return base + ((1024u - (smem_u32(base) & 1023u)) & 1023u);
+}
+
 // ------------------------------------------------------------ mbarrier
 __device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));

@@ -21,7 +21,7 @@ tc_probe_kernel(int a_mode, int b_mode, int M, int N, int K, int a_lbo, int a_sb
   extern __shared__ __align__(1024) uint8_t smraw[];
   __shared__ uint64_t bar;
   __shared__ uint32_t tbase;
-  uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~(uintptr_t)1023);
+  uint8_t *sm = tc::smem_align1024(smraw);
   uint8_t *sA = sm;                 // up to 64 KB
   uint8_t *sB = sm + 64 * 1024;     // up to 64 KB
   const int tid = threadIdx.x, warp = tid >> 5;
