@@ -44,18 +44,24 @@ def peaks():
 
 # ------------------------------------------------------------------ clocks
 class ClockSampler:
+    """nvidia-smi samples (every 50 ms) with their host timestamps.  The
+    sampler is started before the warm-up, `wait_first` blocks until the
+    first sample exists, and `summary` keeps the samples taken inside the
+    marked timed region (if the region is shorter than the sampling period,
+    the samples nearest to it, within 0.25 s, and says so)."""
     FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
               "clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
     def __init__(self, index):
         self.index, self.rows, self.proc = index, [], None
+        self.t0 = self.t1 = None
 
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
@@ -65,10 +71,22 @@ class ClockSampler:
 
     def _read(self):
         for line in self.proc.stdout:
-            self.rows.append([c.strip() for c in line.split(",")])
+            self.rows.append((time.monotonic(), [c.strip() for c in line.split(",")]))
+
+    def wait_first(self, timeout=10.0):
+        end = time.monotonic() + timeout
+        while self.proc and not self.rows and time.monotonic() < end:
+            time.sleep(0.01)
+
+    def mark_start(self):
+        self.t0 = time.monotonic()
+
+    def mark_end(self):
+        self.t1 = time.monotonic()
 
     def __exit__(self, *exc):
         if self.proc:
+            time.sleep(0.2)  # let the sample after the region arrive
             self.proc.terminate()
             try:
                 self.proc.wait(timeout=5)
@@ -77,15 +95,26 @@ class ClockSampler:
         return False
 
     def summary(self):
-        if not self.rows:
+        rows, window = self.rows, "timed region"
+        if self.t0 is not None and self.t1 is not None:
+            inside = [r for t, r in rows if self.t0 <= t <= self.t1]
+            if not inside:
+                inside = [r for t, r in rows if self.t0 - 0.25 <= t <= self.t1 + 0.25]
+                window = "nearest to the timed region (within 0.25 s)"
+            rows = inside
+        else:
+            rows = [r for _, r in rows]
+        if not rows:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
-        sm = sorted(float(r[0]) for r in self.rows if r[0].replace(".", "").isdigit())
-        mx = max(float(r[1]) for r in self.rows if r[1].replace(".", "").isdigit())
+        num = lambda x: x.replace(".", "", 1).isdigit()
+        sm = sorted(float(r[0]) for r in rows if num(r[0]))
+        mxs = [float(r[1]) for r in rows if len(r) > 1 and num(r[1])]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for r in self.rows for i in range(4)
+        reasons = sorted({names[i] for r in rows for i in range(4)
                           if len(r) > 2 + i and r[2 + i].lower() == "active"})
-        return {"sm_mhz": sm[len(sm) // 2] if sm else None, "sm_max_mhz": mx,
-                "reasons": reasons, "samples": len(self.rows)}
+        return {"sm_mhz": sm[len(sm) // 2] if sm else None,
+                "sm_max_mhz": max(mxs) if mxs else None,
+                "reasons": reasons, "samples": len(rows), "window": window}
 
 
 # ------------------------------------------------------------------ helpers
@@ -205,19 +234,22 @@ def run_ours(args):
         R.chunkwise_fwd(q, k, v, gam, chunk=args.chunk, norm_flags=R.NORM_ALL, out=o,
                         S_out=S, workspace=ws, stream=stream)
 
-    for _ in range(args.warmup):
-        step()
-    barrier()
-    R.lib.retention_kernel_timer_reset()
-    R.lib.retention_kernel_timer_enable(1)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(local) as clk:
+        clk.wait_first()
+        for _ in range(args.warmup):
+            step()
         barrier()
+        R.lib.retention_kernel_timer_reset()
+        R.lib.retention_kernel_timer_enable(1)
+        barrier()
+        clk.mark_start()
         e0.record(stream)
         for _ in range(args.steps):
             step()
         e1.record(stream)
         barrier()
+        clk.mark_end()
     R.lib.retention_kernel_timer_enable(0)
     ms = max_over_ranks(e0.elapsed_time(e1))
     launches = int(R.lib.retention_launch_count())
@@ -375,7 +407,7 @@ def bench_msr(args, R, dev, stream, tflops, world, max_over_ranks):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=400)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--chunk", type=int, default=64)

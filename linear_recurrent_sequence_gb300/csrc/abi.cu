@@ -165,6 +165,16 @@ SegPlan plan_segments(const ret_desc *d, int NV) {
   return pl;
 }
 
+// The tensor-core kernels work in 64-token chunks.  The chunkwise form is
+// the same function for every chunk length (up to rounding), so a request
+// for a chunk of 128 or 256 tokens runs there as 64-token chunks; other
+// lengths keep the CUDA-core path and their own chunk.
+ret_desc tc_desc(const ret_desc *d) {
+  ret_desc t = *d;
+  if (d->chunk % 64 == 0) t.chunk = 64;
+  return t;
+}
+
 template <typename T>
 T *at(void *ws, size_t off) {
   return reinterpret_cast<T *>(reinterpret_cast<char *>(ws) + off);
@@ -183,11 +193,13 @@ ret_status chunkwise_impl(const ret_desc *d, const void *q, const void *k, const
   if (!desc_ok(d)) return RET_EINVAL;
   const bool empty = d->B == 0 || d->H == 0;
   if (!empty && d->N > 0 && (!q || !k || !v || !o)) return RET_EINVAL;
-  KParams p;
+  KParams p, pt;
   make_params(d, ws, p);
-  const bool tc = !empty && d->N > 0 && chunk_tc_supported(p, v, p.sv);
+  const ret_desc dt = tc_desc(d);
+  make_params(&dt, ws, pt);
+  const bool tc = !empty && d->N > 0 && chunk_tc_supported(pt, v, pt.sv);
   const SimtWs w = simt_ws(d);
-  const TcWs tw = tc_ws(d);
+  const TcWs tw = tc_ws(&dt);
   // The requirement is the one retention_workspace_size reports, whichever
   // kernel runs.
   ret_status rs = check_ws(ws, ws_bytes, w.total > tw.total ? w.total : tw.total);
@@ -211,12 +223,12 @@ ret_status chunkwise_impl(const ret_desc *d, const void *q, const void *k, const
     ChunkMeta *meta = at<ChunkMeta>(ws, tw.meta);
     float *ks = at<float>(ws, tw.ks);
     const int need_z = (d->norm_flags & RET_NORM_RSUM) || z_out != nullptr;
-    RET_CUDA(RET_TIMED_LAUNCH(kKRotate, st, launch_rotate_qk(p, q, k, Qp, Kp, meta, need_z ? ks : nullptr, st)));
+    RET_CUDA(RET_TIMED_LAUNCH(kKRotate, st, launch_rotate_qk(pt, q, k, Qp, Kp, meta, need_z ? ks : nullptr, st)));
     if (z_in && z_out == z_in) {  // every CTA of a head reads z_in; one writes z_out
       RET_CUDA(cudaMemcpyAsync(at<float>(ws, tw.zc), z_in, zbytes, cudaMemcpyDeviceToDevice, st));
       z_in = at<float>(ws, tw.zc);
     }
-    SegPlan seg = plan_segments(d, d->d_v / 128);
+    SegPlan seg = plan_segments(&dt, d->d_v / 128);
     if (seg.P > 1) {
       // Segments read S_in at their start while the last one writes S_out.
       if (S_in && S_out == S_in) {
@@ -225,9 +237,9 @@ ret_status chunkwise_impl(const ret_desc *d, const void *q, const void *k, const
       }
       seg.Part = at<float>(ws, tw.part);
       seg.zPart = at<float>(ws, tw.zpart);
-      RET_CUDA(RET_TIMED_LAUNCH(kKStatePass, st, launch_state_tc(p, Kp, v, meta, ks, seg.npieces, seg.piece_len, seg.Part, seg.zPart, need_z, st)));
+      RET_CUDA(RET_TIMED_LAUNCH(kKStatePass, st, launch_state_tc(pt, Kp, v, meta, ks, seg.npieces, seg.piece_len, seg.Part, seg.zPart, need_z, st)));
     }
-    RET_CUDA(RET_TIMED_LAUNCH(kKChunkTc, st, launch_chunk_tc(p, Qp, Kp, v, meta, ks, S_in, z_in, S_out, z_out, o, gate, need_z, seg, st)));
+    RET_CUDA(RET_TIMED_LAUNCH(kKChunkTc, st, launch_chunk_tc(pt, Qp, Kp, v, meta, ks, S_in, z_in, S_out, z_out, o, gate, need_z, seg, st)));
     return RET_OK;
   }
   float *Qr = at<float>(ws, w.qr), *Kr = at<float>(ws, w.kr);
@@ -271,7 +283,8 @@ void retention_desc_init(ret_desc *d, int B, int H, int N, int d_k, int d_v,
 
 size_t retention_workspace_size(const ret_desc *d) {
   if (!desc_ok(d)) return 0;
-  const size_t a = simt_ws(d).total, b = tc_ws(d).total;
+  const ret_desc dt = tc_desc(d);
+  const size_t a = simt_ws(d).total, b = tc_ws(&dt).total;
   return a > b ? a : b;
 }
 

@@ -26,18 +26,21 @@
 //   O^T = V^T R^T            (M=128 v, N=64 i, K=64 j)     -> TMEM
 //   O^T += S^T Q'^T          (A = fp16 copy of S^T in TMEM, K=d_k)
 //   S^T += V^T K'            (M=128 v, N=d_k, K=64 j)      -> TMEM fp32 state
+// O^T is double-buffered in TMEM (chunk parity); the scores of chunk c live
+// in O^T buffer c&1 until the R group has read them.
 //
-// Warp roles (12 warps): warp 0 issues TMA loads (2-stage ring), warp 1
-// issues MMAs (one thread) and owns TMEM, warps 2-3 ("helper" group)
-// convert V to fp16, compute Q'.z for the third normalisation and carry z,
-// warps 4-7 ("state" group) build R and the row factors, then refresh the
-// state copy, warps 8-11 ("output" group) drain O^T and run GroupNorm and
-// the stores.  The MMA order per chunk c is O^T = V^T R^T (once R is built),
-// the scores of chunk c+1, then (once the state copy is refreshed) the cross
-// term and the state update, so R of chunk c+1 is built while the state MMAs
-// of chunk c run.  Every wait is bounded; a wait that runs out sets the
-// status word and an abort flag, and every role leaves after draining its
-// own asynchronous work.
+// Warp roles (16 warps):
+//   warp 0       TMA loads (2-stage ring) and the scores MMAs
+//   warp 1       O^T = V^T R^T, then per half of d_k the cross term and the
+//                state update (two issuing threads keep the tensor pipe fed:
+//                one thread issues at most about one MMA per 28 ns)
+//   warps 2-3    helper: max |V|, the chunk's block exponents, V -> fp16
+//   warps 4-7    R group: scores -> masked fp16 R, Q'.z, row factors, z carry
+//   warps 8-11   state group: fp16 copy of the state and gamma^L, per half
+//                of d_k, so it overlaps the MMAs of the other half
+//   warps 12-15  output group: drain O^T, GroupNorm (+ gate), stores
+// Every wait is bounded; a wait that runs out sets the status word and an
+// abort flag, and every role leaves after draining its own asynchronous work.
 #include <cooperative_groups.h>
 #include <cudaTypedefs.h>
 
@@ -54,7 +57,7 @@ namespace {
 
 constexpr int kC = 64;    // tokens per chunk
 constexpr int kW = 128;   // value columns per CTA
-constexpr int kNT = 384;  // threads per CTA
+constexpr int kNT = 512;  // threads per CTA
 
 // Shared-memory map (offsets from a 1024-byte aligned base).
 // Stage: Q' 32K | K' 32K | V 16K | key column sums (d_k fp32) | ChunkMeta.
@@ -62,31 +65,50 @@ constexpr uint32_t kOffQ = 0, kOffK = 32 * 1024, kOffV = 64 * 1024;
 constexpr uint32_t kOffKs = 80 * 1024, kOffMeta = kOffKs + 1024;
 constexpr uint32_t kStage = 82 * 1024;
 constexpr uint32_t kOffR = 2 * kStage;                  // 64 x 128 B, fp16
-constexpr uint32_t kOTPitch = 132;                      // floats per O^T row
-constexpr uint32_t kOffOT = kOffR + 8 * 1024;           // [64][132] fp32
+constexpr uint32_t kOTPitch = 144;                      // floats per O^T row
+constexpr uint32_t kOffOT = kOffR + 8 * 1024;           // [64][144] fp32
 constexpr uint32_t kOffZ = kOffOT + 64 * kOTPitch * 4;  // [256] fp32
 constexpr uint32_t kOffF = kOffZ + 256 * 4;             // [2][64] fp32 row factors
-constexpr uint32_t kOffE = kOffF + 2 * 64 * 4;          // [2] int chunk exponents
-constexpr uint32_t kOffRed = kOffE + 16;                // [2 groups][8] fp32 scratch
-constexpr uint32_t kOffGN = kOffRed + 64;               // [2][8][64][2] fp32
+constexpr uint32_t kOffOS = kOffF + 2 * 64 * 4;         // [2] fp32 2^E for the output group
+constexpr uint32_t kOffSc = kOffOS + 16;                // [2] Scales (helper -> R, state)
+constexpr uint32_t kOffRed = kOffSc + 2 * 32;           // [4 groups][8] fp32 scratch
+constexpr uint32_t kOffGN = kOffRed + 128;              // [2][8][64][2] fp32
 constexpr uint32_t kOffNrm = kOffGN + 2 * 8 * 64 * 2 * 4;  // [64][2] fp32 shift, scale
-constexpr uint32_t kOffVX = kOffNrm + 64 * 2 * 4;          // [2] int vx, [2] float max|V|
-constexpr uint32_t kOffQZ = kOffVX + 16;                   // [2][64] fp32 Q'_i . z
-constexpr uint32_t kOffHRed = kOffQZ + 2 * 64 * 4;         // [2][2] fp32 helper scratch
-constexpr uint32_t kOffBar = kOffHRed + 16;
-constexpr int kNumBars = 17;
+constexpr uint32_t kOffVX = kOffNrm + 64 * 2 * 4;          // [2] float max|V|, s_bound entry
+constexpr uint32_t kOffQZ = kOffVX + 16;                   // [64] fp32 R row sums, scratch
+constexpr uint32_t kOffBar = kOffQZ + 2 * 64 * 4;
+constexpr int kNumBars = 27;
 constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;
 constexpr uint32_t kSmemBytes = kOffMisc + 16 + 1024;   // + alignment slack
 static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 
+// Barriers with a 0/1 pair exist per stage or per O^T buffer (chunk parity),
+// so a producer may run one chunk ahead of a consumer without two phases of
+// one barrier completing before the consumer looks.
 enum Bar {
-  FULL0 = 0, FULL1, EMPTY0, EMPTY1, QK, RRDY, OFULL, SFULL, OFREE, GN0, GN1, DRAIN,
-  VRDY0, VRDY1, QZRDY0, QZRDY1,  // per parity: the helper may run one chunk ahead
-  SRDY
+  FULL0 = 0, FULL1, EMPTY0, EMPTY1, QK0, QK1, RRDY, RFREE, OFULL0, OFULL1, OFREE0, OFREE1,
+  SFULL0, SFULL1, SRDY0, SRDY1, GN0, GN1, DRAIN, DRAIN2, VRDY0, VRDY1, VCONV0, VCONV1,
+  FRDY0, FRDY1, SB0
 };
 
-// TMEM column map.
-constexpr uint32_t kTS = 0, kTSh = 256, kTO = 384, kTQK = 448;
+// Per-chunk block exponents and state factors, chosen by the helper from
+// rigorous magnitude bounds (see the helper group) and read by the R and
+// state groups.
+struct Scales {
+  int E;           // O^T accumulator holds O * 2^-E
+  int rr;          // R is stored as fp16 R * 2^-rr
+  float f_cp;      // fp16 state copy = TMEM state * f_cp
+  float f_pre;     // TMEM state <- TMEM state * f_pre before the update
+  int sigma_next;  // TMEM state holds S * 2^-sigma_next after the update
+  int pad[3];
+};
+static_assert(sizeof(Scales) == 32, "Scales record");
+
+// TMEM column map: fp32 state, its fp16 copy, two O^T buffers (chunk
+// parity).  The scores T of chunk c (M=64 layout) live in O^T buffer c&1
+// until the R group has read them; O^T of chunk c then overwrites them.
+constexpr uint32_t kTS = 0, kTSh = 256, kTO0 = 384;
+__device__ __forceinline__ uint32_t tcol_o(int c) { return kTO0 + 64u * (uint32_t)(c & 1); }
 
 constexpr uint32_t kBudget = 1u << 24;
 
@@ -107,10 +129,11 @@ struct TcArgs {
   int NV;        // CTAs per head (d_v / 128)
   int need_z;    // carry z (third normalisation or z_out)
   int vec_out;   // o rows are 16-byte aligned: vector stores
+  int vec_gate;  // gate rows are 16-byte aligned bf16: vector loads
 };
 
 // Named barrier among the n threads of group g (1 = state, 2 = output,
-// 3 = helper).
+// 3 = helper, 4 = R).
 __device__ __forceinline__ void grp_sync(int g, int n = 128) {
   asm volatile("bar.sync %0, %1;" ::"r"(g), "r"(n) : "memory");
 }
@@ -139,6 +162,15 @@ __device__ __forceinline__ float grp_max(int g, float v, float *red, int &slot, 
   if ((et & 31) == 0) r[et >> 5] = v;
   grp_sync(g);
   return fmaxf(fmaxf(r[0], r[1]), fmaxf(r[2], r[3]));
+}
+
+// K-step ks (16 elements) of a K-major operand stored as 64-element swizzled
+// rows in 8 KB blocks of 64 rows, in the 16-byte units of a descriptor's
+// start-address field.  Descriptors are built once; a K-step adds this
+// offset (every shared-memory address stays below 256 KB, so the 14-bit
+// field never carries).
+__device__ __forceinline__ uint64_t kmaj_off(int ks) {
+  return (uint64_t)(((ks >> 2) * 8192 + (ks & 3) * 32) >> 4);
 }
 
 // Bounded wait that also gives up when another role has aborted.
@@ -188,6 +220,61 @@ __device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 
 
 }  // namespace
 
+// Store variants, fixed at compile time so the hot loop carries no unused
+// paths: kStoreAny handles every output dtype, alignment and gate;
+// kStoreBf16 is 16-byte aligned bf16 rows without a gate; kStoreBf16Gate
+// adds a 16-byte aligned bf16 gate.
+enum StoreMode { kStoreAny = 0, kStoreBf16 = 1, kStoreBf16Gate = 2 };
+
+// Entry state of this CTA's value columns into the TMEM state columns at
+// `ts` (one warp, its 32 lanes): S_in, or for a later segment the decayed sum
+// of S_in and the pieces before it.  Returns the lane's max |S|.
+__device__ __noinline__ float load_entry_state(const KParams &p, const TcArgs &a, uint32_t ts,
+                                               int bh, long long vglob, int seg, int c0, int npc,
+                                               float lng) {
+  const int DK = p.dk;
+  const float w_in = seg > 0 ? gpow(lng, kC * c0) : 1.f;
+  float m0 = 0.f;
+  for (int g = 0; g < DK / 32; ++g) {
+    uint32_t r[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      const long long e = ((long long)bh * DK + g * 32 + i) * p.dv + vglob;
+      r[i] = __float_as_uint(a.S_in ? w_in * a.S_in[e] : 0.f);
+    }
+    for (int pi = 0; pi < npc; ++pi) {
+      const float w = gpow(lng, kC * (c0 - (pi + 1) * a.piece_len));
+      const float *src = a.Part + (long long)pi * p.B * p.H * DK * p.dv;
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        const long long e = ((long long)bh * DK + g * 32 + i) * p.dv + vglob;
+        r[i] = __float_as_uint(fmaf(w, src[e], __uint_as_float(r[i])));
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < 32; ++i) m0 = fmaxf(m0, fabsf(__uint_as_float(r[i])));
+    tc::tmem_st32(ts + g * 32, r);
+  }
+  tc::tmem_st_wait();
+  return m0;
+}
+
+// The TMEM state columns at `ts` (one warp, its 32 lanes) times `back` to
+// S_out.
+__device__ __noinline__ void store_state(const KParams &p, float *S_out, uint32_t ts, int bh,
+                                         long long vglob, float back) {
+  const int DK = p.dk;
+  for (int g = 0; g < DK / 32; ++g) {
+    uint32_t r[32];
+    tc::tmem_ld32(ts + g * 32, r);
+    tc::tmem_ld_wait_on(r);
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+      S_out[((long long)bh * DK + g * 32 + i) * p.dv + vglob] = __uint_as_float(r[i]) * back;
+  }
+}
+
+template <int kStore>
 __global__ void __launch_bounds__(kNT, 1)
 chunk_tc_kernel(const __grid_constant__ KParams p, const __grid_constant__ CUtensorMap tmQ,
                 const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
@@ -199,15 +286,14 @@ chunk_tc_kernel(const __grid_constant__ KParams p, const __grid_constant__ CUten
   volatile int *abort_p = reinterpret_cast<volatile int *>(sm + kOffMisc + 4);
   float *zsm = reinterpret_cast<float *>(sm + kOffZ);
   float *fsm = reinterpret_cast<float *>(sm + kOffF);
-  int *Esm = reinterpret_cast<int *>(sm + kOffE);
+  float *oss = reinterpret_cast<float *>(sm + kOffOS);
+  Scales *scs = reinterpret_cast<Scales *>(sm + kOffSc);
   float *red = reinterpret_cast<float *>(sm + kOffRed);
   float *OT = reinterpret_cast<float *>(sm + kOffOT);
   float *gns = reinterpret_cast<float *>(sm + kOffGN);
   float *nrm = reinterpret_cast<float *>(sm + kOffNrm);
-  int *vxs = reinterpret_cast<int *>(sm + kOffVX);
-  float *vmxs = reinterpret_cast<float *>(sm + kOffVX + 8);
+  float *vmxs = reinterpret_cast<float *>(sm + kOffVX);  // [0] max|V| scratch, [1] entry bound
   float *qzs = reinterpret_cast<float *>(sm + kOffQZ);
-  float *hred = reinterpret_cast<float *>(sm + kOffHRed);
 
   cg::cluster_group cluster = cg::this_cluster();
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -225,25 +311,15 @@ chunk_tc_kernel(const __grid_constant__ KParams p, const __grid_constant__ CUten
   const bool last_seg = c0 + ncl >= nch;
   const int npc = seg > 0 ? c0 / a.piece_len : 0;  // pieces before c0
   const float lng = p.lng[h];
+  const bool rsum = (p.norm_flags & RET_NORM_RSUM) != 0;
 
   if (tid == 0) {
     tc::mbar_init(&bars[FULL0], 1);
     tc::mbar_init(&bars[FULL1], 1);
     tc::mbar_init(&bars[EMPTY0], 2);
     tc::mbar_init(&bars[EMPTY1], 2);
-    tc::mbar_init(&bars[QK], 1);
-    tc::mbar_init(&bars[RRDY], 1);
-    tc::mbar_init(&bars[SRDY], 1);
-    tc::mbar_init(&bars[OFULL], 1);
-    tc::mbar_init(&bars[SFULL], 1);
-    tc::mbar_init(&bars[OFREE], 1);
-    tc::mbar_init(&bars[GN0], 1);
-    tc::mbar_init(&bars[GN1], 1);
-    tc::mbar_init(&bars[DRAIN], 1);
-    tc::mbar_init(&bars[VRDY0], 1);
-    tc::mbar_init(&bars[VRDY1], 1);
-    tc::mbar_init(&bars[QZRDY0], 1);
-    tc::mbar_init(&bars[QZRDY1], 1);
+    for (int i = QK0; i <= SB0; ++i)
+      if (i != EMPTY0 && i != EMPTY1) tc::mbar_init(&bars[i], 1);
     *abort_p = 0;
     tc::fence_mbar_init();
   }
@@ -258,120 +334,147 @@ chunk_tc_kernel(const __grid_constant__ KParams p, const __grid_constant__ CUten
   const uint32_t tb = *tbase_p;
 
   if (warp == 0) {
-    // ------------------------------------------------------------ TMA
+    // ------------------------------------------------------------ TMA and scores
+    // One thread issues the stage loads and the scores T = Q' K'^T of each
+    // chunk, into O^T buffer c&1 once the output group has drained that
+    // buffer's previous chunk (c-2).
     if (lane == 0) {
       tc::prefetch_tmap(&tmQ);
       tc::prefetch_tmap(&tmK);
       tc::prefetch_tmap(&tmV);
       const uint32_t bytes = (uint32_t)NKB * 8192u * 2u + 16384u + 16u +
                              (a.need_z ? (uint32_t)DK * 4u : 0u);
-      int issued = 0;
-      for (int lc = 0; lc < ncl; ++lc) {
-        const int s = lc & 1, c = c0 + lc;
-        if (lc >= 2 && !wait_bar(&bars[EMPTY0 + s], ((lc >> 1) - 1) & 1, abort_p, p.status)) break;
-        uint8_t *st = sm + s * kStage;
-        tc::mbar_arrive_expect_tx(&bars[FULL0 + s], bytes);
-        for (int kb = 0; kb < NKB; ++kb)
-          tc::tma_load_3d(st + kOffQ + kb * 8192, &tmQ, &bars[FULL0 + s], kb * 64, c * kC, bh);
-        for (int kb = 0; kb < NKB; ++kb)
-          tc::tma_load_3d(st + kOffK + kb * 8192, &tmK, &bars[FULL0 + s], kb * 64, c * kC, bh);
-        for (int vb = 0; vb < 2; ++vb)
-          tc::tma_load_4d(st + kOffV + vb * 8192, &tmV, &bars[FULL0 + s], v0 + vb * 64, c * kC,
-                          h, b);
-        tc::bulk_load(st + kOffMeta, a.meta + (long long)bh * nch + c, 16u, &bars[FULL0 + s]);
-        if (a.need_z)
-          tc::bulk_load(st + kOffKs, a.ksum + ((long long)bh * nch + c) * DK, (uint32_t)DK * 4u,
-                        &bars[FULL0 + s]);
-        ++issued;
+      const uint32_t id_qk = tc::idesc_f16(64, 64, 0, 0);
+      const int nks = DK / 16;
+      const uint32_t sq0 = tc::smem_u32(sm + kOffQ);
+      const uint64_t dq0 = tc::smem_desc(sq0, 16, 1024, tc::kSw128);          // Q' K-major
+      const uint64_t dk0 = tc::smem_desc(sq0 + kOffK, 16, 1024, tc::kSw128);  // K' K-major
+      int t_ld = 0, t_qk = 0;  // next chunk to load / to score
+      for (uint32_t spin = 0; t_qk < ncl;) {
+        bool moved = false;
+        if (t_ld < ncl &&
+            (t_ld < 2 || tc::mbar_test_wait(&bars[EMPTY0 + (t_ld & 1)], ((t_ld >> 1) - 1) & 1))) {
+          const int s = t_ld & 1, c = c0 + t_ld;
+          uint8_t *st = sm + s * kStage;
+          tc::mbar_arrive_expect_tx(&bars[FULL0 + s], bytes);
+          for (int kb = 0; kb < NKB; ++kb)
+            tc::tma_load_3d(st + kOffQ + kb * 8192, &tmQ, &bars[FULL0 + s], kb * 64, c * kC, bh);
+          for (int kb = 0; kb < NKB; ++kb)
+            tc::tma_load_3d(st + kOffK + kb * 8192, &tmK, &bars[FULL0 + s], kb * 64, c * kC, bh);
+          for (int vb = 0; vb < 2; ++vb)
+            tc::tma_load_4d(st + kOffV + vb * 8192, &tmV, &bars[FULL0 + s], v0 + vb * 64, c * kC,
+                            h, b);
+          tc::bulk_load(st + kOffMeta, a.meta + (long long)bh * nch + c, 16u, &bars[FULL0 + s]);
+          if (a.need_z)
+            tc::bulk_load(st + kOffKs, a.ksum + ((long long)bh * nch + c) * DK, (uint32_t)DK * 4u,
+                          &bars[FULL0 + s]);
+          ++t_ld;
+          moved = true;
+        }
+        const int bq = t_qk & 1;
+        if (t_qk < t_ld && tc::mbar_test_wait(&bars[FULL0 + bq], (t_qk >> 1) & 1) &&
+            (t_qk < 2 || tc::mbar_test_wait(&bars[OFREE0 + bq], ((t_qk >> 1) - 1) & 1))) {
+          tc::tc_fence_after();
+          const uint64_t so = bq ? (uint64_t)(kStage >> 4) : 0ull;
+#pragma unroll
+          for (int ks = 0; ks < 16; ++ks)  // T = Q' K'^T
+            if (ks < nks)
+              tc::mma_ss(tb + tcol_o(t_qk), dq0 + so + kmaj_off(ks), dk0 + so + kmaj_off(ks),
+                         id_qk, ks > 0);
+          tc::mma_commit(&bars[QK0 + bq]);
+          ++t_qk;
+          moved = true;
+        }
+        if (!moved) {
+          if (++spin >= kBudget) {
+            report(p.status, kDevTimeout);
+            *abort_p = 1;
+            break;
+          }
+          if ((spin & 255u) == 255u && *abort_p) break;
+          __nanosleep(32);  // leave the issue slots to the other warps
+        }
       }
-      // Let every issued copy land before the CTA can leave.
-      for (int lc = issued > 2 ? issued - 2 : 0; lc < issued; ++lc)
-        drain_wait(&bars[FULL0 + (lc & 1)], (lc >> 1) & 1);
+      // Let every issued copy and MMA finish before the CTA can leave.
+      for (int t = t_qk; t < t_ld; ++t) drain_wait(&bars[FULL0 + (t & 1)], (t >> 1) & 1);
+      tc::mma_commit(&bars[DRAIN]);
+      drain_wait(&bars[DRAIN], 0);
     }
     __syncwarp();
   } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA
+    // ------------------------------------------------------------ O^T and state MMAs
+    // Per chunk: O^T = V^T R^T (starts the accumulator in buffer c&1, after
+    // the R group has read the scores there), then per half of d_k, as soon
+    // as the state group has refreshed it: O^T += S^T Q'^T over the half's
+    // K-steps and S^T[:, half] += V^T K'[:, half].  SFULL0/SFULL1 tell the
+    // state group that the half's copy has been read and its state updated.
     if (lane == 0) {
-      const uint32_t id_qk = tc::idesc_f16(64, 64, 0, 0);
       const uint32_t id_o = tc::idesc_f16(128, 64, 1, 0);
       const uint32_t id_x = tc::idesc_f16(128, 64, 0, 0);
-      const uint32_t id_s = tc::idesc_f16(128, DK, 1, 1);
-      const uint32_t sr = tc::smem_u32(sm + kOffR);
-      auto mma_qk = [&](int lc) {  // T = Q' K'^T
-        const uint32_t sq = tc::smem_u32(sm + (lc & 1) * kStage + kOffQ), sk = sq + kOffK;
-        for (int ks = 0; ks < DK / 16; ++ks) {
-          const uint32_t off = (ks >> 2) * 8192 + (ks & 3) * 32;
-          tc::mma_ss(tb + kTQK, tc::smem_desc(sq + off, 16, 1024, tc::kSw128),
-                     tc::smem_desc(sk + off, 16, 1024, tc::kSw128), id_qk, ks > 0);
-        }
-        tc::mma_commit(&bars[QK]);
-      };
-      bool go = ncl > 0 && wait_bar(&bars[FULL0], 0, abort_p, p.status);
-      if (go) {
-        tc::tc_fence_after();
-        mma_qk(0);
-      }
-      // Per chunk: O^T = V^T R^T once R is built and O^T of the previous
-      // chunk is drained; then the next chunk's scores, so the state group
-      // can build the next R while this chunk's state MMAs run; then, once
-      // the state copy is refreshed, the cross term and the state update.
-      for (int lc = 0; go && lc < ncl; ++lc) {
+      const uint32_t id_s = tc::idesc_f16(128, DK == 256 ? 128 : DK, 1, 1);
+      const int nh = DK == 256 ? 2 : 1;  // d_k = 256 runs in two halves of 128
+      const int nkh = DK / 16 / nh;     // K-steps of the cross term per half
+      const uint32_t sq0 = tc::smem_u32(sm + kOffQ);
+      const uint64_t dq0 = tc::smem_desc(sq0, 16, 1024, tc::kSw128);             // Q' K-major
+      const uint64_t dkm0 = tc::smem_desc(sq0 + kOffK, 8192, 1024, tc::kSw128);  // K' MN-major
+      const uint64_t dv0 = tc::smem_desc(sq0 + kOffV, 8192, 1024, tc::kSw128);   // V^T MN-major
+      const uint64_t dr = tc::smem_desc(tc::smem_u32(sm + kOffR), 16, 1024, tc::kSw128);
+      bool ok = true;
+      for (int lc = 0; lc < ncl && ok; ++lc) {
         const int s = lc & 1;
-        const uint32_t sq = tc::smem_u32(sm + s * kStage + kOffQ);
-        const uint32_t sk = sq + kOffK, sv = sq + kOffV;
-        if (!wait_bar(&bars[RRDY], lc & 1, abort_p, p.status)) break;
-        if (lc > 0 && !wait_bar(&bars[OFREE], (lc - 1) & 1, abort_p, p.status)) break;
+        const uint64_t so = s ? (uint64_t)(kStage >> 4) : 0ull;
+        const uint32_t to = tb + tcol_o(lc);
+        ok = wait_bar(&bars[VCONV0 + s], (lc >> 1) & 1, abort_p, p.status) &&
+             wait_bar(&bars[RRDY], lc & 1, abort_p, p.status);
+        if (!ok) break;
         tc::tc_fence_after();
+#pragma unroll
         for (int ks = 0; ks < 4; ++ks)  // O^T = V^T R^T
-          tc::mma_ss(tb + kTO, tc::smem_desc(sv + ks * 2048, 8192, 1024, tc::kSw128),
-                     tc::smem_desc(sr + ks * 32, 16, 1024, tc::kSw128), id_o, ks > 0);
-        if (lc + 1 < ncl) {
-          if (!wait_bar(&bars[FULL0 + (s ^ 1)], ((lc + 1) >> 1) & 1, abort_p, p.status)) break;
+          tc::mma_ss(to, dv0 + so + ks * 128, dr + ks * 2, id_o, ks > 0);
+        tc::mma_commit(&bars[RFREE]);
+        for (int hh = 0; hh < nh; ++hh) {
+          if (!wait_bar(&bars[SRDY0 + hh], lc & 1, abort_p, p.status)) {
+            ok = false;
+            break;
+          }
           tc::tc_fence_after();
-          mma_qk(lc + 1);
+#pragma unroll
+          for (int k = 0; k < 16; ++k)  // O^T += S^T Q'^T over this half's K-steps
+            if (k < nkh) {
+              const int ks = hh * nkh + k;
+              tc::mma_ts(to, tb + kTSh + ks * 8, dq0 + so + kmaj_off(ks), id_x, 1);
+            }
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks)  // S^T[:, half] += V^T K'[:, half]
+            tc::mma_ss(tb + kTS + hh * 128, dv0 + so + ks * 128,
+                       dkm0 + so + ks * 128 + (uint64_t)hh * 1024, id_s, 1);
+          tc::mma_commit(&bars[nh == 1 ? SFULL1 : SFULL0 + hh]);
         }
-        if (!wait_bar(&bars[SRDY], lc & 1, abort_p, p.status)) break;
-        tc::tc_fence_after();
-        for (int ks = 0; ks < DK / 16; ++ks)  // O^T += S^T Q'^T
-          tc::mma_ts(tb + kTO, tb + kTSh + ks * 8,
-                     tc::smem_desc(sq + (ks >> 2) * 8192 + (ks & 3) * 32, 16, 1024, tc::kSw128),
-                     id_x, 1);
-        tc::mma_commit(&bars[OFULL]);
-        for (int ks = 0; ks < 4; ++ks)  // S^T += V^T K'
-          tc::mma_ss(tb + kTS, tc::smem_desc(sv + ks * 2048, 8192, 1024, tc::kSw128),
-                     tc::smem_desc(sk + ks * 2048, 8192, 1024, tc::kSw128), id_s, 1);
-        tc::mma_commit(&bars[SFULL]);
+        if (!ok) break;
+        tc::mma_commit(&bars[OFULL0 + s]);
         tc::mma_commit(&bars[EMPTY0 + s]);
       }
-      tc::mma_commit(&bars[DRAIN]);  // every MMA issued above is finished
-      drain_wait(&bars[DRAIN], 0);
+      tc::mma_commit(&bars[DRAIN2]);
+      drain_wait(&bars[DRAIN2], 0);
     }
     __syncwarp();
   } else if (warp == 2 || warp == 3) {
     // ------------------------------------------------------------ helper group
     const int G = 3, NT = 64;
     const int ht = tid - 64;  // 0..63
-    const bool rsum = (p.norm_flags & RET_NORM_RSUM) != 0;
+    float *hred = red;        // [2 slots][2 warps]
     int hslot = 0;
-    bool ok = true;
-    if (a.need_z)
-      for (int k2 = ht; k2 < DK; k2 += NT) {
-        float z = a.z_in ? a.z_in[(long long)bh * DK + k2] : 0.f;
-        if (seg > 0) {  // entry z of a later segment
-          z *= gpow(lng, kC * c0);
-          for (int i = 0; i < npc; ++i)
-            z = fmaf(gpow(lng, kC * (c0 - (i + 1) * a.piece_len)),
-                     a.zPart[((long long)i * p.B * p.H + bh) * DK + k2], z);
-        }
-        zsm[k2] = z;
-      }
-    grp_sync(G, NT);
+    // Bound of max |S| entering the first chunk, from the state group.
+    bool ok = grp_all(G, wait_bar(&bars[SB0], 0, abort_p, p.status), NT);
+    float s_bound = vmxs[1];
+    int sigma = 0;  // the TMEM state holds S * 2^-sigma
     for (int lc = 0; lc < ncl && ok; ++lc) {
       const int s = lc & 1, c = c0 + lc;
+      const int L = min(kC, N - c * kC);
       uint8_t *st = sm + s * kStage;
       ok = grp_all(G, wait_bar(&bars[FULL0 + s], (lc >> 1) & 1, abort_p, p.status), NT);
       if (!ok) break;
-      // (1) V tile: bf16 -> fp16 * 2^-vx in place (1024 16-byte words).
+      // (1) max |V| of the tile (1024 16-byte words).
       uint4 vv[16];
       float vm = 0.f;
 #pragma unroll
@@ -389,6 +492,36 @@ chunk_tc_kernel(const __grid_constant__ KParams p, const __grid_constant__ CUten
       grp_sync(G, NT);
       const float vmx = fmaxf(hr[0], hr[1]);
       const int vx = expo14(vmx);
+      // (2) block exponents of the chunk.  R and the state copy share the O
+      // accumulator's scale 2^-E.  |R_ij| = gamma^(i-j) |q_i . k_j| <=
+      // (d_k/2) max|pair of rot q| max|pair of rot k| (j <= i; a dot product
+      // is a sum of d_k/2 pair products), and s_bound >= max |S_c|.
+      const ChunkMeta mt = *reinterpret_cast<const ChunkMeta *>(st + kOffMeta);
+      const float gL = gpow(lng, L);
+      {
+        const int rr_nat = expo14((float)(DK / 2) * mt.qmax * mt.kmax);
+        int E = rr_nat + vx;
+        if (s_bound > 0.f) E = max(E, expo14(s_bound) + mt.qexp);
+        const int ss = E - mt.qexp, sigma_next = vx + mt.kexp;
+        if (ht == 0) {
+          Scales sc;
+          sc.E = E;
+          sc.rr = E - vx;
+          sc.f_cp = exp2f((float)(sigma - ss));
+          sc.f_pre = gL * exp2f((float)(sigma - sigma_next));
+          sc.sigma_next = sigma_next;
+          sc.pad[0] = sc.pad[1] = sc.pad[2] = 0;
+          scs[s] = sc;
+          tc::mbar_arrive(&bars[VRDY0 + s]);
+        }
+        sigma = sigma_next;
+        // |S_{c+1}| <= gamma^L |S_c| + sum_j |K'_j||V_j| with zeta <= 1 (a
+        // pair norm bounds each component of its pair).  Loose by the ratio
+        // of a sum of L terms to their random-sign size, which costs nothing
+        // in floating point.
+        s_bound = gL * s_bound + (float)L * mt.kmax * vmx;
+      }
+      // (3) V tile: bf16 -> fp16 * 2^-vx in place.
       const float vsc = exp2f((float)-vx);
 #pragma unroll
       for (int u = 0; u < 16; ++u) {
@@ -398,280 +531,309 @@ chunk_tc_kernel(const __grid_constant__ KParams p, const __grid_constant__ CUten
         for (int e = 0; e < 4; ++e) o4[e] = tc::pack_f16(bf_lo(w[e]) * vsc, bf_hi(w[e]) * vsc);
         reinterpret_cast<uint4 *>(st + kOffV)[ht + NT * u] = make_uint4(o4[0], o4[1], o4[2], o4[3]);
       }
-      if (ht == 0) {
-        vxs[s] = vx;
-        vmxs[s] = vmx;
-      }
       tc::fence_proxy_async_smem();
       grp_sync(G, NT);
-      if (ht == 0) tc::mbar_arrive(&bars[VRDY0 + s]);
-      // (2) Q'_i . z_c for the row sums of the third normalisation.
-      if (rsum) {
-        const int i = ht;
-        float acc[4] = {0.f, 0.f, 0.f, 0.f};
-        for (int kb = 0; kb < NKB; ++kb)
+      if (ht == 0) tc::mbar_arrive(&bars[VCONV0 + s]);
+    }
+  } else if (warp >= 4 && warp < 8) {
+    // ------------------------------------------------------------ R group
+    const int G = 4;
+    const int q = warp & 3;                 // TMEM lane quarter
+    const int et = tid - 128;               // 0..127
+    const uint32_t lb = (uint32_t)(q * 32) << 16;
+    float *rsm = qzs;                       // [64] R row sums
+    bool ok = true;
+    if (a.need_z) {
+      for (int k2 = et; k2 < DK; k2 += 128) {
+        float z = a.z_in ? a.z_in[(long long)bh * DK + k2] : 0.f;
+        if (seg > 0) {  // entry z of a later segment
+          z *= gpow(lng, kC * c0);
+          for (int i = 0; i < npc; ++i)
+            z = fmaf(gpow(lng, kC * (c0 - (i + 1) * a.piece_len)),
+                     a.zPart[((long long)i * p.B * p.H + bh) * DK + k2], z);
+        }
+        zsm[k2] = z;
+      }
+      grp_sync(G);
+    }
+    for (int lc = 0; lc < ncl && ok; ++lc) {
+      const int s = lc & 1, c = c0 + lc;
+      const int L = min(kC, N - c * kC);
+      uint8_t *st = sm + s * kStage;
+      // RFREE: the previous chunk's O^T = V^T R^T has read R.
+      ok = grp_all(G, wait_bar(&bars[QK0 + s], (lc >> 1) & 1, abort_p, p.status) &&
+                          wait_bar(&bars[VRDY0 + s], (lc >> 1) & 1, abort_p, p.status) &&
+                          (lc == 0 || wait_bar(&bars[RFREE], (lc - 1) & 1, abort_p, p.status)));
+      if (!ok) break;
+      tc::tc_fence_after();
+      uint32_t t0[32], t1[32];
+      tc::tmem_ld32(tb + lb + tcol_o(lc), t0);
+      tc::tmem_ld32(tb + lb + tcol_o(lc) + 32, t1);
+      tc::tmem_ld_wait_on(t0);
+      tc::tmem_ld_wait_on(t1);
+      const ChunkMeta mt = *reinterpret_cast<const ChunkMeta *>(st + kOffMeta);
+      const Scales sc = scs[s];
+      // (1) R (fp16, * 2^-rr) as K-major rows, and its row sums.
+      if (lane < 16) {
+        const int i = q * 16 + lane;  // M=64 accumulator: row i in lane 32(i/16) + i%16
+        const float ginvL = expf(-(float)L * lng);
+        // R_ij = T_ij 2^(aq+bk) gamma^-L on the causal triangle (j <= i < L).
+        const float tsc = exp2f((float)(mt.qexp + mt.kexp)) * ginvL;
+        const float k1 = tsc * exp2f((float)-sc.rr);
+        const float2 k2 = make_float2(k1, k1);
+        const int lim = i < L ? i : -1;  // last unmasked column of the row
+        float2 xs = make_float2(0.f, 0.f);
 #pragma unroll
-          for (int cc = 0; cc < 8; ++cc) {
+        for (int cc = 0; cc < 8; ++cc) {
+          uint32_t w[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int j = cc * 8 + 2 * e;
+            float2 x = make_float2(__uint_as_float(j < 32 ? t0[j] : t1[j - 32]),
+                                   __uint_as_float(j + 1 < 32 ? t0[j + 1] : t1[j + 1 - 32]));
+            x.x = j <= lim ? x.x : 0.f;
+            x.y = j + 1 <= lim ? x.y : 0.f;
+            xs = tc::add2(xs, x);
+            const float2 r = tc::mul2(x, k2);
+            w[e] = tc::pack_f16(r.x, r.y);
+          }
+          *reinterpret_cast<uint4 *>(sm + kOffR + tc::sw128_off(i, cc)) =
+              make_uint4(w[0], w[1], w[2], w[3]);
+        }
+        rsm[i] = (xs.x + xs.y) * tsc;
+      }
+      if (et == 0) oss[s] = exp2f((float)sc.E);
+      tc::fence_proxy_async_smem();
+      tc::tc_fence_before();  // the scores are read; O^T may overwrite them
+      grp_sync(G);
+      if (et == 0) tc::mbar_arrive(&bars[RRDY]);
+      // (2) row factors f(n) = s1 s2(n) r(n).  The third normalisation adds
+      // gamma^(i+1) s1 s2(n) Q_i . z_c to the row sum: Q'_i . z_c, two
+      // threads per row.
+      {
+        const int i = et >> 1, half = et & 1;
+        float qz = 0.f;
+        if (rsum) {
+          float2 p01 = make_float2(0.f, 0.f), p23 = p01, p45 = p01, p67 = p01;
+          for (int t = 0; t < NKB * 4; ++t) {
+            const int kb = t >> 2, cc = (t & 3) + 4 * half;
             const uint4 u =
                 *reinterpret_cast<const uint4 *>(st + kOffQ + kb * 8192 + tc::sw128_off(i, cc));
             const float4 z0 = *reinterpret_cast<const float4 *>(zsm + kb * 64 + cc * 8);
             const float4 z1 = *reinterpret_cast<const float4 *>(zsm + kb * 64 + cc * 8 + 4);
             const float2 a0 = h2f(u.x), a1 = h2f(u.y), a2 = h2f(u.z), a3 = h2f(u.w);
-            acc[0] = fmaf(a0.x, z0.x, fmaf(a0.y, z0.y, acc[0]));
-            acc[1] = fmaf(a1.x, z0.z, fmaf(a1.y, z0.w, acc[1]));
-            acc[2] = fmaf(a2.x, z1.x, fmaf(a2.y, z1.y, acc[2]));
-            acc[3] = fmaf(a3.x, z1.z, fmaf(a3.y, z1.w, acc[3]));
+            p01 = tc::fma2(a0, make_float2(z0.x, z0.y), p01);
+            p23 = tc::fma2(a1, make_float2(z0.z, z0.w), p23);
+            p45 = tc::fma2(a2, make_float2(z1.x, z1.y), p45);
+            p67 = tc::fma2(a3, make_float2(z1.z, z1.w), p67);
           }
-        qzs[s * 64 + i] = ((acc[0] + acc[1]) + (acc[2] + acc[3])) *
-                          exp2f((float)reinterpret_cast<const ChunkMeta *>(st + kOffMeta)->qexp);
-        grp_sync(G, NT);
-        if (ht == 0) tc::mbar_arrive(&bars[QZRDY0 + s]);
-      }
-      // (3) z_{c+1} = gamma^L z_c + sum_j K'_j (column sums from the prologue).
-      if (a.need_z) {
-        const int L = min(kC, N - c * kC);
-        const float gL = gpow(lng, L);
-        const float *ks = reinterpret_cast<const float *>(st + kOffKs);
-        for (int k2 = ht; k2 < DK; k2 += NT) zsm[k2] = fmaf(gL, zsm[k2], ks[k2]);
-      }
-      grp_sync(G, NT);
-      if (ht == 0) tc::mbar_arrive(&bars[EMPTY0 + s]);
-    }
-    if (ok && a.z_out && rank == 0 && last_seg)
-      for (int k2 = ht; k2 < DK; k2 += NT) a.z_out[(long long)bh * DK + k2] = zsm[k2];
-  } else if (warp >= 4 && warp < 8) {
-    // ------------------------------------------------------------ state group
-    const int G = 1;
-    const int q = warp & 3;                 // TMEM lane quarter
-    const int et = tid - 128;               // 0..127
-    const int vrow = q * 32 + lane;
-    const uint32_t lb = (uint32_t)(q * 32) << 16;
-    const long long vglob = v0 + vrow;
-    const bool rsum = (p.norm_flags & RET_NORM_RSUM) != 0;
-    float *rd = red;
-    int rslot = 0;
-    bool ok = true;
-    // Entry state (S_in, or for a later segment the decayed sum of S_in and
-    // the pieces before it) goes to the TMEM state columns; s_bound = max |S|.
-    const bool has_state = a.S_in != nullptr || npc > 0;
-    float m0 = 0.f;
-    if (has_state) {
-      const float w_in = seg > 0 ? gpow(lng, kC * c0) : 1.f;
-      for (int g = 0; g < DK / 32; ++g) {
-        uint32_t r[32];
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const long long e = ((long long)bh * DK + g * 32 + i) * p.dv + vglob;
-          r[i] = __float_as_uint(a.S_in ? w_in * a.S_in[e] : 0.f);
+          const float2 ps = tc::add2(tc::add2(p01, p23), tc::add2(p45, p67));
+          qz = ps.x + ps.y;
+          qz += __shfl_xor_sync(0xffffffffu, qz, 1);
+          qz *= exp2f((float)mt.qexp);
         }
-        for (int pi = 0; pi < npc; ++pi) {
-          const float w = gpow(lng, kC * (c0 - (pi + 1) * a.piece_len));
-          const float *src = a.Part + (long long)pi * p.B * p.H * DK * p.dv;
-#pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const long long e = ((long long)bh * DK + g * 32 + i) * p.dv + vglob;
-            r[i] = __float_as_uint(fmaf(w, src[e], __uint_as_float(r[i])));
-          }
-        }
-#pragma unroll
-        for (int i = 0; i < 32; ++i) m0 = fmaxf(m0, fabsf(__uint_as_float(r[i])));
-        tc::tmem_st32(tb + lb + kTS + g * 32, r);
-      }
-      tc::tmem_st_wait();
-    }
-    float s_bound = grp_max(G, m0, rd, rslot, et);
-    int sigma = 0;  // TMEM state holds S * 2^-sigma
-    for (int lc = 0; lc < ncl && ok; ++lc) {
-      const int s = lc & 1, c = c0 + lc;
-      const int L = min(kC, N - c * kC);
-      const float gL = gpow(lng, L);
-      const float ginvL = expf(-(float)L * lng);
-      ok = grp_all(G, wait_bar(&bars[VRDY0 + s], (lc >> 1) & 1, abort_p, p.status));
-      if (!ok) break;
-      const ChunkMeta mt = *reinterpret_cast<const ChunkMeta *>(sm + s * kStage + kOffMeta);
-      const int aq = mt.qexp, bk = mt.kexp;
-      const float qmx = mt.qmax, kmx = mt.kmax;
-      const int vx = vxs[s];
-      const float vmx = vmxs[s];
-      // (2) exponents: R and the state copy share the O accumulator's scale.
-      // |R_ij| = gamma^(i-j) |q_i . k_j| <= (d_k/2) max|pair of rot q| max|pair of rot k|
-      // (j <= i; a dot product is a sum of d_k/2 pair products).
-      const int rr_nat = expo14((float)(DK / 2) * qmx * kmx);
-      int E = rr_nat + vx;
-      if (s_bound > 0.f) E = max(E, expo14(s_bound) + aq);
-      const int rr = E - vx, ss = E - aq;
-      const int sigma_next = vx + bk;
-      // (3) R (fp16, * 2^-rr) as K-major rows; row factors.  The scores'
-      // completion (QK) means every earlier MMA is finished: MMA2 of the
-      // previous chunk, the last reader of R, and, through MMA2's wait on
-      // OFREE two chunks back, the output group's reads of slot s.
-      ok = grp_all(G, wait_bar(&bars[QK], lc & 1, abort_p, p.status) &&
-                          (!rsum || wait_bar(&bars[QZRDY0 + s], (lc >> 1) & 1, abort_p, p.status)));
-      if (!ok) break;
-      tc::tc_fence_after();
-      if (et == 0) Esm[s] = E;
-      {
-        uint32_t t0[32], t1[32];
-        tc::tmem_ld32(tb + lb + kTQK, t0);
-        tc::tmem_ld32(tb + lb + kTQK + 32, t1);
-        tc::tmem_ld_wait();
-        if (lane < 16) {
-          const int i = q * 16 + lane;  // M=64 accumulator: row i in lane 32(i/16) + i%16
-          const float tsc = exp2f((float)(aq + bk)) * ginvL;
-          const float rsc = exp2f((float)-rr);
-          float rs = 0.f;
-#pragma unroll
-          for (int cc = 0; cc < 8; ++cc) {
-            uint32_t w[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int j = cc * 8 + 2 * e;
-              const float x0 = __uint_as_float(j < 32 ? t0[j] : t1[j - 32]);
-              const float x1 = __uint_as_float(j + 1 < 32 ? t0[j + 1] : t1[j + 1 - 32]);
-              const float r0 = (j <= i && i < L) ? x0 * tsc : 0.f;
-              const float r1 = (j + 1 <= i && i < L) ? x1 * tsc : 0.f;
-              rs += r0 + r1;
-              w[e] = tc::pack_f16(r0 * rsc, r1 * rsc);
-            }
-            *reinterpret_cast<uint4 *>(sm + kOffR + tc::sw128_off(i, cc)) =
-                make_uint4(w[0], w[1], w[2], w[3]);
-          }
+        if (half == 0) {
           float f = 0.f;
           if (i < L) {
-            if (rsum) rs += qzs[s * 64 + i];
             const float sn = row_scale(p, h, p.pos0 + (long long)c * kC + i + 1);
-            f = sn * rsum_scale(p, sn * rs);
+            f = sn * rsum_scale(p, sn * (rsm[i] + qz));
           }
           fsm[s * 64 + i] = f;
         }
       }
-      tc::fence_proxy_async_smem();
-      tc::tc_fence_before();
       grp_sync(G);
-      if (et == 0) tc::mbar_arrive(&bars[RRDY]);
-      // (4) state pass: fp16 copy of S_c * 2^-ss; S_acc <- gamma^L S_c * 2^-sigma_next
-      if (lc > 0) {
-        ok = grp_all(G, wait_bar(&bars[SFULL], (lc - 1) & 1, abort_p, p.status));
+      if (et == 0) tc::mbar_arrive(&bars[FRDY0 + s]);
+      // (3) z_{c+1} = gamma^L z_c + sum_j K'_j (column sums from the prologue).
+      if (a.need_z) {
+        const float gL = gpow(lng, L);
+        const float *ks = reinterpret_cast<const float *>(st + kOffKs);
+        for (int k2 = et; k2 < DK; k2 += 128) zsm[k2] = fmaf(gL, zsm[k2], ks[k2]);
+      }
+      grp_sync(G);
+      if (et == 0) tc::mbar_arrive(&bars[EMPTY0 + s]);  // done with Q' and the key sums
+    }
+    if (ok && a.z_out && rank == 0 && last_seg)
+      for (int k2 = et; k2 < DK; k2 += 128) a.z_out[(long long)bh * DK + k2] = zsm[k2];
+  } else if (warp >= 8 && warp < 12) {
+    // ------------------------------------------------------------ state group
+    const int G = 1;
+    const int q = warp & 3;                 // TMEM lane quarter
+    const int et = tid - 256;               // 0..127
+    const int vrow = q * 32 + lane;
+    const uint32_t lb = (uint32_t)(q * 32) << 16;
+    const long long vglob = v0 + vrow;
+    float *rd = red + 16;
+    int rslot = 0;
+    bool ok = true;
+    // Entry state (S_in, or for a later segment the decayed sum of S_in and
+    // the pieces before it) goes to the TMEM state columns; its max |S| is
+    // the helper's first state bound.
+    const bool has_state = a.S_in != nullptr || npc > 0;
+    const float m0 = has_state ? load_entry_state(p, a, tb + lb + kTS, bh, vglob, seg, c0, npc, lng)
+                               : 0.f;
+    {
+      const float sb = grp_max(G, m0, rd, rslot, et);
+      if (et == 0) {
+        vmxs[1] = sb;
+        tc::mbar_arrive(&bars[SB0]);
+      }
+    }
+    int sigma = 0;  // TMEM state holds S * 2^-sigma
+    // d_k = 256 runs in two halves of 128 columns, each handed to the MMA
+    // thread as soon as it is done (SRDY0/SRDY1), and each refreshed for the
+    // next chunk as soon as the MMAs of its half are done (SFULL0/SFULL1).
+    const int nh = DK == 256 ? 2 : 1;
+    const int gh = DK / 32 / nh;  // 32-column blocks per half (even)
+    for (int lc = 0; lc < ncl && ok; ++lc) {
+      const int s = lc & 1;
+      Scales sc;
+      for (int hh = 0; hh < nh && ok; ++hh) {
+        const int sf = nh == 1 ? SFULL1 : SFULL0 + hh;
+        ok = grp_all(G, (hh > 0 || wait_bar(&bars[VRDY0 + s], (lc >> 1) & 1, abort_p, p.status)) &&
+                            (lc == 0 || wait_bar(&bars[sf], (lc - 1) & 1, abort_p, p.status)));
         if (!ok) break;
         tc::tc_fence_after();
-      }
-      {
-        const float f_cp = exp2f((float)(sigma - ss));
-        const float f_pre = gL * exp2f((float)(sigma - sigma_next));
-        for (int g0 = 0; g0 < DK / 32; g0 += 2) {
-          uint32_t r[2][32];
-          if (lc == 0 && !has_state) {
+        if (hh == 0) sc = scs[s];
+        // fp16 copy of S_c * 2^-ss for the cross term; S_acc <- gamma^L S_c *
+        // 2^-sigma_next.  The loads of the next 32 columns overlap the work
+        // on the current ones.
+        const int g0 = hh * gh, g1 = g0 + gh;
+        if (lc == 0 && !has_state) {
+          uint32_t z32[32], z16[16];
 #pragma unroll
-            for (int hh = 0; hh < 2; ++hh)
+          for (int i = 0; i < 32; ++i) z32[i] = 0u;
 #pragma unroll
-              for (int i = 0; i < 32; ++i) r[hh][i] = 0u;
-          } else {
-            tc::tmem_ld32(tb + lb + kTS + g0 * 32, r[0]);
-            tc::tmem_ld32(tb + lb + kTS + g0 * 32 + 32, r[1]);
-            tc::tmem_ld_wait();
+          for (int i = 0; i < 16; ++i) z16[i] = 0u;
+          for (int g = g0; g < g1; ++g) {
+            tc::tmem_st16(tb + lb + kTSh + g * 16, z16);
+            tc::tmem_st32(tb + lb + kTS + g * 32, z32);
           }
+        } else {
+          const float2 fcp2 = make_float2(sc.f_cp, sc.f_cp), fpre2 = make_float2(sc.f_pre, sc.f_pre);
+          uint32_t ra[32], rb[32];
+          tc::tmem_ld32(tb + lb + kTS + g0 * 32, ra);
+          for (int g = g0; g < g1; g += 2) {
+            tc::tmem_ld_wait_on(ra);
+            tc::tmem_ld32(tb + lb + kTS + (g + 1) * 32, rb);
+            {
+              uint32_t pk[16];
 #pragma unroll
-          for (int hh = 0; hh < 2; ++hh) {
-            uint32_t pk[16];
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              const float x0 = __uint_as_float(r[hh][2 * i]), x1 = __uint_as_float(r[hh][2 * i + 1]);
-              pk[i] = tc::pack_f16(x0 * f_cp, x1 * f_cp);
+              for (int i = 0; i < 16; ++i) {
+                const float2 x = make_float2(__uint_as_float(ra[2 * i]), __uint_as_float(ra[2 * i + 1]));
+                const float2 y = tc::mul2(x, fcp2);
+                pk[i] = tc::pack_f16(y.x, y.y);
+                const float2 w = tc::mul2(x, fpre2);
+                ra[2 * i] = __float_as_uint(w.x);
+                ra[2 * i + 1] = __float_as_uint(w.y);
+              }
+              tc::tmem_st16(tb + lb + kTSh + g * 16, pk);
+              tc::tmem_st32(tb + lb + kTS + g * 32, ra);
             }
-            tc::tmem_st16(tb + lb + kTSh + (g0 + hh) * 16, pk);
+            tc::tmem_ld_wait_on(rb);
+            if (g + 2 < g1) tc::tmem_ld32(tb + lb + kTS + (g + 2) * 32, ra);
+            {
+              uint32_t pk[16];
 #pragma unroll
-            for (int i = 0; i < 32; ++i) r[hh][i] = __float_as_uint(__uint_as_float(r[hh][i]) * f_pre);
-            tc::tmem_st32(tb + lb + kTS + (g0 + hh) * 32, r[hh]);
+              for (int i = 0; i < 16; ++i) {
+                const float2 x = make_float2(__uint_as_float(rb[2 * i]), __uint_as_float(rb[2 * i + 1]));
+                const float2 y = tc::mul2(x, fcp2);
+                pk[i] = tc::pack_f16(y.x, y.y);
+                const float2 w = tc::mul2(x, fpre2);
+                rb[2 * i] = __float_as_uint(w.x);
+                rb[2 * i + 1] = __float_as_uint(w.y);
+              }
+              tc::tmem_st16(tb + lb + kTSh + (g + 1) * 16, pk);
+              tc::tmem_st32(tb + lb + kTS + (g + 1) * 32, rb);
+            }
           }
         }
         tc::tmem_st_wait();
+        tc::tc_fence_before();
+        grp_sync(G);
+        if (et == 0) tc::mbar_arrive(&bars[SRDY0 + hh]);
       }
-      tc::tc_fence_before();
-      grp_sync(G);
-      if (et == 0) tc::mbar_arrive(&bars[SRDY]);
-      // Upper bound of max |S_{c+1}|: |S_{c+1}| <= gamma^L |S_c| + sum_j |K'_j||V_j|
-      // with zeta <= 1 (a pair norm bounds each component of its pair).  It is
-      // loose by the ratio of a sum of L terms to their random-sign size,
-      // which costs nothing in floating point.
-      s_bound = gL * s_bound + (float)L * kmx * vmx;
-      sigma = sigma_next;
+      sigma = sc.sigma_next;
     }
     if (ok && a.S_out && last_seg) {
-      ok = grp_all(G, wait_bar(&bars[SFULL], (ncl - 1) & 1, abort_p, p.status));
+      ok = grp_all(G, wait_bar(&bars[SFULL1], (ncl - 1) & 1, abort_p, p.status));
       if (ok) {
         tc::tc_fence_after();
-        const float back = exp2f((float)sigma);
-        for (int g = 0; g < DK / 32; ++g) {
-          uint32_t r[32];
-          tc::tmem_ld32(tb + lb + kTS + g * 32, r);
-          tc::tmem_ld_wait();
-#pragma unroll
-          for (int i = 0; i < 32; ++i)
-            a.S_out[((long long)bh * DK + g * 32 + i) * p.dv + vglob] = __uint_as_float(r[i]) * back;
-        }
+        store_state(p, a.S_out, tb + lb + kTS, bh, vglob, exp2f((float)sigma));
       }
     }
-  } else if (warp >= 8) {
+  } else if (warp >= 12) {
     // ------------------------------------------------------------ output group
     const int G = 2;
     const int q = warp & 3;
-    const int et = tid - 256;  // 0..127
+    const int et = tid - 384;  // 0..127
     const int vrow = q * 32 + lane;
     const uint32_t lb = (uint32_t)(q * 32) << 16;
     const bool gn = p.gn_eps >= 0.f;
-    // Statistics: 4 threads per token, interleaved columns (conflict-free
-    // with a row pitch of 132 floats); 32 tokens per pass, two passes.
+    // Statistics: 4 threads per token, each reading eight 16-byte column
+    // groups (conflict-free with a row pitch of 144 floats); 32 tokens per
+    // pass, two passes.
     const int sq4 = et & 3, st0 = et >> 2;
+    const float inv_nv = 1.f / (float)NV;
     bool ok = true;
     for (int lc = 0; lc < ncl && ok; ++lc) {
       const int s = lc & 1, c = c0 + lc;
       const int L = min(kC, N - c * kC);
-      ok = grp_all(G, wait_bar(&bars[OFULL], lc & 1, abort_p, p.status));
+      ok = grp_all(G, wait_bar(&bars[OFULL0 + s], (lc >> 1) & 1, abort_p, p.status) &&
+                          wait_bar(&bars[FRDY0 + s], (lc >> 1) & 1, abort_p, p.status));
       if (!ok) break;
       tc::tc_fence_after();
-      const float osc = exp2f((float)Esm[s]);
+      // Per-chunk factors are read before OFREE: the R group rewrites them
+      // for chunk lc+2 only after the scores of lc+2, which go to this O^T
+      // buffer after OFREE.
+      const float osc = oss[s];
+      const float osc_inv = 1.f / osc;
       float fr[2];
       fr[0] = fsm[s * 64 + st0];
       fr[1] = fsm[s * 64 + st0 + 32];
       {
         uint32_t t0[32], t1[32];
-        tc::tmem_ld32(tb + lb + kTO, t0);
-        tc::tmem_ld32(tb + lb + kTO + 32, t1);
-        tc::tmem_ld_wait();
+        tc::tmem_ld32(tb + lb + tcol_o(lc), t0);
+        tc::tmem_ld32(tb + lb + tcol_o(lc) + 32, t1);
+        tc::tmem_ld_wait_on(t0);
+        tc::tmem_ld_wait_on(t1);
+        tc::tc_fence_before();
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
           OT[i * kOTPitch + vrow] = __uint_as_float(t0[i]);
           OT[(32 + i) * kOTPitch + vrow] = __uint_as_float(t1[i]);
         }
       }
-      tc::tc_fence_before();
       grp_sync(G);
-      if (et == 0) tc::mbar_arrive(&bars[OFREE]);
+      if (et == 0) tc::mbar_arrive(&bars[OFREE0 + s]);
       float mloc[2], M2loc[2];
 #pragma unroll
       for (int pass = 0; pass < 2; ++pass) {
-        const float *row = OT + (st0 + 32 * pass) * kOTPitch + sq4;
-        float sm0 = 0.f, sm1 = 0.f;
+        const float4 *row =
+            reinterpret_cast<const float4 *>(OT + (st0 + 32 * pass) * kOTPitch) + sq4;
+        float4 x[8];
 #pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          sm0 += row[4 * e];
-          sm1 += row[4 * e + 4];
-        }
-        float m = sm0 + sm1;
-        m += __shfl_xor_sync(0xffffffffu, m, 1);
-        m += __shfl_xor_sync(0xffffffffu, m, 2);
-        m *= (1.f / kW);
-        float q0 = 0.f, q1 = 0.f;
+        for (int m = 0; m < 8; ++m) x[m] = row[4 * m];
+        float sa = 0.f, sb = 0.f;
 #pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          const float d0 = row[4 * e] - m, d1 = row[4 * e + 4] - m;
-          q0 = fmaf(d0, d0, q0);
-          q1 = fmaf(d1, d1, q1);
+        for (int m = 0; m < 8; ++m) {
+          sa += x[m].x + x[m].y;
+          sb += x[m].z + x[m].w;
         }
-        float M2 = q0 + q1;
+        float mu = sa + sb;
+        mu += __shfl_xor_sync(0xffffffffu, mu, 1);
+        mu += __shfl_xor_sync(0xffffffffu, mu, 2);
+        mu *= (1.f / kW);
+        float qa = 0.f, qb = 0.f;
+#pragma unroll
+        for (int m = 0; m < 8; ++m) {
+          const float d0 = x[m].x - mu, d1 = x[m].y - mu, d2 = x[m].z - mu, d3 = x[m].w - mu;
+          qa = fmaf(d0, d0, fmaf(d1, d1, qa));
+          qb = fmaf(d2, d2, fmaf(d3, d3, qb));
+        }
+        float M2 = qa + qb;
         M2 += __shfl_xor_sync(0xffffffffu, M2, 1);
         M2 += __shfl_xor_sync(0xffffffffu, M2, 2);
-        mloc[pass] = m * osc;  // O^T holds O * 2^-E; osc = 2^E
+        mloc[pass] = mu * osc;  // O^T holds O * 2^-E; osc = 2^E
         M2loc[pass] = M2 * osc * osc;
       }
       float mean[2] = {mloc[0], mloc[1]};
@@ -686,25 +848,33 @@ chunk_tc_kernel(const __grid_constant__ KParams p, const __grid_constant__ CUten
 #pragma unroll
           for (int pass = 0; pass < 2; ++pass) {
             const float *slot = gns + ((par * 8 + rank) * 64 + st0 + 32 * pass) * 2;
-            for (int r2 = 0; r2 < NV; ++r2)
-              tc::st_async_v2(slot, &bars[GN0 + par], r2, mloc[pass], M2loc[pass]);
+#pragma unroll
+            for (int r2 = 0; r2 < 8; ++r2)
+              if (r2 < NV) tc::st_async_v2(slot, &bars[GN0 + par], r2, mloc[pass], M2loc[pass]);
           }
         ok = grp_all(G, wait_bar_cluster(&bars[GN0 + par], (lc >> 1) & 1, abort_p, p.status));
         if (!ok) break;
+        // Chan's merge of the NV partial (mean, M2) pairs of kW columns each.
 #pragma unroll
         for (int pass = 0; pass < 2; ++pass) {
           const int ti = st0 + 32 * pass;
+          float2 pr[8];
+#pragma unroll
+          for (int r2 = 0; r2 < 8; ++r2)
+            pr[r2] = r2 < NV ? *reinterpret_cast<const float2 *>(gns + ((par * 8 + r2) * 64 + ti) * 2)
+                             : make_float2(0.f, 0.f);
           float msum = 0.f;
-          for (int r2 = 0; r2 < NV; ++r2) msum += gns[((par * 8 + r2) * 64 + ti) * 2];
-          const float mu = msum / NV;
+#pragma unroll
+          for (int r2 = 0; r2 < 8; ++r2) msum += pr[r2].x;
+          const float mu = msum * inv_nv;
           float M2t = 0.f;
-          for (int r2 = 0; r2 < NV; ++r2) {
-            const float *sl = gns + ((par * 8 + r2) * 64 + ti) * 2;
-            const float d = sl[0] - mu;
-            M2t += sl[1] + (float)kW * d * d;
+#pragma unroll
+          for (int r2 = 0; r2 < 8; ++r2) {
+            const float d = pr[r2].x - mu;
+            M2t += r2 < NV ? pr[r2].y + (float)kW * d * d : 0.f;
           }
           mean[pass] = mu;
-          var[pass] = M2t / (float)(kW * NV);
+          var[pass] = M2t * (inv_nv * (1.f / kW));
         }
       }
       // GroupNorm of x = f o: y = (o - mean) f / sqrt(f^2 var + eps); no
@@ -714,48 +884,66 @@ chunk_tc_kernel(const __grid_constant__ KParams p, const __grid_constant__ CUten
 #pragma unroll
         for (int pass = 0; pass < 2; ++pass) {
           const float f = fr[pass];
-          nrm[(st0 + 32 * pass) * 2] = gn ? mean[pass] / osc : 0.f;
+          nrm[(st0 + 32 * pass) * 2] = gn ? mean[pass] * osc_inv : 0.f;
           nrm[(st0 + 32 * pass) * 2 + 1] =
               (gn ? f * rsqrtf(f * f * var[pass] + p.gn_eps) : f) * osc;
         }
       grp_sync(G);
       // Stores: warp q writes token rows 2q + 8k and 2q + 8k + 1; half-warp
-      // per row, 8 columns per lane (one 16-byte bf16 store).
+      // per row, lane l of the half takes columns [4l, 4l+4) and
+      // [64+4l, 64+4l+4) (conflict-free shared-memory reads, 128 contiguous
+      // output bytes per quarter-warp).
       {
-        const int rsel = lane >> 4, col = 8 * (lane & 15);
+        const int rsel = lane >> 4, l4 = 4 * (lane & 15);
         const long long rstride = 8 * p.so[2];
-        long long ob = b * p.so[0] + h * p.so[1] + ((long long)c * kC + 2 * q + rsel) * p.so[2] +
-                       v0 + col;
-        long long gb = b * a.gate.s[0] + h * a.gate.s[1] +
-                       ((long long)c * kC + 2 * q + rsel) * a.gate.s[2] + v0 + col;
+        const long long grstride = 8 * a.gate.s[2];
+        const long long ob0 = b * p.so[0] + h * p.so[1] +
+                              ((long long)c * kC + 2 * q + rsel) * p.so[2] + v0 + l4;
+        const long long gb0 = b * a.gate.s[0] + h * a.gate.s[1] +
+                              ((long long)c * kC + 2 * q + rsel) * a.gate.s[2] + v0 + l4;
 #pragma unroll 2
-        for (int it = 0; it < 8; ++it, ob += rstride, gb += 8 * a.gate.s[2]) {
+        for (int it = 0; it < 8; ++it) {
           const int ti = 2 * q + 8 * it + rsel;
           if (ti < L) {
-            const float shift = nrm[ti * 2], scale = nrm[ti * 2 + 1];
-            const float4 x0 = *reinterpret_cast<const float4 *>(OT + ti * kOTPitch + col);
-            const float4 x1 = *reinterpret_cast<const float4 *>(OT + ti * kOTPitch + col + 4);
-            float y[8] = {(x0.x - shift) * scale, (x0.y - shift) * scale, (x0.z - shift) * scale,
-                          (x0.w - shift) * scale, (x1.x - shift) * scale, (x1.y - shift) * scale,
-                          (x1.z - shift) * scale, (x1.w - shift) * scale};
-            if (a.gate.ptr) {
+            const float2 ns = *reinterpret_cast<const float2 *>(nrm + ti * 2);
+            const float2 sh2 = make_float2(-ns.x, -ns.x), sc2 = make_float2(ns.y, ns.y);
 #pragma unroll
-              for (int e = 0; e < 8; ++e) {
-                const float g = ld_elem(a.gate.ptr, gb + e, 1);
-                y[e] *= g / (1.f + expf(-g));
+            for (int part = 0; part < 2; ++part) {
+              const long long ob = ob0 + it * rstride + 64 * part;
+              const long long gb = gb0 + it * grstride + 64 * part;
+              const float4 x = *reinterpret_cast<const float4 *>(OT + ti * kOTPitch + l4 + 64 * part);
+              float2 y0 = tc::mul2(tc::add2(make_float2(x.x, x.y), sh2), sc2);
+              float2 y1 = tc::mul2(tc::add2(make_float2(x.z, x.w), sh2), sc2);
+              if (kStore == kStoreBf16Gate || (kStore == kStoreAny && a.gate.ptr)) {
+                float g[4];
+                if (kStore == kStoreBf16Gate) {
+                  const uint2 u = *reinterpret_cast<const uint2 *>(
+                      reinterpret_cast<const __nv_bfloat16 *>(a.gate.ptr) + gb);
+                  g[0] = bf_lo(u.x);
+                  g[1] = bf_hi(u.x);
+                  g[2] = bf_lo(u.y);
+                  g[3] = bf_hi(u.y);
+                } else {
+#pragma unroll
+                  for (int e = 0; e < 4; ++e) g[e] = ld_elem(a.gate.ptr, gb + e, 1);
+                }
+                y0.x *= g[0] / (1.f + expf(-g[0]));
+                y0.y *= g[1] / (1.f + expf(-g[1]));
+                y1.x *= g[2] / (1.f + expf(-g[2]));
+                y1.y *= g[3] / (1.f + expf(-g[3]));
               }
-            }
-            if (a.vec_out && p.out_bf16) {
-              *reinterpret_cast<uint4 *>(reinterpret_cast<__nv_bfloat16 *>(a.o) + ob) =
-                  make_uint4(tc::pack_bf16(y[0], y[1]), tc::pack_bf16(y[2], y[3]),
-                             tc::pack_bf16(y[4], y[5]), tc::pack_bf16(y[6], y[7]));
-            } else if (a.vec_out) {
-              float4 *dst = reinterpret_cast<float4 *>(reinterpret_cast<float *>(a.o) + ob);
-              dst[0] = make_float4(y[0], y[1], y[2], y[3]);
-              dst[1] = make_float4(y[4], y[5], y[6], y[7]);
-            } else {
-#pragma unroll
-              for (int e = 0; e < 8; ++e) st_elem(a.o, ob + e, y[e], p.out_bf16);
+              if (kStore != kStoreAny || (a.vec_out && p.out_bf16)) {
+                *reinterpret_cast<uint2 *>(reinterpret_cast<__nv_bfloat16 *>(a.o) + ob) =
+                    make_uint2(tc::pack_bf16(y0.x, y0.y), tc::pack_bf16(y1.x, y1.y));
+              } else if (a.vec_out) {
+                *reinterpret_cast<float4 *>(reinterpret_cast<float *>(a.o) + ob) =
+                    make_float4(y0.x, y0.y, y1.x, y1.y);
+              } else {
+                st_elem(a.o, ob, y0.x, p.out_bf16);
+                st_elem(a.o, ob + 1, y0.y, p.out_bf16);
+                st_elem(a.o, ob + 2, y1.x, p.out_bf16);
+                st_elem(a.o, ob + 3, y1.y, p.out_bf16);
+              }
             }
           }
         }
@@ -829,8 +1017,14 @@ cudaError_t launch_chunk_tc(const KParams &p, const void *Qp, const void *Kp, co
   const uintptr_t abytes = 16;
   a.vec_out = (reinterpret_cast<uintptr_t>(o) % abytes == 0) && p.so[0] % al == 0 &&
               p.so[1] % al == 0 && p.so[2] % al == 0;
-  cudaError_t e = cudaFuncSetAttribute(chunk_tc_kernel,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  a.vec_gate = gate.ptr && (reinterpret_cast<uintptr_t>(gate.ptr) % abytes == 0) &&
+               gate.s[0] % 8 == 0 && gate.s[1] % 8 == 0 && gate.s[2] % 8 == 0;
+  const bool bf16vec = a.vec_out && p.out_bf16;
+  void (*kern)(KParams, CUtensorMap, CUtensorMap, CUtensorMap, TcArgs) =
+      bf16vec && !gate.ptr                 ? chunk_tc_kernel<kStoreBf16>
+      : bf16vec && gate.ptr && a.vec_gate  ? chunk_tc_kernel<kStoreBf16Gate>
+                                           : chunk_tc_kernel<kStoreAny>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(P * BH * a.NV));
@@ -844,7 +1038,7 @@ cudaError_t launch_chunk_tc(const KParams &p, const void *Qp, const void *Kp, co
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, chunk_tc_kernel, p, tq, tk, tv, a);
+  return cudaLaunchKernelEx(&cfg, kern, p, tq, tk, tv, a);
 }
 
 }  // namespace ret
