@@ -73,8 +73,7 @@ constexpr uint32_t kOffOS = kOffF + 2 * 64 * 4;         // [2] fp32 2^E for the 
 constexpr uint32_t kOffSc = kOffOS + 16;                // [2] Scales (helper -> R, state)
 constexpr uint32_t kOffRed = kOffSc + 2 * 32;           // [4 groups][8] fp32 scratch
 constexpr uint32_t kOffGN = kOffRed + 128;              // [2][8][64][2] fp32
-constexpr uint32_t kOffNrm = kOffGN + 2 * 8 * 64 * 2 * 4;  // [64][2] fp32 shift, scale
-constexpr uint32_t kOffVX = kOffNrm + 64 * 2 * 4;          // [2] float max|V|, s_bound entry
+constexpr uint32_t kOffVX = kOffGN + 2 * 8 * 64 * 2 * 4;   // [2] float max|V|, s_bound entry
 constexpr uint32_t kOffQZ = kOffVX + 16;                   // [64] fp32 R row sums, scratch
 constexpr uint32_t kOffBar = kOffQZ + 2 * 64 * 4;
 constexpr int kNumBars = 27;
@@ -291,7 +290,6 @@ chunk_tc_kernel(const __grid_constant__ KParams p, const __grid_constant__ CUten
   float *red = reinterpret_cast<float *>(sm + kOffRed);
   float *OT = reinterpret_cast<float *>(sm + kOffOT);
   float *gns = reinterpret_cast<float *>(sm + kOffGN);
-  float *nrm = reinterpret_cast<float *>(sm + kOffNrm);
   float *vmxs = reinterpret_cast<float *>(sm + kOffVX);  // [0] max|V| scratch, [1] entry bound
   float *qzs = reinterpret_cast<float *>(sm + kOffQZ);
 
@@ -805,32 +803,39 @@ chunk_tc_kernel(const __grid_constant__ KParams p, const __grid_constant__ CUten
       }
       grp_sync(G);
       if (et == 0) tc::mbar_arrive(&bars[OFREE0 + s]);
+      // Each thread keeps its 2 x 32 values (tokens st0 and st0+32, column
+      // groups 4(sq4 + 4m)) in registers for the statistics and the stores.
+      float4 x[2][8];
       float mloc[2], M2loc[2];
 #pragma unroll
       for (int pass = 0; pass < 2; ++pass) {
         const float4 *row =
             reinterpret_cast<const float4 *>(OT + (st0 + 32 * pass) * kOTPitch) + sq4;
-        float4 x[8];
 #pragma unroll
-        for (int m = 0; m < 8; ++m) x[m] = row[4 * m];
-        float sa = 0.f, sb = 0.f;
+        for (int m = 0; m < 8; ++m) x[pass][m] = row[4 * m];
+      }
+      grp_sync(G);  // OT may be refilled by the next chunk's drain
 #pragma unroll
-        for (int m = 0; m < 8; ++m) {
-          sa += x[m].x + x[m].y;
-          sb += x[m].z + x[m].w;
-        }
-        float mu = sa + sb;
+      for (int pass = 0; pass < 2; ++pass) {
+        float2 sab = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int m = 0; m < 8; ++m)
+          sab = tc::add2(sab, tc::add2(make_float2(x[pass][m].x, x[pass][m].y),
+                                       make_float2(x[pass][m].z, x[pass][m].w)));
+        float mu = sab.x + sab.y;
         mu += __shfl_xor_sync(0xffffffffu, mu, 1);
         mu += __shfl_xor_sync(0xffffffffu, mu, 2);
         mu *= (1.f / kW);
-        float qa = 0.f, qb = 0.f;
+        const float2 nmu = make_float2(-mu, -mu);
+        float2 q2 = make_float2(0.f, 0.f);
 #pragma unroll
         for (int m = 0; m < 8; ++m) {
-          const float d0 = x[m].x - mu, d1 = x[m].y - mu, d2 = x[m].z - mu, d3 = x[m].w - mu;
-          qa = fmaf(d0, d0, fmaf(d1, d1, qa));
-          qb = fmaf(d2, d2, fmaf(d3, d3, qb));
+          const float2 d0 = tc::add2(make_float2(x[pass][m].x, x[pass][m].y), nmu);
+          const float2 d1 = tc::add2(make_float2(x[pass][m].z, x[pass][m].w), nmu);
+          q2 = tc::fma2(d0, d0, q2);
+          q2 = tc::fma2(d1, d1, q2);
         }
-        float M2 = qa + qb;
+        float M2 = q2.x + q2.y;
         M2 += __shfl_xor_sync(0xffffffffu, M2, 1);
         M2 += __shfl_xor_sync(0xffffffffu, M2, 2);
         mloc[pass] = mu * osc;  // O^T holds O * 2^-E; osc = 2^E
@@ -878,73 +883,55 @@ chunk_tc_kernel(const __grid_constant__ KParams p, const __grid_constant__ CUten
         }
       }
       // GroupNorm of x = f o: y = (o - mean) f / sqrt(f^2 var + eps); no
-      // GroupNorm: y = f o.
-      // Stored O^T is O * 2^-E: fold 2^E into the per-token shift and scale.
-      if (sq4 == 0)
+      // GroupNorm: y = f o.  Stored O^T is O * 2^-E: fold 2^E into the
+      // per-token shift and scale.  Each thread stores its own values: for a
+      // column group m, the 4 threads of a token write 16 consecutive
+      // columns (32 bytes of bf16).
 #pragma unroll
-        for (int pass = 0; pass < 2; ++pass) {
-          const float f = fr[pass];
-          nrm[(st0 + 32 * pass) * 2] = gn ? mean[pass] * osc_inv : 0.f;
-          nrm[(st0 + 32 * pass) * 2 + 1] =
-              (gn ? f * rsqrtf(f * f * var[pass] + p.gn_eps) : f) * osc;
-        }
-      grp_sync(G);
-      // Stores: warp q writes token rows 2q + 8k and 2q + 8k + 1; half-warp
-      // per row, lane l of the half takes columns [4l, 4l+4) and
-      // [64+4l, 64+4l+4) (conflict-free shared-memory reads, 128 contiguous
-      // output bytes per quarter-warp).
-      {
-        const int rsel = lane >> 4, l4 = 4 * (lane & 15);
-        const long long rstride = 8 * p.so[2];
-        const long long grstride = 8 * a.gate.s[2];
-        const long long ob0 = b * p.so[0] + h * p.so[1] +
-                              ((long long)c * kC + 2 * q + rsel) * p.so[2] + v0 + l4;
-        const long long gb0 = b * a.gate.s[0] + h * a.gate.s[1] +
-                              ((long long)c * kC + 2 * q + rsel) * a.gate.s[2] + v0 + l4;
-#pragma unroll 2
-        for (int it = 0; it < 8; ++it) {
-          const int ti = 2 * q + 8 * it + rsel;
-          if (ti < L) {
-            const float2 ns = *reinterpret_cast<const float2 *>(nrm + ti * 2);
-            const float2 sh2 = make_float2(-ns.x, -ns.x), sc2 = make_float2(ns.y, ns.y);
+      for (int pass = 0; pass < 2; ++pass) {
+        const int ti = st0 + 32 * pass;
+        if (ti >= L) continue;
+        const float f = fr[pass];
+        const float shift = gn ? mean[pass] * osc_inv : 0.f;
+        const float scale = (gn ? f * rsqrtf(f * f * var[pass] + p.gn_eps) : f) * osc;
+        const float2 sh2 = make_float2(-shift, -shift), sc2 = make_float2(scale, scale);
+        const long long tok = (long long)c * kC + ti;
+        const long long ob0 = b * p.so[0] + h * p.so[1] + tok * p.so[2] + v0 + 4 * sq4;
+        const long long gb0 = b * a.gate.s[0] + h * a.gate.s[1] + tok * a.gate.s[2] + v0 + 4 * sq4;
 #pragma unroll
-            for (int part = 0; part < 2; ++part) {
-              const long long ob = ob0 + it * rstride + 64 * part;
-              const long long gb = gb0 + it * grstride + 64 * part;
-              const float4 x = *reinterpret_cast<const float4 *>(OT + ti * kOTPitch + l4 + 64 * part);
-              float2 y0 = tc::mul2(tc::add2(make_float2(x.x, x.y), sh2), sc2);
-              float2 y1 = tc::mul2(tc::add2(make_float2(x.z, x.w), sh2), sc2);
-              if (kStore == kStoreBf16Gate || (kStore == kStoreAny && a.gate.ptr)) {
-                float g[4];
-                if (kStore == kStoreBf16Gate) {
-                  const uint2 u = *reinterpret_cast<const uint2 *>(
-                      reinterpret_cast<const __nv_bfloat16 *>(a.gate.ptr) + gb);
-                  g[0] = bf_lo(u.x);
-                  g[1] = bf_hi(u.x);
-                  g[2] = bf_lo(u.y);
-                  g[3] = bf_hi(u.y);
-                } else {
+        for (int m = 0; m < 8; ++m) {
+          const long long ob = ob0 + 16 * m, gb = gb0 + 16 * m;
+          float2 y0 = tc::mul2(tc::add2(make_float2(x[pass][m].x, x[pass][m].y), sh2), sc2);
+          float2 y1 = tc::mul2(tc::add2(make_float2(x[pass][m].z, x[pass][m].w), sh2), sc2);
+          if (kStore == kStoreBf16Gate || (kStore == kStoreAny && a.gate.ptr)) {
+            float g[4];
+            if (kStore == kStoreBf16Gate) {
+              const uint2 u = *reinterpret_cast<const uint2 *>(
+                  reinterpret_cast<const __nv_bfloat16 *>(a.gate.ptr) + gb);
+              g[0] = bf_lo(u.x);
+              g[1] = bf_hi(u.x);
+              g[2] = bf_lo(u.y);
+              g[3] = bf_hi(u.y);
+            } else {
 #pragma unroll
-                  for (int e = 0; e < 4; ++e) g[e] = ld_elem(a.gate.ptr, gb + e, 1);
-                }
-                y0.x *= g[0] / (1.f + expf(-g[0]));
-                y0.y *= g[1] / (1.f + expf(-g[1]));
-                y1.x *= g[2] / (1.f + expf(-g[2]));
-                y1.y *= g[3] / (1.f + expf(-g[3]));
-              }
-              if (kStore != kStoreAny || (a.vec_out && p.out_bf16)) {
-                *reinterpret_cast<uint2 *>(reinterpret_cast<__nv_bfloat16 *>(a.o) + ob) =
-                    make_uint2(tc::pack_bf16(y0.x, y0.y), tc::pack_bf16(y1.x, y1.y));
-              } else if (a.vec_out) {
-                *reinterpret_cast<float4 *>(reinterpret_cast<float *>(a.o) + ob) =
-                    make_float4(y0.x, y0.y, y1.x, y1.y);
-              } else {
-                st_elem(a.o, ob, y0.x, p.out_bf16);
-                st_elem(a.o, ob + 1, y0.y, p.out_bf16);
-                st_elem(a.o, ob + 2, y1.x, p.out_bf16);
-                st_elem(a.o, ob + 3, y1.y, p.out_bf16);
-              }
+              for (int e = 0; e < 4; ++e) g[e] = ld_elem(a.gate.ptr, gb + e, 1);
             }
+            y0.x *= g[0] / (1.f + expf(-g[0]));
+            y0.y *= g[1] / (1.f + expf(-g[1]));
+            y1.x *= g[2] / (1.f + expf(-g[2]));
+            y1.y *= g[3] / (1.f + expf(-g[3]));
+          }
+          if (kStore != kStoreAny || (a.vec_out && p.out_bf16)) {
+            *reinterpret_cast<uint2 *>(reinterpret_cast<__nv_bfloat16 *>(a.o) + ob) =
+                make_uint2(tc::pack_bf16(y0.x, y0.y), tc::pack_bf16(y1.x, y1.y));
+          } else if (a.vec_out) {
+            *reinterpret_cast<float4 *>(reinterpret_cast<float *>(a.o) + ob) =
+                make_float4(y0.x, y0.y, y1.x, y1.y);
+          } else {
+            st_elem(a.o, ob, y0.x, p.out_bf16);
+            st_elem(a.o, ob + 1, y0.y, p.out_bf16);
+            st_elem(a.o, ob + 2, y1.x, p.out_bf16);
+            st_elem(a.o, ob + 3, y1.y, p.out_bf16);
           }
         }
       }
