@@ -76,7 +76,7 @@ constexpr uint32_t kOffGN = kOffRed + 128;              // [2][8][64][2] fp32
 constexpr uint32_t kOffVX = kOffGN + 2 * 8 * 64 * 2 * 4;   // [2] float max|V|, s_bound entry
 constexpr uint32_t kOffQZ = kOffVX + 16;                   // [64] fp32 R row sums, scratch
 constexpr uint32_t kOffBar = kOffQZ + 2 * 64 * 4;
-constexpr int kNumBars = 27;
+constexpr int kNumBars = 29;
 constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;
 constexpr uint32_t kSmemBytes = kOffMisc + 16 + 1024;   // + alignment slack
 static_assert(kSmemBytes <= 232448, "shared memory per CTA");
@@ -85,7 +85,7 @@ static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 // so a producer may run one chunk ahead of a consumer without two phases of
 // one barrier completing before the consumer looks.
 enum Bar {
-  FULL0 = 0, FULL1, EMPTY0, EMPTY1, QK0, QK1, RRDY, RFREE, OFULL0, OFULL1, OFREE0, OFREE1,
+  FULLQ0 = 0, FULLQ1, FULLV0, FULLV1, EMPTY0, EMPTY1, QK0, QK1, RRDY, RFREE, OFULL0, OFULL1, OFREE0, OFREE1,
   SFULL0, SFULL1, SRDY0, SRDY1, GN0, GN1, DRAIN, DRAIN2, VRDY0, VRDY1, VCONV0, VCONV1,
   FRDY0, FRDY1, SB0
 };
@@ -172,8 +172,10 @@ __device__ __forceinline__ uint64_t kmaj_off(int ks) {
   return (uint64_t)(((ks >> 2) * 8192 + (ks & 3) * 32) >> 4);
 }
 
-// Bounded wait that also gives up when another role has aborted.
-__device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, volatile int *abort_p,
+// Bounded wait that also gives up when another role has aborted.  Out of
+// line: every role waits in many places, and the kernel's speed depends on
+// its instruction footprint (all roles run on every SM sub-partition).
+__device__ __noinline__ bool wait_bar(uint64_t *bar, uint32_t parity, volatile int *abort_p,
                                          unsigned *status) {
   for (uint32_t i = 0; i < kBudget; ++i) {
     if (tc::mbar_try_wait(bar, parity)) return true;
@@ -184,7 +186,7 @@ __device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, volatil
   return false;
 }
 
-__device__ __forceinline__ bool wait_bar_cluster(uint64_t *bar, uint32_t parity,
+__device__ __noinline__ bool wait_bar_cluster(uint64_t *bar, uint32_t parity,
                                                  volatile int *abort_p, unsigned *status) {
   for (uint32_t i = 0; i < kBudget; ++i) {
     if (tc::mbar_try_wait_cluster(bar, parity)) return true;
@@ -273,6 +275,30 @@ __device__ __noinline__ void store_state(const KParams &p, float *S_out, uint32_
   }
 }
 
+// Entry z of this head (z_in, or for a later segment the decayed sum of
+// z_in and the pieces before it) into zsm; thread et of 128.
+__device__ __noinline__ void load_entry_z(const KParams &p, const TcArgs &a, float *zsm, int et,
+                                          int bh, int seg, int c0, int npc, float lng) {
+  const int DK = p.dk;
+  for (int k2 = et; k2 < DK; k2 += 128) {
+    float z = a.z_in ? a.z_in[(long long)bh * DK + k2] : 0.f;
+    if (seg > 0) {
+      z *= gpow(lng, kC * c0);
+      for (int i = 0; i < npc; ++i)
+        z = fmaf(gpow(lng, kC * (c0 - (i + 1) * a.piece_len)),
+                 a.zPart[((long long)i * p.B * p.H + bh) * DK + k2], z);
+    }
+    zsm[k2] = z;
+  }
+}
+
+// Row factor f(n) = s1 s2(n) r(n) of 1-based position n whose unnormalised
+// row sum of R is rs (out of line: code size).
+__device__ __noinline__ float row_factor(const KParams &p, int h, long long n, float rs) {
+  const float sn = row_scale(p, h, n);
+  return sn * rsum_scale(p, sn * rs);
+}
+
 template <int kStore>
 __global__ void __launch_bounds__(kNT, 1)
 chunk_tc_kernel(const __grid_constant__ KParams p, const __grid_constant__ CUtensorMap tmQ,
@@ -312,12 +338,8 @@ chunk_tc_kernel(const __grid_constant__ KParams p, const __grid_constant__ CUten
   const bool rsum = (p.norm_flags & RET_NORM_RSUM) != 0;
 
   if (tid == 0) {
-    tc::mbar_init(&bars[FULL0], 1);
-    tc::mbar_init(&bars[FULL1], 1);
-    tc::mbar_init(&bars[EMPTY0], 2);
-    tc::mbar_init(&bars[EMPTY1], 2);
-    for (int i = QK0; i <= SB0; ++i)
-      if (i != EMPTY0 && i != EMPTY1) tc::mbar_init(&bars[i], 1);
+    for (int i = 0; i < kNumBars; ++i)
+      tc::mbar_init(&bars[i], (i == EMPTY0 || i == EMPTY1) ? 2 : 1);
     *abort_p = 0;
     tc::fence_mbar_init();
   }
@@ -340,8 +362,10 @@ chunk_tc_kernel(const __grid_constant__ KParams p, const __grid_constant__ CUten
       tc::prefetch_tmap(&tmQ);
       tc::prefetch_tmap(&tmK);
       tc::prefetch_tmap(&tmV);
-      const uint32_t bytes = (uint32_t)NKB * 8192u * 2u + 16384u + 16u +
-                             (a.need_z ? (uint32_t)DK * 4u : 0u);
+      // V and the chunk's record land first (FULLV, for the helper); Q', K'
+      // and the key sums after them (FULLQ, for the scores).
+      const uint32_t bytes_v = 16384u + 16u;
+      const uint32_t bytes_q = (uint32_t)NKB * 8192u * 2u + (a.need_z ? (uint32_t)DK * 4u : 0u);
       const uint32_t id_qk = tc::idesc_f16(64, 64, 0, 0);
       const int nks = DK / 16;
       const uint32_t sq0 = tc::smem_u32(sm + kOffQ);
@@ -354,31 +378,31 @@ chunk_tc_kernel(const __grid_constant__ KParams p, const __grid_constant__ CUten
             (t_ld < 2 || tc::mbar_test_wait(&bars[EMPTY0 + (t_ld & 1)], ((t_ld >> 1) - 1) & 1))) {
           const int s = t_ld & 1, c = c0 + t_ld;
           uint8_t *st = sm + s * kStage;
-          tc::mbar_arrive_expect_tx(&bars[FULL0 + s], bytes);
-          for (int kb = 0; kb < NKB; ++kb)
-            tc::tma_load_3d(st + kOffQ + kb * 8192, &tmQ, &bars[FULL0 + s], kb * 64, c * kC, bh);
-          for (int kb = 0; kb < NKB; ++kb)
-            tc::tma_load_3d(st + kOffK + kb * 8192, &tmK, &bars[FULL0 + s], kb * 64, c * kC, bh);
+          tc::mbar_arrive_expect_tx(&bars[FULLV0 + s], bytes_v);
           for (int vb = 0; vb < 2; ++vb)
-            tc::tma_load_4d(st + kOffV + vb * 8192, &tmV, &bars[FULL0 + s], v0 + vb * 64, c * kC,
+            tc::tma_load_4d(st + kOffV + vb * 8192, &tmV, &bars[FULLV0 + s], v0 + vb * 64, c * kC,
                             h, b);
-          tc::bulk_load(st + kOffMeta, a.meta + (long long)bh * nch + c, 16u, &bars[FULL0 + s]);
+          tc::bulk_load(st + kOffMeta, a.meta + (long long)bh * nch + c, 16u, &bars[FULLV0 + s]);
+          tc::mbar_arrive_expect_tx(&bars[FULLQ0 + s], bytes_q);
+          for (int kb = 0; kb < NKB; ++kb)
+            tc::tma_load_3d(st + kOffQ + kb * 8192, &tmQ, &bars[FULLQ0 + s], kb * 64, c * kC, bh);
+          for (int kb = 0; kb < NKB; ++kb)
+            tc::tma_load_3d(st + kOffK + kb * 8192, &tmK, &bars[FULLQ0 + s], kb * 64, c * kC, bh);
           if (a.need_z)
             tc::bulk_load(st + kOffKs, a.ksum + ((long long)bh * nch + c) * DK, (uint32_t)DK * 4u,
-                          &bars[FULL0 + s]);
+                          &bars[FULLQ0 + s]);
           ++t_ld;
           moved = true;
         }
         const int bq = t_qk & 1;
-        if (t_qk < t_ld && tc::mbar_test_wait(&bars[FULL0 + bq], (t_qk >> 1) & 1) &&
+        if (t_qk < t_ld && tc::mbar_test_wait(&bars[FULLQ0 + bq], (t_qk >> 1) & 1) &&
             (t_qk < 2 || tc::mbar_test_wait(&bars[OFREE0 + bq], ((t_qk >> 1) - 1) & 1))) {
           tc::tc_fence_after();
           const uint64_t so = bq ? (uint64_t)(kStage >> 4) : 0ull;
-#pragma unroll
-          for (int ks = 0; ks < 16; ++ks)  // T = Q' K'^T
-            if (ks < nks)
-              tc::mma_ss(tb + tcol_o(t_qk), dq0 + so + kmaj_off(ks), dk0 + so + kmaj_off(ks),
-                         id_qk, ks > 0);
+#pragma unroll 1
+          for (int ks = 0; ks < nks; ++ks)  // T = Q' K'^T
+            tc::mma_ss(tb + tcol_o(t_qk), dq0 + so + kmaj_off(ks), dk0 + so + kmaj_off(ks), id_qk,
+                       ks > 0);
           tc::mma_commit(&bars[QK0 + bq]);
           ++t_qk;
           moved = true;
@@ -394,7 +418,12 @@ chunk_tc_kernel(const __grid_constant__ KParams p, const __grid_constant__ CUten
         }
       }
       // Let every issued copy and MMA finish before the CTA can leave.
-      for (int t = t_qk; t < t_ld; ++t) drain_wait(&bars[FULL0 + (t & 1)], (t >> 1) & 1);
+      // (Earlier stages were reused, so only the last two loads can be
+      // outstanding.)
+      for (int t = t_ld > 2 ? t_ld - 2 : 0; t < t_ld; ++t) {
+        drain_wait(&bars[FULLV0 + (t & 1)], (t >> 1) & 1);
+        drain_wait(&bars[FULLQ0 + (t & 1)], (t >> 1) & 1);
+      }
       tc::mma_commit(&bars[DRAIN]);
       drain_wait(&bars[DRAIN], 0);
     }
@@ -422,11 +451,12 @@ chunk_tc_kernel(const __grid_constant__ KParams p, const __grid_constant__ CUten
         const int s = lc & 1;
         const uint64_t so = s ? (uint64_t)(kStage >> 4) : 0ull;
         const uint32_t to = tb + tcol_o(lc);
-        ok = wait_bar(&bars[VCONV0 + s], (lc >> 1) & 1, abort_p, p.status) &&
+        ok = wait_bar(&bars[FULLQ0 + s], (lc >> 1) & 1, abort_p, p.status) &&
+             wait_bar(&bars[VCONV0 + s], (lc >> 1) & 1, abort_p, p.status) &&
              wait_bar(&bars[RRDY], lc & 1, abort_p, p.status);
         if (!ok) break;
         tc::tc_fence_after();
-#pragma unroll
+#pragma unroll 1
         for (int ks = 0; ks < 4; ++ks)  // O^T = V^T R^T
           tc::mma_ss(to, dv0 + so + ks * 128, dr + ks * 2, id_o, ks > 0);
         tc::mma_commit(&bars[RFREE]);
@@ -436,13 +466,10 @@ chunk_tc_kernel(const __grid_constant__ KParams p, const __grid_constant__ CUten
             break;
           }
           tc::tc_fence_after();
-#pragma unroll
-          for (int k = 0; k < 16; ++k)  // O^T += S^T Q'^T over this half's K-steps
-            if (k < nkh) {
-              const int ks = hh * nkh + k;
-              tc::mma_ts(to, tb + kTSh + ks * 8, dq0 + so + kmaj_off(ks), id_x, 1);
-            }
-#pragma unroll
+#pragma unroll 1
+          for (int ks = hh * nkh; ks < (hh + 1) * nkh; ++ks)  // O^T += S^T Q'^T, this half
+            tc::mma_ts(to, tb + kTSh + ks * 8, dq0 + so + kmaj_off(ks), id_x, 1);
+#pragma unroll 1
           for (int ks = 0; ks < 4; ++ks)  // S^T[:, half] += V^T K'[:, half]
             tc::mma_ss(tb + kTS + hh * 128, dv0 + so + ks * 128,
                        dkm0 + so + ks * 128 + (uint64_t)hh * 1024, id_s, 1);
@@ -470,18 +497,20 @@ chunk_tc_kernel(const __grid_constant__ KParams p, const __grid_constant__ CUten
       const int s = lc & 1, c = c0 + lc;
       const int L = min(kC, N - c * kC);
       uint8_t *st = sm + s * kStage;
-      ok = grp_all(G, wait_bar(&bars[FULL0 + s], (lc >> 1) & 1, abort_p, p.status), NT);
+      ok = grp_all(G, wait_bar(&bars[FULLV0 + s], (lc >> 1) & 1, abort_p, p.status), NT);
       if (!ok) break;
-      // (1) max |V| of the tile (1024 16-byte words).
-      uint4 vv[16];
-      float vm = 0.f;
-#pragma unroll
+      // (1) max |V| of the tile (1024 16-byte words), on bf16 pairs.
+      const uint4 *vt = reinterpret_cast<const uint4 *>(st + kOffV);
+      __nv_bfloat162 m2 = __float2bfloat162_rn(0.f);
+#pragma unroll 4
       for (int u = 0; u < 16; ++u) {
-        vv[u] = reinterpret_cast<const uint4 *>(st + kOffV)[ht + NT * u];
-        const uint32_t w[4] = {vv[u].x, vv[u].y, vv[u].z, vv[u].w};
+        const uint4 v4 = vt[ht + NT * u];
+        const uint32_t w[4] = {v4.x, v4.y, v4.z, v4.w};
 #pragma unroll
-        for (int e = 0; e < 4; ++e) vm = fmaxf(vm, fmaxf(fabsf(bf_lo(w[e])), fabsf(bf_hi(w[e]))));
+        for (int e = 0; e < 4; ++e)
+          m2 = __hmax2(m2, __habs2(*reinterpret_cast<const __nv_bfloat162 *>(&w[e])));
       }
+      float vm = fmaxf(__low2float(m2), __high2float(m2));
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) vm = fmaxf(vm, __shfl_xor_sync(0xffffffffu, vm, o));
       float *hr = hred + 2 * hslot;
@@ -489,22 +518,24 @@ chunk_tc_kernel(const __grid_constant__ KParams p, const __grid_constant__ CUten
       if ((ht & 31) == 0) hr[ht >> 5] = vm;
       grp_sync(G, NT);
       const float vmx = fmaxf(hr[0], hr[1]);
-      const int vx = expo14(vmx);
-      // (2) block exponents of the chunk.  R and the state copy share the O
-      // accumulator's scale 2^-E.  |R_ij| = gamma^(i-j) |q_i . k_j| <=
-      // (d_k/2) max|pair of rot q| max|pair of rot k| (j <= i; a dot product
-      // is a sum of d_k/2 pair products), and s_bound >= max |S_c|.
+      // (2) block exponents of the chunk.  R is stored at its own scale
+      // 2^-rr, rr from the bound |R_ij| = gamma^(i-j) |q_i . k_j| <= (d_k/2)
+      // max|pair of rot q| max|pair of rot k| (j <= i; a dot product is a sum
+      // of d_k/2 pair products), so the R group needs nothing from here.  R
+      // and the state copy share the O accumulator's scale 2^-E, E = rr + vx
+      // = ss + aq; V takes the larger exponent when the state bound s_bound
+      // >= max |S_c| needs it, which keeps every fp16 operand below 2^15.
       const ChunkMeta mt = *reinterpret_cast<const ChunkMeta *>(st + kOffMeta);
       const float gL = gpow(lng, L);
+      const int rr = expo14((float)(DK / 2) * mt.qmax * mt.kmax);
+      int vx = expo14(vmx);
+      if (s_bound > 0.f) vx = max(vx, expo14(s_bound) + mt.qexp - rr);
       {
-        const int rr_nat = expo14((float)(DK / 2) * mt.qmax * mt.kmax);
-        int E = rr_nat + vx;
-        if (s_bound > 0.f) E = max(E, expo14(s_bound) + mt.qexp);
-        const int ss = E - mt.qexp, sigma_next = vx + mt.kexp;
+        const int E = rr + vx, ss = E - mt.qexp, sigma_next = vx + mt.kexp;
         if (ht == 0) {
           Scales sc;
           sc.E = E;
-          sc.rr = E - vx;
+          sc.rr = rr;
           sc.f_cp = exp2f((float)(sigma - ss));
           sc.f_pre = gL * exp2f((float)(sigma - sigma_next));
           sc.sigma_next = sigma_next;
@@ -521,12 +552,17 @@ chunk_tc_kernel(const __grid_constant__ KParams p, const __grid_constant__ CUten
       }
       // (3) V tile: bf16 -> fp16 * 2^-vx in place.
       const float vsc = exp2f((float)-vx);
-#pragma unroll
+      const float2 vsc2 = make_float2(vsc, vsc);
+#pragma unroll 4
       for (int u = 0; u < 16; ++u) {
-        const uint32_t w[4] = {vv[u].x, vv[u].y, vv[u].z, vv[u].w};
+        const uint4 v4 = vt[ht + NT * u];
+        const uint32_t w[4] = {v4.x, v4.y, v4.z, v4.w};
         uint32_t o4[4];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) o4[e] = tc::pack_f16(bf_lo(w[e]) * vsc, bf_hi(w[e]) * vsc);
+        for (int e = 0; e < 4; ++e) {
+          const float2 f = tc::mul2(make_float2(bf_lo(w[e]), bf_hi(w[e])), vsc2);
+          o4[e] = tc::pack_f16(f.x, f.y);
+        }
         reinterpret_cast<uint4 *>(st + kOffV)[ht + NT * u] = make_uint4(o4[0], o4[1], o4[2], o4[3]);
       }
       tc::fence_proxy_async_smem();
@@ -542,16 +578,7 @@ chunk_tc_kernel(const __grid_constant__ KParams p, const __grid_constant__ CUten
     float *rsm = qzs;                       // [64] R row sums
     bool ok = true;
     if (a.need_z) {
-      for (int k2 = et; k2 < DK; k2 += 128) {
-        float z = a.z_in ? a.z_in[(long long)bh * DK + k2] : 0.f;
-        if (seg > 0) {  // entry z of a later segment
-          z *= gpow(lng, kC * c0);
-          for (int i = 0; i < npc; ++i)
-            z = fmaf(gpow(lng, kC * (c0 - (i + 1) * a.piece_len)),
-                     a.zPart[((long long)i * p.B * p.H + bh) * DK + k2], z);
-        }
-        zsm[k2] = z;
-      }
+      load_entry_z(p, a, zsm, et, bh, seg, c0, npc, lng);
       grp_sync(G);
     }
     for (int lc = 0; lc < ncl && ok; ++lc) {
@@ -560,51 +587,61 @@ chunk_tc_kernel(const __grid_constant__ KParams p, const __grid_constant__ CUten
       uint8_t *st = sm + s * kStage;
       // RFREE: the previous chunk's O^T = V^T R^T has read R.
       ok = grp_all(G, wait_bar(&bars[QK0 + s], (lc >> 1) & 1, abort_p, p.status) &&
-                          wait_bar(&bars[VRDY0 + s], (lc >> 1) & 1, abort_p, p.status) &&
+                          wait_bar(&bars[FULLV0 + s], (lc >> 1) & 1, abort_p, p.status) &&
+                          wait_bar(&bars[FULLQ0 + s], (lc >> 1) & 1, abort_p, p.status) &&
                           (lc == 0 || wait_bar(&bars[RFREE], (lc - 1) & 1, abort_p, p.status)));
       if (!ok) break;
       tc::tc_fence_after();
-      uint32_t t0[32], t1[32];
-      tc::tmem_ld32(tb + lb + tcol_o(lc), t0);
-      tc::tmem_ld32(tb + lb + tcol_o(lc) + 32, t1);
-      tc::tmem_ld_wait_on(t0);
-      tc::tmem_ld_wait_on(t1);
       const ChunkMeta mt = *reinterpret_cast<const ChunkMeta *>(st + kOffMeta);
-      const Scales sc = scs[s];
-      // (1) R (fp16, * 2^-rr) as K-major rows, and its row sums.
-      if (lane < 16) {
-        const int i = q * 16 + lane;  // M=64 accumulator: row i in lane 32(i/16) + i%16
-        const float ginvL = expf(-(float)L * lng);
-        // R_ij = T_ij 2^(aq+bk) gamma^-L on the causal triangle (j <= i < L).
-        const float tsc = exp2f((float)(mt.qexp + mt.kexp)) * ginvL;
-        const float k1 = tsc * exp2f((float)-sc.rr);
-        const float2 k2 = make_float2(k1, k1);
-        const int lim = i < L ? i : -1;  // last unmasked column of the row
-        float2 xs = make_float2(0.f, 0.f);
+      // (1) R (fp16, * 2^-rr) as K-major rows, and its row sums; rr is the
+      // exponent of R's magnitude bound (the helper uses the same one).
+      const int rr = expo14((float)(DK / 2) * mt.qmax * mt.kmax);
+      // Row i of the M=64 accumulator is in lane 32(i/16) + i%16: lanes 0-15
+      // of each warp hold rows, lanes 16-31 only join the warp-wide loads
+      // (tcgen05.ld is warp-collective, so every lane executes the same one).
+      const int i = q * 16 + (lane & 15);
+      const float ginvL = expf(-(float)L * lng);
+      // R_ij = T_ij 2^(aq+bk) gamma^-L on the causal triangle (j <= i < L).
+      const float tsc = exp2f((float)(mt.qexp + mt.kexp)) * ginvL;
+      const float k1 = tsc * exp2f((float)-rr);
+      const float2 k2 = make_float2(k1, k1);
+      const int lim = i < L ? i : -1;  // last unmasked column of the row
+      float2 xs = make_float2(0.f, 0.f);
+#pragma unroll 1
+      for (int half = 0; half < 2; ++half) {  // 32 columns at a time (code size)
+        uint32_t t[32];
+        tc::tmem_ld32(tb + lb + tcol_o(lc) + 32 * half, t);
+        tc::tmem_ld_wait_on(t);
+        if (lane < 16) {
 #pragma unroll
-        for (int cc = 0; cc < 8; ++cc) {
-          uint32_t w[4];
+          for (int cc = 0; cc < 4; ++cc) {
+            uint32_t w[4];
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int j = cc * 8 + 2 * e;
-            float2 x = make_float2(__uint_as_float(j < 32 ? t0[j] : t1[j - 32]),
-                                   __uint_as_float(j + 1 < 32 ? t0[j + 1] : t1[j + 1 - 32]));
-            x.x = j <= lim ? x.x : 0.f;
-            x.y = j + 1 <= lim ? x.y : 0.f;
-            xs = tc::add2(xs, x);
-            const float2 r = tc::mul2(x, k2);
-            w[e] = tc::pack_f16(r.x, r.y);
+            for (int e = 0; e < 4; ++e) {
+              const int jl = cc * 8 + 2 * e, j = 32 * half + jl;
+              float2 x = make_float2(__uint_as_float(t[jl]), __uint_as_float(t[jl + 1]));
+              x.x = j <= lim ? x.x : 0.f;
+              x.y = j + 1 <= lim ? x.y : 0.f;
+              xs = tc::add2(xs, x);
+              const float2 r = tc::mul2(x, k2);
+              w[e] = tc::pack_f16(r.x, r.y);
+            }
+            *reinterpret_cast<uint4 *>(sm + kOffR + tc::sw128_off(i, 4 * half + cc)) =
+                make_uint4(w[0], w[1], w[2], w[3]);
           }
-          *reinterpret_cast<uint4 *>(sm + kOffR + tc::sw128_off(i, cc)) =
-              make_uint4(w[0], w[1], w[2], w[3]);
         }
-        rsm[i] = (xs.x + xs.y) * tsc;
       }
-      if (et == 0) oss[s] = exp2f((float)sc.E);
+      if (lane < 16) rsm[i] = (xs.x + xs.y) * tsc;
       tc::fence_proxy_async_smem();
       tc::tc_fence_before();  // the scores are read; O^T may overwrite them
       grp_sync(G);
       if (et == 0) tc::mbar_arrive(&bars[RRDY]);
+      // O's scale 2^E for the output group, once the helper has chosen it
+      // (the helper rewrites this stage's record only after EMPTY, which
+      // this group gives below).
+      ok = grp_all(G, wait_bar(&bars[VRDY0 + s], (lc >> 1) & 1, abort_p, p.status));
+      if (!ok) break;
+      if (et == 0) oss[s] = exp2f((float)scs[s].E);
       // (2) row factors f(n) = s1 s2(n) r(n).  The third normalisation adds
       // gamma^(i+1) s1 s2(n) Q_i . z_c to the row sum: Q'_i . z_c, two
       // threads per row.
@@ -613,6 +650,7 @@ chunk_tc_kernel(const __grid_constant__ KParams p, const __grid_constant__ CUten
         float qz = 0.f;
         if (rsum) {
           float2 p01 = make_float2(0.f, 0.f), p23 = p01, p45 = p01, p67 = p01;
+#pragma unroll 1
           for (int t = 0; t < NKB * 4; ++t) {
             const int kb = t >> 2, cc = (t & 3) + 4 * half;
             const uint4 u =
@@ -632,10 +670,7 @@ chunk_tc_kernel(const __grid_constant__ KParams p, const __grid_constant__ CUten
         }
         if (half == 0) {
           float f = 0.f;
-          if (i < L) {
-            const float sn = row_scale(p, h, p.pos0 + (long long)c * kC + i + 1);
-            f = sn * rsum_scale(p, sn * (rsm[i] + qz));
-          }
+          if (i < L) f = row_factor(p, h, p.pos0 + (long long)c * kC + i + 1, rsm[i] + qz);
           fsm[s * 64 + i] = f;
         }
       }
@@ -702,6 +737,7 @@ chunk_tc_kernel(const __grid_constant__ KParams p, const __grid_constant__ CUten
           for (int i = 0; i < 32; ++i) z32[i] = 0u;
 #pragma unroll
           for (int i = 0; i < 16; ++i) z16[i] = 0u;
+#pragma unroll 1
           for (int g = g0; g < g1; ++g) {
             tc::tmem_st16(tb + lb + kTSh + g * 16, z16);
             tc::tmem_st32(tb + lb + kTS + g * 32, z32);
@@ -710,6 +746,7 @@ chunk_tc_kernel(const __grid_constant__ KParams p, const __grid_constant__ CUten
           const float2 fcp2 = make_float2(sc.f_cp, sc.f_cp), fpre2 = make_float2(sc.f_pre, sc.f_pre);
           uint32_t ra[32], rb[32];
           tc::tmem_ld32(tb + lb + kTS + g0 * 32, ra);
+#pragma unroll 1
           for (int g = g0; g < g1; g += 2) {
             tc::tmem_ld_wait_on(ra);
             tc::tmem_ld32(tb + lb + kTS + (g + 1) * 32, rb);
