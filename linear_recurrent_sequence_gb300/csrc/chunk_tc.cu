@@ -840,8 +840,8 @@ chunk_tc_kernel(const __grid_constant__ KParams p, const __grid_constant__ CUten
       }
       grp_sync(G);
       if (et == 0) tc::mbar_arrive(&bars[OFREE0 + s]);
-      // Each thread keeps its 2 x 32 values (tokens st0 and st0+32, column
-      // groups 4(sq4 + 4m)) in registers for the statistics and the stores.
+      // Each thread reads its 2 x 32 values (tokens st0 and st0+32, column
+      // groups 4(sq4 + 4m)) for the statistics, and again for the stores.
       float4 x[2][8];
       float mloc[2], M2loc[2];
 #pragma unroll
@@ -851,7 +851,6 @@ chunk_tc_kernel(const __grid_constant__ KParams p, const __grid_constant__ CUten
 #pragma unroll
         for (int m = 0; m < 8; ++m) x[pass][m] = row[4 * m];
       }
-      grp_sync(G);  // OT may be refilled by the next chunk's drain
 #pragma unroll
       for (int pass = 0; pass < 2; ++pass) {
         float2 sab = make_float2(0.f, 0.f);
@@ -887,33 +886,28 @@ chunk_tc_kernel(const __grid_constant__ KParams p, const __grid_constant__ CUten
         const int par = lc & 1;
         if (et == 0) tc::mbar_arrive_expect_tx(&bars[GN0 + par], (uint32_t)(NV * 64 * 8));
         if (sq4 == 0)
+#pragma unroll 1
+          for (int r2 = 0; r2 < NV; ++r2)
 #pragma unroll
-          for (int pass = 0; pass < 2; ++pass) {
-            const float *slot = gns + ((par * 8 + rank) * 64 + st0 + 32 * pass) * 2;
-#pragma unroll
-            for (int r2 = 0; r2 < 8; ++r2)
-              if (r2 < NV) tc::st_async_v2(slot, &bars[GN0 + par], r2, mloc[pass], M2loc[pass]);
-          }
+            for (int pass = 0; pass < 2; ++pass)
+              tc::st_async_v2(gns + ((par * 8 + rank) * 64 + st0 + 32 * pass) * 2, &bars[GN0 + par],
+                              r2, mloc[pass], M2loc[pass]);
         ok = grp_all(G, wait_bar_cluster(&bars[GN0 + par], (lc >> 1) & 1, abort_p, p.status));
         if (!ok) break;
         // Chan's merge of the NV partial (mean, M2) pairs of kW columns each.
 #pragma unroll
         for (int pass = 0; pass < 2; ++pass) {
-          const int ti = st0 + 32 * pass;
-          float2 pr[8];
-#pragma unroll
-          for (int r2 = 0; r2 < 8; ++r2)
-            pr[r2] = r2 < NV ? *reinterpret_cast<const float2 *>(gns + ((par * 8 + r2) * 64 + ti) * 2)
-                             : make_float2(0.f, 0.f);
+          const float2 *sl = reinterpret_cast<const float2 *>(gns) + (par * 8) * 64 + st0 + 32 * pass;
           float msum = 0.f;
-#pragma unroll
-          for (int r2 = 0; r2 < 8; ++r2) msum += pr[r2].x;
+#pragma unroll 1
+          for (int r2 = 0; r2 < NV; ++r2) msum += sl[r2 * 64].x;
           const float mu = msum * inv_nv;
           float M2t = 0.f;
-#pragma unroll
-          for (int r2 = 0; r2 < 8; ++r2) {
-            const float d = pr[r2].x - mu;
-            M2t += r2 < NV ? pr[r2].y + (float)kW * d * d : 0.f;
+#pragma unroll 1
+          for (int r2 = 0; r2 < NV; ++r2) {
+            const float2 pr = sl[r2 * 64];
+            const float d = pr.x - mu;
+            M2t += pr.y + (float)kW * d * d;
           }
           mean[pass] = mu;
           var[pass] = M2t * (inv_nv * (1.f / kW));
@@ -924,22 +918,25 @@ chunk_tc_kernel(const __grid_constant__ KParams p, const __grid_constant__ CUten
       // per-token shift and scale.  Each thread stores its own values: for a
       // column group m, the 4 threads of a token write 16 consecutive
       // columns (32 bytes of bf16).
-#pragma unroll
+#pragma unroll 1
       for (int pass = 0; pass < 2; ++pass) {
         const int ti = st0 + 32 * pass;
         if (ti >= L) continue;
-        const float f = fr[pass];
-        const float shift = gn ? mean[pass] * osc_inv : 0.f;
-        const float scale = (gn ? f * rsqrtf(f * f * var[pass] + p.gn_eps) : f) * osc;
+        const float4 *row = reinterpret_cast<const float4 *>(OT + ti * kOTPitch) + sq4;
+        const float f = pass ? fr[1] : fr[0];
+        const float mn = pass ? mean[1] : mean[0], vr = pass ? var[1] : var[0];
+        const float shift = gn ? mn * osc_inv : 0.f;
+        const float scale = (gn ? f * rsqrtf(f * f * vr + p.gn_eps) : f) * osc;
         const float2 sh2 = make_float2(-shift, -shift), sc2 = make_float2(scale, scale);
         const long long tok = (long long)c * kC + ti;
         const long long ob0 = b * p.so[0] + h * p.so[1] + tok * p.so[2] + v0 + 4 * sq4;
         const long long gb0 = b * a.gate.s[0] + h * a.gate.s[1] + tok * a.gate.s[2] + v0 + 4 * sq4;
-#pragma unroll
+#pragma unroll 1
         for (int m = 0; m < 8; ++m) {
           const long long ob = ob0 + 16 * m, gb = gb0 + 16 * m;
-          float2 y0 = tc::mul2(tc::add2(make_float2(x[pass][m].x, x[pass][m].y), sh2), sc2);
-          float2 y1 = tc::mul2(tc::add2(make_float2(x[pass][m].z, x[pass][m].w), sh2), sc2);
+          const float4 xm = row[4 * m];
+          float2 y0 = tc::mul2(tc::add2(make_float2(xm.x, xm.y), sh2), sc2);
+          float2 y1 = tc::mul2(tc::add2(make_float2(xm.z, xm.w), sh2), sc2);
           if (kStore == kStoreBf16Gate || (kStore == kStoreAny && a.gate.ptr)) {
             float g[4];
             if (kStore == kStoreBf16Gate) {
