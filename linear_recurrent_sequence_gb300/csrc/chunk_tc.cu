@@ -203,14 +203,12 @@ __device__ __forceinline__ void drain_wait(uint64_t *bar, uint32_t parity) {
     if (tc::mbar_try_wait(bar, parity)) return;
 }
 
-// e such that m * 2^-e < 2^14 (0 for m = 0).
+// e such that m * 2^-e < 2^14 (0 for m = 0, infinite or NaN): read off the
+// exponent field, m = f 2^(be - 126) with f in [0.5, 1) for normal m; a
+// subnormal m < 2^-126 takes the exponent of 2^-126, which still bounds it.
 __device__ __forceinline__ int expo14(float m) {
-  int e = 0;
-  if (m > 0.f && m < INFINITY) {
-    frexpf(m, &e);
-    e -= 14;
-  }
-  return e;
+  const int be = (int)((__float_as_uint(m) >> 23) & 0xffu);
+  return (m > 0.f && be < 255) ? max(be, 1) - 126 - 14 : 0;
 }
 
 __device__ __forceinline__ float2 h2f(uint32_t w) {
@@ -290,13 +288,6 @@ __device__ __noinline__ void load_entry_z(const KParams &p, const TcArgs &a, flo
     }
     zsm[k2] = z;
   }
-}
-
-// Row factor f(n) = s1 s2(n) r(n) of 1-based position n whose unnormalised
-// row sum of R is rs (out of line: code size).
-__device__ __noinline__ float row_factor(const KParams &p, int h, long long n, float rs) {
-  const float sn = row_scale(p, h, n);
-  return sn * rsum_scale(p, sn * rs);
 }
 
 template <int kStore>
@@ -493,6 +484,7 @@ chunk_tc_kernel(const __grid_constant__ KParams p, const __grid_constant__ CUten
     bool ok = grp_all(G, wait_bar(&bars[SB0], 0, abort_p, p.status), NT);
     float s_bound = vmxs[1];
     int sigma = 0;  // the TMEM state holds S * 2^-sigma
+    const float g64 = gpow(lng, kC);
     for (int lc = 0; lc < ncl && ok; ++lc) {
       const int s = lc & 1, c = c0 + lc;
       const int L = min(kC, N - c * kC);
@@ -526,7 +518,7 @@ chunk_tc_kernel(const __grid_constant__ KParams p, const __grid_constant__ CUten
       // = ss + aq; V takes the larger exponent when the state bound s_bound
       // >= max |S_c| needs it, which keeps every fp16 operand below 2^15.
       const ChunkMeta mt = *reinterpret_cast<const ChunkMeta *>(st + kOffMeta);
-      const float gL = gpow(lng, L);
+      const float gL = L == kC ? g64 : gpow(lng, L);
       const int rr = expo14((float)(DK / 2) * mt.qmax * mt.kmax);
       int vx = expo14(vmx);
       if (s_bound > 0.f) vx = max(vx, expo14(s_bound) + mt.qexp - rr);
@@ -576,7 +568,23 @@ chunk_tc_kernel(const __grid_constant__ KParams p, const __grid_constant__ CUten
     const int et = tid - 128;               // 0..127
     const uint32_t lb = (uint32_t)(q * 32) << 16;
     float *rsm = qzs;                       // [64] R row sums
+    float *tbl = qzs + 64;                  // [64] 1 - gamma^i
     bool ok = true;
+    // Second normalisation: the decay row sum of 1-based position n is
+    // (1 - gamma^n)/(1 - gamma) (n for gamma = 1).  With n0 the position of a
+    // chunk's first row, 1 - gamma^(n0+i) = A + B (1 - gamma^i), A = 1 -
+    // gamma^n0, B = gamma^n0: a sum of non-negative terms, so no
+    // cancellation; A and B advance by 64 positions per chunk the same way.
+    const float omg = p.omg[h], inv_omg = omg > 0.f ? 1.f / omg : 0.f;
+    const float g64 = gpow(lng, kC), t64 = -expm1f((float)kC * lng);
+    const float gi64 = expf(-(float)kC * lng);
+    float rowA, rowB;
+    {
+      const float n0 = (float)(p.pos0 + (long long)c0 * kC + 1);
+      rowA = -expm1f(n0 * lng);
+      rowB = expf(n0 * lng);
+      if (et < 64) tbl[et] = et == 0 ? 0.f : -expm1f((float)et * lng);
+    }
     if (a.need_z) {
       load_entry_z(p, a, zsm, et, bh, seg, c0, npc, lng);
       grp_sync(G);
@@ -600,7 +608,7 @@ chunk_tc_kernel(const __grid_constant__ KParams p, const __grid_constant__ CUten
       // of each warp hold rows, lanes 16-31 only join the warp-wide loads
       // (tcgen05.ld is warp-collective, so every lane executes the same one).
       const int i = q * 16 + (lane & 15);
-      const float ginvL = expf(-(float)L * lng);
+      const float ginvL = L == kC ? gi64 : expf(-(float)L * lng);
       // R_ij = T_ij 2^(aq+bk) gamma^-L on the causal triangle (j <= i < L).
       const float tsc = exp2f((float)(mt.qexp + mt.kexp)) * ginvL;
       const float k1 = tsc * exp2f((float)-rr);
@@ -670,15 +678,23 @@ chunk_tc_kernel(const __grid_constant__ KParams p, const __grid_constant__ CUten
         }
         if (half == 0) {
           float f = 0.f;
-          if (i < L) f = row_factor(p, h, p.pos0 + (long long)c * kC + i + 1, rsm[i] + qz);
+          if (i < L) {
+            float sn = (p.norm_flags & RET_NORM_SCALE) ? p.inv_sqrt_dk : 1.f;
+            if (p.norm_flags & RET_NORM_DROW)
+              sn *= rsqrtf(omg > 0.f ? fmaf(rowB, tbl[i], rowA) * inv_omg
+                                     : (float)(p.pos0 + (long long)c * kC + i + 1));
+            f = rsum ? sn * __frcp_rn(fmaxf(fabsf(sn * (rsm[i] + qz)), 1.f)) : sn;
+          }
           fsm[s * 64 + i] = f;
         }
       }
       grp_sync(G);
       if (et == 0) tc::mbar_arrive(&bars[FRDY0 + s]);
       // (3) z_{c+1} = gamma^L z_c + sum_j K'_j (column sums from the prologue).
+      rowA = fmaf(rowB, t64, rowA);  // next chunk's first row is 64 positions on
+      rowB *= g64;
       if (a.need_z) {
-        const float gL = gpow(lng, L);
+        const float gL = L == kC ? g64 : gpow(lng, L);
         const float *ks = reinterpret_cast<const float *>(st + kOffKs);
         for (int k2 = et; k2 < DK; k2 += 128) zsm[k2] = fmaf(gL, zsm[k2], ks[k2]);
       }
@@ -821,7 +837,7 @@ chunk_tc_kernel(const __grid_constant__ KParams p, const __grid_constant__ CUten
       // for chunk lc+2 only after the scores of lc+2, which go to this O^T
       // buffer after OFREE.
       const float osc = oss[s];
-      const float osc_inv = 1.f / osc;
+      const float osc_inv = __frcp_rn(osc);  // osc is a power of two
       float fr[2];
       fr[0] = fsm[s * 64 + st0];
       fr[1] = fsm[s * 64 + st0 + 32];
