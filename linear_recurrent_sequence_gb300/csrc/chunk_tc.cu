@@ -172,11 +172,12 @@ __device__ __forceinline__ uint64_t kmaj_off(int ks) {
   return (uint64_t)(((ks >> 2) * 8192 + (ks & 3) * 32) >> 4);
 }
 
-// Bounded wait that also gives up when another role has aborted.  Out of
-// line: every role waits in many places, and the kernel's speed depends on
+// Bounded wait that also gives up when another role has aborted.  The
+// first try_wait (which already suspends the thread for a while) is inline;
+// the bounded retry loop is out of line, since the kernel's speed depends on
 // its instruction footprint (all roles run on every SM sub-partition).
-__device__ __noinline__ bool wait_bar(uint64_t *bar, uint32_t parity, volatile int *abort_p,
-                                         unsigned *status) {
+__device__ __noinline__ bool wait_bar_slow(uint64_t *bar, uint32_t parity, volatile int *abort_p,
+                                           unsigned *status) {
   for (uint32_t i = 0; i < kBudget; ++i) {
     if (tc::mbar_try_wait(bar, parity)) return true;
     if ((i & 255u) == 255u && *abort_p) return false;
@@ -186,8 +187,13 @@ __device__ __noinline__ bool wait_bar(uint64_t *bar, uint32_t parity, volatile i
   return false;
 }
 
+__device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, volatile int *abort_p,
+                                         unsigned *status) {
+  return tc::mbar_try_wait(bar, parity) || wait_bar_slow(bar, parity, abort_p, status);
+}
+
 __device__ __noinline__ bool wait_bar_cluster(uint64_t *bar, uint32_t parity,
-                                                 volatile int *abort_p, unsigned *status) {
+                                              volatile int *abort_p, unsigned *status) {
   for (uint32_t i = 0; i < kBudget; ++i) {
     if (tc::mbar_try_wait_cluster(bar, parity)) return true;
     if ((i & 255u) == 255u && *abort_p) return false;
