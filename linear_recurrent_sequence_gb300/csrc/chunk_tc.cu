@@ -178,9 +178,12 @@ __device__ __forceinline__ uint64_t kmaj_off(int ks) {
 // its instruction footprint (all roles run on every SM sub-partition).
 __device__ __noinline__ bool wait_bar_slow(uint64_t *bar, uint32_t parity, volatile int *abort_p,
                                            unsigned *status) {
-  for (uint32_t i = 0; i < kBudget; ++i) {
-    if (tc::mbar_try_wait(bar, parity)) return true;
-    if ((i & 255u) == 255u && *abort_p) return false;
+  // Each try sleeps up to 20 us unless the phase completes first (fewer
+  // wake-ups of waiting warps); 2^17 tries bound the wait to seconds and
+  // the abort flag is checked every 16 tries.
+  for (uint32_t i = 0; i < (1u << 17); ++i) {
+    if (tc::mbar_try_wait_hint(bar, parity, 20000u)) return true;
+    if ((i & 15u) == 15u && *abort_p) return false;
   }
   report(status, kDevTimeout);
   *abort_p = 1;
