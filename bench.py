@@ -118,6 +118,26 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------ helpers
+def profiled_traffic():
+    """DRAM bytes per launch of the chunk kernel from the committed ncu
+    summary, or None when the kernel source has changed since the capture."""
+    import hashlib
+    import re
+    try:
+        summ = open(os.path.join(ROOT, "profiles",
+                                 "chunk_tc_kernel_B1_H16_N8192_dk256_dv512.md")).read()
+        src = open(os.path.join(ROOT, "linear_recurrent_sequence_gb300", "csrc",
+                                "chunk_tc.cu"), "rb").read()
+    except OSError:
+        return None
+    h = re.search(r"source_sha256 \(.*?\): ([0-9a-f]{64})", summ)
+    b = re.search(r"dram_bytes_per_launch: (\d+)", summ)
+    if not h or not b or h.group(1) != hashlib.sha256(src).hexdigest():
+        return None
+    return int(b.group(1))
+
+
+
 def gen_bf16(shape, seed, device):
     import torch
     g = torch.Generator(device=device).manual_seed(seed)
@@ -265,7 +285,8 @@ def run_ours(args):
     alg_bytes = BYTES_PER_TOKEN_HEAD * H * N  # per launch of the chunk kernel
     achieved = alg_bytes / avg_s / 1e9
     roofline = {"kernel": top_name, "bound": "hbm", "achieved": achieved, "peak": hbm,
-                "unit": "GB/s", "frac": achieved / hbm, "traffic": None,
+                "unit": "GB/s", "frac": achieved / hbm,
+                "traffic": profiled_traffic() if top_name == "chunk_tc" else None,
                 "peak_source": f"{src} (MEASURED_PEAKS.json hbm_gbs)" if src == "measured"
                 else "fallback 6.8 TB/s",
                 "alg_bytes_per_launch": alg_bytes, "avg_launch_us": avg_s * 1e6,
