@@ -118,6 +118,36 @@ def test_config4_decode_after_prefill(R, B, steps):
     assert rel < 1e-2, rel
 
 
+@pytest.mark.parametrize("dk,dv,flags,gn,odt", [
+    (256, 1024, 0, 1e-6, torch.bfloat16),             # 8 CTAs, two column slices a thread
+    (64, 20, oracle.NORM_ALL, 1e-6, torch.float32),   # one CTA: two row blocks, 20 columns
+    (96, 96, oracle.NORM_ALL, None, torch.float32),   # 8 CTAs of 12 rows, no GroupNorm
+    (2, 4, 0, 1e-6, torch.float32),                   # smallest shape
+    (256, 512, oracle.NORM_ALL, 1e-6, torch.float32),  # decode head shape, with z
+])
+def test_decode_shapes(R, dk, dv, flags, gn, odt):
+    """Decode steps from a random fp32 (S, z) at absolute positions 5000..,
+    on shapes that take each path of the decode kernel (cluster sizes 1 and
+    8, several row blocks or column slices per thread, GroupNorm off)."""
+    B, H, T, pos = 2, 3, 4, 5000
+    (q, k, v), (q64, k64, v64) = inputs(4242 + dk + dv, B, H, T, dk, dv, "bf16")
+    gam = [0.9, 0.99, 1.0]
+    S, S64 = seeded(4343, "S", (B, H, dk, dv), "f32")
+    z, z64 = seeded(4343, "z", (B, H, dk), "f32")
+    outs = [R.recurrent_step(q[:, :, t], k[:, :, t], v[:, :, t], S, gam, z=z, pos=pos + t,
+                             norm_flags=flags, gn_eps=gn, out_dtype=odt) for t in range(T)]
+    p = oracle.Problem(B, H, T, dk, dv, gam, pos0=pos, norm_flags=flags, gn_eps=gn)
+    ref, S_ref, z_ref = oracle.recurrent(p, q64, k64, v64, S_in=S64, z_in=z64)
+    got = host(torch.cat(outs, dim=2))
+    if odt == torch.bfloat16:
+        check_bf16(got, ref, "decode out")
+    else:
+        check_f32(got, ref, "decode out")
+    check_f32(host(S), S_ref, "decode S")
+    if flags & oracle.NORM_RSUM:
+        check_f32(host(z), z_ref, "decode z")
+
+
 # ------------------------------------------------------------------ config 5
 def test_config5_msr_layer(R):
     from oracle.msr import msr_layer
