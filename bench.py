@@ -293,36 +293,80 @@ def run_ours(args):
                 "kernels": {k2: {"ms_total": v2[0], "launches": v2[1]}
                             for k2, v2 in ktimes.items()}}
 
-    # end to end through the C ABI from pinned host buffers
+    # End to end through the C ABI from pinned host buffers: every step copies
+    # its q, k, v host->device and its output device->host.  Two ways:
+    # serial (copy in, compute, copy out on one stream) and pipelined (a
+    # copy-in stream, the compute stream and a copy-out stream with
+    # double-buffered device tensors, so step i+1's inputs and step i-1's
+    # output move while step i computes).  The pipelined number is reported;
+    # it is bound by the host link (about 280 GB/s of copies in both
+    # directions at once; spreading q, k, v over three copy streams gave the
+    # same).
     hq = torch.empty(q.shape, dtype=q.dtype, pin_memory=True)
     hk = torch.empty(k.shape, dtype=k.dtype, pin_memory=True)
     hv = torch.empty(v.shape, dtype=v.dtype, pin_memory=True)
-    ho = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
     hq.copy_(q.cpu()), hk.copy_(k.cpu()), hv.copy_(v.cpu())
-    dq, dk_, dv_ = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ho = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for _ in range(2)]
+    dq = [torch.empty_like(q) for _ in range(2)]
+    dk_ = [torch.empty_like(k) for _ in range(2)]
+    dv_ = [torch.empty_like(v) for _ in range(2)]
+    do = [torch.empty_like(o) for _ in range(2)]
+    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    ev_in = [torch.cuda.Event() for _ in range(2)]
+    ev_cmp = [torch.cuda.Event() for _ in range(2)]
+    ev_out = [torch.cuda.Event() for _ in range(2)]
 
-    def e2e_step():
-        dq.copy_(hq, non_blocking=True)
-        dk_.copy_(hk, non_blocking=True)
-        dv_.copy_(hv, non_blocking=True)
-        R.chunkwise_fwd(dq, dk_, dv_, gam, chunk=args.chunk, norm_flags=R.NORM_ALL, out=o,
-                        S_out=S, workspace=ws, stream=stream)
-        ho.copy_(o, non_blocking=True)
+    def e2e_serial(i):
+        dq[0].copy_(hq, non_blocking=True)
+        dk_[0].copy_(hk, non_blocking=True)
+        dv_[0].copy_(hv, non_blocking=True)
+        R.chunkwise_fwd(dq[0], dk_[0], dv_[0], gam, chunk=args.chunk, norm_flags=R.NORM_ALL,
+                        out=do[0], S_out=S, workspace=ws, stream=stream)
+        ho[0].copy_(do[0], non_blocking=True)
 
-    for _ in range(2):
-        e2e_step()
-    barrier()
-    e0.record(stream)
-    for _ in range(args.steps):
-        e2e_step()
-    e1.record(stream)
-    barrier()
-    e2e_ms = max_over_ranks(e0.elapsed_time(e1))
+    def e2e_pipelined(i):
+        j = i & 1
+        with torch.cuda.stream(s_in):
+            if i >= 2:
+                s_in.wait_event(ev_cmp[j])  # step i-2 has read dq[j] etc.
+            dq[j].copy_(hq, non_blocking=True)
+            dk_[j].copy_(hk, non_blocking=True)
+            dv_[j].copy_(hv, non_blocking=True)
+            ev_in[j].record(s_in)
+        stream.wait_event(ev_in[j])
+        if i >= 2:
+            stream.wait_event(ev_out[j])  # do[j] of step i-2 is on the host
+        R.chunkwise_fwd(dq[j], dk_[j], dv_[j], gam, chunk=args.chunk, norm_flags=R.NORM_ALL,
+                        out=do[j], S_out=S, workspace=ws, stream=stream)
+        ev_cmp[j].record(stream)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(ev_cmp[j])
+            ho[j].copy_(do[j], non_blocking=True)
+            ev_out[j].record(s_out)
+
+    def time_e2e(fn):
+        for i in range(3):
+            fn(i)
+        barrier()
+        e0.record(stream)
+        for i in range(args.steps):
+            fn(i)
+        stream.wait_stream(s_in)
+        stream.wait_stream(s_out)
+        e1.record(stream)
+        barrier()
+        return max_over_ranks(e0.elapsed_time(e1))
+
+    serial_ms = time_e2e(e2e_serial)
+    e2e_ms = time_e2e(e2e_pipelined)
     h2d = (q.numel() + k.numel() + v.numel()) * 2
     d2h = o.numel() * 2
     e2e = {"value": tokens / (e2e_ms * 1e-3), "unit": "tokens/s",
-           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
-    del hq, hk, hv, ho, dq, dk_, dv_
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+           "mode": "pipelined: copy-in, compute and copy-out streams, double-buffered",
+           "serial_value": tokens / (serial_ms * 1e-3),
+           "h2d_d2h_GBps": (h2d + d2h) * args.steps / (e2e_ms * 1e-3) / 1e9}
+    del hq, hk, hv, ho, dq, dk_, dv_, do
 
     extra = {}
     if not args.skip_extra:
