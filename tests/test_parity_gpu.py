@@ -132,6 +132,20 @@ def test_decode_shapes(R, dk, dv, flags, gn, odt):
     B, H, T, pos = 2, 3, 4, 5000
     (q, k, v), (q64, k64, v64) = inputs(4242 + dk + dv, B, H, T, dk, dv, "bf16")
     gam = [0.9, 0.99, 1.0]
+    _decode_steps_vs_oracle(R, B, H, T, pos, dk, dv, flags, gn, odt, gam, q, k, v, q64, k64, v64)
+
+
+def test_decode_many_heads_with_z(R):
+    """B*H*8 CTAs above the SM count take the 8-rows-a-thread form of the
+    decode kernel; all three normalisations and z on, fp32 output."""
+    B, H, T, pos, dk, dv = 3, 16, 3, 777, 256, 512
+    (q, k, v), (q64, k64, v64) = inputs(4747, B, H, T, dk, dv, "bf16")
+    gam = synth.head_gammas(H)
+    _decode_steps_vs_oracle(R, B, H, T, pos, dk, dv, oracle.NORM_ALL, 1e-6, torch.float32, gam,
+                            q, k, v, q64, k64, v64)
+
+
+def _decode_steps_vs_oracle(R, B, H, T, pos, dk, dv, flags, gn, odt, gam, q, k, v, q64, k64, v64):
     S, S64 = seeded(4343, "S", (B, H, dk, dv), "f32")
     z, z64 = seeded(4343, "z", (B, H, dk), "f32")
     outs = [R.recurrent_step(q[:, :, t], k[:, :, t], v[:, :, t], S, gam, z=z, pos=pos + t,
