@@ -33,6 +33,12 @@ H, N, DK, DV = 16, 8192, 256, 512
 BYTES_PER_TOKEN_HEAD = 2 * 2 * DK + 2 * DV + 2 * DV  # q,k,v read + o written (bf16)
 
 
+def flops_per_token_head(C):
+    # Algorithmic flops of the chunkwise form per (token, head): the causal
+    # half of the intra-chunk scores and R V, the cross term and the carry.
+    return 2 * ((C + 1) / 2 * (DK + DV) + 2 * DK * DV)
+
+
 def peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -292,6 +298,14 @@ def run_ours(args):
                 "alg_bytes_per_launch": alg_bytes, "avg_launch_us": avg_s * 1e6,
                 "kernels": {k2: {"ms_total": v2[0], "launches": v2[1]}
                             for k2, v2 in ktimes.items()}}
+    # The same kernel against the dense bf16 tensor-core peak (burst figure:
+    # the kernel is timed per launch).
+    alg_flops = flops_per_token_head(args.chunk) * H * N
+    tens = alg_flops / avg_s / 1e12
+    tensor = {"kernel": top_name, "achieved": tens, "peak": tflops, "unit": "TFLOP/s",
+              "frac": tens / tflops, "alg_flops_per_launch": alg_flops,
+              "peak_source": "MEASURED_PEAKS.json bf16_tflops" if src == "measured"
+              else "fallback 1.9 PFLOP/s"}
 
     # End to end through the C ABI from pinned host buffers: every step copies
     # its q, k, v host->device and its output device->host.  Two ways:
@@ -385,7 +399,7 @@ def run_ours(args):
                 "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
                 "dtype": "bf16", "data": "synthetic", "config": workload_config(args, world),
-                "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+                "roofline": roofline, "tensor": tensor, "cpu_baseline": cpu, "e2e": e2e,
                 "gpu_launches": launches, "clocks": clk.summary()}
         line.update(extra)
         print(json.dumps(line), flush=True)
