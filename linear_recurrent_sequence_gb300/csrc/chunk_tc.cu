@@ -956,7 +956,7 @@ chunk_tc_kernel(const __grid_constant__ KParams p, const __grid_constant__ CUten
         const long long tok = (long long)c * kC + ti;
         const long long ob0 = b * p.so[0] + h * p.so[1] + tok * p.so[2] + v0 + 4 * sq4;
         const long long gb0 = b * a.gate.s[0] + h * a.gate.s[1] + tok * a.gate.s[2] + v0 + 4 * sq4;
-#pragma unroll 1
+#pragma unroll 4  // loads and stores of four groups in flight (unrolled 1 or 8 is slower)
         for (int m = 0; m < 8; ++m) {
           const long long ob = ob0 + 16 * m, gb = gb0 + 16 * m;
           const float4 xm = row[4 * m];
