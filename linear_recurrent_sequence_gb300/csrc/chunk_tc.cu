@@ -624,8 +624,8 @@ chunk_tc_kernel(const __grid_constant__ KParams p, const __grid_constant__ CUten
       const float2 k2 = make_float2(k1, k1);
       const int lim = i < L ? i : -1;  // last unmasked column of the row
       float2 xs = make_float2(0.f, 0.f);
-#pragma unroll 1
-      for (int half = 0; half < 2; ++half) {  // 32 columns at a time (code size)
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {  // 32 columns at a time
         uint32_t t[32];
         tc::tmem_ld32(tb + lb + tcol_o(lc) + 32 * half, t);
         tc::tmem_ld_wait_on(t);
@@ -667,7 +667,7 @@ chunk_tc_kernel(const __grid_constant__ KParams p, const __grid_constant__ CUten
         float qz = 0.f;
         if (rsum) {
           float2 p01 = make_float2(0.f, 0.f), p23 = p01, p45 = p01, p67 = p01;
-#pragma unroll 1
+#pragma unroll 4
           for (int t = 0; t < NKB * 4; ++t) {
             const int kb = t >> 2, cc = (t & 3) + 4 * half;
             const uint4 u =
@@ -911,7 +911,7 @@ chunk_tc_kernel(const __grid_constant__ KParams p, const __grid_constant__ CUten
         const int par = lc & 1;
         if (et == 0) tc::mbar_arrive_expect_tx(&bars[GN0 + par], (uint32_t)(NV * 64 * 8));
         if (sq4 == 0)
-#pragma unroll 1
+#pragma unroll 4
           for (int r2 = 0; r2 < NV; ++r2)
 #pragma unroll
             for (int pass = 0; pass < 2; ++pass)
