@@ -71,4 +71,53 @@ cudaError_t launch_groupnorm(const KParams &p, const float *Oraw, const float *F
   return cudaGetLastError();
 }
 
+// The MSR layer's gate on the retention output, y <- y * swish(g), bf16
+// in and out, fp32 arithmetic (fast exponential and divide: a few ulp before
+// the bf16 rounding).  Eight values per thread when both pointers are
+// 16-byte aligned; a scalar pass covers the rest.
+__global__ void __launch_bounds__(256)
+swish_gate_kernel(__nv_bfloat16 *__restrict__ y, const __nv_bfloat16 *__restrict__ g,
+                  long long n, int vec) {
+  const long long nv = vec ? n / 8 : 0;
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < nv; i += stride) {
+    uint4 yu = reinterpret_cast<const uint4 *>(y)[i];
+    const uint4 gu = reinterpret_cast<const uint4 *>(g)[i];
+    uint32_t *yw = reinterpret_cast<uint32_t *>(&yu);
+    const uint32_t *gw = reinterpret_cast<const uint32_t *>(&gu);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      __nv_bfloat162 yv = *reinterpret_cast<const __nv_bfloat162 *>(&yw[e]);
+      const __nv_bfloat162 gv = *reinterpret_cast<const __nv_bfloat162 *>(&gw[e]);
+      const float g0 = __low2float(gv), g1 = __high2float(gv);
+      const float a = __low2float(yv) * __fdividef(g0, 1.f + __expf(-g0));
+      const float c = __high2float(yv) * __fdividef(g1, 1.f + __expf(-g1));
+      yv = __floats2bfloat162_rn(a, c);
+      yw[e] = *reinterpret_cast<const uint32_t *>(&yv);
+    }
+    reinterpret_cast<uint4 *>(y)[i] = yu;
+  }
+  for (long long i = nv * 8 + (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride) {
+    const float gi = __bfloat162float(g[i]);
+    y[i] = __float2bfloat16_rn(__bfloat162float(y[i]) * __fdividef(gi, 1.f + __expf(-gi)));
+  }
+}
+
+cudaError_t launch_swish_gate(void *y, const void *g, long long n, cudaStream_t st) {
+  if (n <= 0) return cudaSuccess;
+  const int vec = (reinterpret_cast<uintptr_t>(y) % 16 == 0) &&
+                  (reinterpret_cast<uintptr_t>(g) % 16 == 0);
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    sms = 1;
+  const long long work = vec ? (n + 7) / 8 : n;
+  long long blocks = (work + 255) / 256;
+  if (blocks > 8LL * sms) blocks = 8LL * sms;
+  swish_gate_kernel<<<(unsigned)blocks, 256, 0, st>>>(reinterpret_cast<__nv_bfloat16 *>(y),
+                                                     reinterpret_cast<const __nv_bfloat16 *>(g),
+                                                     n, vec);
+  return cudaGetLastError();
+}
+
 }  // namespace ret

@@ -17,6 +17,7 @@ enum KernelId {
   kKChunkTc,
   kKGemmTc,
   kKStatePass,
+  kKGate,
   kKernelCount
 };
 

@@ -50,6 +50,9 @@ struct Gate {
   const void *ptr;      // bf16, NULL = no gate
   long long s[3];       // element strides of (b, h, n); feature contiguous
 };
+// y <- y * swish(g) elementwise over n bf16 values (the MSR layer's gate).
+cudaError_t launch_swish_gate(void *y, const void *g, long long n, cudaStream_t st);
+
 cudaError_t launch_groupnorm(const KParams &p, const float *Oraw, const float *F,
                              void *o, Gate gate, cudaStream_t st);
 
