@@ -437,15 +437,20 @@ ret_status msr_layer_fwd(const msr_desc *m, const void *X, const void *WQ, const
   RET_CUDA(gemm_any(X, WQ, Q, T, HK, m->d_model, status, st));
   RET_CUDA(gemm_any(X, WK, K, T, HK, m->d_model, status, st));
   RET_CUDA(gemm_any(X, WV, V, T, HV, m->d_model, status, st));
-  RET_CUDA(gemm_any(X, WG, G, T, HV, m->d_model, status, st));
-  // Retention (with GroupNorm) into Yg, then the gate swish(G) (.) Yg as
-  // its own bandwidth pass: fused into the chunk kernel's stores, the gate
-  // loads and exponentials made that kernel 2.3 times slower at
-  // B=2, N=4096, H=8 than the extra read and write cost here.
+  // Retention (with GroupNorm) into Yg, then the gate: swish(X W_G) (.) Yg.
+  // Fused into the chunk kernel's stores, the gate loads and exponentials
+  // made that kernel 2.3 times slower at B=2, N=4096, H=8; here it is the
+  // epilogue of the W_G product (which then never writes G), or, where the
+  // tensor-core GEMM does not take the shape, a separate bandwidth pass.
   rs = chunkwise_impl(&inner, Q, K, V, nullptr, nullptr, nullptr, nullptr, Yg,
                       Gate{nullptr, {0, 0, 0}}, at<char>(ws, w.inner), ws_bytes - w.inner, st);
   if (rs != RET_OK) return rs;
-  RET_CUDA(RET_TIMED_LAUNCH(kKGate, st, launch_swish_gate(Yg, G, (long long)T * HV, st)));
+  if (gemm_tc_supported(X, WG, Yg, T, HV, m->d_model)) {
+    RET_CUDA(RET_TIMED_LAUNCH(kKGemmTc, st, launch_gemm_tc(X, WG, Yg, T, HV, m->d_model, status, st, true)));
+  } else {
+    RET_CUDA(gemm_any(X, WG, G, T, HV, m->d_model, status, st));
+    RET_CUDA(RET_TIMED_LAUNCH(kKGate, st, launch_swish_gate(Yg, G, (long long)T * HV, st)));
+  }
   RET_CUDA(gemm_any(Yg, WO, Y, T, m->d_model, HV, status, st));
   return RET_OK;
 }

@@ -9,6 +9,10 @@
 // accumulators, warps 2-5 drain the other accumulator (TMEM -> registers ->
 // bf16 -> global) while the next tile is being computed.  Every wait is
 // bounded (a timeout sets the status word and all roles leave).
+//
+// Gated form (the MSR layer's G = X W_G): C = swish(A B) (.) C, the gate
+// applied in the epilogue to the retention output already in C, so G is
+// never written.
 #include <cudaTypedefs.h>
 
 #include "ktimer.h"
@@ -48,6 +52,7 @@ __device__ __forceinline__ void gdrain(uint64_t *bar, uint32_t parity) {
 
 }  // namespace
 
+template <bool kGate>
 __global__ void __launch_bounds__(kNT, 1)
 gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                __nv_bfloat16 *__restrict__ C, int M, int N, int K, unsigned *status) {
@@ -169,13 +174,35 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         tc::tmem_ld32(tb + lb + buf * BN + g * 32, r);
         tc::tmem_ld_wait();
         uint4 *dst = reinterpret_cast<uint4 *>(crow + g * 32);
+        if constexpr (kGate) {
+          // C <- swish(acc) (.) C: fast exponential and divide, a few ulp in
+          // fp32 before the bf16 rounding; swish -> 0 as acc -> -inf.
+          uint4 cur[4];
 #pragma unroll
-        for (int v = 0; v < 4; ++v)
-          dst[v] = make_uint4(
-              tc::pack_bf16(__uint_as_float(r[8 * v + 0]), __uint_as_float(r[8 * v + 1])),
-              tc::pack_bf16(__uint_as_float(r[8 * v + 2]), __uint_as_float(r[8 * v + 3])),
-              tc::pack_bf16(__uint_as_float(r[8 * v + 4]), __uint_as_float(r[8 * v + 5])),
-              tc::pack_bf16(__uint_as_float(r[8 * v + 6]), __uint_as_float(r[8 * v + 7])));
+          for (int v = 0; v < 4; ++v) cur[v] = dst[v];
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            const uint32_t cw[4] = {cur[v].x, cur[v].y, cur[v].z, cur[v].w};
+            uint32_t ow[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float a0 = __uint_as_float(r[8 * v + 2 * e]);
+              const float a1 = __uint_as_float(r[8 * v + 2 * e + 1]);
+              const float y0 = __uint_as_float(cw[e] << 16), y1 = __uint_as_float(cw[e] & 0xffff0000u);
+              ow[e] = tc::pack_bf16(y0 * __fdividef(a0, 1.f + __expf(-a0)),
+                                    y1 * __fdividef(a1, 1.f + __expf(-a1)));
+            }
+            dst[v] = make_uint4(ow[0], ow[1], ow[2], ow[3]);
+          }
+        } else {
+#pragma unroll
+          for (int v = 0; v < 4; ++v)
+            dst[v] = make_uint4(
+                tc::pack_bf16(__uint_as_float(r[8 * v + 0]), __uint_as_float(r[8 * v + 1])),
+                tc::pack_bf16(__uint_as_float(r[8 * v + 2]), __uint_as_float(r[8 * v + 3])),
+                tc::pack_bf16(__uint_as_float(r[8 * v + 4]), __uint_as_float(r[8 * v + 5])),
+                tc::pack_bf16(__uint_as_float(r[8 * v + 6]), __uint_as_float(r[8 * v + 7])));
+        }
       }
       tc::tc_fence_before();
       asm volatile("bar.sync 1, 128;" ::: "memory");
@@ -200,7 +227,7 @@ bool gemm_tc_supported(const void *A, const void *Bm, const void *C, int M, int 
 }
 
 cudaError_t launch_gemm_tc(const void *A, const void *Bm, void *C, int M, int N, int K,
-                           unsigned *status, cudaStream_t st) {
+                           unsigned *status, cudaStream_t st, bool gate) {
   CUtensorMap ta, tbm;
   const cuuint64_t da[2] = {(cuuint64_t)K, (cuuint64_t)M};
   const cuuint64_t sa[1] = {(cuuint64_t)K * 2};
@@ -213,16 +240,15 @@ cudaError_t launch_gemm_tc(const void *A, const void *Bm, void *C, int M, int N,
       !tmap_encode(&tbm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, Bm, db, sb, bb,
                    CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
-  cudaError_t e =
-      cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+  auto kern = gate ? gemm_tc_kernel<true> : gemm_tc_kernel<false>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
   if (e != cudaSuccess) return e;
   int dev = 0, sms = 0;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const int tiles = (M / BM) * (N / BN);
   const int grid = tiles < sms ? tiles : sms;
-  gemm_tc_kernel<<<grid, kNT, kSmem, st>>>(ta, tbm, reinterpret_cast<__nv_bfloat16 *>(C), M, N,
-                                            K, status);
+  kern<<<grid, kNT, kSmem, st>>>(ta, tbm, reinterpret_cast<__nv_bfloat16 *>(C), M, N, K, status);
   return cudaGetLastError();
 }
 

@@ -84,8 +84,9 @@ cudaError_t launch_recurrent_step(const KParams &p, const void *q, const void *k
 // gemm_tc.cu: tensor-core C[M,N] = A[M,K] B[K,N] (bf16 row-major, fp32
 // accumulate); M % 128, N % 256, K % 64 == 0 and 16-byte aligned pointers.
 bool gemm_tc_supported(const void *A, const void *Bm, const void *C, int M, int N, int K);
+// gate: C <- swish(A B) (.) C (bf16 C read and rewritten in the epilogue).
 cudaError_t launch_gemm_tc(const void *A, const void *Bm, void *C, int M, int N, int K,
-                           unsigned *status, cudaStream_t st);
+                           unsigned *status, cudaStream_t st, bool gate = false);
 
 // gemm_simt.cu: C[M,N] = A[M,K] B[K,N], bf16 in (row-major), fp32 accumulate.
 cudaError_t launch_gemm_bf16(const void *A, const void *Bm, void *C, int M, int N,
