@@ -186,10 +186,10 @@ ret_status check_ws(void *ws, size_t have, size_t need) {
   return RET_OK;
 }
 
-// Chunkwise form with an optional swish gate on the GroupNorm output.
+// Chunkwise form: the tensor-core path where it applies, else CUDA cores.
 ret_status chunkwise_impl(const ret_desc *d, const void *q, const void *k, const void *v,
                           const float *S_in, const float *z_in, float *S_out, float *z_out,
-                          void *o, Gate gate, void *ws, size_t ws_bytes, cudaStream_t st) {
+                          void *o, void *ws, size_t ws_bytes, cudaStream_t st) {
   if (!desc_ok(d)) return RET_EINVAL;
   const bool empty = d->B == 0 || d->H == 0;
   if (!empty && d->N > 0 && (!q || !k || !v || !o)) return RET_EINVAL;
@@ -239,7 +239,7 @@ ret_status chunkwise_impl(const ret_desc *d, const void *q, const void *k, const
       seg.zPart = at<float>(ws, tw.zpart);
       RET_CUDA(RET_TIMED_LAUNCH(kKStatePass, st, launch_state_tc(pt, Kp, v, meta, ks, seg.npieces, seg.piece_len, seg.Part, seg.zPart, need_z, st)));
     }
-    RET_CUDA(RET_TIMED_LAUNCH(kKChunkTc, st, launch_chunk_tc(pt, Qp, Kp, v, meta, ks, S_in, z_in, S_out, z_out, o, gate, need_z, seg, st)));
+    RET_CUDA(RET_TIMED_LAUNCH(kKChunkTc, st, launch_chunk_tc(pt, Qp, Kp, v, meta, ks, S_in, z_in, S_out, z_out, o, need_z, seg, st)));
     return RET_OK;
   }
   float *Qr = at<float>(ws, w.qr), *Kr = at<float>(ws, w.kr);
@@ -251,7 +251,7 @@ ret_status chunkwise_impl(const ret_desc *d, const void *q, const void *k, const
     z_in = at<float>(ws, w.zc);
   }
   RET_CUDA(RET_TIMED_LAUNCH(kKChunkSimt, st, launch_chunk_simt(p, Qr, Kr, v, S_in, z_in, S_out, z_out, Oraw, F, st)));
-  RET_CUDA(RET_TIMED_LAUNCH(kKGroupNorm, st, launch_groupnorm(p, Oraw, F, o, gate, st)));
+  RET_CUDA(RET_TIMED_LAUNCH(kKGroupNorm, st, launch_groupnorm(p, Oraw, F, o, st)));
   return RET_OK;
 }
 
@@ -325,7 +325,7 @@ ret_status retention_parallel_fwd(const ret_desc *d, const void *q, const void *
   RET_CUDA(RET_TIMED_LAUNCH(kKRotate, st, launch_rotate(p, q, p.sq, d->d_k, Qr, 0, nullptr, kScaleNone, st)));
   RET_CUDA(RET_TIMED_LAUNCH(kKRotate, st, launch_rotate(p, k, p.sk, d->d_k, Kr, 0, nullptr, kScaleNone, st)));
   RET_CUDA(RET_TIMED_LAUNCH(kKParallelSimt, st, launch_parallel_simt(p, Qr, Kr, v, Oraw, F, st)));
-  RET_CUDA(RET_TIMED_LAUNCH(kKGroupNorm, st, launch_groupnorm(p, Oraw, F, o, Gate{nullptr, {0, 0, 0}}, st)));
+  RET_CUDA(RET_TIMED_LAUNCH(kKGroupNorm, st, launch_groupnorm(p, Oraw, F, o, st)));
   return RET_OK;
 }
 
@@ -333,7 +333,7 @@ ret_status retention_chunkwise_fwd(const ret_desc *d, const void *q, const void 
                                    const void *v, const float *S_in, const float *z_in,
                                    float *S_out, float *z_out, void *o, void *ws,
                                    size_t ws_bytes, ret_stream_t stream) {
-  return chunkwise_impl(d, q, k, v, S_in, z_in, S_out, z_out, o, Gate{nullptr, {0, 0, 0}},
+  return chunkwise_impl(d, q, k, v, S_in, z_in, S_out, z_out, o,
                         ws, ws_bytes, (cudaStream_t)stream);
 }
 
@@ -443,7 +443,7 @@ ret_status msr_layer_fwd(const msr_desc *m, const void *X, const void *WQ, const
   // epilogue of the W_G product (which then never writes G), or, where the
   // tensor-core GEMM does not take the shape, a separate bandwidth pass.
   rs = chunkwise_impl(&inner, Q, K, V, nullptr, nullptr, nullptr, nullptr, Yg,
-                      Gate{nullptr, {0, 0, 0}}, at<char>(ws, w.inner), ws_bytes - w.inner, st);
+                      at<char>(ws, w.inner), ws_bytes - w.inner, st);
   if (rs != RET_OK) return rs;
   if (gemm_tc_supported(X, WG, Yg, T, HV, m->d_model)) {
     RET_CUDA(RET_TIMED_LAUNCH(kKGemmTc, st, launch_gemm_tc(X, WG, Yg, T, HV, m->d_model, status, st, true)));

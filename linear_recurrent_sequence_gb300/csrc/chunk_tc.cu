@@ -5,7 +5,7 @@
 // chunkwise representation):
 //   O_[c] = (Q_[c] K_[c]^T (.) D) V_[c] + (Q_[c] S_c) (.) xi,  xi_i = gamma^(i+1)
 //   S_{c+1} = gamma^L S_c + K_[c]^T (V_[c] (.) zeta),          zeta_j = gamma^(L-1-j)
-// then the three normalisations and the per-head GroupNorm (+ swish gate).
+// then the three normalisations and the per-head GroupNorm.
 //
 // Operands.  The prologue writes Q' = xi (.) rot(q) and K' = zeta (.) rot(k)
 // per chunk as fp16 times a power of two.  Then Q'_i . K'_j =
@@ -38,7 +38,7 @@
 //   warps 4-7    R group: scores -> masked fp16 R, Q'.z, row factors, z carry
 //   warps 8-11   state group: fp16 copy of the state and gamma^L, per half
 //                of d_k, so it overlaps the MMAs of the other half
-//   warps 12-15  output group: drain O^T, GroupNorm (+ gate), stores
+//   warps 12-15  output group: drain O^T, GroupNorm, stores
 // Every wait is bounded; a wait that runs out sets the status word and an
 // abort flag, and every role leaves after draining its own asynchronous work.
 #include <cooperative_groups.h>
@@ -115,7 +115,6 @@ struct TcArgs {
   const float *S_in, *z_in;
   float *S_out, *z_out;
   void *o;
-  Gate gate;
   const ChunkMeta *meta;       // per (bh, chunk): exponents and magnitudes of Q', K'
   const float *ksum;           // per (bh, chunk) column sums of K' (d_k floats)
   // Sequence segments: segment k (blockIdx.x / (B H NV)) runs chunks
@@ -128,7 +127,6 @@ struct TcArgs {
   int NV;        // CTAs per head (d_v / 128)
   int need_z;    // carry z (third normalisation or z_out)
   int vec_out;   // o rows are 16-byte aligned: vector stores
-  int vec_gate;  // gate rows are 16-byte aligned bf16: vector loads
 };
 
 // Named barrier among the n threads of group g (1 = state, 2 = output,
@@ -229,10 +227,9 @@ __device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 
 }  // namespace
 
 // Store variants, fixed at compile time so the hot loop carries no unused
-// paths: kStoreAny handles every output dtype, alignment and gate;
-// kStoreBf16 is 16-byte aligned bf16 rows without a gate; kStoreBf16Gate
-// adds a 16-byte aligned bf16 gate.
-enum StoreMode { kStoreAny = 0, kStoreBf16 = 1, kStoreBf16Gate = 2 };
+// paths: kStoreAny handles every output dtype and alignment; kStoreBf16 is
+// 16-byte aligned bf16 rows.
+enum StoreMode { kStoreAny = 0, kStoreBf16 = 1 };
 
 // Entry state of this CTA's value columns into the TMEM state columns at
 // `ts` (one warp, its 32 lanes): S_in, or for a later segment the decayed sum
@@ -955,31 +952,12 @@ chunk_tc_kernel(const __grid_constant__ KParams p, const __grid_constant__ CUten
         const float2 sh2 = make_float2(-shift, -shift), sc2 = make_float2(scale, scale);
         const long long tok = (long long)c * kC + ti;
         const long long ob0 = b * p.so[0] + h * p.so[1] + tok * p.so[2] + v0 + 4 * sq4;
-        const long long gb0 = b * a.gate.s[0] + h * a.gate.s[1] + tok * a.gate.s[2] + v0 + 4 * sq4;
 #pragma unroll 4  // loads and stores of four groups in flight (unrolled 1 or 8 is slower)
         for (int m = 0; m < 8; ++m) {
-          const long long ob = ob0 + 16 * m, gb = gb0 + 16 * m;
+          const long long ob = ob0 + 16 * m;
           const float4 xm = row[4 * m];
-          float2 y0 = tc::mul2(tc::add2(make_float2(xm.x, xm.y), sh2), sc2);
-          float2 y1 = tc::mul2(tc::add2(make_float2(xm.z, xm.w), sh2), sc2);
-          if (kStore == kStoreBf16Gate || (kStore == kStoreAny && a.gate.ptr)) {
-            float g[4];
-            if (kStore == kStoreBf16Gate) {
-              const uint2 u = *reinterpret_cast<const uint2 *>(
-                  reinterpret_cast<const __nv_bfloat16 *>(a.gate.ptr) + gb);
-              g[0] = bf_lo(u.x);
-              g[1] = bf_hi(u.x);
-              g[2] = bf_lo(u.y);
-              g[3] = bf_hi(u.y);
-            } else {
-#pragma unroll
-              for (int e = 0; e < 4; ++e) g[e] = ld_elem(a.gate.ptr, gb + e, 1);
-            }
-            y0.x *= g[0] / (1.f + expf(-g[0]));
-            y0.y *= g[1] / (1.f + expf(-g[1]));
-            y1.x *= g[2] / (1.f + expf(-g[2]));
-            y1.y *= g[3] / (1.f + expf(-g[3]));
-          }
+          const float2 y0 = tc::mul2(tc::add2(make_float2(xm.x, xm.y), sh2), sc2);
+          const float2 y1 = tc::mul2(tc::add2(make_float2(xm.z, xm.w), sh2), sc2);
           if (kStore != kStoreAny || (a.vec_out && p.out_bf16)) {
             *reinterpret_cast<uint2 *>(reinterpret_cast<__nv_bfloat16 *>(a.o) + ob) =
                 make_uint2(tc::pack_bf16(y0.x, y0.y), tc::pack_bf16(y1.x, y1.y));
@@ -1023,7 +1001,7 @@ bool chunk_tc_supported(const KParams &p, const void *v, const long long sv[3]) 
 
 cudaError_t launch_chunk_tc(const KParams &p, const void *Qp, const void *Kp, const void *v,
                             const ChunkMeta *meta, const float *ksum, const float *S_in,
-                            const float *z_in, float *S_out, float *z_out, void *o, Gate gate,
+                            const float *z_in, float *S_out, float *z_out, void *o,
                             int need_z, const SegPlan &seg, cudaStream_t st) {
   const int BH = p.B * p.H;
   CUtensorMap tq, tk, tv;
@@ -1047,7 +1025,6 @@ cudaError_t launch_chunk_tc(const KParams &p, const void *Qp, const void *Kp, co
   a.S_out = S_out;
   a.z_out = z_out;
   a.o = o;
-  a.gate = gate;
   a.meta = meta;
   a.ksum = ksum;
   a.NV = p.dv / kW;
@@ -1063,13 +1040,8 @@ cudaError_t launch_chunk_tc(const KParams &p, const void *Qp, const void *Kp, co
   const uintptr_t abytes = 16;
   a.vec_out = (reinterpret_cast<uintptr_t>(o) % abytes == 0) && p.so[0] % al == 0 &&
               p.so[1] % al == 0 && p.so[2] % al == 0;
-  a.vec_gate = gate.ptr && (reinterpret_cast<uintptr_t>(gate.ptr) % abytes == 0) &&
-               gate.s[0] % 8 == 0 && gate.s[1] % 8 == 0 && gate.s[2] % 8 == 0;
-  const bool bf16vec = a.vec_out && p.out_bf16;
   void (*kern)(KParams, CUtensorMap, CUtensorMap, CUtensorMap, TcArgs) =
-      bf16vec && !gate.ptr                 ? chunk_tc_kernel<kStoreBf16>
-      : bf16vec && gate.ptr && a.vec_gate  ? chunk_tc_kernel<kStoreBf16Gate>
-                                           : chunk_tc_kernel<kStoreAny>;
+      a.vec_out && p.out_bf16 ? chunk_tc_kernel<kStoreBf16> : chunk_tc_kernel<kStoreAny>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};

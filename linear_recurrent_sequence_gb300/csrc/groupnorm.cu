@@ -1,9 +1,10 @@
-// Per-head GroupNorm (+ swish gate) epilogue for the CUDA-core forms.
-// GroupNorm per (token, head) over d_v, biased variance, no affine
-// (hwhale.com/article/285883: heads use different gamma, so their variances
-// differ and each head is normalised on its own).  The gate is
+// Per-head GroupNorm epilogue for the CUDA-core forms, and the MSR layer's
+// swish gate as a separate pass.  GroupNorm per (token, head) over d_v,
+// biased variance, no affine (hwhale.com/article/285883: heads use
+// different gamma, so their variances differ and each head is normalised on
+// its own); input rows are F[row] * Oraw[row, :].  The gate is
 // swish(g) = g sigmoid(g) (m0nads.wordpress.com, "Gated Multi-Scale
-// Retention").  Input rows are F[row] * Oraw[row, :].
+// Retention").
 #include "common.cuh"
 #include "launch.h"
 
@@ -13,7 +14,7 @@ constexpr int kGnMaxPerLane = 32;  // d_v <= 1024
 
 __global__ void __launch_bounds__(256)
 groupnorm_kernel(KParams p, const float *__restrict__ Oraw, const float *__restrict__ F,
-                 void *__restrict__ o, Gate gate) {
+                 void *__restrict__ o) {
   const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   const long long rows = (long long)p.B * p.H * p.N;
@@ -48,26 +49,20 @@ groupnorm_kernel(KParams p, const float *__restrict__ Oraw, const float *__restr
     inv = rsqrtf(var / dv + p.gn_eps);
   }
   const long long obase = b * p.so[0] + h * p.so[1] + (long long)n * p.so[2];
-  const long long gbase = b * gate.s[0] + h * gate.s[1] + (long long)n * gate.s[2];
 #pragma unroll
   for (int i = 0; i < kGnMaxPerLane; ++i) {
     const int e = lane + 32 * i;
     if (e >= dv) break;
-    float y = (x[i] - mu) * inv;
-    if (gate.ptr) {
-      const float g = ld_elem(gate.ptr, gbase + e, 1);
-      y *= g / (1.f + expf(-g));
-    }
-    st_elem(o, obase + e, y, p.out_bf16);
+    st_elem(o, obase + e, (x[i] - mu) * inv, p.out_bf16);
   }
 }
 
 cudaError_t launch_groupnorm(const KParams &p, const float *Oraw, const float *F, void *o,
-                             Gate gate, cudaStream_t st) {
+                             cudaStream_t st) {
   const long long rows = (long long)p.B * p.H * p.N;
   if (rows == 0) return cudaSuccess;
   const long long blocks = (rows * 32 + 255) / 256;
-  groupnorm_kernel<<<(unsigned)blocks, 256, 0, st>>>(p, Oraw, F, o, gate);
+  groupnorm_kernel<<<(unsigned)blocks, 256, 0, st>>>(p, Oraw, F, o);
   return cudaGetLastError();
 }
 

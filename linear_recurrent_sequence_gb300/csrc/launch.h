@@ -42,19 +42,13 @@ cudaError_t launch_parallel_simt(const KParams &p, const float *Qr, const float 
 // Qp, Kp: contiguous fp16 [B,H,N,d_k] from the rotate-and-scale prologue
 // (xi-scaled queries, zeta-scaled keys) with per-chunk records meta
 // ([B*H][chunks]) and key column sums ksum ([B*H][chunks][d_k]).
-struct Gate;
 bool chunk_tc_supported(const KParams &p, const void *v, const long long sv[3]);
 
-// groupnorm.cu: o = GroupNorm(F * Oraw) (* swish(gate)), written through so[].
-struct Gate {
-  const void *ptr;      // bf16, NULL = no gate
-  long long s[3];       // element strides of (b, h, n); feature contiguous
-};
+// groupnorm.cu: o = GroupNorm(F * Oraw), written through so[]; and
 // y <- y * swish(g) elementwise over n bf16 values (the MSR layer's gate).
-cudaError_t launch_swish_gate(void *y, const void *g, long long n, cudaStream_t st);
-
 cudaError_t launch_groupnorm(const KParams &p, const float *Oraw, const float *F,
-                             void *o, Gate gate, cudaStream_t st);
+                             void *o, cudaStream_t st);
+cudaError_t launch_swish_gate(void *y, const void *g, long long n, cudaStream_t st);
 
 // Sequence segments of the tensor-core chunk kernel.  P segments of seg_len
 // chunks run as separate CTA groups; the entry state of segment k > 0 is
@@ -67,7 +61,7 @@ struct SegPlan {
 
 cudaError_t launch_chunk_tc(const KParams &p, const void *Qp, const void *Kp, const void *v,
                             const ChunkMeta *meta, const float *ksum, const float *S_in,
-                            const float *z_in, float *S_out, float *z_out, void *o, Gate gate,
+                            const float *z_in, float *S_out, float *z_out, void *o,
                             int need_z, const SegPlan &seg, cudaStream_t st);
 
 // state_tc.cu: partial states of the pieces of a SegPlan (tensor cores).
