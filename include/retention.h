@@ -26,7 +26,7 @@
  * [hwhale, the three normalisations] and a GroupNorm per (token, head) over
  * d_v with no affine [hwhale, multi-head GroupNorm].
  *
- * Readings where the pages are silent (each one is listed in the design doc):
+ * Readings where the pages are silent or ambiguous:
  *   - the phase pairs element (2j, 2j+1) as x_2j + i x_2j+1 and multiplies
  *     by e^{+i t theta_j}; the key's conjugate is carried by the dot product,
  *     so score(t, m) = Re(q~_t conj(k~_m) e^{i (t-m) theta}) [hwhale closed form];
