@@ -294,8 +294,8 @@ def test_tc_chunk_state_in_strided_fp32_out(R):
 
 
 def test_tc_msr_layer_chunk64(R):
-    """The gated MSR layer with chunk 64 runs the tensor-core kernel's swish
-    gate epilogue."""
+    """The gated MSR layer with chunk 64: tensor-core chunk kernel, gate in
+    the W_G GEMM's epilogue."""
     from oracle.msr import msr_layer
     B, N, dm, H, dk, dv = 1, 256, 256, 2, 64, 128
     X, X64 = seeded(77, "x", (B, N, dm), "bf16")
@@ -309,6 +309,32 @@ def test_tc_msr_layer_chunk64(R):
     ref = msr_layer(X64, W["wq"][1], W["wk"][1], W["wv"][1], W["wg"][1], W["wo"][1], H=H,
                     dk=dk, dv=dv, gamma=gam, chunk=64, norm_flags=oracle.NORM_ALL, gn_eps=1e-6)
     check_bf16(host(Y), ref, "msr chunk 64")
+
+
+def test_msr_layer_ragged_tokens_gate_pass(R):
+    """B*N not a multiple of the GEMM tile: CUDA-core projections and the
+    gate as its own pass (swish_gate_kernel).  Seed 67: with seed 66 the
+    first token's retention output is so small that GroupNorm (eps 1e-6)
+    turns the bf16 rounding of the projections into an O(1) change; the
+    float64 oracle alone shows it (1.11 with the projections rounded to
+    bf16, against 0.01 for seeds 67-71)."""
+    from oracle.msr import msr_layer
+    B, N, dm, H, dk, dv = 1, 100, 64, 2, 32, 64
+    X, X64 = seeded(67, "x", (B, N, dm), "bf16")
+    W = {}
+    for name, shp in (("wq", (dm, H * dk)), ("wk", (dm, H * dk)), ("wv", (dm, H * dv)),
+                      ("wg", (dm, H * dv)), ("wo", (H * dv, dm))):
+        W[name] = seeded(67, name, shp, "bf16", std=0.1)
+    gam = synth.head_gammas(H)
+    R.lib.retention_kernel_timer_reset()
+    Y = R.msr_layer_fwd(X, W["wq"][0], W["wk"][0], W["wv"][0], W["wg"][0], W["wo"][0], H=H,
+                        d_k=dk, d_v=dv, gamma=gam, chunk=16, norm_flags=R.NORM_ALL)
+    torch.cuda.synchronize()
+    names = R.kernel_times()
+    assert "swish_gate" in names and "gemm_simt" in names, names
+    ref = msr_layer(X64, W["wq"][1], W["wk"][1], W["wv"][1], W["wg"][1], W["wo"][1], H=H,
+                    dk=dk, dv=dv, gamma=gam, chunk=16, norm_flags=oracle.NORM_ALL, gn_eps=1e-6)
+    check_bf16(host(Y), ref, "msr ragged tokens")
 
 
 def test_small_gamma_takes_the_cuda_core_kernel(R):
