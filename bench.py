@@ -211,6 +211,35 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+# ------------------------------------------------------------------ ranks
+# One process per GPU, each on its own batch (replicas: every (batch, head)
+# is independent, so there is no data-path collective).  The host logic the
+# multi-rank run needs is kept here, apart from the GPU work, so that it can
+# be exercised with the gloo backend on CPU.
+def max_over_ranks_fn(world, device):
+    """x -> the maximum of x over all ranks (identity for one rank)."""
+    def f(x):
+        if world == 1:
+            return x
+        import torch
+        import torch.distributed as dist
+        t = torch.tensor([x], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+    return f
+
+
+def job_throughput(world, units_per_rank_step, steps, max_ms):
+    """Units per second of the whole job: every rank's units over the
+    slowest rank's time (weak scaling: per-rank work is fixed)."""
+    return world * units_per_rank_step * steps / (max_ms * 1e-3)
+
+
+def rank_seed(base, rank):
+    """Each rank draws its own inputs."""
+    return base + 7 * rank
+
+
 def workload_config(args, world):
     return {"workload": f"chunkwise retention fwd B=1/GPU H={H} N={N} d_k={DK} d_v={DV} "
                         f"chunk={args.chunk} bf16 in/out, fp32 state, norms 1+2+3, GroupNorm",
@@ -239,17 +268,12 @@ def run_ours(args):
             dist.barrier()
         torch.cuda.synchronize()
 
-    def max_over_ranks(x):
-        if world == 1:
-            return x
-        t = torch.tensor([x], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
+    max_over_ranks = max_over_ranks_fn(world, dev)
 
     gam = synth.head_gammas(H)
-    q = gen_bf16((1, H, N, DK), 1003 + 7 * rank, dev)
-    k = gen_bf16((1, H, N, DK), 1103 + 7 * rank, dev)
-    v = gen_bf16((1, H, N, DV), 1203 + 7 * rank, dev)
+    q = gen_bf16((1, H, N, DK), rank_seed(1003, rank), dev)
+    k = gen_bf16((1, H, N, DK), rank_seed(1103, rank), dev)
+    v = gen_bf16((1, H, N, DV), rank_seed(1203, rank), dev)
     o = torch.empty(1, H, N, DV, dtype=torch.bfloat16, device=dev)
     S = torch.empty(1, H, DK, DV, dtype=torch.float32, device=dev)
     d, _g = R.make_desc(q, k, v, o, gam, chunk=args.chunk, norm_flags=R.NORM_ALL)
@@ -281,7 +305,7 @@ def run_ours(args):
     launches = int(R.lib.retention_launch_count())
     ktimes = R.kernel_times()
     tokens = world * N * args.steps
-    value = tokens / (ms * 1e-3)
+    value = job_throughput(world, N, args.steps, ms)
 
     # dominant kernel and its roofline
     hbm, tflops, src = peaks()
@@ -375,10 +399,10 @@ def run_ours(args):
     e2e_ms = time_e2e(e2e_pipelined)
     h2d = (q.numel() + k.numel() + v.numel()) * 2
     d2h = o.numel() * 2
-    e2e = {"value": tokens / (e2e_ms * 1e-3), "unit": "tokens/s",
+    e2e = {"value": job_throughput(world, N, args.steps, e2e_ms), "unit": "tokens/s",
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
            "mode": "pipelined: copy-in, compute and copy-out streams, double-buffered",
-           "serial_value": tokens / (serial_ms * 1e-3),
+           "serial_value": job_throughput(world, N, args.steps, serial_ms),
            "h2d_d2h_GBps": (h2d + d2h) * args.steps / (e2e_ms * 1e-3) / 1e9}
     del hq, hk, hv, ho, dq, dk_, dv_, do
 
