@@ -304,7 +304,6 @@ def run_ours(args):
     ms = max_over_ranks(e0.elapsed_time(e1))
     launches = int(R.lib.retention_launch_count())
     ktimes = R.kernel_times()
-    tokens = world * N * args.steps
     value = job_throughput(world, N, args.steps, ms)
 
     # dominant kernel and its roofline
