@@ -162,6 +162,35 @@ def _decode_steps_vs_oracle(R, B, H, T, pos, dk, dv, flags, gn, odt, gam, q, k, 
         check_f32(host(z), z_ref, "decode z")
 
 
+def test_config4_decode_full_batch_sampled(R):
+    """Decode at the largest bench batch (B=128, H=16: 16384 CTAs, the
+    8-rows-a-thread form) after a one-chunk prefill; three (batch, head)
+    pairs carry seeded inputs and are compared with the oracle, the others
+    are torch random numbers that only fill the launch."""
+    B, H, dk, dv, P, T = 128, 16, 256, 512, 64, 3
+    g = torch.Generator(device="cuda").manual_seed(4040)
+    q = torch.randn(B, H, P + T, dk, device="cuda", generator=g).bfloat16()
+    k = torch.randn(B, H, P + T, dk, device="cuda", generator=g).bfloat16()
+    v = torch.randn(B, H, P + T, dv, device="cuda", generator=g).bfloat16()
+    samples = [(0, 0), (63, 7), (127, 15)]
+    ref_in = {}
+    for i, (b, h) in enumerate(samples):
+        (qs, ks, vs), ref_in[(b, h)] = inputs(4100 + i, 1, 1, P + T, dk, dv, "bf16")
+        q[b, h], k[b, h], v[b, h] = qs[0, 0], ks[0, 0], vs[0, 0]
+    gam = synth.head_gammas(H)
+    S = torch.empty(B, H, dk, dv, device="cuda")
+    R.chunkwise_fwd(q[:, :, :P], k[:, :, :P], v[:, :, :P], gam, chunk=64, S_out=S)
+    outs = torch.cat([R.recurrent_step(q[:, :, t], k[:, :, t], v[:, :, t], S, gam, pos=t)
+                      for t in range(P, P + T)], dim=2)
+    torch.cuda.synchronize()
+    for (b, h), (q64, k64, v64) in ref_in.items():
+        p = oracle.Problem(1, 1, P + T, dk, dv, [gam[h]], gn_eps=1e-6)
+        ref, S_ref, _ = oracle.chunkwise(p, 64, q64, k64, v64)
+        check_bf16(host(outs[b:b + 1, h:h + 1]), ref[:, :, P:], f"decode B=128 ({b},{h})")
+        rel = np.max(np.abs(host(S[b:b + 1, h:h + 1]) - S_ref)) / np.max(np.abs(S_ref))
+        assert rel < 1e-2, ((b, h), rel)
+
+
 # ------------------------------------------------------------------ config 5
 def test_config5_msr_layer(R):
     from oracle.msr import msr_layer
