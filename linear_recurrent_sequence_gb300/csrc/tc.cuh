@@ -98,16 +98,6 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, unsign
   return false;
 }
 
-// Arrive once on the mbarrier at the same shared-memory offset in cluster
-// CTA `rank` (release at cluster scope: this thread's earlier shared-memory
-// writes to that CTA are visible to whoever observes the phase).
-__device__ __forceinline__ void mbar_arrive_remote(uint64_t *bar, uint32_t rank) {
-  uint32_t ra;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(smem_u32(bar)), "r"(rank));
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(ra)
-               : "memory");
-}
-
 // 8-byte store into cluster CTA `rank`'s shared memory (same offset as
 // `local`) that completes 8 bytes of transaction count on that CTA's
 // mbarrier at the same offset as `bar`.
@@ -122,7 +112,8 @@ __device__ __forceinline__ void st_async_v2(const float *local, uint64_t *bar, u
       : "memory");
 }
 
-// Bounded wait with acquire at cluster scope (pairs with mbar_arrive_remote).
+// Wait with acquire at cluster scope: the phase completed by st_async_v2's
+// transaction bytes from other CTAs of the cluster.
 __device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t *bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
@@ -177,21 +168,6 @@ __device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t b
       "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
       ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
       : "memory");
-}
-
-__device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, const void *src, int c0,
-                                             int c1) {
-  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%2, %3}], [%1];"
-               ::"l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(src)), "r"(c0), "r"(c1)
-               : "memory");
-}
-
-__device__ __forceinline__ void tma_store_commit() {
-  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-}
-
-__device__ __forceinline__ void tma_store_wait_all() {
-  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap *map) {
@@ -312,11 +288,6 @@ __device__ __forceinline__ void tmem_ld_wait_on(uint32_t (&r)[32]) {
 
 __device__ __forceinline__ void tmem_st_wait() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-}
-
-// TMEM address of (lane, column).
-__device__ __forceinline__ uint32_t taddr(uint32_t base, uint32_t lane, uint32_t col) {
-  return base + (lane << 16) + col;
 }
 
 // ------------------------------------------------------------ descriptors
