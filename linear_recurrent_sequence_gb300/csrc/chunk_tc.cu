@@ -176,11 +176,12 @@ __device__ __forceinline__ uint64_t kmaj_off(int ks) {
 // its instruction footprint (all roles run on every SM sub-partition).
 __device__ __noinline__ bool wait_bar_slow(uint64_t *bar, uint32_t parity, volatile int *abort_p,
                                            unsigned *status) {
-  // Each try sleeps up to 20 us unless the phase completes first (fewer
-  // wake-ups of waiting warps); 2^17 tries bound the wait to seconds and
-  // the abort flag is checked every 16 tries.
-  for (uint32_t i = 0; i < (1u << 17); ++i) {
-    if (tc::mbar_try_wait_hint(bar, parity, 20000u)) return true;
+  // Each try suspends the thread for the hardware's own time limit unless
+  // the phase completes first (measured slightly faster than a 20 us or
+  // 1 us suspend hint); 2^20 tries bound the wait to well under seconds
+  // beyond any legitimate wait, and the abort flag is checked every 16.
+  for (uint32_t i = 0; i < (1u << 20); ++i) {
+    if (tc::mbar_try_wait(bar, parity)) return true;
     if ((i & 15u) == 15u && *abort_p) return false;
   }
   report(status, kDevTimeout);
@@ -411,7 +412,7 @@ chunk_tc_kernel(const __grid_constant__ KParams p, const __grid_constant__ CUten
             break;
           }
           if ((spin & 255u) == 255u && *abort_p) break;
-          __nanosleep(32);  // leave the issue slots to the other warps
+          // No back-off: a sleep here (32 or 128 ns) measured slower.
         }
       }
       // Let every issued copy and MMA finish before the CTA can leave.
