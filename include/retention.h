@@ -245,6 +245,16 @@ long long retention_launch_count(void);
  * ret_status value. */
 int retention_kernel_timer_read(int id, double *total_ms, long long *launches, int *timed);
 
+/* ---- Failure-path check (a test aid). ----
+ * Sets the number of tries of the rotate-and-scale prologue's first,
+ * reporting wait on each TMA copy (default 2^24; applies to launches made
+ * after the call, process-wide).  A wait that runs out records RET_ETIMEOUT
+ * in the status word; the prologue then waits (bounded, with the default
+ * budget) for the copy before it reads it, so results stay valid.  With 0
+ * every such wait reports at once, which lets a test see a device timeout
+ * reach retention_poll_status without stalling or faulting the GPU. */
+void retention_set_report_wait_budget(unsigned tries);
+
 #ifdef __cplusplus
 }
 #endif

@@ -4,6 +4,8 @@
 #include <math.h>
 #include <string.h>
 
+#include <atomic>
+
 #include "common.cuh"
 #include "ktimer.h"
 #include "launch.h"
@@ -13,6 +15,9 @@ using namespace ret;
 namespace {
 
 thread_local int g_last_cuda_error = 0;
+
+// Tries of the prologue's reporting wait (retention_set_report_wait_budget).
+std::atomic<unsigned> g_report_budget{1u << 24};
 
 ret_status cuda_fail(cudaError_t e) {
   g_last_cuda_error = (int)e;
@@ -78,6 +83,7 @@ void make_params(const ret_desc *d, void *ws, KParams &p) {
     p.th_lo[j] = (float)(th - (double)p.th_hi[j]);
   }
   p.status = reinterpret_cast<unsigned *>(ws);
+  p.report_budget = g_report_budget.load(std::memory_order_relaxed);
 }
 
 // Workspace of the CUDA-core forms: status | Qr | Kr | Oraw | F | z copy.
@@ -479,6 +485,10 @@ const char *retention_status_string(ret_status s) {
 }
 
 int retention_last_cuda_error(void) { return g_last_cuda_error; }
+
+void retention_set_report_wait_budget(unsigned tries) {
+  g_report_budget.store(tries, std::memory_order_relaxed);
+}
 
 ret_status retention_poll_status(void *ws, ret_stream_t stream) {
   if (!ws) return RET_EINVAL;

@@ -30,6 +30,7 @@ struct KParams {
   float th_hi[kMaxPairs];    // theta_j rounded to float
   float th_lo[kMaxPairs];    // theta_j - th_hi[j]
   unsigned *status;          // device status word (workspace start)
+  unsigned report_budget;    // tries of a reporting wait (see retention.h)
 };
 
 // ---------------------------------------------------------------- numbers

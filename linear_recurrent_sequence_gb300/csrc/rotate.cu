@@ -134,7 +134,7 @@ rotate_qk_kernel(const __grid_constant__ KParams p, const __grid_constant__ RotQ
       if (tid == 0 && t + (int)gridDim.x < a.ntiles) issue(t + gridDim.x, buf ^ 1);
       // Bounded wait; if it ever ran out, wait (bounded) again for the copy
       // to land before reading or leaving.
-      if (!tc::mbar_wait(&tbar[buf], (k >> 1) & 1, p.status, 1u << 24))
+      if (!tc::mbar_wait(&tbar[buf], (k >> 1) & 1, p.status, p.report_budget))
         tc::mbar_wait(&tbar[buf], (k >> 1) & 1, nullptr, 1u << 24);
     } else {
       const long long *sx = a.s[which];

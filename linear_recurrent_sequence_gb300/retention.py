@@ -70,6 +70,7 @@ _SIGS = {
     "retention_last_cuda_error": (ctypes.c_int, []),
     "retention_poll_status": (ctypes.c_int, [_P, _P]),
     "retention_kernel_timer_enable": (None, [ctypes.c_int]),
+    "retention_set_report_wait_budget": (None, [ctypes.c_uint]),
     "retention_kernel_timer_reset": (None, []),
     "retention_kernel_count": (ctypes.c_int, []),
     "retention_kernel_name": (ctypes.c_char_p, [ctypes.c_int]),

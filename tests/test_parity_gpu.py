@@ -275,6 +275,32 @@ def test_workspace_status_is_clean(R):
     assert R.poll_status(ws) == 0
 
 
+def test_zero_report_budget_surfaces_a_timeout(R):
+    """With no tries for the prologue's reporting wait, every TMA wait there
+    records RET_ETIMEOUT; the bounded data wait behind it keeps the output
+    valid, retention_poll_status reports and clears the word, and the next
+    call runs clean (the context stays usable)."""
+    B, H, N, dk, dv = 1, 2, 256, 64, 128
+    (q, k, v), (q64, k64, v64) = inputs(31, B, H, N, dk, dv, "bf16")
+    gam = synth.head_gammas(H)
+    o = torch.empty(B, H, N, dv, device="cuda", dtype=torch.bfloat16)
+    d, _g = R.make_desc(q, k, v, o, gam, chunk=64, norm_flags=R.NORM_ALL)
+    ws = R.new_workspace(R.workspace_size(d), "cuda")
+    R.lib.retention_set_report_wait_budget(0)
+    try:
+        R.chunkwise_fwd(q, k, v, gam, chunk=64, norm_flags=R.NORM_ALL, out=o, workspace=ws)
+        st = R.poll_status(ws)
+    finally:
+        R.lib.retention_set_report_wait_budget(1 << 24)
+    assert R.STATUS[st] == "RET_ETIMEOUT", st
+    p = oracle.Problem(B, H, N, dk, dv, gam, norm_flags=oracle.NORM_ALL, gn_eps=1e-6)
+    ref, _, _ = oracle.chunkwise(p, 64, q64, k64, v64)
+    check_bf16(host(o), ref, "output under a reported timeout")
+    o2 = R.chunkwise_fwd(q, k, v, gam, chunk=64, norm_flags=R.NORM_ALL, workspace=ws)
+    assert R.poll_status(ws) == 0
+    assert torch.equal(o2, o)
+
+
 # ------------------------------------------------------------------ tensor-core chunk kernel
 @pytest.mark.parametrize("B,H,N,dk,dv", [
     (1, 2, 64, 64, 128),      # one chunk, cluster of 1
