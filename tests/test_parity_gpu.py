@@ -253,6 +253,38 @@ def test_state_passing_and_aliasing(R):
     assert torch.equal(S2, S) and torch.equal(z2, z)
 
 
+def test_checkpoint_through_host_is_bitwise(R):
+    """The resumable state of the method is (S, z, position).  Prefill, copy
+    (S, z) to the host, wipe and restore them, then continue with a second
+    chunkwise call and decode steps: bitwise equal to the same calls without
+    the round trip (every reduction has a fixed order)."""
+    B, H, N, dk, dv, P = 1, 4, 640, 256, 512, 384
+    (q, k, v), _ = inputs(515, B, H, N, dk, dv, "bf16")
+    gam = synth.head_gammas(H)
+
+    def run(via_host):
+        S = torch.empty(B, H, dk, dv, device="cuda")
+        z = torch.empty(B, H, dk, device="cuda")
+        o1 = R.chunkwise_fwd(q[:, :, :P], k[:, :, :P], v[:, :, :P], gam, chunk=64,
+                             norm_flags=R.NORM_ALL, S_out=S, z_out=z)
+        if via_host:
+            S_h, z_h = S.cpu(), z.cpu()
+            S.fill_(float("nan"))
+            z.fill_(float("nan"))
+            S.copy_(S_h)
+            z.copy_(z_h)
+        o2 = R.chunkwise_fwd(q[:, :, P:N - 2], k[:, :, P:N - 2], v[:, :, P:N - 2], gam,
+                             chunk=64, pos0=P, norm_flags=R.NORM_ALL, S_in=S, z_in=z,
+                             S_out=S, z_out=z)
+        o3 = [R.recurrent_step(q[:, :, t], k[:, :, t], v[:, :, t], S, gam, z=z, pos=t,
+                               norm_flags=R.NORM_ALL) for t in (N - 2, N - 1)]
+        return torch.cat([o1, o2] + o3, dim=2), S, z
+
+    a, Sa, za = run(False)
+    b, Sb, zb = run(True)
+    assert torch.equal(a, b) and torch.equal(Sa, Sb) and torch.equal(za, zb)
+
+
 def test_single_token_and_no_groupnorm(R):
     B, H, N, dk, dv = 2, 2, 1, 16, 8
     (q, k, v), (q64, k64, v64) = inputs(5, B, H, N, dk, dv, "f32")
