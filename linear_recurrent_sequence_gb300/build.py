@@ -20,6 +20,10 @@ LIB = os.path.join(BUILD, "libretention.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
                      "-I" + os.path.join(ROOT, "include"), "--expt-relaxed-constexpr"]
+# RET_NVTX=1: an NVTX range around each ABI call (build with force=True when
+# switching, since objects are only rebuilt when sources change).
+if os.environ.get("RET_NVTX") == "1":
+    NVCC_FLAGS = NVCC_FLAGS + ["-DRET_NVTX"]
 
 
 def _nvcc():

@@ -6,6 +6,10 @@
 
 #include <atomic>
 
+#ifdef RET_NVTX
+#include <nvtx3/nvToolsExt.h>
+#endif
+
 #include "common.cuh"
 #include "ktimer.h"
 #include "launch.h"
@@ -15,6 +19,18 @@ using namespace ret;
 namespace {
 
 thread_local int g_last_cuda_error = 0;
+
+// Optional NVTX range per ABI call (build with RET_NVTX=1 in the environment):
+// names the calls on a profiler's timeline.
+#ifdef RET_NVTX
+struct NvtxRange {
+  explicit NvtxRange(const char *name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+};
+#define RET_RANGE(name) NvtxRange ret_range_(name)
+#else
+#define RET_RANGE(name) ((void)0)
+#endif
 
 // Tries of the prologue's reporting wait (retention_set_report_wait_budget).
 std::atomic<unsigned> g_report_budget{1u << 24};
@@ -297,6 +313,7 @@ size_t retention_workspace_size(const ret_desc *d) {
 ret_status retention_rotate(const ret_desc *d, const void *x, const int64_t sx[3], int dim,
                             void *out, ret_dtype out_dtype, const float *scale,
                             ret_stream_t stream) {
+  RET_RANGE("retention_rotate");
   if (!desc_ok(d) || !sx || dim != d->d_k) return RET_EINVAL;
   if (out_dtype != RET_F32 && out_dtype != RET_BF16) return RET_EINVAL;
   if ((long long)d->B * d->H * d->N == 0) return RET_OK;
@@ -316,6 +333,7 @@ ret_status retention_rotate(const ret_desc *d, const void *x, const int64_t sx[3
 ret_status retention_parallel_fwd(const ret_desc *d, const void *q, const void *k,
                                   const void *v, void *o, void *ws, size_t ws_bytes,
                                   ret_stream_t stream) {
+  RET_RANGE("retention_parallel_fwd");
   if (!desc_ok(d)) return RET_EINVAL;
   const bool empty = (long long)d->B * d->H * d->N == 0;
   if (!empty && (!q || !k || !v || !o)) return RET_EINVAL;
@@ -339,6 +357,7 @@ ret_status retention_chunkwise_fwd(const ret_desc *d, const void *q, const void 
                                    const void *v, const float *S_in, const float *z_in,
                                    float *S_out, float *z_out, void *o, void *ws,
                                    size_t ws_bytes, ret_stream_t stream) {
+  RET_RANGE("retention_chunkwise_fwd");
   return chunkwise_impl(d, q, k, v, S_in, z_in, S_out, z_out, o,
                         ws, ws_bytes, (cudaStream_t)stream);
 }
@@ -346,6 +365,7 @@ ret_status retention_chunkwise_fwd(const ret_desc *d, const void *q, const void 
 ret_status retention_recurrent_step(const ret_desc *d, const void *q, const void *k,
                                     const void *v, float *S, float *z, void *o, void *ws,
                                     size_t ws_bytes, ret_stream_t stream) {
+  RET_RANGE("retention_recurrent_step");
   if (!desc_ok(d) || d->N != 1) return RET_EINVAL;
   if (d->d_v % 4) return RET_EINVAL;
   const bool empty = (long long)d->B * d->H == 0;
@@ -425,6 +445,7 @@ size_t msr_workspace_size(const msr_desc *m) {
 ret_status msr_layer_fwd(const msr_desc *m, const void *X, const void *WQ, const void *WK,
                          const void *WV, const void *WG, const void *WO, void *Y, void *ws,
                          size_t ws_bytes, ret_stream_t stream) {
+  RET_RANGE("msr_layer_fwd");
   if (!msr_ok(m)) return RET_EINVAL;
   ret_desc inner;
   msr_inner_desc(m, &inner);
@@ -463,6 +484,7 @@ ret_status msr_layer_fwd(const msr_desc *m, const void *X, const void *WQ, const
 
 ret_status retention_gemm_bf16(const void *A, const void *Bm, void *C, int M, int N, int K,
                                void *ws, size_t ws_bytes, ret_stream_t stream) {
+  RET_RANGE("retention_gemm_bf16");
   if (M < 0 || N < 0 || K < 1) return RET_EINVAL;
   if ((long long)M * N == 0) return RET_OK;
   if (!A || !Bm || !C) return RET_EINVAL;
