@@ -65,6 +65,7 @@ def _bind(lib):
         "orc_chunkwise": [C, ctypes.c_int, P, P, P, P, P, P, P, P],
         "orc_closed_form": [C, P, P, P, P],
         "orc_groupnorm": [ctypes.c_longlong, ctypes.c_int, ctypes.c_double, P, P],
+        "orc_recurrent_bwd": [C, P, P, P, P, P, P, P, P, P, P],
     }.items():
         f = getattr(lib, name)
         f.argtypes = args
@@ -212,3 +213,22 @@ def groupnorm(x, eps):
 
 def decay_row_sum(gamma, n):
     return _load().orc_decay_row_sum(float(gamma), int(n))
+
+
+def recurrent_bwd(p: Problem, q, k, v, dO, S_in=None, dS_out=None):
+    """Gradients of the recurrent form: returns (dq, dk, dv, dS_in).
+
+    dO is the gradient of o, dS_out that of the final state (None = zero).
+    Needs gn_eps < 0 (no GroupNorm) and no third normalisation."""
+    lib = _load()
+    sq, sv, sS, _ = _shape(p)
+    q, k, v = _f64(q).reshape(sq), _f64(k).reshape(sq), _f64(v).reshape(sv)
+    dO = _f64(dO).reshape(sv)
+    S_in = None if S_in is None else _f64(S_in).reshape(sS)
+    dS_out = None if dS_out is None else _f64(dS_out).reshape(sS)
+    dq, dk, dv, dS = np.empty(sq), np.empty(sq), np.empty(sv), np.empty(sS)
+    c = p.cfg()
+    _check(lib.orc_recurrent_bwd(ctypes.byref(c), _ptr(q), _ptr(k), _ptr(v), _ptr(S_in),
+                                 _ptr(dO), _ptr(dS_out), _ptr(dq), _ptr(dk), _ptr(dv),
+                                 _ptr(dS)), "orc_recurrent_bwd")
+    return dq, dk, dv, dS

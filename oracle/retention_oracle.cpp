@@ -56,6 +56,17 @@ void rotate_row(const double *x, int d, long long t, double base, double *y) {
   }
 }
 
+// Multiply pair j by e^{-i t theta_j}: the inverse (and transpose) of rotate_row.
+void unrotate_row(const double *x, int d, long long t, double base, double *y) {
+  for (int j = 0; j < d / 2; ++j) {
+    const double phi = static_cast<double>(t) * theta_of(base, j, d);
+    const double cs = std::cos(phi), sn = std::sin(phi);
+    const double a = x[2 * j], b = x[2 * j + 1];
+    y[2 * j] = a * cs + b * sn;
+    y[2 * j + 1] = b * cs - a * sn;
+  }
+}
+
 double dot(const double *a, const double *b, int d) {
   double s = 0.0;
   for (int i = 0; i < d; ++i) s += a[i] * b[i];
@@ -358,6 +369,88 @@ int orc_closed_form(const orc_cfg *c, const double *q, const double *k,
     }
   }
   finish_groupnorm(c, o);
+  return 0;
+}
+
+// Gradients of the recurrent form by reverse mode, token by token.
+// Forward ([hwhale] recurrent equations, as orc_recurrent): with q', k' the
+// rotated rows and s_n the data-independent row factor of the first two
+// normalisations, S_n = gamma S_{n-1} + k'_n^T v_n and o_n = s_n q'_n S_n.
+// Reverse mode of that recurrence:
+//   dq'_n = s_n S_n do_n                      (S_n: the state after token n)
+//   G_n   = gradient of the loss w.r.t. S_n
+//         = gamma G_{n+1} + s_n q'_n^T do_n,  G_{N} := dS_out (the last state)
+//   dk'_n = G_n v_n,   dv_n = k'_n G_n,   dS_in = gamma G_0
+// and dq, dk are dq', dk' turned back by e^{-i t theta_j} (the transpose of
+// the rotation).  The third normalisation and GroupNorm are not covered.
+int orc_recurrent_bwd(const orc_cfg *c, const double *q, const double *k,
+                      const double *v, const double *S_in, const double *dO,
+                      const double *dS_out, double *dq, double *dk, double *dv,
+                      double *dS_in) {
+  if (!cfg_ok(c) || !q || !k || !v || !dO || !dq || !dk || !dv) return -1;
+  if ((c->norm_flags & ORC_NORM_RSUM) || c->gn_eps >= 0.0) return -1;
+  const int N = c->N, dK = c->dk, dV = c->dv;
+  const long long BH = (long long)c->B * c->H;
+#pragma omp parallel for schedule(dynamic) num_threads(nthreads(c))
+  for (long long bh = 0; bh < BH; ++bh) {
+    const double g = c->gamma[bh % c->H];
+    const size_t qo = (size_t)bh * N * dK, vo = (size_t)bh * N * dV;
+    const size_t so = (size_t)bh * dK * dV;
+    std::vector<double> qr((size_t)N * dK), kr((size_t)N * dK);
+    rotated_copy(c, q + qo, dK, qr.data());
+    rotated_copy(c, k + qo, dK, kr.data());
+    const std::vector<double> crow = decay_row_sums(g, c->pos0, N);
+    std::vector<double> dqr((size_t)N * dK), dkr((size_t)N * dK);
+    // Forward sweep: the state after each token, and dq'.
+    std::vector<double> S((size_t)dK * dV, 0.0);
+    if (S_in) for (size_t i = 0; i < S.size(); ++i) S[i] = S_in[so + i];
+    for (int n = 0; n < N; ++n) {
+      const double *kn = &kr[(size_t)n * dK];
+      const double *vn = v + vo + (size_t)n * dV;
+      const double *don = dO + vo + (size_t)n * dV;
+      for (int a = 0; a < dK; ++a)
+        for (int e = 0; e < dV; ++e)
+          S[(size_t)a * dV + e] = g * S[(size_t)a * dV + e] + kn[a] * vn[e];
+      const double sn = row_scale(c, crow[n]);
+      for (int a = 0; a < dK; ++a)
+        dqr[(size_t)n * dK + a] = sn * dot(&S[(size_t)a * dV], don, dV);
+    }
+    // Reverse sweep: G runs from the last token to the first.
+    std::vector<double> G((size_t)dK * dV, 0.0);
+    if (dS_out) for (size_t i = 0; i < G.size(); ++i) G[i] = dS_out[so + i];
+    for (int n = N - 1; n >= 0; --n) {
+      const double *qn = &qr[(size_t)n * dK];
+      const double *kn = &kr[(size_t)n * dK];
+      const double *vn = v + vo + (size_t)n * dV;
+      const double *don = dO + vo + (size_t)n * dV;
+      const double sn = row_scale(c, crow[n]);
+      for (int a = 0; a < dK; ++a)
+        for (int e = 0; e < dV; ++e) G[(size_t)a * dV + e] += sn * qn[a] * don[e];
+      for (int a = 0; a < dK; ++a) dkr[(size_t)n * dK + a] = dot(&G[(size_t)a * dV], vn, dV);
+      double *dvn = dv + vo + (size_t)n * dV;
+      for (int e = 0; e < dV; ++e) {
+        double acc = 0.0;
+        for (int a = 0; a < dK; ++a) acc += kn[a] * G[(size_t)a * dV + e];
+        dvn[e] = acc;
+      }
+      for (size_t i = 0; i < G.size(); ++i) G[i] *= g;  // now w.r.t. S_{n-1}
+    }
+    if (dS_in) for (size_t i = 0; i < G.size(); ++i) dS_in[so + i] = G[i];
+    for (int n = 0; n < N; ++n) {
+      if (c->rotate) {
+        // The transpose of a turn by +t theta_j is a turn by -t theta_j.
+        unrotate_row(&dqr[(size_t)n * dK], dK, c->pos0 + n, c->theta_base,
+                     dq + qo + (size_t)n * dK);
+        unrotate_row(&dkr[(size_t)n * dK], dK, c->pos0 + n, c->theta_base,
+                     dk + qo + (size_t)n * dK);
+      } else {
+        for (int a = 0; a < dK; ++a) {
+          dq[qo + (size_t)n * dK + a] = dqr[(size_t)n * dK + a];
+          dk[qo + (size_t)n * dK + a] = dkr[(size_t)n * dK + a];
+        }
+      }
+    }
+  }
   return 0;
 }
 

@@ -79,6 +79,17 @@ int orc_chunkwise(const orc_cfg *c, int chunk, const double *q,
 int orc_closed_form(const orc_cfg *c, const double *q, const double *k,
                     const double *v, double *o);
 
+/* Gradients of the recurrent form (reverse mode of the recurrence, token by
+ * token): dO [B][H][N][dv] is the gradient of o, dS_out [B][H][dk][dv] that of
+ * the final state (NULL = zero); S_in NULL = zero state.  Writes dq, dk (with
+ * respect to the unrotated q, k), dv and, unless NULL, dS_in.  Covers the
+ * first two normalisations (row factors that do not depend on the data);
+ * returns -1 when ORC_NORM_RSUM is set or GroupNorm is on (gn_eps >= 0). */
+int orc_recurrent_bwd(const orc_cfg *c, const double *q, const double *k,
+                      const double *v, const double *S_in, const double *dO,
+                      const double *dS_out, double *dq, double *dk, double *dv,
+                      double *dS_in);
+
 /* GroupNorm of `rows` groups of `dv` contiguous values; no affine. */
 int orc_groupnorm(long long rows, int dv, double eps, const double *x,
                   double *y);
