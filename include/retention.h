@@ -163,6 +163,31 @@ ret_status retention_recurrent_step(const ret_desc *d, const void *q,
                                     ret_stream_t stream);
 
 /*
+ * Backward of the chunkwise / recurrent form: reverse mode of
+ * S_n = gamma S_{n-1} + K_n^T V_n, O_n = s_n Q_n S_n [hwhale, recurrent and
+ * chunkwise equations], s_n the row factor of the first two normalisations.
+ * Given dO (gradient of o: out_dtype through the `so` strides) and dS_out
+ * (gradient of the final state, fp32 [B,H,d_k,d_v] contiguous; NULL = zero),
+ * writes
+ *   dq, dk, dv: gradients of q, k, v, with their layouts (sq, sk, sv strides)
+ *               and element type (in_dtype); dq, dk are with respect to the
+ *               unrotated inputs when `rotate` is set;
+ *   dS_in:      gradient of the entry state (fp32 [B,H,d_k,d_v]; NULL = not
+ *               wanted).  It may alias dS_out.
+ * S_in: the entry state of the forward call (NULL = zeros).  The gradient of
+ * the z row sums is not produced (z enters only the third normalisation).
+ * Requires gn_eps < 0 (no GroupNorm) and norm_flags without RET_NORM_RSUM:
+ * RET_EUNSUPPORTED otherwise.  No output may overlap an input, except dS_in
+ * and dS_out.  The chunk field does not change the result.
+ */
+size_t retention_backward_workspace_size(const ret_desc *d);
+ret_status retention_chunkwise_bwd(const ret_desc *d, const void *q, const void *k,
+                                   const void *v, const float *S_in, const void *dO,
+                                   const float *dS_out, void *dq, void *dk, void *dv,
+                                   float *dS_in, void *ws, size_t ws_bytes,
+                                   ret_stream_t stream);
+
+/*
  * Chunkwise forward without a caller-supplied workspace.  No counterpart on
  * the pages: it exists for callers that cannot allocate device memory, such
  * as a plugin that an inference runtime hands only its input and output

@@ -120,6 +120,23 @@ SimtWs simt_ws(const ret_desc *d) {
   return w;
 }
 
+// Workspace of the backward: status | Q' | K' | dQ' | dK' (fp32 rows).
+struct BwdWs {
+  size_t qr, kr, dq, dk, total;
+};
+
+BwdWs bwd_ws(const ret_desc *d) {
+  BwdWs w;
+  const size_t bytes = (size_t)d->B * d->H * d->N * d->d_k * sizeof(float);
+  size_t off = kStatusBytes;
+  w.qr = off; off = align256(off + bytes);
+  w.kr = off; off = align256(off + bytes);
+  w.dq = off; off = align256(off + bytes);
+  w.dk = off; off = align256(off + bytes);
+  w.total = off;
+  return w;
+}
+
 // Sequence segments of the tensor-core chunk kernel: at most kMaxSegments
 // segments of at least kMinSegChunks chunks, and at most kMaxPieces pieces
 // of partial state.
@@ -389,6 +406,49 @@ ret_status retention_recurrent_step(const ret_desc *d, const void *q, const void
   KParams p;
   make_params(d, ws, p);
   RET_CUDA(RET_TIMED_LAUNCH(kKRecurrent, (cudaStream_t)stream, launch_recurrent_step(p, q, k, v, S, z, o, (cudaStream_t)stream)));
+  return RET_OK;
+}
+
+size_t retention_backward_workspace_size(const ret_desc *d) {
+  if (!desc_ok(d)) return 0;
+  return bwd_ws(d).total;
+}
+
+ret_status retention_chunkwise_bwd(const ret_desc *d, const void *q, const void *k,
+                                   const void *v, const float *S_in, const void *dO,
+                                   const float *dS_out, void *dq, void *dk, void *dv,
+                                   float *dS_in, void *ws, size_t ws_bytes,
+                                   ret_stream_t stream) {
+  RET_RANGE("retention_chunkwise_bwd");
+  if (!desc_ok(d)) return RET_EINVAL;
+  if ((d->norm_flags & RET_NORM_RSUM) || d->gn_eps >= 0.f) return RET_EUNSUPPORTED;
+  const bool empty = d->B == 0 || d->H == 0;
+  if (!empty && d->N > 0 && (!q || !k || !v || !dO || !dq || !dk || !dv)) return RET_EINVAL;
+  const BwdWs w = bwd_ws(d);
+  ret_status rs = check_ws(ws, ws_bytes, w.total);
+  if (rs != RET_OK) return rs;
+  if (empty) return RET_OK;
+  cudaStream_t st = (cudaStream_t)stream;
+  if (d->N == 0) {  // no tokens: the state gradient passes through
+    const size_t sbytes = (size_t)d->B * d->H * d->d_k * d->d_v * sizeof(float);
+    if (dS_in && dS_in != dS_out)
+      RET_CUDA(dS_out ? cudaMemcpyAsync(dS_in, dS_out, sbytes, cudaMemcpyDeviceToDevice, st)
+                      : cudaMemsetAsync(dS_in, 0, sbytes, st));
+    return RET_OK;
+  }
+  KParams p;
+  make_params(d, ws, p);
+  float *Qr = at<float>(ws, w.qr), *Kr = at<float>(ws, w.kr);
+  float *DQr = at<float>(ws, w.dq), *DKr = at<float>(ws, w.dk);
+  RET_CUDA(RET_TIMED_LAUNCH(kKRotate, st, launch_rotate(p, q, p.sq, d->d_k, Qr, 0, nullptr, kScaleNone, st)));
+  RET_CUDA(RET_TIMED_LAUNCH(kKRotate, st, launch_rotate(p, k, p.sk, d->d_k, Kr, 0, nullptr, kScaleNone, st)));
+  RET_CUDA(RET_TIMED_LAUNCH(kKBwdRows, st, launch_bwd_rows(p, false, Kr, v, dO, S_in, DQr, st)));
+  // The reverse sweeps read dS_out before the value kernel writes dS_in, so
+  // the two may be one buffer.
+  RET_CUDA(RET_TIMED_LAUNCH(kKBwdRows, st, launch_bwd_rows(p, true, Qr, v, dO, dS_out, DKr, st)));
+  RET_CUDA(RET_TIMED_LAUNCH(kKBwdValues, st, launch_bwd_values(p, Qr, Kr, dO, dS_out, dv, dS_in, st)));
+  RET_CUDA(RET_TIMED_LAUNCH(kKUnrotate, st, launch_unrotate(p, DQr, p.sq, dq, p.in_bf16, st)));
+  RET_CUDA(RET_TIMED_LAUNCH(kKUnrotate, st, launch_unrotate(p, DKr, p.sk, dk, p.in_bf16, st)));
   return RET_OK;
 }
 

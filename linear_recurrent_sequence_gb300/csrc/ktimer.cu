@@ -14,7 +14,8 @@ namespace {
 constexpr int kMaxPairs = 16384;
 const char *kNames[kKernelCount] = {
     "rotate_scale", "chunk_simt", "parallel_simt", "groupnorm", "recurrent_step",
-    "gemm_simt", "chunk_tc", "gemm_tc", "state_pass", "swish_gate"};
+    "gemm_simt", "chunk_tc", "gemm_tc", "state_pass", "swish_gate",
+    "bwd_rows", "bwd_values", "unrotate"};
 
 struct Slot {
   std::vector<cudaEvent_t> start, stop;

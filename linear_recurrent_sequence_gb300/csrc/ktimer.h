@@ -18,6 +18,9 @@ enum KernelId {
   kKGemmTc,
   kKStatePass,
   kKGate,
+  kKBwdRows,
+  kKBwdValues,
+  kKUnrotate,
   kKernelCount
 };
 

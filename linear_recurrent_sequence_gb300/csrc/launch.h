@@ -86,4 +86,18 @@ cudaError_t launch_gemm_tc(const void *A, const void *Bm, void *C, int M, int N,
 cudaError_t launch_gemm_bf16(const void *A, const void *Bm, void *C, int M, int N,
                              int K, int out_bf16, cudaStream_t st);
 
+// backward.cu: gradients on CUDA cores (fp32).  Z, Qr, Kr: rotated
+// contiguous fp32 [B*H][N][d_k]; dO through so[] (out dtype); row outputs
+// fp32 [B*H][N][d_k]; dv through sv[] (in dtype); states fp32 [B*H][d_k][d_v].
+// rev = false: dQ' from S_in (T0) and K' (Z); rev = true: dK' from dS_out
+// (T0) and Q' (Z).
+cudaError_t launch_bwd_rows(const KParams &p, bool rev, const float *Z, const void *v,
+                            const void *dO, const float *T0, float *out, cudaStream_t st);
+cudaError_t launch_bwd_values(const KParams &p, const float *Qr, const float *Kr,
+                              const void *dO, const float *dS_out, void *dv, float *dS_in,
+                              cudaStream_t st);
+// x (contiguous fp32 [B*H][N][d_k]) turned by e^{-i t theta} into out (strides s).
+cudaError_t launch_unrotate(const KParams &p, const float *x, const long long s[3], void *out,
+                            int out_bf16, cudaStream_t st);
+
 }  // namespace ret

@@ -61,6 +61,9 @@ _SIGS = {
                                                 _P, _P, ctypes.c_size_t, _P]),
     "retention_chunkwise_fwd_noalloc": (ctypes.c_int, [ctypes.POINTER(RetDesc), _P, _P, _P, _P,
                                                        _P, _P, _P, _P, _P]),
+    "retention_backward_workspace_size": (ctypes.c_size_t, [ctypes.POINTER(RetDesc)]),
+    "retention_chunkwise_bwd": (ctypes.c_int, [ctypes.POINTER(RetDesc), _P, _P, _P, _P, _P,
+                                               _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
     "msr_workspace_size": (ctypes.c_size_t, [ctypes.POINTER(MsrDesc)]),
     "retention_gemm_bf16": (ctypes.c_int, [_P, _P, _P, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                            _P, ctypes.c_size_t, _P]),
@@ -203,6 +206,40 @@ def chunkwise_fwd(q, k, v, gamma, *, chunk=64, norm_flags=0, gn_eps=1e-6, pos0=0
                                      _ptr(workspace), workspace.numel(), _stream(stream))
     _check(st, "retention_chunkwise_fwd")
     return out
+
+
+def backward_workspace_size(desc):
+    return int(lib.retention_backward_workspace_size(ctypes.byref(desc)))
+
+
+def chunkwise_bwd(q, k, v, dO, gamma, *, norm_flags=0, pos0=0, rotate=True,
+                  theta_base=10000.0, S_in=None, dS_out=None, dS_in=None, dq=None, dk=None,
+                  dv=None, workspace=None, stream=None):
+    """Gradients of retention without GroupNorm (gn_eps < 0) and without the
+    third normalisation: returns (dq, dk, dv, dS_in).  dq, dk, dv take the
+    layouts and dtype of q, k, v; dS_in (fp32 [B,H,d_k,d_v]) is returned only
+    when passed in (it may be dS_out itself)."""
+    if not (q.dtype == k.dtype == v.dtype):
+        raise TypeError("q, k, v must share one dtype")
+
+    def like(x, given, name):
+        if given is None:
+            return torch.empty_strided(x.shape, x.stride(), dtype=x.dtype, device=x.device)
+        if given.shape != x.shape or given.stride() != x.stride() or given.dtype != x.dtype:
+            raise ValueError(f"{name} must have the shape, strides and dtype of its input")
+        return given
+
+    dq, dk, dv = like(q, dq, "dq"), like(k, dk, "dk"), like(v, dv, "dv")
+    d, g = make_desc(q, k, v, dO, gamma, norm_flags=norm_flags, gn_eps=None, pos0=pos0,
+                     rotate=rotate, theta_base=theta_base)
+    if workspace is None:
+        workspace = new_workspace(backward_workspace_size(d), q.device)
+    st = lib.retention_chunkwise_bwd(ctypes.byref(d), _ptr(q), _ptr(k), _ptr(v), _ptr(S_in),
+                                     _ptr(dO), _ptr(dS_out), _ptr(dq), _ptr(dk), _ptr(dv),
+                                     _ptr(dS_in), _ptr(workspace), workspace.numel(),
+                                     _stream(stream))
+    _check(st, "retention_chunkwise_bwd")
+    return dq, dk, dv, dS_in
 
 
 def chunkwise_fwd_noalloc(q, k, v, gamma, *, chunk=64, norm_flags=0, gn_eps=1e-6, pos0=0,

@@ -140,3 +140,28 @@ def test_msr_workspace_and_checks(R):
     assert ws >= 2 * 4096 * (2 * 8 * 256 + 3 * 8 * 512) * 2
     m2, g2 = R.msr_desc(2, 4096, 2048, 8, 3, 512, [0.9] * 8)  # odd d_k
     assert R.lib.msr_workspace_size(ctypes.byref(m2)) == 0
+
+
+def test_backward_checks(R):
+    dummy = ctypes.c_void_p(256)
+
+    def bwd(d, dO=dummy, ws=dummy, nbytes=1 << 30):
+        return R.lib.retention_chunkwise_bwd(ctypes.byref(d), dummy, dummy, dummy, None, dO,
+                                             None, dummy, dummy, dummy, None, ws, nbytes, None)
+    # GroupNorm on (the descriptor default) and the third normalisation are
+    # not differentiated: RET_EUNSUPPORTED before any launch.
+    d, g = _desc(R)
+    assert bwd(d) == 2
+    d, g = _desc(R, gn_eps=-1.0, norm_flags=4)
+    assert bwd(d) == 2
+    d, g = _desc(R, gn_eps=-1.0, norm_flags=3)
+    need = R.lib.retention_backward_workspace_size(ctypes.byref(d))
+    rows = 1 * 2 * 8 * 4 * 4  # B*H*N*d_k fp32 bytes
+    assert need == 256 + 4 * ((rows + 255) // 256 * 256)
+    assert bwd(d, dO=None) == 1
+    assert bwd(d, nbytes=need - 1) == 3
+    d, g = _desc(R, gn_eps=-1.0, d_k=3)
+    assert R.lib.retention_backward_workspace_size(ctypes.byref(d)) == 0
+    assert bwd(d) == 1
+    d, g = _desc(R, gn_eps=-1.0, B=0)
+    assert bwd(d, dO=None) == 0
