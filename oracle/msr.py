@@ -1,4 +1,5 @@
-"""Gated multi-scale retention layer, float64 -- TEST INFRASTRUCTURE ONLY.
+"""Gated multi-scale retention layer and the RetNet block, float64 -- TEST
+INFRASTRUCTURE ONLY.
 
 MSR(X) = (swish(X W_G) (.) Y) W_O with Y = GroupNorm_h(head_1, ..., head_H)
 and head_h = Retention(X, gamma_h), Q = (X W_Q) (.) Theta,
@@ -41,3 +42,36 @@ def msr_layer(X, WQ, WK, WV, WG, WO, *, H, dk, dv, gamma, chunk,
     o, _, _ = chunkwise(p, chunk, q, k, v)
     Y = o.transpose(0, 2, 1, 3).reshape(B, N, H * dv)
     return (swish(G) * Y) @ np.asarray(WO, dtype=np.float64)
+
+
+def layernorm(x, w, b, eps):
+    """LayerNorm over the last axis: (x - mean) / sqrt(var + eps) * w + b, with
+    the biased variance (the mean of squared deviations)."""
+    x = np.asarray(x, dtype=np.float64)
+    mu = x.mean(axis=-1, keepdims=True)
+    var = ((x - mu) ** 2).mean(axis=-1, keepdims=True)
+    return (x - mu) / np.sqrt(var + eps) * np.asarray(w, np.float64) + np.asarray(b, np.float64)
+
+
+def gelu(x):
+    """x * Phi(x), Phi the standard normal distribution function, written with
+    the error function: Phi(x) = (1 + erf(x / sqrt(2))) / 2."""
+    from scipy.special import erf
+    x = np.asarray(x, dtype=np.float64)
+    return 0.5 * x * (1.0 + erf(x / np.sqrt(2.0)))
+
+
+def retnet_block(X, ln1_w, ln1_b, WQ, WK, WV, WG, WO, ln2_w, ln2_b, W1, W2, *, H, dk, dv,
+                 gamma, chunk, ln_eps=1e-5, theta_base=10000.0, norm_flags=0, gn_eps=1e-6,
+                 pos0=0, threads=0):
+    """One RetNet block (m0nads.wordpress.com "A dubious successor to
+    Transformer", section "Overall architecture": MSR and FFN, each after a
+    LayerNorm and each with a skip connection):
+        Y = MSR(LN(X)) + X,   X' = FFN(LN(Y)) + Y,   FFN(x) = gelu(x W1) W2.
+    The pages name the FFN but not its activation; GELU is the reading taken."""
+    X = np.asarray(X, dtype=np.float64)
+    Y = msr_layer(layernorm(X, ln1_w, ln1_b, ln_eps), WQ, WK, WV, WG, WO, H=H, dk=dk, dv=dv,
+                  gamma=gamma, chunk=chunk, theta_base=theta_base, norm_flags=norm_flags,
+                  gn_eps=gn_eps, pos0=pos0, threads=threads) + X
+    F = gelu(layernorm(Y, ln2_w, ln2_b, ln_eps) @ np.asarray(W1, np.float64))
+    return F @ np.asarray(W2, np.float64) + Y
