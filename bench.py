@@ -409,6 +409,8 @@ def run_ours(args):
     if not args.skip_extra:
         extra["decode"] = bench_decode(args, R, dev, stream, hbm, world, max_over_ranks)
         extra["msr_layer"] = bench_msr(args, R, dev, stream, tflops, world, max_over_ranks)
+        extra["backward"] = bench_backward(args, R, dev, world, max_over_ranks)
+        extra["retnet_block"] = bench_block(args, R, dev, tflops, world, max_over_ranks)
 
     cpu = None
     if rank == 0 and not args.skip_cpu:
@@ -504,6 +506,103 @@ def bench_msr(args, R, dev, stream, tflops, world, max_over_ranks):
     return {"tokens_per_s": world * B * Nm / (ms * 1e-3), "ms": ms,
             "gemm_TFLOPs": gemm_flops / (ms * 1e-3) / 1e12,
             "frac_bf16_peak_if_all_gemm": gemm_flops / (ms * 1e-3) / 1e12 / tflops}
+
+
+def bench_block(args, R, dev, tflops, world, max_over_ranks):
+    """One RetNet block (LN, MSR, skip; LN, FFN, skip) at the MSR layer's
+    shape with an FFN of 4096: B=2, N=4096, d_model=2048, H=8."""
+    import torch
+    from linear_recurrent_sequence_gb300 import synth
+    B, Nm, dm, Hm, dk, dv, dff = 2, 4096, 2048, 8, 256, 512, 4096
+    X = gen_bf16((B, Nm, dm), 5001, dev)
+    W = [gen_bf16(s, 5002 + i, dev) * 0.02 for i, s in enumerate(
+        [(dm, Hm * dk), (dm, Hm * dk), (dm, Hm * dv), (dm, Hm * dv), (Hm * dv, dm),
+         (dm, dff), (dff, dm)])]
+    ones, zeros = (torch.ones(dm, device=dev), torch.zeros(dm, device=dev))
+    gam = synth.head_gammas(Hm)
+    d, _g = R.block_desc(B, Nm, dm, Hm, dk, dv, dff, gam, chunk=128, norm_flags=R.NORM_ALL)
+    ws = R.new_workspace(int(R.lib.retnet_block_workspace_size(d)), dev)
+    Y = torch.empty(B, Nm, dm, dtype=torch.bfloat16, device=dev)
+
+    def f():
+        R.retnet_block_fwd(X, ones, zeros, *W[:5], ones, zeros, W[5], W[6], H=Hm, d_k=dk,
+                           d_v=dv, gamma=gam, chunk=128, norm_flags=R.NORM_ALL, out=Y,
+                           workspace=ws)
+    for _ in range(2):
+        f()
+    torch.cuda.synchronize()
+    reps = 3
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        f()
+    e1.record()
+    torch.cuda.synchronize()
+    ms = max_over_ranks(e0.elapsed_time(e1)) / reps
+    T = B * Nm
+    gemm_flops = 2.0 * T * dm * (2 * Hm * dk + 2 * Hm * dv) + 2.0 * T * Hm * dv * dm + \
+        2.0 * 2 * T * dm * dff
+    del X, W, Y, ws
+    torch.cuda.empty_cache()
+    return {"tokens_per_s": world * T / (ms * 1e-3), "ms": ms,
+            "gemm_TFLOPs": gemm_flops / (ms * 1e-3) / 1e12,
+            "frac_bf16_peak_if_all_gemm": gemm_flops / (ms * 1e-3) / 1e12 / tflops,
+            "config": {"B": B, "N": Nm, "d_model": dm, "H": Hm, "d_k": dk, "d_v": dv,
+                       "d_ffn": dff}}
+
+
+def flops_bwd_per_token_head(C):
+    # Algorithmic flops of the chunkwise backward per (token, head): three
+    # retention-shaped passes (dQ', dK', dV), each with the causal half of
+    # its intra-chunk scores and products, a cross term and a carry.
+    return 2 * (3 * (C + 1) / 2 * (DK + DV) + 6 * DK * DV)
+
+
+# fp32 CUDA-core peak: 152 SMs x 128 FP32 lanes x 2 flops (FMA) x 2.07 GHz.
+FP32_ALU_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
+
+
+def bench_backward(args, R, dev, world, max_over_ranks):
+    """Gradients of retention (no GroupNorm, no normalisations) at the
+    headline shape, bf16 inputs: dq, dk, dv from dO, fp32 on CUDA cores."""
+    import torch
+    from linear_recurrent_sequence_gb300 import synth
+    gam = synth.head_gammas(H)
+    q = gen_bf16((1, H, N, DK), 4001, dev)
+    k = gen_bf16((1, H, N, DK), 4002, dev)
+    v = gen_bf16((1, H, N, DV), 4003, dev)
+    dO = gen_bf16((1, H, N, DV), 4004, dev)
+    dq, dk_, dv_ = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    d, _g = R.make_desc(q, k, v, dO, gam, gn_eps=None)
+    ws = R.new_workspace(R.backward_workspace_size(d), dev)
+
+    def f():
+        R.chunkwise_bwd(q, k, v, dO, gam, dq=dq, dk=dk_, dv=dv_, workspace=ws)
+    f()
+    f()
+    torch.cuda.synchronize()
+    R.lib.retention_kernel_timer_reset()
+    R.lib.retention_kernel_timer_enable(1)
+    reps = 3
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        f()
+    e1.record()
+    torch.cuda.synchronize()
+    R.lib.retention_kernel_timer_enable(0)
+    kt = {name: ms / max(n, 1) for name, (ms, n, t) in R.kernel_times().items()}
+    ms = max_over_ranks(e0.elapsed_time(e1)) / reps
+    fl = flops_bwd_per_token_head(16) * H * N
+    achieved = fl / (ms * 1e-3) / 1e12
+    del q, k, v, dO, dq, dk_, dv_, ws
+    torch.cuda.empty_cache()
+    return {"tokens_per_s": world * N / (ms * 1e-3), "ms": ms,
+            "kernel_ms": kt,
+            "roofline": {"bound": "alu", "achieved": achieved, "peak": FP32_ALU_TFLOPS,
+                         "unit": "TFLOP/s", "frac": achieved / FP32_ALU_TFLOPS,
+                         "note": "algorithmic flops at 16-token chunks; peak derived from "
+                                 "the unit counts and the maximum SM clock"}}
 
 
 def main():

@@ -244,6 +244,30 @@ ret_status msr_layer_fwd(const msr_desc *d, const void *X, const void *WQ,
                          const void *WO, void *Y, void *ws, size_t ws_bytes,
                          ret_stream_t stream);
 
+/* One RetNet block [m0nads, "Overall architecture": an MSR and an FFN, each
+ * after a LayerNorm, each with a skip connection]:
+ *   Y  = MSR(LN1(X)) + X,    X' = FFN(LN2(Y)) + Y,    FFN(x) = gelu(x W1) W2,
+ * LN(x) = (x - mean) / sqrt(var + ln_eps) (.) w + b over d_model (biased
+ * variance), gelu(x) = x Phi(x).  The pages name the FFN but not its
+ * activation; GELU is the reading taken.
+ * X, Xout: [B, N, d_model] bf16 contiguous (Xout may alias X); ln*_w, ln*_b:
+ * fp32 [d_model] device arrays; W_Q..W_O as for msr_layer_fwd; W1:
+ * [d_model, d_ffn], W2: [d_ffn, d_model] bf16 row-major.  Intermediates are
+ * rounded to bf16 between the steps.  d_model <= 32768. */
+typedef struct {
+  msr_desc msr;  /* the MSR layer: shapes, decays, normalisations          */
+  int d_ffn;     /* FFN hidden width                                       */
+  float ln_eps;  /* LayerNorm epsilon (>= 0)                               */
+} retnet_block_desc;
+
+size_t retnet_block_workspace_size(const retnet_block_desc *d);
+
+ret_status retnet_block_fwd(const retnet_block_desc *d, const void *X, const float *ln1_w,
+                            const float *ln1_b, const void *WQ, const void *WK, const void *WV,
+                            const void *WG, const void *WO, const float *ln2_w,
+                            const float *ln2_b, const void *W1, const void *W2, void *Xout,
+                            void *ws, size_t ws_bytes, ret_stream_t stream);
+
 /* Human-readable text of a status code (static storage). */
 const char *retention_status_string(ret_status s);
 

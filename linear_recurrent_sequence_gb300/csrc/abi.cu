@@ -553,6 +553,71 @@ ret_status msr_layer_fwd(const msr_desc *m, const void *X, const void *WQ, const
   return RET_OK;
 }
 
+// ------------------------------------------------------------ RetNet block
+static bool block_ok(const retnet_block_desc *d) {
+  if (!d || !msr_ok(&d->msr)) return false;
+  if (d->d_ffn < 1 || d->msr.d_model > 32768) return false;
+  if (!(d->ln_eps >= 0.f)) return false;
+  return msr_workspace_size(&d->msr) > 0;
+}
+
+struct BlockWs {
+  size_t msr, xn, y, hf, total;
+};
+
+// The MSR layer's workspace comes first, so that its status word is the
+// block's.
+static BlockWs block_ws(const retnet_block_desc *d) {
+  BlockWs w;
+  const size_t T = (size_t)d->msr.B * d->msr.N;
+  size_t off = 0;
+  w.msr = off; off = align256(off + msr_workspace_size(&d->msr));
+  w.xn = off; off = align256(off + T * d->msr.d_model * 2);
+  w.y = off; off = align256(off + T * d->msr.d_model * 2);
+  w.hf = off; off = align256(off + T * (size_t)d->d_ffn * 2);
+  w.total = off;
+  return w;
+}
+
+size_t retnet_block_workspace_size(const retnet_block_desc *d) {
+  if (!block_ok(d)) return 0;
+  return block_ws(d).total;
+}
+
+ret_status retnet_block_fwd(const retnet_block_desc *d, const void *X, const float *ln1_w,
+                            const float *ln1_b, const void *WQ, const void *WK, const void *WV,
+                            const void *WG, const void *WO, const float *ln2_w,
+                            const float *ln2_b, const void *W1, const void *W2, void *Xout,
+                            void *ws, size_t ws_bytes, ret_stream_t stream) {
+  RET_RANGE("retnet_block_fwd");
+  if (!block_ok(d)) return RET_EINVAL;
+  const BlockWs w = block_ws(d);
+  ret_status rs = check_ws(ws, ws_bytes, w.total);
+  if (rs != RET_OK) return rs;
+  const long long T = (long long)d->msr.B * d->msr.N;
+  if (T == 0) return RET_OK;
+  if (!X || !ln1_w || !ln1_b || !WQ || !WK || !WV || !WG || !WO || !ln2_w || !ln2_b || !W1 ||
+      !W2 || !Xout)
+    return RET_EINVAL;
+  cudaStream_t st = (cudaStream_t)stream;
+  const int dm = d->msr.d_model;
+  void *Xn = at<char>(ws, w.xn), *Y = at<char>(ws, w.y), *Hf = at<char>(ws, w.hf);
+  unsigned *status = reinterpret_cast<unsigned *>(ws);
+  // Y = MSR(LN(X)) + X
+  RET_CUDA(RET_TIMED_LAUNCH(kKLayerNorm, st, launch_layernorm(X, ln1_w, ln1_b, Xn, T, dm, d->ln_eps, st)));
+  rs = msr_layer_fwd(&d->msr, Xn, WQ, WK, WV, WG, WO, Y, at<char>(ws, w.msr), w.xn - w.msr,
+                     stream);
+  if (rs != RET_OK) return rs;
+  RET_CUDA(RET_TIMED_LAUNCH(kKResidual, st, launch_residual_add(Y, X, T * dm, st)));
+  // X' = gelu(LN(Y) W1) W2 + Y   (X is not read again: Xout may alias it)
+  RET_CUDA(RET_TIMED_LAUNCH(kKLayerNorm, st, launch_layernorm(Y, ln2_w, ln2_b, Xn, T, dm, d->ln_eps, st)));
+  RET_CUDA(gemm_any(Xn, W1, Hf, (int)T, d->d_ffn, dm, status, st));
+  RET_CUDA(RET_TIMED_LAUNCH(kKGelu, st, launch_gelu(Hf, T * d->d_ffn, st)));
+  RET_CUDA(gemm_any(Hf, W2, Xout, (int)T, dm, d->d_ffn, status, st));
+  RET_CUDA(RET_TIMED_LAUNCH(kKResidual, st, launch_residual_add(Xout, Y, T * dm, st)));
+  return RET_OK;
+}
+
 ret_status retention_gemm_bf16(const void *A, const void *Bm, void *C, int M, int N, int K,
                                void *ws, size_t ws_bytes, ret_stream_t stream) {
   RET_RANGE("retention_gemm_bf16");

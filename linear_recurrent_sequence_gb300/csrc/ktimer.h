@@ -21,6 +21,9 @@ enum KernelId {
   kKBwdRows,
   kKBwdValues,
   kKUnrotate,
+  kKLayerNorm,
+  kKResidual,
+  kKGelu,
   kKernelCount
 };
 

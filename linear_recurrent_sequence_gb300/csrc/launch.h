@@ -100,4 +100,11 @@ cudaError_t launch_bwd_values(const KParams &p, const float *Qr, const float *Kr
 cudaError_t launch_unrotate(const KParams &p, const float *x, const long long s[3], void *out,
                             int out_bf16, cudaStream_t st);
 
+// block.cu: the RetNet block's LayerNorm (bf16 rows of d, fp32 gain and
+// bias), skip connection y <- y + r and in-place GELU (bf16, n values).
+cudaError_t launch_layernorm(const void *x, const float *w, const float *b, void *y, long long rows,
+                             int d, float eps, cudaStream_t st);
+cudaError_t launch_residual_add(void *y, const void *r, long long n, cudaStream_t st);
+cudaError_t launch_gelu(void *y, long long n, cudaStream_t st);
+
 }  // namespace ret

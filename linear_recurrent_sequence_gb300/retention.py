@@ -43,6 +43,10 @@ class MsrDesc(ctypes.Structure):
                 ("gn_eps", ctypes.c_float), ("pos0", ctypes.c_int64)]
 
 
+class BlockDesc(ctypes.Structure):
+    _fields_ = [("msr", MsrDesc), ("d_ffn", ctypes.c_int), ("ln_eps", ctypes.c_float)]
+
+
 # Every symbol include/retention.h declares, with its ctypes signature.
 _P = ctypes.c_void_p
 _SIGS = {
@@ -69,6 +73,9 @@ _SIGS = {
                                            _P, ctypes.c_size_t, _P]),
     "msr_layer_fwd": (ctypes.c_int, [ctypes.POINTER(MsrDesc), _P, _P, _P, _P, _P, _P, _P, _P,
                                      ctypes.c_size_t, _P]),
+    "retnet_block_workspace_size": (ctypes.c_size_t, [ctypes.POINTER(BlockDesc)]),
+    "retnet_block_fwd": (ctypes.c_int, [ctypes.POINTER(BlockDesc)] + [_P] * 14 +
+                         [ctypes.c_size_t, _P]),
     "retention_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "retention_last_cuda_error": (ctypes.c_int, []),
     "retention_poll_status": (ctypes.c_int, [_P, _P]),
@@ -333,6 +340,46 @@ def msr_layer_fwd(X, WQ, WK, WV, WG, WO, *, H, d_k, d_v, gamma, chunk=128, norm_
                            _ptr(WO), _ptr(out), _ptr(workspace), workspace.numel(),
                            _stream(stream))
     _check(st, "msr_layer_fwd")
+    return out
+
+
+def block_desc(B, N, d_model, H, d_k, d_v, d_ffn, gamma, *, chunk=128, norm_flags=0,
+               gn_eps=1e-6, ln_eps=1e-5, pos0=0, theta_base=10000.0):
+    m, g = msr_desc(B, N, d_model, H, d_k, d_v, gamma, chunk=chunk, norm_flags=norm_flags,
+                    gn_eps=gn_eps, pos0=pos0, theta_base=theta_base)
+    d = BlockDesc()
+    d.msr = m
+    d.d_ffn = int(d_ffn)
+    d.ln_eps = float(ln_eps)
+    return d, g
+
+
+def retnet_block_fwd(X, ln1_w, ln1_b, WQ, WK, WV, WG, WO, ln2_w, ln2_b, W1, W2, *, H, d_k, d_v,
+                     gamma, chunk=128, norm_flags=0, gn_eps=1e-6, ln_eps=1e-5, pos0=0,
+                     theta_base=10000.0, out=None, workspace=None, stream=None):
+    """One RetNet block: Y = MSR(LN1(X)) + X, X' = gelu(LN2(Y) W1) W2 + Y.
+    bf16 activations and weights, fp32 LayerNorm gains and biases."""
+    B, N, dm = X.shape
+    d, g = block_desc(B, N, dm, H, d_k, d_v, W1.shape[1], gamma, chunk=chunk,
+                      norm_flags=norm_flags, gn_eps=gn_eps, ln_eps=ln_eps, pos0=pos0,
+                      theta_base=theta_base)
+    if out is None:
+        out = torch.empty((B, N, dm), dtype=torch.bfloat16, device=X.device)
+    if workspace is None:
+        workspace = new_workspace(int(lib.retnet_block_workspace_size(ctypes.byref(d))),
+                                  X.device)
+    for name, t in (("X", X), ("WQ", WQ), ("WK", WK), ("WV", WV), ("WG", WG), ("WO", WO),
+                    ("W1", W1), ("W2", W2)):
+        if t.dtype != torch.bfloat16 or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous bf16 tensor")
+    for name, t in (("ln1_w", ln1_w), ("ln1_b", ln1_b), ("ln2_w", ln2_w), ("ln2_b", ln2_b)):
+        if t.dtype != torch.float32 or not t.is_contiguous() or t.numel() != dm:
+            raise ValueError(f"{name} must be a contiguous fp32 tensor of d_model values")
+    st = lib.retnet_block_fwd(ctypes.byref(d), _ptr(X), _ptr(ln1_w), _ptr(ln1_b), _ptr(WQ),
+                              _ptr(WK), _ptr(WV), _ptr(WG), _ptr(WO), _ptr(ln2_w), _ptr(ln2_b),
+                              _ptr(W1), _ptr(W2), _ptr(out), _ptr(workspace), workspace.numel(),
+                              _stream(stream))
+    _check(st, "retnet_block_fwd")
     return out
 
 

@@ -24,7 +24,8 @@ _M2 = np.uint64(0x94D049BB133111EB)
 
 # Stream ids: one sub-stream per named tensor.
 STREAMS = {"q": 1, "k": 2, "v": 3, "x": 4, "wq": 5, "wk": 6, "wv": 7, "wg": 8,
-           "wo": 9, "S": 10, "z": 11, "dq": 12, "dk": 13, "dv": 14, "dO": 15, "dS": 16}
+           "wo": 9, "S": 10, "z": 11, "dq": 12, "dk": 13, "dv": 14, "dO": 15, "dS": 16,
+           "w1": 17, "w2": 18, "ln": 19}
 
 
 def _mix(z: np.ndarray) -> np.ndarray:

@@ -165,3 +165,26 @@ def test_backward_checks(R):
     assert bwd(d) == 1
     d, g = _desc(R, gn_eps=-1.0, B=0)
     assert bwd(d, dO=None) == 0
+
+
+def test_block_layout_workspace_and_checks(R):
+    assert ctypes.sizeof(R.BlockDesc) == 72
+    d, g = R.block_desc(2, 4096, 2048, 8, 256, 512, 4096, [0.9] * 8)
+    m, g2 = R.msr_desc(2, 4096, 2048, 8, 256, 512, [0.9] * 8)
+    need = R.lib.retnet_block_workspace_size(ctypes.byref(d))
+    T = 2 * 4096
+    assert need >= R.lib.msr_workspace_size(ctypes.byref(m)) + T * (2 * 2048 + 4096) * 2
+    dummy = ctypes.c_void_p(256)
+    args = [dummy] * 13
+    # missing weight, small workspace, bad FFN width, bad LayerNorm epsilon
+    bad = list(args)
+    bad[11] = None
+    assert R.lib.retnet_block_fwd(ctypes.byref(d), *bad, dummy, need, None) == 1
+    assert R.lib.retnet_block_fwd(ctypes.byref(d), *args, dummy, need - 1, None) == 3
+    d.d_ffn = 0
+    assert R.lib.retnet_block_workspace_size(ctypes.byref(d)) == 0
+    d.d_ffn, d.ln_eps = 4096, -1.0
+    assert R.lib.retnet_block_fwd(ctypes.byref(d), *args, dummy, need, None) == 1
+    d.ln_eps = 1e-5
+    d.msr.B = 0
+    assert R.lib.retnet_block_fwd(ctypes.byref(d), *([None] * 13), dummy, 1 << 30, None) == 0
