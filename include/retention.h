@@ -268,6 +268,40 @@ ret_status retnet_block_fwd(const retnet_block_desc *d, const void *X, const flo
                             const float *ln2_b, const void *W1, const void *W2, void *Xout,
                             void *ws, size_t ws_bytes, ret_stream_t stream);
 
+/* One decode step of a stack of RetNet blocks [m0nads, "Overall
+ * architecture": L stacked blocks; hwhale, the recurrent form for
+ * inference]: B sequences advance by one token through n_layers blocks, each
+ * layer's retention on its own recurrent state.  `block` gives the shapes
+ * shared by every layer (block.msr.N is ignored: one token, at absolute
+ * position block.msr.pos0).  Per layer, as retnet_block_fwd with N = 1:
+ *   Y1 = MSR(LN1(X)) + X with the decode step on S[l] (and z[l]),
+ *   X  = gelu(LN2(Y1) W1) W2 + Y1.
+ * X: [B, d_model] bf16, the token's input on entry and the stack's output on
+ * return.  layers: HOST array of n_layers records of DEVICE pointers (layouts
+ * as for retnet_block_fwd).  S: HOST array of n_layers DEVICE pointers to fp32
+ * [B, H, d_k, d_v] states (16-byte aligned), read and updated in place;
+ * z: HOST array of fp32 [B, H, d_k] row-sum states, needed only with
+ * RET_NORM_RSUM (may be NULL otherwise).  Requires d_v % 4 == 0.
+ * Projections with up to 16 rows (B <= 16) stream the weights with split-K
+ * partial sums added in a fixed order. */
+typedef struct {
+  retnet_block_desc block;
+  int n_layers;
+} retnet_stack_desc;
+
+typedef struct {
+  const float *ln1_w, *ln1_b;
+  const void *WQ, *WK, *WV, *WG, *WO;
+  const float *ln2_w, *ln2_b;
+  const void *W1, *W2;
+} retnet_layer_weights;
+
+size_t retnet_decode_workspace_size(const retnet_stack_desc *d);
+
+ret_status retnet_decode_step(const retnet_stack_desc *d, const retnet_layer_weights *layers,
+                              float *const *S, float *const *z, void *X, void *ws,
+                              size_t ws_bytes, ret_stream_t stream);
+
 /* Human-readable text of a status code (static storage). */
 const char *retention_status_string(ret_status s);
 

@@ -618,6 +618,136 @@ ret_status retnet_block_fwd(const retnet_block_desc *d, const void *X, const flo
   return RET_OK;
 }
 
+// ------------------------------------------------- multi-layer decode step
+struct DecWs {
+  size_t xn, q, k, v, g, y, m, h1, part, total;
+};
+
+static size_t dec_partial_bytes(const retnet_stack_desc *d) {
+  const msr_desc &m = d->block.msr;
+  const int B = m.B, dm = m.d_model, HK = m.H * m.d_k, HV = m.H * m.d_v, F = d->block.d_ffn;
+  if (B > 16) return 0;
+  const size_t c[5] = {gemm_skinny_partial_bytes(B, HK, dm), gemm_skinny_partial_bytes(B, HV, dm),
+                       gemm_skinny_partial_bytes(B, dm, HV), gemm_skinny_partial_bytes(B, F, dm),
+                       gemm_skinny_partial_bytes(B, dm, F)};
+  size_t mx = 0;
+  for (size_t x : c) mx = x > mx ? x : mx;
+  return mx;
+}
+
+static DecWs dec_ws(const retnet_stack_desc *d) {
+  DecWs w;
+  const msr_desc &m = d->block.msr;
+  const size_t B = m.B, dm = m.d_model, HK = (size_t)m.H * m.d_k, HV = (size_t)m.H * m.d_v;
+  size_t off = kStatusBytes;
+  w.xn = off; off = align256(off + B * dm * 2);
+  w.q = off; off = align256(off + B * HK * 2);
+  w.k = off; off = align256(off + B * HK * 2);
+  w.v = off; off = align256(off + B * HV * 2);
+  w.g = off; off = align256(off + B * HV * 2);
+  w.y = off; off = align256(off + B * HV * 2);
+  w.m = off; off = align256(off + B * dm * 2);
+  w.h1 = off; off = align256(off + B * (size_t)d->block.d_ffn * 2);
+  w.part = off; off = align256(off + dec_partial_bytes(d));
+  w.total = off;
+  return w;
+}
+
+// The descriptor of one layer's decode step on the [B, H*d] projection rows.
+static void dec_step_desc(const retnet_stack_desc *d, ret_desc *r) {
+  const msr_desc &m = d->block.msr;
+  retention_desc_init(r, m.B, m.H, 1, m.d_k, m.d_v, m.gamma);
+  r->theta_base = m.theta_base;
+  r->norm_flags = m.norm_flags;
+  r->gn_eps = m.gn_eps;
+  r->pos0 = m.pos0;
+  r->rotate = 1;
+  const int64_t HK = (int64_t)m.H * m.d_k, HV = (int64_t)m.H * m.d_v;
+  r->sq[0] = r->sk[0] = HK;
+  r->sq[1] = r->sk[1] = m.d_k;
+  r->sq[2] = r->sk[2] = HK;
+  r->sv[0] = r->so[0] = HV;
+  r->sv[1] = r->so[1] = m.d_v;
+  r->sv[2] = r->so[2] = HV;
+}
+
+static bool dec_ok(const retnet_stack_desc *d) {
+  if (!d || d->n_layers < 0 || !block_ok(&d->block)) return false;
+  ret_desc r;
+  dec_step_desc(d, &r);
+  return desc_ok(&r) && r.d_v % 4 == 0;
+}
+
+size_t retnet_decode_workspace_size(const retnet_stack_desc *d) {
+  if (!dec_ok(d)) return 0;
+  return dec_ws(d).total;
+}
+
+// Decode-batch GEMM: the weight-streaming kernel for up to 16 rows, else the
+// general path.
+static cudaError_t gemm_dec(const void *A, const void *Bm, void *C, int M, int N, int K,
+                            float *part, unsigned *status, cudaStream_t st) {
+  if (gemm_skinny_supported(A, Bm, C, M, N, K)) {
+    cudaError_t e = RET_TIMED_LAUNCH(kKGemmSkinny, st, launch_gemm_skinny(A, Bm, M, N, K, part, st));
+    if (e != cudaSuccess) return e;
+    return RET_TIMED_LAUNCH(kKSkinnyReduce, st, launch_skinny_reduce(part, C, M, N, K, st));
+  }
+  return gemm_any(A, Bm, C, M, N, K, status, st);
+}
+
+ret_status retnet_decode_step(const retnet_stack_desc *d, const retnet_layer_weights *layers,
+                              float *const *S, float *const *z, void *X, void *ws,
+                              size_t ws_bytes, ret_stream_t stream) {
+  RET_RANGE("retnet_decode_step");
+  if (!dec_ok(d)) return RET_EINVAL;
+  const DecWs w = dec_ws(d);
+  ret_status rs = check_ws(ws, ws_bytes, w.total);
+  if (rs != RET_OK) return rs;
+  const msr_desc &m = d->block.msr;
+  if (m.B == 0 || d->n_layers == 0) return RET_OK;
+  if (!X || !layers || !S) return RET_EINVAL;
+  const bool rsum = (m.norm_flags & RET_NORM_RSUM) != 0;
+  if (rsum && !z) return RET_EINVAL;
+  for (int l = 0; l < d->n_layers; ++l) {
+    const retnet_layer_weights &L = layers[l];
+    if (!L.ln1_w || !L.ln1_b || !L.WQ || !L.WK || !L.WV || !L.WG || !L.WO || !L.ln2_w ||
+        !L.ln2_b || !L.W1 || !L.W2 || !S[l] || (reinterpret_cast<uintptr_t>(S[l]) & 15))
+      return RET_EINVAL;
+    if (rsum && !z[l]) return RET_EINVAL;
+  }
+  cudaStream_t st = (cudaStream_t)stream;
+  const int B = m.B, dm = m.d_model, HK = m.H * m.d_k, HV = m.H * m.d_v, F = d->block.d_ffn;
+  void *Xn = at<char>(ws, w.xn), *Q = at<char>(ws, w.q), *K = at<char>(ws, w.k);
+  void *V = at<char>(ws, w.v), *G = at<char>(ws, w.g), *Y = at<char>(ws, w.y);
+  void *Mo = at<char>(ws, w.m), *H1 = at<char>(ws, w.h1);
+  float *part = at<float>(ws, w.part);
+  unsigned *status = reinterpret_cast<unsigned *>(ws);
+  ret_desc rd;
+  dec_step_desc(d, &rd);
+  KParams p;
+  make_params(&rd, ws, p);
+  for (int l = 0; l < d->n_layers; ++l) {
+    const retnet_layer_weights &L = layers[l];
+    // Y1 = MSR(LN1(X)) + X, the retention step on this layer's state.
+    RET_CUDA(RET_TIMED_LAUNCH(kKLayerNorm, st, launch_layernorm(X, L.ln1_w, L.ln1_b, Xn, B, dm, d->block.ln_eps, st)));
+    RET_CUDA(gemm_dec(Xn, L.WQ, Q, B, HK, dm, part, status, st));
+    RET_CUDA(gemm_dec(Xn, L.WK, K, B, HK, dm, part, status, st));
+    RET_CUDA(gemm_dec(Xn, L.WV, V, B, HV, dm, part, status, st));
+    RET_CUDA(gemm_dec(Xn, L.WG, G, B, HV, dm, part, status, st));
+    RET_CUDA(RET_TIMED_LAUNCH(kKRecurrent, st, launch_recurrent_step(p, Q, K, V, S[l], rsum ? z[l] : nullptr, Y, st)));
+    RET_CUDA(RET_TIMED_LAUNCH(kKGate, st, launch_swish_gate(Y, G, (long long)B * HV, st)));
+    RET_CUDA(gemm_dec(Y, L.WO, Mo, B, dm, HV, part, status, st));
+    RET_CUDA(RET_TIMED_LAUNCH(kKResidual, st, launch_residual_add(Mo, X, (long long)B * dm, st)));
+    // X = gelu(LN2(Y1) W1) W2 + Y1.
+    RET_CUDA(RET_TIMED_LAUNCH(kKLayerNorm, st, launch_layernorm(Mo, L.ln2_w, L.ln2_b, Xn, B, dm, d->block.ln_eps, st)));
+    RET_CUDA(gemm_dec(Xn, L.W1, H1, B, F, dm, part, status, st));
+    RET_CUDA(RET_TIMED_LAUNCH(kKGelu, st, launch_gelu(H1, (long long)B * F, st)));
+    RET_CUDA(gemm_dec(H1, L.W2, X, B, dm, F, part, status, st));
+    RET_CUDA(RET_TIMED_LAUNCH(kKResidual, st, launch_residual_add(X, Mo, (long long)B * dm, st)));
+  }
+  return RET_OK;
+}
+
 ret_status retention_gemm_bf16(const void *A, const void *Bm, void *C, int M, int N, int K,
                                void *ws, size_t ws_bytes, ret_stream_t stream) {
   RET_RANGE("retention_gemm_bf16");

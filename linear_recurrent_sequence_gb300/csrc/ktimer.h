@@ -24,6 +24,8 @@ enum KernelId {
   kKLayerNorm,
   kKResidual,
   kKGelu,
+  kKGemmSkinny,
+  kKSkinnyReduce,
   kKernelCount
 };
 

@@ -107,4 +107,15 @@ cudaError_t launch_layernorm(const void *x, const float *w, const float *b, void
 cudaError_t launch_residual_add(void *y, const void *r, long long n, cudaStream_t st);
 cudaError_t launch_gelu(void *y, long long n, cudaStream_t st);
 
+// gemm_skinny.cu: C[M,N] = A[M,K] B[K,N] for M <= 16 rows (bf16 row-major,
+// fp32 accumulation), split over K into fp32 partials [split][M][N] that
+// launch_skinny_reduce adds in order into bf16 C.  Needs N % 8 == 0 and a
+// 16-byte aligned B.
+bool gemm_skinny_supported(const void *A, const void *Bm, const void *C, int M, int N, int K);
+size_t gemm_skinny_partial_bytes(int M, int N, int K);
+cudaError_t launch_gemm_skinny(const void *A, const void *Bm, int M, int N, int K,
+                               float *partial, cudaStream_t st);
+cudaError_t launch_skinny_reduce(const float *partial, void *C, int M, int N, int K,
+                                 cudaStream_t st);
+
 }  // namespace ret

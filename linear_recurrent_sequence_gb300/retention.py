@@ -47,6 +47,17 @@ class BlockDesc(ctypes.Structure):
     _fields_ = [("msr", MsrDesc), ("d_ffn", ctypes.c_int), ("ln_eps", ctypes.c_float)]
 
 
+class StackDesc(ctypes.Structure):
+    _fields_ = [("block", BlockDesc), ("n_layers", ctypes.c_int)]
+
+
+LAYER_KEYS = ("ln1_w", "ln1_b", "WQ", "WK", "WV", "WG", "WO", "ln2_w", "ln2_b", "W1", "W2")
+
+
+class LayerWeights(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in LAYER_KEYS]
+
+
 # Every symbol include/retention.h declares, with its ctypes signature.
 _P = ctypes.c_void_p
 _SIGS = {
@@ -76,6 +87,11 @@ _SIGS = {
     "retnet_block_workspace_size": (ctypes.c_size_t, [ctypes.POINTER(BlockDesc)]),
     "retnet_block_fwd": (ctypes.c_int, [ctypes.POINTER(BlockDesc)] + [_P] * 14 +
                          [ctypes.c_size_t, _P]),
+    "retnet_decode_workspace_size": (ctypes.c_size_t, [ctypes.POINTER(StackDesc)]),
+    "retnet_decode_step": (ctypes.c_int, [ctypes.POINTER(StackDesc), ctypes.POINTER(LayerWeights),
+                                          ctypes.POINTER(ctypes.c_void_p),
+                                          ctypes.POINTER(ctypes.c_void_p), _P, _P,
+                                          ctypes.c_size_t, _P]),
     "retention_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "retention_last_cuda_error": (ctypes.c_int, []),
     "retention_poll_status": (ctypes.c_int, [_P, _P]),
@@ -381,6 +397,52 @@ def retnet_block_fwd(X, ln1_w, ln1_b, WQ, WK, WV, WG, WO, ln2_w, ln2_b, W1, W2, 
                               _stream(stream))
     _check(st, "retnet_block_fwd")
     return out
+
+
+def stack_desc(B, d_model, H, d_k, d_v, d_ffn, n_layers, gamma, *, pos, norm_flags=0,
+               gn_eps=1e-6, ln_eps=1e-5, theta_base=10000.0):
+    b, g = block_desc(B, 1, d_model, H, d_k, d_v, d_ffn, gamma, norm_flags=norm_flags,
+                      gn_eps=gn_eps, ln_eps=ln_eps, pos0=pos, theta_base=theta_base)
+    d = StackDesc()
+    d.block = b
+    d.n_layers = int(n_layers)
+    return d, g
+
+
+def retnet_decode_step(X, layers, S, z=None, *, H, d_k, d_v, gamma, pos, norm_flags=0,
+                       gn_eps=1e-6, ln_eps=1e-5, theta_base=10000.0, workspace=None,
+                       stream=None):
+    """One decode step of a stack of RetNet blocks: X [B, d_model] bf16 is the
+    token's input and is overwritten with the stack's output; `layers` is a
+    list of dicts with the keys LAYER_KEYS (bf16 weights, fp32 LayerNorm
+    gains and biases); S (and z, with the third normalisation) lists of the
+    layers' fp32 states, updated in place."""
+    if X.dim() != 2 or X.dtype != torch.bfloat16 or not X.is_contiguous():
+        raise ValueError("X must be a contiguous bf16 [B, d_model] tensor")
+    B, dm = X.shape
+    n = len(layers)
+    if len(S) != n or (z is not None and len(z) != n):
+        raise ValueError("one state per layer")
+    d_ffn = layers[0]["W1"].shape[1] if n else 1
+    d, g = stack_desc(B, dm, H, d_k, d_v, d_ffn, n, gamma, pos=pos, norm_flags=norm_flags,
+                      gn_eps=gn_eps, ln_eps=ln_eps, theta_base=theta_base)
+    if workspace is None:
+        workspace = new_workspace(int(lib.retnet_decode_workspace_size(ctypes.byref(d))),
+                                  X.device)
+    recs = (LayerWeights * max(n, 1))()
+    for i, L in enumerate(layers):
+        for k in LAYER_KEYS:
+            t = L[k]
+            want = torch.float32 if k.startswith("ln") else torch.bfloat16
+            if t.dtype != want or not t.is_contiguous():
+                raise ValueError(f"layer {i} {k}: contiguous {want} expected")
+            setattr(recs[i], k, t.data_ptr())
+    Sp = (ctypes.c_void_p * max(n, 1))(*[s.data_ptr() for s in S])
+    zp = None if z is None else (ctypes.c_void_p * max(n, 1))(*[t.data_ptr() for t in z])
+    st = lib.retnet_decode_step(ctypes.byref(d), recs, Sp, zp, _ptr(X), _ptr(workspace),
+                                workspace.numel(), _stream(stream))
+    _check(st, "retnet_decode_step")
+    return X
 
 
 def gemm_bf16(A, B, out=None, workspace=None, stream=None):

@@ -188,3 +188,36 @@ def test_block_layout_workspace_and_checks(R):
     d.ln_eps = 1e-5
     d.msr.B = 0
     assert R.lib.retnet_block_fwd(ctypes.byref(d), *([None] * 13), dummy, 1 << 30, None) == 0
+
+
+def test_decode_stack_layout_and_checks(R):
+    assert ctypes.sizeof(R.StackDesc) == 80 and ctypes.sizeof(R.LayerWeights) == 88
+    d, g = R.stack_desc(4, 2048, 8, 256, 512, 4096, 2, [0.9] * 8, pos=10)
+    need = R.lib.retnet_decode_workspace_size(ctypes.byref(d))
+    assert need >= 256 + 4 * (2 * 2048 + 2 * 2048 + 3 * 4096 + 2 * 2048 + 4096)
+    dummy = ctypes.c_void_p(256)
+    recs = (R.LayerWeights * 2)()
+    for i in range(2):
+        for k in R.LAYER_KEYS:
+            setattr(recs[i], k, 256)
+    S = (ctypes.c_void_p * 2)(256, 256)
+    # a missing weight, a misaligned state, a small workspace, the third
+    # normalisation without z
+    recs[1].W2 = None
+    assert R.lib.retnet_decode_step(ctypes.byref(d), recs, S, None, dummy, dummy, need, None) == 1
+    recs[1].W2 = 256
+    S[1] = 260
+    assert R.lib.retnet_decode_step(ctypes.byref(d), recs, S, None, dummy, dummy, need, None) == 1
+    S[1] = 256
+    assert R.lib.retnet_decode_step(ctypes.byref(d), recs, S, None, dummy, dummy, need - 1,
+                                    None) == 3
+    d4, g4 = R.stack_desc(4, 2048, 8, 256, 512, 4096, 2, [0.9] * 8, pos=10, norm_flags=4)
+    need4 = R.lib.retnet_decode_workspace_size(ctypes.byref(d4))
+    assert R.lib.retnet_decode_step(ctypes.byref(d4), recs, S, None, dummy, dummy, need4,
+                                    None) == 1
+    # d_v % 4 != 0 and an empty stack
+    d5, g5 = R.stack_desc(4, 64, 2, 16, 6, 32, 1, [0.9] * 2, pos=0)
+    assert R.lib.retnet_decode_workspace_size(ctypes.byref(d5)) == 0
+    d6, g6 = R.stack_desc(4, 2048, 8, 256, 512, 4096, 0, [0.9] * 8, pos=0)
+    assert R.lib.retnet_decode_step(ctypes.byref(d6), None, None, None, None, dummy, 1 << 20,
+                                    None) == 0
