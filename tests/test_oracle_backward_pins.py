@@ -11,7 +11,8 @@ mathematics fixes, independently of the gradient code itself:
     <dq, q> = <dO, o> and <dk, k> + <dS_in, S_in> = <dv, v> + <dS_in, S_in> = L;
   * textbook special cases: gamma = 1 without rotation is causal linear
     attention (dQ = tril(dO V^T) K, dK = tril(dO V^T)^T Q,
-    dV = tril(Q K^T)^T dO); gamma = 0 keeps only each token's own term.
+    dV = tril(Q K^T)^T dO); gamma = 0 keeps only each token's own term;
+  * a two-token example worked by hand (tests/golden/).
 
 The forward they differentiate is the recurrent form of
 hwhale.com/article/285883 (S_n = gamma S_{n-1} + K_n^T V_n, O_n = Q_n S_n)
@@ -159,6 +160,7 @@ MUTANTS = [
 ]
 
 PINS = [
+    lambda: test_hand_derived_two_token_gradients(),
     lambda: test_gradient_matches_finite_differences("all", True, TWO_NORMS),
     lambda: test_gradient_matches_finite_differences("S", True, TWO_NORMS),
     lambda: test_euler_identities(True, True),
@@ -191,3 +193,23 @@ def test_planted_gradient_mistakes_are_caught(desc, find, repl):
         assert caught, f"planted mistake not caught: {desc}"
     finally:
         shutil.rmtree(tmp, ignore_errors=True)
+
+
+def test_hand_derived_two_token_gradients():
+    """tests/golden/backward_two_tokens_hand.txt: a two-token example worked
+    by hand (derivation in the file)."""
+    path = os.path.join(os.path.dirname(__file__), "golden", "backward_two_tokens_hand.txt")
+    want = {}
+    for line in open(path):
+        if line.startswith("#") or "|" not in line:
+            continue
+        name, vals = (s.strip() for s in line.split("|"))
+        want[name] = np.array([float(x) for x in vals.split()])
+    p = Problem(1, 1, 2, 2, 1, 0.5, rotate=False, norm_flags=0, gn_eps=-1.0)
+    q = np.array([[1.0, 0.0], [0.0, 1.0]])[None, None]
+    k = np.array([[1.0, 1.0], [2.0, 0.0]])[None, None]
+    v = np.array([[3.0], [-1.0]])[None, None]
+    dO = np.array([[1.0], [2.0]])[None, None]
+    dq, dk, dv, dS = oracle.recurrent_bwd(p, q, k, v, dO)
+    for name, got in (("dq", dq), ("dk", dk), ("dv", dv), ("dS_in", dS)):
+        assert np.max(np.abs(got.ravel() - want[name])) < 1e-15, name
