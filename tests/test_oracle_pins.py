@@ -223,6 +223,26 @@ def test_hand_derived_two_token_example():
     assert abs(o[0, 0, 0, 0] - 2.0) < 1e-14
 
 
+def test_hand_derived_negative_row_sum():
+    """The third normalisation divides by |sum R| when the row sum is below
+    -1 (tests/golden/retention_negative_rowsum_hand.txt)."""
+    q = np.array([[1.0, 0.0], [-3.0, 0.0]])[None, None]
+    k = np.array([[1.0, 0.0], [1.0, 0.0]])[None, None]
+    v = np.array([[2.0], [3.0]])[None, None]
+    rows = _golden_rows("retention_negative_rowsum_hand.txt")
+    assert len(rows) == 3
+    for name, flags, expect in rows:
+        exp = np.array([eval(e, {"math": math}) for e in expect.split(";")])
+        p = Problem(1, 1, 2, 2, 1, 0.5, theta_base=10000.0, rotate=True,
+                    norm_flags=int(flags), gn_eps=-1.0)
+        for f in (oracle.parallel, oracle.closed_form):
+            assert np.max(np.abs(f(p, q, k, v)[0, 0, :, 0] - exp)) < 1e-14, name
+        assert np.max(np.abs(oracle.recurrent(p, q, k, v)[0][0, 0, :, 0] - exp)) < 1e-14, name
+        for chunk in (1, 2):
+            got = oracle.chunkwise(p, chunk, q, k, v)[0][0, 0, :, 0]
+            assert np.max(np.abs(got - exp)) < 1e-14, (name, chunk)
+
+
 def test_hand_derived_groupnorm():
     for eps, xs, expect in _golden_rows("groupnorm_hand.txt"):
         x = np.array([float(t) for t in xs.split()])
@@ -245,6 +265,7 @@ MUTANTS = [
     ("parallel decay exponent", "std::pow(g, n - m) : 0.0", "std::pow(g, n - m + 1) : 0.0"),
     ("theta exponent", "std::pow(base, -2.0 * j / static_cast<double>(d))",
      "std::pow(base, -1.0 * j / static_cast<double>(d))"),
+    ("third normalisation without the absolute value", "std::fabs(rowsum)", "rowsum"),
 ]
 
 PINS = [
@@ -255,6 +276,7 @@ PINS = [
     test_gamma_one_no_rotation_is_causal_linear_attention,
     test_gamma_zero_keeps_only_the_diagonal,
     test_hand_derived_two_token_example,
+    test_hand_derived_negative_row_sum,
     test_hand_derived_groupnorm,
     lambda: test_decay_row_sum_is_geometric_series(0.9),
     test_rotation_preserves_norm_and_relative_phase,
@@ -321,3 +343,46 @@ def test_msr_layer_matches_direct_loops():
     ref = np.array([[[sum(Z[b, n, j] * WO[j, i] for j in range(H * dv)) for i in range(d)]
                      for n in range(N)] for b in range(B)])
     assert relerr(out, ref) < 1e-12
+
+
+# ------------------------------------------------------------------ swish
+# The gate's swish(x) = x sigmoid(x) (m0nads.wordpress.com "A dubious
+# successor to Transformer", section "Last piece: Gated Multi-Scale
+# Retention"; sigmoid with unit slope), pinned by what the mathematics fixes
+# rather than by a second copy of its formula:
+#   swish(0) = 0;  swish(x) - swish(-x) = x  (since sigmoid(x) + sigmoid(-x) = 1);
+#   swish(x)/x -> 1 as x -> +inf and swish(x) -> 0 as x -> -inf;
+#   swish(1) = 1/(1 + e^-1) = 0.7310585786300049 (the logistic function at 1,
+#   printed to 16 digits from its series value).
+SWISH_AT_1 = 0.7310585786300049
+
+
+def _swish_pins(sw):
+    assert sw(np.array([0.0]))[0] == 0.0
+    x = np.linspace(-30.0, 30.0, 241)
+    assert np.max(np.abs(sw(x) - sw(-x) - x)) < 1e-12
+    assert abs(sw(np.array([1.0]))[0] - SWISH_AT_1) < 1e-15
+    big = np.array([40.0, 60.0])
+    assert np.max(np.abs(sw(big) / big - 1.0)) < 1e-15
+    assert np.max(np.abs(sw(-big))) < 1e-15
+
+
+def test_swish_pins():
+    from oracle.msr import swish
+    _swish_pins(swish)
+
+
+SWISH_MUTANTS = [
+    ("sigmoid of -x", lambda x: x / (1.0 + np.exp(x))),
+    ("slope 2", lambda x: x / (1.0 + np.exp(-2.0 * x))),
+    ("tanh gate", lambda x: x * np.tanh(x)),
+    ("sigmoid without x", lambda x: 1.0 / (1.0 + np.exp(-x))),
+    ("x times (1 + sigmoid)", lambda x: x + x / (1.0 + np.exp(-x))),
+]
+
+
+@pytest.mark.parametrize("desc,sw", SWISH_MUTANTS, ids=[m[0] for m in SWISH_MUTANTS])
+def test_swish_mutants_are_caught(desc, sw):
+    with np.errstate(over="ignore"):
+        with pytest.raises(AssertionError):
+            _swish_pins(sw)
