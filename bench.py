@@ -319,6 +319,10 @@ def run_ours(args):
                 "peak_source": f"{src} (MEASURED_PEAKS.json hbm_gbs)" if src == "measured"
                 else "fallback 6.8 TB/s",
                 "alg_bytes_per_launch": alg_bytes, "avg_launch_us": avg_s * 1e6,
+                "path": {"achieved": alg_bytes / (ms / args.steps * 1e-3) / 1e9,
+                         "frac": alg_bytes / (ms / args.steps * 1e-3) / 1e9 / hbm,
+                         "note": "the same algorithmic bytes over the whole step "
+                                 "(every kernel of the path)"},
                 "kernels": {k2: {"ms_total": v2[0], "launches": v2[1]}
                             for k2, v2 in ktimes.items()}}
     # The same kernel against the dense bf16 tensor-core peak (burst figure:
@@ -408,6 +412,7 @@ def run_ours(args):
     extra = {}
     if not args.skip_extra:
         extra["decode"] = bench_decode(args, R, dev, stream, hbm, world, max_over_ranks)
+        extra["decode_stack"] = bench_decode_stack(args, R, dev, hbm, world, max_over_ranks)
         extra["msr_layer"] = bench_msr(args, R, dev, stream, tflops, world, max_over_ranks)
         extra["backward"] = bench_backward(args, R, dev, world, max_over_ranks)
         extra["retnet_block"] = bench_block(args, R, dev, tflops, world, max_over_ranks)
@@ -456,23 +461,113 @@ def bench_decode(args, R, dev, stream, hbm, world, max_over_ranks):
         for _ in range(max(1, args.warmup // 3)):
             S.copy_(S0)
             g.replay()
-        S.copy_(S0)
-        torch.cuda.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record()
-        g.replay()
-        e1.record()
-        torch.cuda.synchronize()
-        ms = max_over_ranks(e0.elapsed_time(e1))
+        # Each replay runs all the steps from the same prefilled state; the
+        # median of the replays is reported with their spread.
+        times = []
+        for _ in range(args.decode_reps):
+            S.copy_(S0)
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            g.replay()
+            e1.record()
+            torch.cuda.synchronize()
+            times.append(max_over_ranks(e0.elapsed_time(e1)))
+        times.sort()
+        ms = times[len(times) // 2]
         state_bytes = B * H * DK * DV * 4 * 2  # read + write per step
         gbs = state_bytes * STEPS / (ms * 1e-3) / 1e9
         out[f"B{B}"] = {"steps_per_s": STEPS / (ms * 1e-3),
                         "tokens_per_s": world * B * STEPS / (ms * 1e-3),
                         "us_per_step": 1e3 * ms / STEPS, "state_GBps": gbs,
-                        "frac_hbm": gbs / hbm,
+                        "frac_hbm": gbs / hbm, "replays": len(times),
+                        "us_per_step_min_max": [1e3 * times[0] / STEPS,
+                                                1e3 * times[-1] / STEPS],
                         "note": "state fits in L2" if state_bytes / 2 < 100e6 else "HBM-bound"}
         del q, k, v, S, S0, o, g
         torch.cuda.empty_cache()
+    return out
+
+
+# 6.7B-scale block shapes for the multi-layer decode step: d_model 4096,
+# 16 heads of d_k 256 / d_v 512, FFN 8192.  Bytes of bf16 weights per layer.
+STACK_DM, STACK_H, STACK_FFN = 4096, 16, 8192
+STACK_WEIGHT_BYTES = 2 * (2 * STACK_DM * STACK_H * DK + 3 * STACK_DM * STACK_H * DV
+                          + 2 * STACK_DM * STACK_FFN)
+
+
+def bench_decode_stack(args, R, dev, hbm, world, max_over_ranks):
+    """One decode step of a stack of RetNet blocks (LayerNorm, projections,
+    the recurrent retention step on the layer's state, gate, W_O, skip,
+    LayerNorm, FFN, skip) with synthetic 6.7B-scale weights, B sequences
+    advancing one token.  A CUDA graph of `stack_steps` steps is replayed
+    `decode_reps` times; the median is reported.  Bytes per step: every
+    layer's weights once plus its state read and written."""
+    import torch
+    from linear_recurrent_sequence_gb300 import synth
+    L, dm, Hs, dff = args.stack_layers, STACK_DM, STACK_H, STACK_FFN
+    gam = synth.head_gammas(Hs)
+    shapes = dict(WQ=(dm, Hs * DK), WK=(dm, Hs * DK), WV=(dm, Hs * DV), WG=(dm, Hs * DV),
+                  WO=(Hs * DV, dm), W1=(dm, dff), W2=(dff, dm))
+    layers = []
+    for li in range(L):
+        W = {k: gen_bf16(shp, 6000 + 16 * li + i, dev) * 0.02
+             for i, (k, shp) in enumerate(shapes.items())}
+        for k in ("ln1_w", "ln2_w"):
+            W[k] = torch.ones(dm, device=dev)
+        for k in ("ln1_b", "ln2_b"):
+            W[k] = torch.zeros(dm, device=dev)
+        layers.append(W)
+    out = {"config": {"layers": L, "d_model": dm, "H": Hs, "d_k": DK, "d_v": DV, "d_ffn": dff,
+                      "weight_bytes_per_layer": STACK_WEIGHT_BYTES,
+                      "steps_per_graph": args.stack_steps, "replays": args.decode_reps}}
+    P = 1024
+    for B in args.decode_batches:
+        S = [torch.zeros(B, Hs, DK, DV, device=dev) for _ in range(L)]
+        X = gen_bf16((B, dm), 6500 + B, dev)
+        d, _g = R.stack_desc(B, dm, Hs, DK, DV, dff, L, gam, pos=P)
+        ws = R.new_workspace(int(R.lib.retnet_decode_workspace_size(d)), dev)
+
+        def run(t):
+            R.retnet_decode_step(X, layers, S, H=Hs, d_k=DK, d_v=DV, gamma=gam, pos=P + t,
+                                 workspace=ws)
+        for t in range(2):
+            run(t)
+        torch.cuda.synchronize()
+        R.lib.retention_kernel_timer_reset()
+        launches0 = int(R.lib.retention_launch_count())
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for t in range(args.stack_steps):
+                run(t)
+        per_step_launches = (int(R.lib.retention_launch_count()) - launches0) // args.stack_steps
+        for _ in range(2):
+            g.replay()
+        times = []
+        for _ in range(args.decode_reps):
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            g.replay()
+            e1.record()
+            torch.cuda.synchronize()
+            times.append(max_over_ranks(e0.elapsed_time(e1)))
+        times.sort()
+        ms = times[len(times) // 2] / args.stack_steps
+        state_bytes = L * B * Hs * DK * DV * 4 * 2
+        byts = L * STACK_WEIGHT_BYTES + state_bytes
+        out[f"B{B}"] = {"us_per_step": 1e3 * ms, "us_per_layer": 1e3 * ms / L,
+                        "tokens_per_s": world * B / (ms * 1e-3),
+                        "weight_GBps": L * STACK_WEIGHT_BYTES / (ms * 1e-3) / 1e9,
+                        "GBps_weights_and_state": byts / (ms * 1e-3) / 1e9,
+                        "frac_hbm": byts / (ms * 1e-3) / 1e9 / hbm,
+                        "kernels_per_step": per_step_launches,
+                        "us_per_step_min_max": [1e3 * times[0] / args.stack_steps,
+                                                1e3 * times[-1] / args.stack_steps]}
+        del S, X, ws, g
+        torch.cuda.empty_cache()
+    del layers
+    torch.cuda.empty_cache()
     return out
 
 
@@ -614,6 +709,9 @@ def main():
     ap.add_argument("--chunk", type=int, default=64)
     ap.add_argument("--decode-steps", type=int, default=2048)
     ap.add_argument("--decode-batches", type=int, nargs="*", default=[1, 8, 32, 128])
+    ap.add_argument("--decode-reps", type=int, default=5)
+    ap.add_argument("--stack-layers", type=int, default=4)
+    ap.add_argument("--stack-steps", type=int, default=16)
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--skip-extra", action="store_true")
     ap.add_argument("--skip-cpu", action="store_true")

@@ -202,8 +202,13 @@ ret_status retention_chunkwise_bwd(const ret_desc *d, const void *q, const void 
  *     (cudaGetSymbolAddress); make that first call before any stream capture.
  *   - All calls share the one array: calls that may overlap on the GPU (on
  *     different streams, or from several threads) race and must not be used.
- *   - No memory is allocated or freed.  Device-side status words are cleared
- *     at the start of each call and are not reported.
+ *   - No memory is allocated or freed.  The device status word at the start
+ *     of the array is cleared at the start of each call and is not
+ *     reported: if a bounded device-side wait ran out (possible only when
+ *     the GPU stalls for seconds), that call's outputs are undefined and
+ *     this entry point cannot tell the caller.  Callers that must detect
+ *     it use retention_chunkwise_fwd with their own workspace and
+ *     retention_poll_status.
  */
 #define RET_NOALLOC_SCRATCH_BYTES (32u << 20)
 ret_status retention_chunkwise_fwd_noalloc(const ret_desc *d, const void *q,
@@ -232,9 +237,15 @@ size_t msr_workspace_size(const msr_desc *d);
 /* The layer's projections as a plain GEMM [m0nads, "Gated Multi-Scale
  * Retention": X W_Q, X W_K, X W_V, X W_G, Y W_O]: C[M,N] = A[M,K] B[K,N],
  * bf16 row-major device buffers, fp32 accumulation, bf16 result.  Runs on
- * the tensor cores when M % 128 == 0, N % 256 == 0, K % 64 == 0 and the
- * pointers are 16-byte aligned, on CUDA cores otherwise.  ws: at least 256
- * bytes (the device status word). */
+ * the tensor cores when N % 256 == 0, K % 64 == 0 and the pointers are
+ * 16-byte aligned (any M; 128-row tiles, the rows past M neither read nor
+ * written).  With 1 <= M <= 16 rows (a decode batch),
+ * N % 8 == 0, a 16-byte aligned B and a workspace of at least
+ * retention_gemm_workspace_size(M, N, K) bytes it runs on the
+ * weight-streaming kernel (split-K fp32 partials in the workspace, added in
+ * a fixed order); every other shape runs on CUDA cores.  ws: at least 256
+ * bytes (the device status word), 256-byte aligned. */
+size_t retention_gemm_workspace_size(int M, int N, int K);
 ret_status retention_gemm_bf16(const void *A, const void *B, void *C, int M, int N, int K,
                                void *ws, size_t ws_bytes, ret_stream_t stream);
 
@@ -282,6 +293,10 @@ ret_status retnet_block_fwd(const retnet_block_desc *d, const void *X, const flo
  * [B, H, d_k, d_v] states (16-byte aligned), read and updated in place;
  * z: HOST array of fp32 [B, H, d_k] row-sum states, needed only with
  * RET_NORM_RSUM (may be NULL otherwise).  Requires d_v % 4 == 0.
+ * Aliasing: X is updated in place and must not overlap the workspace; each
+ * S[l] and z[l] is updated in place and must not overlap X, the workspace
+ * or each other (RET_EINVAL where a state overlaps X or the workspace).
+ * Weights are only read and may be shared between layers.
  * Projections with up to 16 rows (B <= 16) stream the weights with split-K
  * partial sums added in a fixed order. */
 typedef struct {

@@ -230,6 +230,13 @@ T *at(void *ws, size_t off) {
   return reinterpret_cast<T *>(reinterpret_cast<char *>(ws) + off);
 }
 
+// Do the byte ranges [a, a + na) and [b, b + nb) share a byte?
+bool overlaps(const void *a, size_t na, const void *b, size_t nb) {
+  if (!a || !b || na == 0 || nb == 0) return false;
+  const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+  return x < y + nb && y < x + na;
+}
+
 ret_status check_ws(void *ws, size_t have, size_t need) {
   if (need > 0 && (!ws || have < need)) return RET_EWORKSPACE;
   if (ws && (reinterpret_cast<uintptr_t>(ws) & 255)) return RET_EWORKSPACE;
@@ -715,6 +722,19 @@ ret_status retnet_decode_step(const retnet_stack_desc *d, const retnet_layer_wei
       return RET_EINVAL;
     if (rsum && !z[l]) return RET_EINVAL;
   }
+  // X is the only buffer updated in place besides the states; it must not
+  // overlap the workspace, and no state may overlap X or the workspace.
+  const size_t xbytes = (size_t)m.B * m.d_model * 2;
+  const size_t sbytes = (size_t)m.B * m.H * m.d_k * m.d_v * sizeof(float);
+  const size_t zbytes = (size_t)m.B * m.H * m.d_k * sizeof(float);
+  if (overlaps(X, xbytes, ws, w.total)) return RET_EINVAL;
+  for (int l = 0; l < d->n_layers; ++l) {
+    if (overlaps(S[l], sbytes, X, xbytes) || overlaps(S[l], sbytes, ws, w.total))
+      return RET_EINVAL;
+    if (rsum && (overlaps(z[l], zbytes, X, xbytes) || overlaps(z[l], zbytes, ws, w.total) ||
+                 overlaps(z[l], zbytes, S[l], sbytes)))
+      return RET_EINVAL;
+  }
   cudaStream_t st = (cudaStream_t)stream;
   const int B = m.B, dm = m.d_model, HK = m.H * m.d_k, HV = m.H * m.d_v, F = d->block.d_ffn;
   void *Xn = at<char>(ws, w.xn), *Q = at<char>(ws, w.q), *K = at<char>(ws, w.k);
@@ -748,6 +768,14 @@ ret_status retnet_decode_step(const retnet_stack_desc *d, const retnet_layer_wei
   return RET_OK;
 }
 
+size_t retention_gemm_workspace_size(int M, int N, int K) {
+  if (M < 0 || N < 0 || K < 1) return 0;
+  size_t need = kStatusBytes;
+  if (M >= 1 && M <= 16 && N >= 8 && N % 8 == 0)
+    need += align256(gemm_skinny_partial_bytes(M, N, K));
+  return need;
+}
+
 ret_status retention_gemm_bf16(const void *A, const void *Bm, void *C, int M, int N, int K,
                                void *ws, size_t ws_bytes, ret_stream_t stream) {
   RET_RANGE("retention_gemm_bf16");
@@ -756,7 +784,15 @@ ret_status retention_gemm_bf16(const void *A, const void *Bm, void *C, int M, in
   if (!A || !Bm || !C) return RET_EINVAL;
   ret_status rs = check_ws(ws, ws_bytes, kStatusBytes);
   if (rs != RET_OK) return rs;
-  RET_CUDA(gemm_any(A, Bm, C, M, N, K, reinterpret_cast<unsigned *>(ws), (cudaStream_t)stream));
+  cudaStream_t st = (cudaStream_t)stream;
+  unsigned *status = reinterpret_cast<unsigned *>(ws);
+  // Few rows with room for the split-K partials: the weight-streaming kernel.
+  if (gemm_skinny_supported(A, Bm, C, M, N, K) &&
+      ws_bytes >= retention_gemm_workspace_size(M, N, K)) {
+    RET_CUDA(gemm_dec(A, Bm, C, M, N, K, at<float>(ws, kStatusBytes), status, st));
+    return RET_OK;
+  }
+  RET_CUDA(gemm_any(A, Bm, C, M, N, K, status, st));
   return RET_OK;
 }
 

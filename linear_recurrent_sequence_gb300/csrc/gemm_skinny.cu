@@ -97,16 +97,16 @@ bool gemm_skinny_supported(const void *A, const void *Bm, const void *C, int M, 
          reinterpret_cast<uintptr_t>(Bm) % 16 == 0 && A && C;
 }
 
-// Slices of K: about two CTAs per SM, at most kSkMaxSplit slices, at most
-// kSkMaxRowsPerSlice rows per slice, and at most K / (16 M) slices so that
-// the fp32 partials (split * M * N * 4 bytes) stay near 1/8 of B's bytes.
+// Slices of K: about two CTAs per SM of a 152-SM GB300, at most kSkMaxSplit
+// slices, at most kSkMaxRowsPerSlice rows per slice, and at most K / (16 M)
+// slices so that the fp32 partials (split * M * N * 4 bytes) stay near 1/8
+// of B's bytes.  The plan depends on the shape alone (not on the device
+// that happens to be current), so a workspace sized for a shape always fits
+// the launch of that shape.
+constexpr int kSkPlanSms = 152;
 static void skinny_plan(int M, int N, int K, int &split, int &rows) {
-  int dev = 0, sms = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess ||
-      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-    sms = 1;
   const int colblocks = (N + kSkCtaCols - 1) / kSkCtaCols;
-  int s = (2 * sms + colblocks - 1) / colblocks;
+  int s = (2 * kSkPlanSms + colblocks - 1) / colblocks;
   s = s < kSkMaxSplit ? s : kSkMaxSplit;
   const int sm = K / (16 * (M > 0 ? M : 1));
   s = s < sm ? s : sm;

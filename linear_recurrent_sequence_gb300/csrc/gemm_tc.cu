@@ -66,7 +66,9 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   uint32_t *tbase_p = reinterpret_cast<uint32_t *>(sm + kOffMisc);
   volatile int *abort_p = reinterpret_cast<volatile int *>(sm + kOffMisc + 4);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int tiles_n = N / BN, tiles = (M / BM) * tiles_n, nk = K / BK;
+  // M may be ragged: the last row tile's missing rows of A are outside the
+  // tensor map and arrive as zeros; their rows of C are not stored.
+  const int tiles_n = N / BN, tiles = ((M + BM - 1) / BM) * tiles_n, nk = K / BK;
 
   if (tid == 0) {
     for (int i = 0; i < kStages; ++i) {
@@ -168,12 +170,14 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       if (!ok) break;
       tc::tc_fence_after();
       const int m0 = (t / tiles_n) * BM, n0 = (t % tiles_n) * BN;
-      __nv_bfloat16 *crow = C + (long long)(m0 + row) * N + n0;
+      const bool live = m0 + row < M;  // the TMEM loads stay warp-wide
+      __nv_bfloat16 *crow = C + (long long)(live ? m0 + row : 0) * N + n0;
       for (int g = 0; g < BN / 32; ++g) {
         uint32_t r[32];
         tc::tmem_ld32(tb + lb + buf * BN + g * 32, r);
         tc::tmem_ld_wait();
         uint4 *dst = reinterpret_cast<uint4 *>(crow + g * 32);
+        if (!live) continue;
         if constexpr (kGate) {
           // C <- swish(acc) (.) C: fast exponential and divide, a few ulp in
           // fp32 before the bf16 rounding; swish -> 0 as acc -> -inf.
@@ -219,7 +223,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
 
 bool gemm_tc_supported(const void *A, const void *Bm, const void *C, int M, int N, int K) {
   if (M <= 0 || N <= 0 || K <= 0) return false;
-  if (M % BM || N % BN || K % BK) return false;
+  if (N % BN || K % BK) return false;
   if ((reinterpret_cast<uintptr_t>(A) | reinterpret_cast<uintptr_t>(Bm) |
        reinterpret_cast<uintptr_t>(C)) & 15)
     return false;
@@ -246,7 +250,7 @@ cudaError_t launch_gemm_tc(const void *A, const void *Bm, void *C, int M, int N,
   int dev = 0, sms = 0;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  const int tiles = (M / BM) * (N / BN);
+  const int tiles = ((M + BM - 1) / BM) * (N / BN);
   const int grid = tiles < sms ? tiles : sms;
   kern<<<grid, kNT, kSmem, st>>>(ta, tbm, reinterpret_cast<__nv_bfloat16 *>(C), M, N, K, status);
   return cudaGetLastError();

@@ -76,7 +76,7 @@ cudaError_t launch_recurrent_step(const KParams &p, const void *q, const void *k
                                   cudaStream_t st);
 
 // gemm_tc.cu: tensor-core C[M,N] = A[M,K] B[K,N] (bf16 row-major, fp32
-// accumulate); M % 128, N % 256, K % 64 == 0 and 16-byte aligned pointers.
+// accumulate); N % 256, K % 64 == 0 (any M >= 1) and 16-byte aligned pointers.
 bool gemm_tc_supported(const void *A, const void *Bm, const void *C, int M, int N, int K);
 // gate: C <- swish(A B) (.) C (bf16 C read and rewritten in the epilogue).
 cudaError_t launch_gemm_tc(const void *A, const void *Bm, void *C, int M, int N, int K,

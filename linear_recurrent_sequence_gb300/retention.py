@@ -80,6 +80,8 @@ _SIGS = {
     "retention_chunkwise_bwd": (ctypes.c_int, [ctypes.POINTER(RetDesc), _P, _P, _P, _P, _P,
                                                _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
     "msr_workspace_size": (ctypes.c_size_t, [ctypes.POINTER(MsrDesc)]),
+    "retention_gemm_workspace_size": (ctypes.c_size_t, [ctypes.c_int, ctypes.c_int,
+                                                        ctypes.c_int]),
     "retention_gemm_bf16": (ctypes.c_int, [_P, _P, _P, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                            _P, ctypes.c_size_t, _P]),
     "msr_layer_fwd": (ctypes.c_int, [ctypes.POINTER(MsrDesc), _P, _P, _P, _P, _P, _P, _P, _P,
@@ -452,7 +454,7 @@ def gemm_bf16(A, B, out=None, workspace=None, stream=None):
     if out is None:
         out = torch.empty((M, N), dtype=torch.bfloat16, device=A.device)
     if workspace is None:
-        workspace = new_workspace(256, A.device)
+        workspace = new_workspace(int(lib.retention_gemm_workspace_size(M, N, K)), A.device)
     _check(lib.retention_gemm_bf16(_ptr(A), _ptr(B), _ptr(out), M, N, K, _ptr(workspace),
                                    workspace.numel(), _stream(stream)), "retention_gemm_bf16")
     return out

@@ -4,7 +4,10 @@ tolerances of the parity checks.
 Tolerances (fixed numerically for the two input precisions):
   * fp32 inputs: max |gpu - ref| / max |ref| <= 1e-4 (normwise relative);
   * bf16 inputs (fp32 accumulation and state): max |gpu - ref| <= 2e-2 and
-    RMS(gpu - ref) <= 1e-2, measured after GroupNorm.
+    RMS(gpu - ref) <= 1e-2, measured after GroupNorm.  For outputs stored in
+    bf16 the max-abs bound applies to the error beyond the half ulp of the
+    storage rounding; fp32-output runs of the same workloads are checked
+    with no allowance.
 """
 import numpy as np
 import torch
@@ -36,9 +39,43 @@ def check_f32(got, ref, what=""):
     return err
 
 
+def bf16_half_ulp(x):
+    """Half the spacing of bfloat16 numbers at |x| (8 significant bits): the
+    largest error of rounding x to bf16 (normal range)."""
+    ax = np.maximum(np.abs(np.asarray(x, np.float64)), 2.0 ** -126)
+    return np.exp2(np.floor(np.log2(ax)) - 8.0)
+
+
 def check_bf16(got, ref, what=""):
+    """Max abs and RMS of got - ref after GroupNorm.  When `got` was stored
+    in bf16 (every value representable in bf16), the max-abs check measures
+    the arithmetic error: it allows, on top of the tolerance, the half ulp of
+    rounding the exact result to bf16 for storage (for a GroupNorm output of
+    |y| >= 8 that rounding alone can reach 2^-5, above the tolerance).  The
+    RMS check has no allowance."""
     d = np.abs(got - ref)
-    mx, rms = float(d.max()), float(np.sqrt((d ** 2).mean()))
+    stored_bf16 = bool(np.all(np.asarray(got, np.float32) == bf16_round(got)))
+    e = np.maximum(d - bf16_half_ulp(ref), 0.0) if stored_bf16 else d
+    mx, rms = float(e.max()), float(np.sqrt((d ** 2).mean()))
     assert mx <= TOL_BF16_MAX and rms <= TOL_BF16_RMS, \
-        f"{what}: max abs {mx:.3e} (<= {TOL_BF16_MAX}), rms {rms:.3e} (<= {TOL_BF16_RMS})"
+        f"{what}: max abs {mx:.3e} (<= {TOL_BF16_MAX}{' beyond bf16 storage' if stored_bf16 else ''}), " \
+        f"rms {rms:.3e} (<= {TOL_BF16_RMS})"
     return mx, rms
+
+
+def bf16_round(x):
+    """float64 values rounded as the GPU path stores them in bf16 (through
+    float32, then to nearest even)."""
+    return synth.bf16_bits_to_f64(synth.f32_to_bf16_bits(np.asarray(x, np.float32)))
+
+
+def split_ill_conditioned(ref, ref_rounded, axis_token=-2, tol=TOL_BF16_MAX):
+    """Boolean mask over the token axis of the tokens on which the float64
+    result changes by more than `tol` when the inputs of its steps are
+    rounded to bf16 where the GPU path stores them: there the function itself
+    amplifies the unavoidable input rounding (GroupNorm of a row whose
+    variance is near its epsilon, after a cancelling dot product), so no
+    bf16 implementation can match the unrounded result."""
+    d = np.abs(ref - ref_rounded)
+    axes = tuple(i for i in range(d.ndim) if i != d.ndim + axis_token)
+    return d.max(axis=axes) > tol

@@ -219,5 +219,31 @@ def test_decode_stack_layout_and_checks(R):
     d5, g5 = R.stack_desc(4, 64, 2, 16, 6, 32, 1, [0.9] * 2, pos=0)
     assert R.lib.retnet_decode_workspace_size(ctypes.byref(d5)) == 0
     d6, g6 = R.stack_desc(4, 2048, 8, 256, 512, 4096, 0, [0.9] * 8, pos=0)
-    assert R.lib.retnet_decode_step(ctypes.byref(d6), None, None, None, None, dummy, 1 << 20,
+    assert R.lib.retnet_decode_step(ctypes.byref(d6), None, None, None, None, dummy, 1 << 30,
                                     None) == 0
+
+
+def test_decode_stack_rejects_overlapping_buffers(R):
+    """X and the states are updated in place: a state overlapping X or the
+    workspace, or X overlapping the workspace, is refused before any launch
+    (only refused calls are made here, so nothing is launched)."""
+    d, g = R.stack_desc(4, 2048, 8, 256, 512, 4096, 2, [0.9] * 8, pos=10)
+    need = R.lib.retnet_decode_workspace_size(ctypes.byref(d))
+    ws = 1 << 32
+    X = ws + need + 4096
+    recs = (R.LayerWeights * 2)()
+    for i in range(2):
+        for k in R.LAYER_KEYS:
+            setattr(recs[i], k, 1 << 40)
+    sbytes = 4 * 8 * 256 * 512 * 4
+    base = 1 << 36
+    S = (ctypes.c_void_p * 2)(base, base + sbytes)
+    call = lambda x, w: R.lib.retnet_decode_step(ctypes.byref(d), recs, S, None,
+                                                 ctypes.c_void_p(x), ctypes.c_void_p(w),
+                                                 need, None)
+    S[1] = X - 256          # state ends inside X
+    assert call(X, ws) == 1
+    S[1] = ws + need - 1024  # state starts inside the workspace
+    assert call(X, ws) == 1
+    S[1] = base + sbytes
+    assert call(ws + 512, ws) == 1  # X inside the workspace

@@ -17,9 +17,7 @@ import oracle
 from linear_recurrent_sequence_gb300 import synth
 from tests.helpers import host
 
-pytestmark = [pytest.mark.gpu,
-              pytest.mark.skip(reason="written before its first GPU run; enabled once it "
-                                      "has passed on a GB300")]
+pytestmark = pytest.mark.gpu
 
 TOL_MAX_REL, TOL_RMS_REL = 3e-2, 2e-2
 KEYS = (("wq", "WQ"), ("wk", "WK"), ("wv", "WV"), ("wg", "WG"), ("wo", "WO"), ("w1", "W1"),
