@@ -187,6 +187,40 @@ ret_status retention_chunkwise_bwd(const ret_desc *d, const void *q, const void 
                                    float *dS_in, void *ws, size_t ws_bytes,
                                    ret_stream_t stream);
 
+/* State-only pass [hwhale, recurrent form S_n = gamma S_{n-1} + K_n^T V_n
+ * and its chunkwise carry S_{c+1} = gamma^L S_c + K_[c]^T (V_[c] (.) zeta)]:
+ * the recurrent state after the call's N tokens, without any output,
+ *   S_out = gamma^N S_in + sum_m gamma^(N-1-m) K'_m^T V_m,
+ *   z_out = gamma^N z_in + sum_m gamma^(N-1-m) K'_m          (K'_m = Theta k_m)
+ * with token m at absolute position pos0 + m.  q, o, chunk, norm_flags,
+ * gn_eps and out_dtype of the descriptor are ignored; k, v as for
+ * retention_chunkwise_fwd.  S_in/z_in may be NULL (zero state); S_out/z_out
+ * may be NULL (not produced) or alias S_in/z_in.  This is the first pass of
+ * a sequence split over several devices: each device runs its own segment
+ * from a zero state, the segments' states are joined with
+ * retention_state_combine, and each device then runs retention_chunkwise_fwd
+ * on its segment from the state that enters it.  ws: at least
+ * retention_state_workspace_size(d) bytes, 256-byte aligned. */
+size_t retention_state_workspace_size(const ret_desc *d);
+ret_status retention_chunkwise_state(const ret_desc *d, const void *k, const void *v,
+                                     const float *S_in, const float *z_in, float *S_out,
+                                     float *z_out, void *ws, size_t ws_bytes,
+                                     ret_stream_t stream);
+
+/* Decayed sum of recurrent states [hwhale, recurrent form: the recurrence is
+ * linear, and a state carried over t tokens with no input becomes gamma^t S]:
+ *   S_out[b,h] = sum_i gamma_h^(tokens[i]) S_parts[i][b,h]   (z likewise)
+ * S_parts, z_parts: HOST arrays of `count` (<= 64) DEVICE pointers to fp32
+ * [B, H, d_k, d_v] / [B, H, d_k] states; a NULL entry (or a NULL array)
+ * counts as a zero state.  tokens: HOST array of `count` decay lengths (>= 0;
+ * gamma^0 = 1 for every gamma).  gamma: HOST array of H decays in [0, 1].
+ * S_out / z_out may be NULL (not produced) and may alias one of the parts.
+ * No workspace; asynchronous on `stream`. */
+ret_status retention_state_combine(int B, int H, int d_k, int d_v, const double *gamma,
+                                   int count, const float *const *S_parts,
+                                   const float *const *z_parts, const int64_t *tokens,
+                                   float *S_out, float *z_out, ret_stream_t stream);
+
 /*
  * Chunkwise forward without a caller-supplied workspace.  No counterpart on
  * the pages: it exists for callers that cannot allocate device memory, such

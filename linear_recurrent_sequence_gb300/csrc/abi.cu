@@ -4,6 +4,7 @@
 #include <math.h>
 #include <string.h>
 
+#include <algorithm>
 #include <atomic>
 
 #ifdef RET_NVTX
@@ -312,6 +313,91 @@ ret_status chunkwise_impl(const ret_desc *d, const void *q, const void *k, const
   return RET_OK;
 }
 
+// Workspace of the state-only pass.  Tensor-core path: status | K' fp16 |
+// per-chunk records | key column sums | pieces [P][B*H][d_k][d_v] and
+// [P][B*H][d_k].  CUDA-core path: status | rotated keys fp32.
+struct StateWs {
+  size_t kp, meta, ks, part, zpart, kr, total;
+};
+
+constexpr int kStatePieces = 8;
+
+StateWs state_ws(const ret_desc *d) {
+  StateWs w;
+  const size_t BH = (size_t)d->B * d->H, rows = BH * d->N;
+  const size_t nch = ((size_t)d->N + 63) / 64;
+  size_t off = kStatusBytes;
+  w.kp = off; off = align256(off + rows * d->d_k * 2);
+  w.meta = off; off = align256(off + BH * nch * sizeof(ChunkMeta));
+  w.ks = off; off = align256(off + BH * nch * d->d_k * sizeof(float));
+  w.part = off; off = align256(off + (size_t)kStatePieces * BH * d->d_k * d->d_v * sizeof(float));
+  w.zpart = off; off = align256(off + (size_t)kStatePieces * BH * d->d_k * sizeof(float));
+  const size_t tc_total = off;
+  w.kr = kStatusBytes;
+  const size_t simt_total = align256(kStatusBytes + rows * d->d_k * sizeof(float));
+  w.total = tc_total > simt_total ? tc_total : simt_total;
+  return w;
+}
+
+// The state after the call's tokens, S_out = gamma^N S_in + sum_m
+// gamma^(N-1-m) K'_m^T V_m (z likewise), without outputs.  Tensor cores:
+// keys-only prologue, the state kernel over pieces of whole chunks, then the
+// decayed sum of S_in and the pieces.  CUDA cores otherwise.
+ret_status state_impl(const ret_desc *d, const void *k, const void *v, const float *S_in,
+                      const float *z_in, float *S_out, float *z_out, void *ws,
+                      size_t ws_bytes, cudaStream_t st) {
+  if (!desc_ok(d)) return RET_EINVAL;
+  const StateWs w = state_ws(d);
+  ret_status rs = check_ws(ws, ws_bytes, w.total);
+  if (rs != RET_OK) return rs;
+  if ((long long)d->B * d->H == 0 || (!S_out && !z_out)) return RET_OK;
+  if (d->N > 0 && (!k || !v)) return RET_EINVAL;
+  const size_t sbytes = (size_t)d->B * d->H * d->d_k * d->d_v * sizeof(float);
+  const size_t zbytes = (size_t)d->B * d->H * d->d_k * sizeof(float);
+  if (d->N == 0) {  // no tokens: the state passes through unchanged
+    if (S_out && S_out != S_in)
+      RET_CUDA(S_in ? cudaMemcpyAsync(S_out, S_in, sbytes, cudaMemcpyDeviceToDevice, st)
+                    : cudaMemsetAsync(S_out, 0, sbytes, st));
+    if (z_out && z_out != z_in)
+      RET_CUDA(z_in ? cudaMemcpyAsync(z_out, z_in, zbytes, cudaMemcpyDeviceToDevice, st)
+                    : cudaMemsetAsync(z_out, 0, zbytes, st));
+    return RET_OK;
+  }
+  ret_desc dt = *d;
+  dt.chunk = 64;
+  KParams p;
+  make_params(&dt, ws, p);
+  if (chunk_tc_supported(p, v, p.sv)) {
+    __half *Kp = at<__half>(ws, w.kp);
+    ChunkMeta *meta = at<ChunkMeta>(ws, w.meta);
+    float *ks = at<float>(ws, w.ks);
+    const int need_z = z_out != nullptr;
+    RET_CUDA(RET_TIMED_LAUNCH(kKRotate, st, launch_rotate_qk(p, nullptr, k, nullptr, Kp, meta, need_z ? ks : nullptr, st, true)));
+    const int nch = (d->N + 63) / 64;
+    const int piece_len = (nch + kStatePieces - 1) / kStatePieces;
+    const int P = (nch + piece_len - 1) / piece_len;  // every piece holds a chunk
+    float *Part = at<float>(ws, w.part), *zPart = at<float>(ws, w.zpart);
+    RET_CUDA(RET_TIMED_LAUNCH(kKStatePass, st, launch_state_tc(p, Kp, v, meta, ks, P, piece_len, Part, zPart, need_z, st)));
+    CombineParts parts;
+    parts.S[0] = S_in;
+    parts.z[0] = z_in;
+    parts.t[0] = d->N;
+    for (int i = 0; i < P; ++i) {
+      const long long end = std::min((long long)(i + 1) * piece_len * 64, (long long)d->N);
+      parts.S[1 + i] = Part + (size_t)i * d->B * d->H * d->d_k * d->d_v;
+      parts.z[1 + i] = need_z ? zPart + (size_t)i * d->B * d->H * d->d_k : nullptr;
+      parts.t[1 + i] = d->N - end;
+    }
+    parts.count = 1 + P;
+    RET_CUDA(RET_TIMED_LAUNCH(kKStateCombine, st, launch_state_combine(p, parts, S_out, z_out, st)));
+    return RET_OK;
+  }
+  float *Kr = at<float>(ws, w.kr);
+  RET_CUDA(RET_TIMED_LAUNCH(kKRotate, st, launch_rotate(p, k, p.sk, d->d_k, Kr, 0, nullptr, kScaleNone, st)));
+  RET_CUDA(RET_TIMED_LAUNCH(kKStateSimt, st, launch_state_simt(p, Kr, v, S_in, z_in, S_out, z_out, st)));
+  return RET_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -395,6 +481,50 @@ ret_status retention_chunkwise_fwd(const ret_desc *d, const void *q, const void 
   RET_RANGE("retention_chunkwise_fwd");
   return chunkwise_impl(d, q, k, v, S_in, z_in, S_out, z_out, o,
                         ws, ws_bytes, (cudaStream_t)stream);
+}
+
+size_t retention_state_workspace_size(const ret_desc *d) {
+  if (!desc_ok(d)) return 0;
+  return state_ws(d).total;
+}
+
+ret_status retention_chunkwise_state(const ret_desc *d, const void *k, const void *v,
+                                     const float *S_in, const float *z_in, float *S_out,
+                                     float *z_out, void *ws, size_t ws_bytes,
+                                     ret_stream_t stream) {
+  RET_RANGE("retention_chunkwise_state");
+  return state_impl(d, k, v, S_in, z_in, S_out, z_out, ws, ws_bytes, (cudaStream_t)stream);
+}
+
+ret_status retention_state_combine(int B, int H, int d_k, int d_v, const double *gamma,
+                                   int count, const float *const *S_parts,
+                                   const float *const *z_parts, const int64_t *tokens,
+                                   float *S_out, float *z_out, ret_stream_t stream) {
+  RET_RANGE("retention_state_combine");
+  if (B < 0 || H < 0 || H > RET_MAX_HEADS || d_k < 1 || d_v < 1 || count < 0 ||
+      count > kMaxCombineParts)
+    return RET_EINVAL;
+  if ((long long)B * H == 0 || (!S_out && !z_out)) return RET_OK;
+  if (!gamma || (count > 0 && !tokens)) return RET_EINVAL;
+  for (int h = 0; h < H; ++h)
+    if (!(gamma[h] >= 0.0 && gamma[h] <= 1.0)) return RET_EINVAL;
+  CombineParts parts;
+  parts.count = count;
+  for (int i = 0; i < count; ++i) {
+    if (tokens[i] < 0) return RET_EINVAL;
+    parts.S[i] = S_parts ? S_parts[i] : nullptr;
+    parts.z[i] = z_parts ? z_parts[i] : nullptr;
+    parts.t[i] = tokens[i];
+  }
+  KParams p;
+  memset(&p, 0, sizeof(p));
+  p.B = B; p.H = H; p.dk = d_k; p.dv = d_v;
+  for (int h = 0; h < H; ++h) {
+    p.gam[h] = (float)gamma[h];
+    p.lng[h] = gamma[h] == 0.0 ? -INFINITY : (float)log(gamma[h]);
+  }
+  RET_CUDA(RET_TIMED_LAUNCH(kKStateCombine, (cudaStream_t)stream, launch_state_combine(p, parts, S_out, z_out, (cudaStream_t)stream)));
+  return RET_OK;
 }
 
 ret_status retention_recurrent_step(const ret_desc *d, const void *q, const void *k,

@@ -16,7 +16,8 @@ const char *kNames[kKernelCount] = {
     "rotate_scale", "chunk_simt", "parallel_simt", "groupnorm", "recurrent_step",
     "gemm_simt", "chunk_tc", "gemm_tc", "state_pass", "swish_gate",
     "bwd_rows", "bwd_values", "unrotate",
-    "layernorm", "residual_add", "gelu", "gemm_skinny", "skinny_reduce"};
+    "layernorm", "residual_add", "gelu", "gemm_skinny", "skinny_reduce",
+    "state_combine", "state_simt"};
 
 struct Slot {
   std::vector<cudaEvent_t> start, stop;

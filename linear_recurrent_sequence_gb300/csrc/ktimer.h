@@ -26,6 +26,8 @@ enum KernelId {
   kKGelu,
   kKGemmSkinny,
   kKSkinnyReduce,
+  kKStateCombine,
+  kKStateSimt,
   kKernelCount
 };
 

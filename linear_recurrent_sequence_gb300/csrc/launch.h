@@ -24,8 +24,11 @@ struct ChunkMeta {
 // Rotate-and-scale prologue of the tensor-core path (bf16 q, k; chunk 64):
 // Q' = xi (.) rot(q), K' = zeta (.) rot(k) as contiguous fp16 [B*H][N][d_k]
 // with per-chunk exponents, magnitudes and (if colsum) key column sums.
+// keys_only: rotate k alone (q is not read; Q' and the query fields of meta
+// are left as they are).
 cudaError_t launch_rotate_qk(const KParams &p, const void *q, const void *k, __half *Qp,
-                             __half *Kp, ChunkMeta *meta, float *colsum, cudaStream_t st);
+                             __half *Kp, ChunkMeta *meta, float *colsum, cudaStream_t st,
+                             bool keys_only = false);
 
 // chunk_simt.cu: fp32 CUDA-core forms writing unnormalised rows + row factors.
 // Qr, Kr: rotated contiguous fp32 [B,H,N,dk]; Oraw: fp32 [B,H,N,dv];
@@ -65,10 +68,30 @@ cudaError_t launch_chunk_tc(const KParams &p, const void *Qp, const void *Kp, co
                             int need_z, const SegPlan &seg, cudaStream_t st);
 
 // state_tc.cu: partial states of the pieces of a SegPlan (tensor cores).
+// Piece i covers chunks [i piece_len, min((i+1) piece_len, chunks)).
 cudaError_t launch_state_tc(const KParams &p, const void *Kp, const void *v,
                             const ChunkMeta *meta, const float *ksum, int npieces,
                             int piece_len, float *Part, float *zPart, int need_z,
                             cudaStream_t st);
+
+// state_combine.cu: S_out = sum_i gamma_h^(t_i) S_i over the parts (null
+// entries skipped), z likewise; either output may be null and may alias a
+// part.  States fp32 [B*H][d_k][d_v], z fp32 [B*H][d_k].
+constexpr int kMaxCombineParts = 64;
+struct CombineParts {
+  int count = 0;
+  const float *S[kMaxCombineParts] = {};
+  const float *z[kMaxCombineParts] = {};
+  long long t[kMaxCombineParts] = {};
+};
+cudaError_t launch_state_combine(const KParams &p, const CombineParts &parts, float *S_out,
+                                 float *z_out, cudaStream_t st);
+// The state after the call's tokens on CUDA cores: Kr rotated keys fp32
+// [B*H][N][d_k], v through sv[]; S_out/z_out may alias S_in/z_in; either
+// output may be null.
+cudaError_t launch_state_simt(const KParams &p, const float *Kr, const void *v,
+                              const float *S_in, const float *z_in, float *S_out, float *z_out,
+                              cudaStream_t st);
 
 // recurrent.cu: one decode step, state in place.
 cudaError_t launch_recurrent_step(const KParams &p, const void *q, const void *k,

@@ -81,8 +81,15 @@ struct RotQK {
   __half *out[2];           // Q', K' contiguous [B*H][N][dk] fp16
   ChunkMeta *meta;          // [B*H][nch]
   float *colsum;            // [B*H][nch][dk] or null
-  int ntiles;               // 2 * B*H * nch
+  int ntiles;               // kinds * B*H * nch
+  int kinds;                // 2: queries and keys; 1: keys only
 };
+
+// Tile t: which tensor (0 queries, 1 keys) and which (batch*head, chunk).
+__device__ __forceinline__ void tile_of(const RotQK &a, int t, int &which, int &r) {
+  which = a.kinds == 2 ? (t & 1) : 1;
+  r = a.kinds == 2 ? (t >> 1) : t;
+}
 
 template <bool kTma>
 __global__ void __launch_bounds__(256)
@@ -115,7 +122,9 @@ rotate_qk_kernel(const __grid_constant__ KParams p, const __grid_constant__ RotQ
   }
   __syncthreads();
   auto issue = [&](int t, int buf) {
-    const int which = t & 1, r = t >> 1, bh = r / nch, c = r % nch;
+    int which, r;
+    tile_of(a, t, which, r);
+    const int bh = r / nch, c = r % nch;
     tc::mbar_arrive_expect_tx(&tbar[buf], tile_bytes);
     tc::tma_load_4d(xt + buf * tile_bytes, which ? &tmk : &tmq, &tbar[buf], 0, c * C,
                     bh % p.H, bh / p.H);
@@ -123,7 +132,9 @@ rotate_qk_kernel(const __grid_constant__ KParams p, const __grid_constant__ RotQ
   if (kTma && tid == 0 && (int)blockIdx.x < a.ntiles) issue(blockIdx.x, 0);
   int k = 0;
   for (int t = blockIdx.x; t < a.ntiles; t += gridDim.x, ++k) {
-    const int which = t & 1, r = t >> 1, bh = r / nch, c = r % nch;
+    int which, r;
+    tile_of(a, t, which, r);
+    const int bh = r / nch, c = r % nch;
     const int b = bh / p.H, h = bh % p.H;
     const int buf = kTma ? (k & 1) : 0;
     const uint8_t *tile = xt + buf * tile_bytes;
@@ -250,7 +261,8 @@ rotate_qk_kernel(const __grid_constant__ KParams p, const __grid_constant__ RotQ
 }
 
 cudaError_t launch_rotate_qk(const KParams &p, const void *q, const void *k, __half *Qp,
-                             __half *Kp, ChunkMeta *meta, float *colsum, cudaStream_t st) {
+                             __half *Kp, ChunkMeta *meta, float *colsum, cudaStream_t st,
+                             bool keys_only) {
   if (p.N == 0 || p.B == 0 || p.H == 0) return cudaSuccess;
   if (p.chunk != 64 || p.dk < 4 || p.dk > 256 || p.dk % 4 || !p.in_bf16)
     return cudaErrorInvalidValue;
@@ -266,12 +278,13 @@ cudaError_t launch_rotate_qk(const KParams &p, const void *q, const void *k, __h
   a.meta = meta;
   a.colsum = colsum;
   const int nch = (p.N + 63) / 64;
-  a.ntiles = 2 * p.B * p.H * nch;
+  a.kinds = keys_only ? 1 : 2;
+  a.ntiles = a.kinds * p.B * p.H * nch;
   // TMA source when both inputs are 16-byte aligned with 16-byte strides.
   CUtensorMap tm[2];
   memset(tm, 0, sizeof(tm));
   bool tma = p.dk % 8 == 0;
-  for (int w = 0; w < 2 && tma; ++w) {
+  for (int w = keys_only ? 1 : 0; w < 2 && tma; ++w) {
     const long long *s = a.s[w];
     tma = (reinterpret_cast<uintptr_t>(a.x[w]) % 16 == 0) && s[0] % 8 == 0 && s[1] % 8 == 0 &&
           s[2] % 8 == 0;

@@ -97,7 +97,7 @@ state_tc_kernel(const __grid_constant__ KParams p, const __grid_constant__ CUten
   const int bh = rem / NV, rank = rem % NV, b = bh / p.H, h = bh % p.H;
   const int v0 = rank * kW, DK = p.dk, NKB = DK / 64, N = p.N;
   const int nch = (N + kC - 1) / kC;
-  const int c0 = piece * piece_len, ncl = piece_len;
+  const int c0 = piece * piece_len, ncl = max(0, min(piece_len, nch - c0));
   const float lng = p.lng[h];
 
   if (tid == 0) {

@@ -76,6 +76,14 @@ _SIGS = {
                                                 _P, _P, ctypes.c_size_t, _P]),
     "retention_chunkwise_fwd_noalloc": (ctypes.c_int, [ctypes.POINTER(RetDesc), _P, _P, _P, _P,
                                                        _P, _P, _P, _P, _P]),
+    "retention_state_workspace_size": (ctypes.c_size_t, [ctypes.POINTER(RetDesc)]),
+    "retention_chunkwise_state": (ctypes.c_int, [ctypes.POINTER(RetDesc), _P, _P, _P, _P, _P,
+                                                 _P, _P, ctypes.c_size_t, _P]),
+    "retention_state_combine": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                               ctypes.c_int, ctypes.POINTER(ctypes.c_double),
+                                               ctypes.c_int, ctypes.POINTER(ctypes.c_void_p),
+                                               ctypes.POINTER(ctypes.c_void_p),
+                                               ctypes.POINTER(ctypes.c_int64), _P, _P, _P]),
     "retention_backward_workspace_size": (ctypes.c_size_t, [ctypes.POINTER(RetDesc)]),
     "retention_chunkwise_bwd": (ctypes.c_int, [ctypes.POINTER(RetDesc), _P, _P, _P, _P, _P,
                                                _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
@@ -231,6 +239,47 @@ def chunkwise_fwd(q, k, v, gamma, *, chunk=64, norm_flags=0, gn_eps=1e-6, pos0=0
                                      _ptr(workspace), workspace.numel(), _stream(stream))
     _check(st, "retention_chunkwise_fwd")
     return out
+
+
+def state_workspace_size(desc):
+    return int(lib.retention_state_workspace_size(ctypes.byref(desc)))
+
+
+def chunkwise_state(k, v, gamma, *, pos0=0, rotate=True, theta_base=10000.0, S_in=None,
+                    z_in=None, S_out=None, z_out=None, with_z=True, workspace=None,
+                    stream=None):
+    """The recurrent state after the tokens of k [B,H,N,d_k], v [B,H,N,d_v]
+    (no outputs): S = gamma^N S_in + sum_m gamma^(N-1-m) K'_m^T V_m and z
+    likewise.  Returns (S_out, z_out); z_out is None when with_z is False."""
+    B, H, N, dk = k.shape
+    dv = v.shape[3]
+    if S_out is None:
+        S_out = torch.empty(B, H, dk, dv, dtype=torch.float32, device=k.device)
+    if with_z and z_out is None:
+        z_out = torch.empty(B, H, dk, dtype=torch.float32, device=k.device)
+    d, g = make_desc(k, k, v, v, gamma, pos0=pos0, rotate=rotate, theta_base=theta_base)
+    if workspace is None:
+        workspace = new_workspace(state_workspace_size(d), k.device)
+    st = lib.retention_chunkwise_state(ctypes.byref(d), _ptr(k), _ptr(v), _ptr(S_in),
+                                       _ptr(z_in), _ptr(S_out), _ptr(z_out), _ptr(workspace),
+                                       workspace.numel(), _stream(stream))
+    _check(st, "retention_chunkwise_state")
+    return S_out, (z_out if with_z else None)
+
+
+def state_combine(parts, tokens, gamma, *, S_out, z_out=None, stream=None):
+    """S_out = sum_i gamma_h^(tokens[i]) S_i (z likewise) over parts, a list of
+    (S_i, z_i) pairs of fp32 device tensors (None for a zero state)."""
+    B, H, dk, dv = S_out.shape
+    n = len(parts)
+    Sp = (ctypes.c_void_p * max(n, 1))(*[_ptr(S) for S, _ in parts])
+    zp = (ctypes.c_void_p * max(n, 1))(*[_ptr(z) for _, z in parts])
+    tk = (ctypes.c_int64 * max(n, 1))(*[int(t) for t in tokens])
+    g = (ctypes.c_double * H)(*[float(x) for x in gamma])
+    st = lib.retention_state_combine(B, H, dk, dv, g, n, Sp, zp, tk, _ptr(S_out), _ptr(z_out),
+                                     _stream(stream))
+    _check(st, "retention_state_combine")
+    return S_out, z_out
 
 
 def backward_workspace_size(desc):

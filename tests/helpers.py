@@ -46,21 +46,47 @@ def bf16_half_ulp(x):
     return np.exp2(np.floor(np.log2(ax)) - 8.0)
 
 
-def check_bf16(got, ref, what=""):
+def check_bf16(got, ref, what="", spread=None):
     """Max abs and RMS of got - ref after GroupNorm.  When `got` was stored
     in bf16 (every value representable in bf16), the max-abs check measures
     the arithmetic error: it allows, on top of the tolerance, the half ulp of
     rounding the exact result to bf16 for storage (for a GroupNorm output of
-    |y| >= 8 that rounding alone can reach 2^-5, above the tolerance).  The
-    RMS check has no allowance."""
+    |y| >= 8 that rounding alone can reach 2^-5, above the tolerance).
+    `spread` (optional, one value per output row): the exact function's own
+    sensitivity to rounding its operands (operand_sensitivity); each row's
+    max-abs bound is widened by twice it.  The RMS check has no allowance."""
     d = np.abs(got - ref)
     stored_bf16 = bool(np.all(np.asarray(got, np.float32) == bf16_round(got)))
     e = np.maximum(d - bf16_half_ulp(ref), 0.0) if stored_bf16 else d
+    if spread is not None:
+        e = np.maximum(e - 2.0 * np.asarray(spread)[..., None], 0.0)
     mx, rms = float(e.max()), float(np.sqrt((d ** 2).mean()))
+    where = np.unravel_index(int(np.argmax(e)), e.shape)
     assert mx <= TOL_BF16_MAX and rms <= TOL_BF16_RMS, \
-        f"{what}: max abs {mx:.3e} (<= {TOL_BF16_MAX}{' beyond bf16 storage' if stored_bf16 else ''}), " \
+        f"{what}: max abs {mx:.3e} at {tuple(int(i) for i in where)} " \
+        f"(<= {TOL_BF16_MAX}{' beyond bf16 storage' if stored_bf16 else ''}), " \
         f"rms {rms:.3e} (<= {TOL_BF16_RMS})"
     return mx, rms
+
+
+# Unit roundoff of the fp16 operands of the tensor-core path (11 significant
+# bits, round to nearest).
+FP16_U = 2.0 ** -11
+
+
+def operand_sensitivity(run, q64, k64, seed=0):
+    """Per output row (the last axis reduced), how far the exact float64
+    result moves when q and k are perturbed by relative errors of up to the
+    fp16 unit roundoff, as the tensor-core path rounds them: `run(q, k)`
+    returns the oracle's output.  Where a row's result is that sensitive
+    (the first tokens of a sequence, whose few score terms can cancel), no
+    implementation with fp16 operands can be closer to the exact value than
+    about this much."""
+    g = np.random.default_rng(seed)
+    ref = run(q64, k64)
+    qp = q64 * (1.0 + FP16_U * g.uniform(-1.0, 1.0, q64.shape))
+    kp = k64 * (1.0 + FP16_U * g.uniform(-1.0, 1.0, k64.shape))
+    return np.abs(run(qp, kp) - ref).max(axis=-1)
 
 
 def bf16_round(x):

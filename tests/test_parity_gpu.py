@@ -18,7 +18,7 @@ import torch
 
 import oracle
 from linear_recurrent_sequence_gb300 import synth
-from tests.helpers import check_bf16, check_f32, host, seeded
+from tests.helpers import check_bf16, check_f32, host, operand_sensitivity, seeded
 
 pytestmark = pytest.mark.gpu
 
@@ -164,11 +164,19 @@ def test_config4_decode_2048_steps(R, B, odt):
     o_pre, out, S = _decode_run(R, qh.cuda(), kh.cuda(), vh.cuda(), gam, odt=odt)
     o_pre, out, S = host(o_pre), host(out), host(S)
     p = oracle.Problem(1, DEC_H, N, DEC_DK, DEC_DV, gam, gn_eps=1e-6)
+    pp = oracle.Problem(1, DEC_H, DEC_P, DEC_DK, DEC_DV, gam, gn_eps=1e-6)
     for b in range(B):
         ref, S_ref, _ = oracle.chunkwise(p, 64, qh[b:b + 1].double().numpy(),
                                          kh[b:b + 1].double().numpy(),
                                          vh[b:b + 1].double().numpy())
-        check_bf16(o_pre[b:b + 1], ref[:, :, :DEC_P], f"prefill b={b}")
+        # The prefill runs on the tensor cores (fp16 operands): rows whose
+        # exact result is itself sensitive to rounding q and k at fp16
+        # precision get that sensitivity added to their bound.
+        v64 = vh[b:b + 1, :, :DEC_P].double().numpy()
+        spread = operand_sensitivity(
+            lambda q_, k_: oracle.chunkwise(pp, 64, q_, k_, v64)[0],
+            qh[b:b + 1, :, :DEC_P].double().numpy(), kh[b:b + 1, :, :DEC_P].double().numpy())
+        check_bf16(o_pre[b:b + 1], ref[:, :, :DEC_P], f"prefill b={b}", spread=spread)
         check_bf16(out[b:b + 1], ref[:, :, DEC_P:], f"decode steps b={b}")
         rel = np.max(np.abs(S[b:b + 1] - S_ref)) / np.max(np.abs(S_ref))
         assert rel < 1e-2, (b, rel)
