@@ -764,9 +764,11 @@ static size_t dec_partial_bytes(const retnet_stack_desc *d) {
   const msr_desc &m = d->block.msr;
   const int B = m.B, dm = m.d_model, HK = m.H * m.d_k, HV = m.H * m.d_v, F = d->block.d_ffn;
   if (B > 16) return 0;
-  const size_t c[5] = {gemm_skinny_partial_bytes(B, HK, dm), gemm_skinny_partial_bytes(B, HV, dm),
+  // the four input projections as one job, W_O, W1, W2, and each alone
+  const size_t c[7] = {gemm_skinny_partial_bytes(B, 2 * HK + 2 * HV, dm),
+                       gemm_skinny_partial_bytes(B, HK, dm), gemm_skinny_partial_bytes(B, HV, dm),
                        gemm_skinny_partial_bytes(B, dm, HV), gemm_skinny_partial_bytes(B, F, dm),
-                       gemm_skinny_partial_bytes(B, dm, F)};
+                       gemm_skinny_partial_bytes(B, dm, F), 0};
   size_t mx = 0;
   for (size_t x : c) mx = x > mx ? x : mx;
   return mx;
@@ -832,6 +834,26 @@ static cudaError_t gemm_dec(const void *A, const void *Bm, void *C, int M, int N
   return gemm_any(A, Bm, C, M, N, K, status, st);
 }
 
+// Several decode-batch GEMMs of one A (same K) as one weight-streaming job,
+// with the reduce's epilogue (GELU, or a skip connection with R); false
+// when the job does not fit the kernel (the caller then runs them apart).
+static bool skinny_job_fits(int M, int count, const void *const *Bs, const int *Ns) {
+  if (M < 1 || M > 16) return false;
+  for (int i = 0; i < count; ++i)
+    if (Ns[i] < 8 || Ns[i] % 8 || !Bs[i] || reinterpret_cast<uintptr_t>(Bs[i]) % 16) return false;
+  return true;
+}
+
+static cudaError_t gemm_dec_job(const void *A, int count, const void *const *Bs, void *const *Cs,
+                                const int *Ns, int M, int K, int epi, const void *R, float *part,
+                                cudaStream_t st) {
+  SkinnyJob job;
+  if (!skinny_job_init(job, count, Bs, Cs, Ns, epi, R)) return cudaErrorInvalidValue;
+  cudaError_t e = RET_TIMED_LAUNCH(kKGemmSkinny, st, launch_gemm_skinny_job(A, job, M, K, part, st));
+  if (e != cudaSuccess) return e;
+  return RET_TIMED_LAUNCH(kKSkinnyReduce, st, launch_skinny_reduce_job(part, job, M, K, st));
+}
+
 ret_status retnet_decode_step(const retnet_stack_desc *d, const retnet_layer_weights *layers,
                               float *const *S, float *const *z, void *X, void *ws,
                               size_t ws_bytes, ret_stream_t stream) {
@@ -880,20 +902,43 @@ ret_status retnet_decode_step(const retnet_stack_desc *d, const retnet_layer_wei
     const retnet_layer_weights &L = layers[l];
     // Y1 = MSR(LN1(X)) + X, the retention step on this layer's state.
     RET_CUDA(RET_TIMED_LAUNCH(kKLayerNorm, st, launch_layernorm(X, L.ln1_w, L.ln1_b, Xn, B, dm, d->block.ln_eps, st)));
-    RET_CUDA(gemm_dec(Xn, L.WQ, Q, B, HK, dm, part, status, st));
-    RET_CUDA(gemm_dec(Xn, L.WK, K, B, HK, dm, part, status, st));
-    RET_CUDA(gemm_dec(Xn, L.WV, V, B, HV, dm, part, status, st));
-    RET_CUDA(gemm_dec(Xn, L.WG, G, B, HV, dm, part, status, st));
+    // Few rows: the four projections of LN1(X) stream their weights in one
+    // job, and the GELU and the skip connections ride on the reduces.
+    const void *Win[4] = {L.WQ, L.WK, L.WV, L.WG};
+    void *Cin[4] = {Q, K, V, G};
+    const int Nin[4] = {HK, HK, HV, HV};
+    const bool fused = skinny_job_fits(B, 4, Win, Nin) && skinny_job_fits(B, 1, &L.WO, &dm) &&
+                       skinny_job_fits(B, 1, &L.W1, &F) && skinny_job_fits(B, 1, &L.W2, &dm);
+    if (fused) {
+      RET_CUDA(gemm_dec_job(Xn, 4, Win, Cin, Nin, B, dm, kSkEpNone, nullptr, part, st));
+    } else {
+      RET_CUDA(gemm_dec(Xn, L.WQ, Q, B, HK, dm, part, status, st));
+      RET_CUDA(gemm_dec(Xn, L.WK, K, B, HK, dm, part, status, st));
+      RET_CUDA(gemm_dec(Xn, L.WV, V, B, HV, dm, part, status, st));
+      RET_CUDA(gemm_dec(Xn, L.WG, G, B, HV, dm, part, status, st));
+    }
     RET_CUDA(RET_TIMED_LAUNCH(kKRecurrent, st, launch_recurrent_step(p, Q, K, V, S[l], rsum ? z[l] : nullptr, Y, st)));
     RET_CUDA(RET_TIMED_LAUNCH(kKGate, st, launch_swish_gate(Y, G, (long long)B * HV, st)));
-    RET_CUDA(gemm_dec(Y, L.WO, Mo, B, dm, HV, part, status, st));
-    RET_CUDA(RET_TIMED_LAUNCH(kKResidual, st, launch_residual_add(Mo, X, (long long)B * dm, st)));
+    if (fused) {
+      void *c = Mo;
+      RET_CUDA(gemm_dec_job(Y, 1, &L.WO, &c, &dm, B, HV, kSkEpResidual, X, part, st));
+    } else {
+      RET_CUDA(gemm_dec(Y, L.WO, Mo, B, dm, HV, part, status, st));
+      RET_CUDA(RET_TIMED_LAUNCH(kKResidual, st, launch_residual_add(Mo, X, (long long)B * dm, st)));
+    }
     // X = gelu(LN2(Y1) W1) W2 + Y1.
     RET_CUDA(RET_TIMED_LAUNCH(kKLayerNorm, st, launch_layernorm(Mo, L.ln2_w, L.ln2_b, Xn, B, dm, d->block.ln_eps, st)));
-    RET_CUDA(gemm_dec(Xn, L.W1, H1, B, F, dm, part, status, st));
-    RET_CUDA(RET_TIMED_LAUNCH(kKGelu, st, launch_gelu(H1, (long long)B * F, st)));
-    RET_CUDA(gemm_dec(H1, L.W2, X, B, dm, F, part, status, st));
-    RET_CUDA(RET_TIMED_LAUNCH(kKResidual, st, launch_residual_add(X, Mo, (long long)B * dm, st)));
+    if (fused) {
+      void *c = H1;
+      RET_CUDA(gemm_dec_job(Xn, 1, &L.W1, &c, &F, B, dm, kSkEpGelu, nullptr, part, st));
+      c = X;
+      RET_CUDA(gemm_dec_job(H1, 1, &L.W2, &c, &dm, B, F, kSkEpResidual, Mo, part, st));
+    } else {
+      RET_CUDA(gemm_dec(Xn, L.W1, H1, B, F, dm, part, status, st));
+      RET_CUDA(RET_TIMED_LAUNCH(kKGelu, st, launch_gelu(H1, (long long)B * F, st)));
+      RET_CUDA(gemm_dec(H1, L.W2, X, B, dm, F, part, status, st));
+      RET_CUDA(RET_TIMED_LAUNCH(kKResidual, st, launch_residual_add(X, Mo, (long long)B * dm, st)));
+    }
   }
   return RET_OK;
 }

@@ -25,11 +25,12 @@ constexpr int kSkMaxSplit = 128;
 constexpr int kSkMaxRowsPerSlice = 512;       // K rows per CTA (A slice in shared memory)
 }  // namespace
 
-// grid: x = column block of 2048, y = K slice.  P: [split][M][N] fp32.
+// grid: x = column block of 2048 (over every matrix of the job), y = K
+// slice.  P: [split][M][Ntot] fp32, matrix i's columns at col0[i].
 template <int MB>
 __global__ void __launch_bounds__(kSkWarps * 32)
-gemm_skinny_kernel(const __nv_bfloat16 *__restrict__ A, const __nv_bfloat16 *__restrict__ Bm,
-                   float *__restrict__ P, int M, int N, int K, int rows_per_slice) {
+gemm_skinny_kernel(const __nv_bfloat16 *__restrict__ A, const SkinnyJob job,
+                   float *__restrict__ P, int M, int K, int rows_per_slice) {
   __shared__ float As[kSkMaxRowsPerSlice][MB];
   const int k0 = blockIdx.y * rows_per_slice;
   const int kn = min(rows_per_slice, K - k0);
@@ -38,15 +39,18 @@ gemm_skinny_kernel(const __nv_bfloat16 *__restrict__ A, const __nv_bfloat16 *__r
     As[r][m] = m < M ? __bfloat162float(A[(long long)m * K + k0 + r]) : 0.f;
   }
   __syncthreads();
+  int mat = 0;
+  while (mat + 1 < job.count && (int)blockIdx.x >= job.blk0[mat + 1]) ++mat;
+  const int N = job.N[mat];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int n0 = blockIdx.x * kSkCtaCols + warp * kSkCols + lane * 8;
+  const int n0 = ((int)blockIdx.x - job.blk0[mat]) * kSkCtaCols + warp * kSkCols + lane * 8;
   if (n0 >= N) return;  // N % 8 == 0: a lane's eight columns are all in or all out
   float acc[MB][8];
 #pragma unroll
   for (int m = 0; m < MB; ++m)
 #pragma unroll
     for (int c = 0; c < 8; ++c) acc[m][c] = 0.f;
-  const __nv_bfloat16 *bcol = Bm + (long long)k0 * N + n0;
+  const __nv_bfloat16 *bcol = job.B[mat] + (long long)k0 * N + n0;
   for (int r0 = 0; r0 < kn; r0 += kSkUnroll) {
     uint4 w[kSkUnroll];
 #pragma unroll
@@ -71,25 +75,38 @@ gemm_skinny_kernel(const __nv_bfloat16 *__restrict__ A, const __nv_bfloat16 *__r
       }
     }
   }
-  float *pt = P + (long long)blockIdx.y * M * N + n0;
+  float *pt = P + (long long)blockIdx.y * M * job.Ntot + job.col0[mat] + n0;
 #pragma unroll
   for (int m = 0; m < MB; ++m) {
     if (m >= M) break;
-    float4 *dst = reinterpret_cast<float4 *>(pt + (long long)m * N);
+    float4 *dst = reinterpret_cast<float4 *>(pt + (long long)m * job.Ntot);
     dst[0] = make_float4(acc[m][0], acc[m][1], acc[m][2], acc[m][3]);
     dst[1] = make_float4(acc[m][4], acc[m][5], acc[m][6], acc[m][7]);
   }
 }
 
-// C[m][n] = bf16(sum over slices s, in order, of P[s][m][n]).
+// C_i[m][n] = epilogue(bf16(sum over slices s, in order, of P[s][m][col0_i + n])):
+// none; GELU x Phi(x) = x (1 + erf(x / sqrt 2)) / 2 of the rounded sum; or
+// the rounded sum plus R[m][n] (the skip connection).  Each epilogue rounds
+// to bf16 where the separate kernels it replaces would.
 __global__ void __launch_bounds__(256)
-skinny_reduce_kernel(const float *__restrict__ P, __nv_bfloat16 *__restrict__ C, long long MN,
-                     int split) {
+skinny_reduce_kernel(const float *__restrict__ P, const SkinnyJob job, int M, int split) {
+  const long long MN = (long long)M * job.Ntot;
   const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= MN) return;
+  const int m = (int)(i / job.Ntot), n = (int)(i % job.Ntot);
+  int mat = 0;
+  while (mat + 1 < job.count && n >= job.col0[mat + 1]) ++mat;
+  const int c = n - job.col0[mat];
   float s = 0.f;
   for (int t = 0; t < split; ++t) s += P[(long long)t * MN + i];
-  C[i] = __float2bfloat16_rn(s);
+  float y = __bfloat162float(__float2bfloat16_rn(s));
+  const long long o = (long long)m * job.N[mat] + c;
+  if (job.epi == kSkEpGelu)
+    y = 0.5f * y * (1.f + erff(y * 0.70710678118654752f));
+  else if (job.epi == kSkEpResidual)
+    y = y + __bfloat162float(job.R[o]);
+  job.C[mat][o] = __float2bfloat16_rn(y);
 }
 
 bool gemm_skinny_supported(const void *A, const void *Bm, const void *C, int M, int N, int K) {
@@ -123,35 +140,78 @@ size_t gemm_skinny_partial_bytes(int M, int N, int K) {
   return (size_t)split * M * N * sizeof(float);
 }
 
-cudaError_t launch_gemm_skinny(const void *A, const void *Bm, int M, int N, int K,
-                               float *partial, cudaStream_t st) {
+bool skinny_job_init(SkinnyJob &job, int count, const void *const *Bs, void *const *Cs,
+                     const int *Ns, int epi, const void *R) {
+  if (count < 1 || count > kSkMaxMats) return false;
+  job.count = count;
+  job.epi = epi;
+  job.R = reinterpret_cast<const __nv_bfloat16 *>(R);
+  int col = 0, blk = 0;
+  for (int i = 0; i < count; ++i) {
+    if (Ns[i] < 8 || Ns[i] % 8 || !Bs[i] || !Cs[i] || reinterpret_cast<uintptr_t>(Bs[i]) % 16)
+      return false;
+    job.B[i] = reinterpret_cast<const __nv_bfloat16 *>(Bs[i]);
+    job.C[i] = reinterpret_cast<__nv_bfloat16 *>(Cs[i]);
+    job.N[i] = Ns[i];
+    job.col0[i] = col;
+    job.blk0[i] = blk;
+    col += Ns[i];
+    blk += (Ns[i] + kSkCtaCols - 1) / kSkCtaCols;
+  }
+  job.Ntot = col;
+  job.blk0[count] = blk;
+  return (epi != kSkEpResidual || (count == 1 && R));
+}
+
+cudaError_t launch_gemm_skinny_job(const void *A, const SkinnyJob &job, int M, int K,
+                                   float *partial, cudaStream_t st) {
   int split = 1, rows = 1;
-  skinny_plan(M, N, K, split, rows);
-  dim3 grid((N + kSkCtaCols - 1) / kSkCtaCols, split);
+  skinny_plan(M, job.Ntot, K, split, rows);
+  dim3 grid(job.blk0[job.count], split);
   const auto *a = reinterpret_cast<const __nv_bfloat16 *>(A);
-  const auto *b = reinterpret_cast<const __nv_bfloat16 *>(Bm);
   const int threads = kSkWarps * 32;
   if (M <= 1)
-    gemm_skinny_kernel<1><<<grid, threads, 0, st>>>(a, b, partial, M, N, K, rows);
+    gemm_skinny_kernel<1><<<grid, threads, 0, st>>>(a, job, partial, M, K, rows);
   else if (M <= 2)
-    gemm_skinny_kernel<2><<<grid, threads, 0, st>>>(a, b, partial, M, N, K, rows);
+    gemm_skinny_kernel<2><<<grid, threads, 0, st>>>(a, job, partial, M, K, rows);
   else if (M <= 4)
-    gemm_skinny_kernel<4><<<grid, threads, 0, st>>>(a, b, partial, M, N, K, rows);
+    gemm_skinny_kernel<4><<<grid, threads, 0, st>>>(a, job, partial, M, K, rows);
   else if (M <= 8)
-    gemm_skinny_kernel<8><<<grid, threads, 0, st>>>(a, b, partial, M, N, K, rows);
+    gemm_skinny_kernel<8><<<grid, threads, 0, st>>>(a, job, partial, M, K, rows);
   else
-    gemm_skinny_kernel<16><<<grid, threads, 0, st>>>(a, b, partial, M, N, K, rows);
+    gemm_skinny_kernel<16><<<grid, threads, 0, st>>>(a, job, partial, M, K, rows);
   return cudaGetLastError();
+}
+
+cudaError_t launch_skinny_reduce_job(const float *partial, const SkinnyJob &job, int M, int K,
+                                     cudaStream_t st) {
+  int split = 1, rows = 1;
+  skinny_plan(M, job.Ntot, K, split, rows);
+  const long long MN = (long long)M * job.Ntot;
+  skinny_reduce_kernel<<<(unsigned)((MN + 255) / 256), 256, 0, st>>>(partial, job, M, split);
+  return cudaGetLastError();
+}
+
+// One matrix, no epilogue.
+static SkinnyJob single_job(const void *Bm, void *C, int N) {
+  SkinnyJob job;
+  job.count = 1;
+  job.B[0] = reinterpret_cast<const __nv_bfloat16 *>(Bm);
+  job.C[0] = reinterpret_cast<__nv_bfloat16 *>(C);
+  job.N[0] = N;
+  job.Ntot = N;
+  job.blk0[1] = (N + kSkCtaCols - 1) / kSkCtaCols;
+  return job;
+}
+
+cudaError_t launch_gemm_skinny(const void *A, const void *Bm, int M, int N, int K,
+                               float *partial, cudaStream_t st) {
+  return launch_gemm_skinny_job(A, single_job(Bm, nullptr, N), M, K, partial, st);
 }
 
 cudaError_t launch_skinny_reduce(const float *partial, void *C, int M, int N, int K,
                                  cudaStream_t st) {
-  int split = 1, rows = 1;
-  skinny_plan(M, N, K, split, rows);
-  const long long MN = (long long)M * N;
-  skinny_reduce_kernel<<<(unsigned)((MN + 255) / 256), 256, 0, st>>>(
-      partial, reinterpret_cast<__nv_bfloat16 *>(C), MN, split);
-  return cudaGetLastError();
+  return launch_skinny_reduce_job(partial, single_job(nullptr, C, N), M, K, st);
 }
 
 }  // namespace ret

@@ -140,5 +140,23 @@ cudaError_t launch_gemm_skinny(const void *A, const void *Bm, int M, int N, int 
                                float *partial, cudaStream_t st);
 cudaError_t launch_skinny_reduce(const float *partial, void *C, int M, int N, int K,
                                  cudaStream_t st);
+// Up to four weight matrices with the same K read in one launch (their
+// columns side by side in the partials), and the reduce's epilogue: none,
+// GELU, or a skip connection (one matrix; C = sum + R, R [M][N] bf16).
+constexpr int kSkMaxMats = 4;
+enum { kSkEpNone = 0, kSkEpGelu = 1, kSkEpResidual = 2 };
+struct SkinnyJob {
+  int count = 0, Ntot = 0, epi = kSkEpNone;
+  const __nv_bfloat16 *B[kSkMaxMats] = {};
+  __nv_bfloat16 *C[kSkMaxMats] = {};
+  int N[kSkMaxMats] = {}, col0[kSkMaxMats] = {}, blk0[kSkMaxMats + 1] = {};
+  const __nv_bfloat16 *R = nullptr;
+};
+bool skinny_job_init(SkinnyJob &job, int count, const void *const *Bs, void *const *Cs,
+                     const int *Ns, int epi, const void *R);
+cudaError_t launch_gemm_skinny_job(const void *A, const SkinnyJob &job, int M, int K,
+                                   float *partial, cudaStream_t st);
+cudaError_t launch_skinny_reduce_job(const float *partial, const SkinnyJob &job, int M, int K,
+                                     cudaStream_t st);
 
 }  // namespace ret
