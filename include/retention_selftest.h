@@ -28,6 +28,16 @@ int retention_tc_probe(int a_mode, int b_mode, int M, int N, int K, int a_lbo, i
                        int b_lbo, int b_sbo, const void *A, const void *B, float *D,
                        unsigned *status, ret_stream_t stream);
 
+/*
+ * The accumulator-scaling operand of tcgen05.mma (PTX ISA, tcgen05.mma
+ * "scale-input-d": D = A * B + D * 2^-n).  One CTA computes D = A * B^T
+ * (A, B: [128][64] bf16 device, K-major in shared memory), then runs the
+ * same MMA chain again with the first MMA given scale n (0..15), so that
+ * D' = A B^T (1 + 2^-n).  D: [128][128] fp32 device.  Returns a ret_status.
+ */
+int retention_tc_probe_scale_d(int n, const void *A, const void *B, float *D,
+                               unsigned *status, ret_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

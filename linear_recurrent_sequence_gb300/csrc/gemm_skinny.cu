@@ -21,7 +21,7 @@ constexpr int kSkWarps = 8;
 constexpr int kSkCols = 256;                  // columns per warp (32 lanes x 8)
 constexpr int kSkCtaCols = kSkWarps * kSkCols;  // 2048
 constexpr int kSkUnroll = 8;                  // rows of B in flight per lane
-constexpr int kSkMaxSplit = 128;
+constexpr int kSkMaxSplit = 608;
 constexpr int kSkMaxRowsPerSlice = 512;       // K rows per CTA (A slice in shared memory)
 }  // namespace
 
@@ -85,23 +85,57 @@ gemm_skinny_kernel(const __nv_bfloat16 *__restrict__ A, const SkinnyJob job,
   }
 }
 
-// C_i[m][n] = epilogue(bf16(sum over slices s, in order, of P[s][m][col0_i + n])):
+// C_i[m][n] = epilogue(bf16(sum over the slices of P[s][m][col0_i + n])):
 // none; GELU x Phi(x) = x (1 + erf(x / sqrt 2)) / 2 of the rounded sum; or
 // the rounded sum plus R[m][n] (the skip connection).  Each epilogue rounds
-// to bf16 where the separate kernels it replaces would.
+// to bf16 where the separate kernels it replaces would.  One warp per (row,
+// 8 adjacent columns): lane l adds slices l, l + 32, ... in order, then the
+// lanes' sums are combined by a fixed butterfly, so the result does not
+// depend on timing (the partials were just written and are read from L2).
 __global__ void __launch_bounds__(256)
 skinny_reduce_kernel(const float *__restrict__ P, const SkinnyJob job, int M, int split) {
   const long long MN = (long long)M * job.Ntot;
-  const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-  if (i >= MN) return;
-  const int m = (int)(i / job.Ntot), n = (int)(i % job.Ntot);
+  const long long g = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;  // 8-column group
+  const int lane = threadIdx.x & 31;
+  if (g * 8 >= MN) return;
+  const long long i0 = g * 8;  // Ntot % 8 == 0: the group lies in one row and one matrix
+  float4 a = make_float4(0.f, 0.f, 0.f, 0.f), b = a;
+  int t = lane;
+  for (; t + 96 < split; t += 128) {  // four slices' loads in flight, added in slice order
+    float4 x[4], y[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const float4 *src = reinterpret_cast<const float4 *>(P + (long long)(t + 32 * u) * MN + i0);
+      x[u] = src[0];
+      y[u] = src[1];
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      a.x += x[u].x; a.y += x[u].y; a.z += x[u].z; a.w += x[u].w;
+      b.x += y[u].x; b.y += y[u].y; b.z += y[u].z; b.w += y[u].w;
+    }
+  }
+  for (; t < split; t += 32) {
+    const float4 *src = reinterpret_cast<const float4 *>(P + (long long)t * MN + i0);
+    const float4 x = src[0], y = src[1];
+    a.x += x.x; a.y += x.y; a.z += x.z; a.w += x.w;
+    b.x += y.x; b.y += y.y; b.z += y.z; b.w += y.w;
+  }
+  float v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+    for (int e = 0; e < 8; ++e) v[e] += __shfl_xor_sync(0xffffffffu, v[e], o);
+  if (lane >= 8) return;
+  const int m = (int)(i0 / job.Ntot), n = (int)(i0 % job.Ntot) + lane;
   int mat = 0;
   while (mat + 1 < job.count && n >= job.col0[mat + 1]) ++mat;
-  const int c = n - job.col0[mat];
-  float s = 0.f;
-  for (int t = 0; t < split; ++t) s += P[(long long)t * MN + i];
-  float y = __bfloat162float(__float2bfloat16_rn(s));
-  const long long o = (long long)m * job.N[mat] + c;
+  float sum = v[0];
+#pragma unroll
+  for (int e = 1; e < 8; ++e)
+    if (lane == e) sum = v[e];
+  float y = __bfloat162float(__float2bfloat16_rn(sum));
+  const long long o = (long long)m * job.N[mat] + (n - job.col0[mat]);
   if (job.epi == kSkEpGelu)
     y = 0.5f * y * (1.f + erff(y * 0.70710678118654752f));
   else if (job.epi == kSkEpResidual)
@@ -114,20 +148,24 @@ bool gemm_skinny_supported(const void *A, const void *Bm, const void *C, int M, 
          reinterpret_cast<uintptr_t>(Bm) % 16 == 0 && A && C;
 }
 
-// Slices of K: about two CTAs per SM of a 152-SM GB300, at most kSkMaxSplit
-// slices, at most kSkMaxRowsPerSlice rows per slice, and at most K / (16 M)
-// slices so that the fp32 partials (split * M * N * 4 bytes) stay near 1/8
-// of B's bytes.  The plan depends on the shape alone (not on the device
-// that happens to be current), so a workspace sized for a shape always fits
-// the launch of that shape.
+// Slices of K: about four CTAs per SM of a 152-SM GB300 (each CTA keeps
+// 32 KB of weight rows in flight, and the register budget allows four), at
+// least kSkUnroll rows and at most kSkMaxRowsPerSlice rows per slice, and
+// fp32 partials (split * M * N * 4 bytes) of at most 16 MB, which stay in
+// L2 between the two kernels.  The plan depends on the shape alone (not on
+// the device that happens to be current), so a workspace sized for a shape
+// always fits the launch of that shape.
 constexpr int kSkPlanSms = 152;
+constexpr long long kSkMaxPartialBytes = 16LL << 20;
 static void skinny_plan(int M, int N, int K, int &split, int &rows) {
   const int colblocks = (N + kSkCtaCols - 1) / kSkCtaCols;
-  int s = (2 * kSkPlanSms + colblocks - 1) / colblocks;
+  int s = (4 * kSkPlanSms + colblocks - 1) / colblocks;
   s = s < kSkMaxSplit ? s : kSkMaxSplit;
-  const int sm = K / (16 * (M > 0 ? M : 1));
-  s = s < sm ? s : sm;
-  s = s < K ? s : K;
+  const long long per_slice = 4LL * (M > 0 ? M : 1) * N;
+  const long long cap = kSkMaxPartialBytes / (per_slice > 0 ? per_slice : 1);
+  s = s < cap ? s : (int)cap;
+  const int rmin = (K + kSkUnroll - 1) / kSkUnroll;  // slices of at least kSkUnroll rows
+  s = s < rmin ? s : rmin;
   if (s < 1) s = 1;
   rows = (K + s - 1) / s;
   if (rows > kSkMaxRowsPerSlice) rows = kSkMaxRowsPerSlice;
@@ -187,8 +225,9 @@ cudaError_t launch_skinny_reduce_job(const float *partial, const SkinnyJob &job,
                                      cudaStream_t st) {
   int split = 1, rows = 1;
   skinny_plan(M, job.Ntot, K, split, rows);
-  const long long MN = (long long)M * job.Ntot;
-  skinny_reduce_kernel<<<(unsigned)((MN + 255) / 256), 256, 0, st>>>(partial, job, M, split);
+  const long long groups = (long long)M * job.Ntot / 8;  // one warp each
+  skinny_reduce_kernel<<<(unsigned)((groups * 32 + 255) / 256), 256, 0, st>>>(partial, job, M,
+                                                                             split);
   return cudaGetLastError();
 }
 

@@ -12,10 +12,19 @@
 // One CTA per (piece, batch, head, 128-wide slice of d_v).  Warp 0 streams K'
 // and V through a 2-stage TMA ring, warp 1 issues the state-update MMAs
 // (S^T += V^T K', M=128 v, N=d_k, K=64 tokens, fp32 accumulator in TMEM),
-// warps 2-5 convert V to fp16 with a power-of-two block scale and rescale the
-// TMEM state between chunks (gamma^L and the exponent bookkeeping).  Every
-// wait is bounded; a wait that runs out sets the status word and an abort
-// flag, and every role leaves after draining its own asynchronous work.
+// warps 2-5 convert V to fp16.  The decay never touches the accumulator:
+// TMEM holds D = S 2^-sigma with a real-valued sigma, and
+//   S_{c+1} = gamma^L S_c + U_c   becomes   D_{c+1} = A B + D_c 2^-n_c,
+// the MMA's own accumulator scale (an integer n_c in 0..15) with
+// sigma_{c+1} = sigma_c + n_c + L log2(gamma): the gamma^L of every chunk
+// goes into the bookkeeping, and V of chunk c is converted with the factor
+// 2^(kexp_c - sigma_{c+1}) that puts A B = U_c 2^-sigma_{c+1} in the same
+// units.  n_c keeps the converted V below 2^15 (fp16's range); a chunk that
+// would need n_c > 15 has its accumulator rescaled on the CUDA cores first.
+// So the MMAs of consecutive chunks follow each other with no CUDA-core
+// step in between.  Every wait is bounded; a wait that runs out sets the
+// status word and an abort flag, and every role leaves after draining its
+// own asynchronous work.
 #include "ktimer.h"
 #include "launch.h"
 #include "tc.cuh"
@@ -30,12 +39,13 @@ constexpr int kC = 64, kW = 128, kNT = 192;
 constexpr uint32_t kOffK = 0, kOffV = 32 * 1024, kOffKs = 48 * 1024, kOffMeta = kOffKs + 1024;
 constexpr uint32_t kStage = 50 * 1024;
 constexpr uint32_t kOffRed = 2 * kStage;
-constexpr uint32_t kOffBar = kOffRed + 64;
+constexpr uint32_t kOffN = kOffRed + 64;   // [2] int: the accumulator scale of each stage's MMA
+constexpr uint32_t kOffBar = kOffN + 16;
 constexpr int kNumBars = 8;
 constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;
 constexpr uint32_t kSmem = kOffMisc + 16 + 1024;
 constexpr uint32_t kBudget = 1u << 24;
-enum { FULL0 = 0, FULL1, EMPTY0, EMPTY1, EPI, SFULL, DRAIN };
+enum { FULL0 = 0, FULL1, EMPTY0, EMPTY1, CONV0, CONV1, SFULL, DRAIN };
 
 __device__ __forceinline__ bool swait(uint64_t *bar, uint32_t parity, volatile int *abort_p,
                                       unsigned *status) {
@@ -101,13 +111,7 @@ state_tc_kernel(const __grid_constant__ KParams p, const __grid_constant__ CUten
   const float lng = p.lng[h];
 
   if (tid == 0) {
-    tc::mbar_init(&bars[FULL0], 1);
-    tc::mbar_init(&bars[FULL1], 1);
-    tc::mbar_init(&bars[EMPTY0], 1);
-    tc::mbar_init(&bars[EMPTY1], 1);
-    tc::mbar_init(&bars[EPI], 1);
-    tc::mbar_init(&bars[SFULL], 1);
-    tc::mbar_init(&bars[DRAIN], 1);
+    for (int i = 0; i < kNumBars; ++i) tc::mbar_init(&bars[i], 1);
     *abort_p = 0;
     tc::fence_mbar_init();
   }
@@ -150,17 +154,24 @@ state_tc_kernel(const __grid_constant__ KParams p, const __grid_constant__ CUten
     __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA
+    // D = A B + D 2^-n: the first K-step of a chunk applies the chunk's
+    // accumulator scale (the first chunk starts from zero), the others add.
     if (lane == 0) {
       const uint32_t id_s = tc::idesc_f16(128, DK, 1, 1);
+      const int *nsm = reinterpret_cast<const int *>(sm + kOffN);
       for (int lc = 0; lc < ncl; ++lc) {
         const int s = lc & 1;
-        if (!swait(&bars[EPI], lc & 1, abort_p, p.status)) break;
+        if (!swait(&bars[CONV0 + s], (lc >> 1) & 1, abort_p, p.status)) break;
         tc::tc_fence_after();
         const uint32_t sk = tc::smem_u32(sm + s * kStage + kOffK), sv = sk + kOffV;
-        for (int ks = 0; ks < 4; ++ks)  // S^T (+)= V^T K'; the first chunk starts from zero
-          tc::mma_ss(tb, tc::smem_desc(sv + ks * 2048, 8192, 1024, tc::kSw128),
-                     tc::smem_desc(sk + ks * 2048, 8192, 1024, tc::kSw128), id_s,
-                     (lc | ks) != 0);
+        for (int ks = 0; ks < 4; ++ks) {
+          const uint64_t da = tc::smem_desc(sv + ks * 2048, 8192, 1024, tc::kSw128);
+          const uint64_t db = tc::smem_desc(sk + ks * 2048, 8192, 1024, tc::kSw128);
+          if (ks == 0 && lc > 0)
+            tc::mma_ss_scale_d(tb, da, db, id_s, nsm[s]);
+          else
+            tc::mma_ss(tb, da, db, id_s, (lc | ks) != 0);
+        }
         tc::mma_commit(&bars[SFULL]);
         tc::mma_commit(&bars[EMPTY0 + s]);
       }
@@ -173,8 +184,11 @@ state_tc_kernel(const __grid_constant__ KParams p, const __grid_constant__ CUten
     const int q = warp & 3, et = tid - 64, vrow = q * 32 + lane;
     const uint32_t lb = (uint32_t)(q * 32) << 16;
     const long long vglob = v0 + vrow;
+    int *nsm = reinterpret_cast<int *>(sm + kOffN);
     int rslot = 0;
-    int sigma = 0;  // TMEM holds S * 2^-sigma
+    // TMEM holds D = S u with u = um 2^-ue (um in [1, 2)), i.e. u = 2^-sigma.
+    float um = 1.f;
+    int ue = 0;
     const bool zown = need_z && rank == 0 && 2 * et < DK;
     float zr0 = 0.f, zr1 = 0.f;  // z entries 2 et, 2 et + 1
     bool ok = true;
@@ -193,7 +207,7 @@ state_tc_kernel(const __grid_constant__ KParams p, const __grid_constant__ CUten
         zr0 = fmaf(gL, zr0, ks[2 * et]);
         zr1 = fmaf(gL, zr1, ks[2 * et + 1]);
       }
-      // (1) V tile: bf16 -> fp16 * 2^-vx in place (1024 16-byte words).
+      // (1) max |V| of the tile (1024 16-byte words).
       uint4 vv[8];
       float vm = 0.f;
 #pragma unroll
@@ -210,50 +224,72 @@ state_tc_kernel(const __grid_constant__ KParams p, const __grid_constant__ CUten
       if (lane == 0) r4[et >> 5] = vm;
       asm volatile("bar.sync 1, 128;" ::: "memory");
       const float vmx = fmaxf(fmaxf(r4[0], r4[1]), fmaxf(r4[2], r4[3]));
-      const int vx = expo14s(vmx);
-      const float vsc = exp2f((float)-vx);
+      // (2) units of this chunk.  V is converted with f = u' 2^kexp, u' the
+      // accumulator's units after the chunk; u' = u gamma^-L 2^-n, n chosen
+      // so that max|V| f < 2^15.  The first chunk starts from zero: its
+      // units are free, taken so that max|V| f is about 2^14.
+      int n = 0, extra = 0;
+      if (lc == 0) {
+        const int e = expo14s(vmx);  // vmx 2^-e < 2^14
+        um = 1.f;
+        ue = e + bk;                 // f = 2^(bk - ue) = 2^-e
+      } else {
+        // u gamma^-L as (mantissa, exponent)
+        int d = 0;
+        float m = frexpf(um * __frcp_rn(gL), &d);  // in [0.5, 1)
+        m *= 2.f;
+        int e = ue - d + 1;
+        // f0 = m 2^(bk - e): need vmx f0 2^-n < 2^15
+        const int need = vmx > 0.f ? expo14s(vmx * ldexpf(m, bk - e)) : 0;  // vmx f0 2^-need < 2^14
+        // at least the decay's own exponent, d - 1, so that the units u do
+        // not drift upward over chunks whose V is small or zero (D then
+        // shrinks with the true state instead of growing)
+        n = max(max(need, d - 1), 0);
+        if (n > 15) {
+          extra = n - 15;
+          n = 15;
+        }
+        um = m;
+        ue = e + n + extra;
+      }
+      const float f = ldexpf(um, bk - ue);
+      if (et == 0) nsm[s] = n;
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
         const uint32_t w[4] = {vv[u].x, vv[u].y, vv[u].z, vv[u].w};
         uint32_t o4[4];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) o4[e] = tc::pack_f16(bfl(w[e]) * vsc, bfh(w[e]) * vsc);
+        for (int e = 0; e < 4; ++e) o4[e] = tc::pack_f16(bfl(w[e]) * f, bfh(w[e]) * f);
         reinterpret_cast<uint4 *>(st + kOffV)[et + 128 * u] = make_uint4(o4[0], o4[1], o4[2], o4[3]);
       }
       tc::fence_proxy_async_smem();
-      // (2) the product of this chunk lands in units of 2^(vx + bk); bring
-      // the running state to those units and apply gamma^L.
-      const int sigma_next = vx + bk;
-      if (lc > 0) {
+      // (3) rare: a chunk far larger than the state so far needs the
+      // accumulator scaled down by more than the MMA's 2^-15; the rest,
+      // 2^-extra, is applied here once the previous chunk's MMAs are done.
+      if (grp_all4(extra == 0) == false) {
         ok = grp_all4(swait(&bars[SFULL], (lc - 1) & 1, abort_p, p.status));
         if (!ok) break;
         tc::tc_fence_after();
-        const float f_pre = gL * exp2f((float)(sigma - sigma_next));
-        for (int g0 = 0; g0 < DK / 32; g0 += 2) {
-          uint32_t r[2][32];
-          tc::tmem_ld32(tb + lb + g0 * 32, r[0]);
-          tc::tmem_ld32(tb + lb + g0 * 32 + 32, r[1]);
-          tc::tmem_ld_wait();
+        const float sc = exp2f((float)-extra);
+        for (int g0 = 0; g0 < DK / 32; ++g0) {
+          uint32_t r[32];
+          tc::tmem_ld32(tb + lb + g0 * 32, r);
+          tc::tmem_ld_wait_on(r);
 #pragma unroll
-          for (int hh = 0; hh < 2; ++hh) {
-#pragma unroll
-            for (int i = 0; i < 32; ++i)
-              r[hh][i] = __float_as_uint(__uint_as_float(r[hh][i]) * f_pre);
-            tc::tmem_st32(tb + lb + (g0 + hh) * 32, r[hh]);
-          }
+          for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * sc);
+          tc::tmem_st32(tb + lb + g0 * 32, r);
         }
         tc::tmem_st_wait();
+        tc::tc_fence_before();
       }
-      sigma = sigma_next;
-      tc::tc_fence_before();
       asm volatile("bar.sync 1, 128;" ::: "memory");
-      if (et == 0) tc::mbar_arrive(&bars[EPI]);
+      if (et == 0) tc::mbar_arrive(&bars[CONV0 + s]);
     }
     if (ok && ncl > 0) {
       ok = grp_all4(swait(&bars[SFULL], (ncl - 1) & 1, abort_p, p.status));
       if (ok) {
         tc::tc_fence_after();
-        const float back = exp2f((float)sigma);
+        const float back = ldexpf(__frcp_rn(um), ue);  // S = D / u
         float *dst = Part + (((long long)piece * BH + bh) * DK) * p.dv + vglob;
         for (int g = 0; g < DK / 32; ++g) {
           uint32_t r[32];

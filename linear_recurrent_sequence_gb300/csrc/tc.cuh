@@ -207,6 +207,42 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
       : "memory");
 }
 
+// D (TMEM) = A (smem desc) * B (smem desc) + D * 2^-kScale (the
+// instruction's scale-input-d operand, an immediate 0..15).
+template <int kScale>
+__device__ __forceinline__ void mma_ss_scaled(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                              uint32_t idesc) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, 1, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p, %4;\n}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "n"(kScale)
+      : "memory");
+}
+
+// The same with the scale chosen at run time (0..15; other values are
+// clamped): one immediate form per value.
+static __device__ __noinline__ void mma_ss_scale_d(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                            uint32_t idesc, int n) {
+  switch (n <= 0 ? 0 : (n >= 15 ? 15 : n)) {
+    case 0: mma_ss_scaled<0>(d_tmem, a_desc, b_desc, idesc); break;
+    case 1: mma_ss_scaled<1>(d_tmem, a_desc, b_desc, idesc); break;
+    case 2: mma_ss_scaled<2>(d_tmem, a_desc, b_desc, idesc); break;
+    case 3: mma_ss_scaled<3>(d_tmem, a_desc, b_desc, idesc); break;
+    case 4: mma_ss_scaled<4>(d_tmem, a_desc, b_desc, idesc); break;
+    case 5: mma_ss_scaled<5>(d_tmem, a_desc, b_desc, idesc); break;
+    case 6: mma_ss_scaled<6>(d_tmem, a_desc, b_desc, idesc); break;
+    case 7: mma_ss_scaled<7>(d_tmem, a_desc, b_desc, idesc); break;
+    case 8: mma_ss_scaled<8>(d_tmem, a_desc, b_desc, idesc); break;
+    case 9: mma_ss_scaled<9>(d_tmem, a_desc, b_desc, idesc); break;
+    case 10: mma_ss_scaled<10>(d_tmem, a_desc, b_desc, idesc); break;
+    case 11: mma_ss_scaled<11>(d_tmem, a_desc, b_desc, idesc); break;
+    case 12: mma_ss_scaled<12>(d_tmem, a_desc, b_desc, idesc); break;
+    case 13: mma_ss_scaled<13>(d_tmem, a_desc, b_desc, idesc); break;
+    case 14: mma_ss_scaled<14>(d_tmem, a_desc, b_desc, idesc); break;
+    default: mma_ss_scaled<15>(d_tmem, a_desc, b_desc, idesc); break;
+  }
+}
+
 // Arrive once on `bar` when every MMA issued so far by this thread is done.
 __device__ __forceinline__ void mma_commit(uint64_t *bar) {
   asm volatile(

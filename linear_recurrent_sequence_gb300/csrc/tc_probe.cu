@@ -116,7 +116,82 @@ tc_probe_kernel(int a_mode, int b_mode, int M, int N, int K, int a_lbo, int a_sb
   if (warp == 0) tc::tmem_dealloc(t0, 512);
 }
 
+// D = A B^T with one MMA chain (K-major A and B, M = N = 128, K = 64), then
+// the same chain again with the first MMA scaling the accumulator:
+// D' = A B^T + D 2^-n.  Checks the scale-input-d operand of tcgen05.mma.
+__global__ void __launch_bounds__(128)
+tc_probe_scale_kernel(int n, const __nv_bfloat16 *__restrict__ A,
+                      const __nv_bfloat16 *__restrict__ B, float *__restrict__ D,
+                      unsigned *status) {
+  extern __shared__ __align__(1024) uint8_t smraw[];
+  __shared__ uint64_t bar;
+  __shared__ uint32_t tbase;
+  uint8_t *sm = tc::smem_align1024(smraw);
+  uint8_t *sA = sm, *sB = sm + 16 * 1024;
+  const int tid = threadIdx.x, warp = tid >> 5;
+  constexpr int M = 128, N = 128, K = 64;
+  if (tid == 0) {
+    tc::mbar_init(&bar, 1);
+    tc::fence_mbar_init();
+  }
+  if (warp == 0) {
+    tc::tmem_alloc(&tbase, 128);
+    tc::tmem_relinquish();
+  }
+  for (int e = tid; e < M * K; e += 128) {
+    const int r = e / K, k = e % K;
+    *reinterpret_cast<__nv_bfloat16 *>(sA + tc::sw128_off(r, k / 8) + (k % 8) * 2) = A[e];
+    *reinterpret_cast<__nv_bfloat16 *>(sB + tc::sw128_off(r, k / 8) + (k % 8) * 2) = B[e];
+  }
+  tc::fence_proxy_async_smem();
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t t0 = tbase;
+  if (tid == 0) {
+    const uint32_t idesc = tc::idesc_bf16(M, N, 0, 0);
+    for (int pass = 0; pass < 2; ++pass)
+      for (int s = 0; s < K / 16; ++s) {
+        const uint64_t a = tc::smem_desc(tc::smem_u32(sA) + s * 32, 16, 1024, tc::kSw128);
+        const uint64_t b = tc::smem_desc(tc::smem_u32(sB) + s * 32, 16, 1024, tc::kSw128);
+        if (pass == 1 && s == 0)
+          tc::mma_ss_scale_d(t0, a, b, idesc, n);
+        else
+          tc::mma_ss(t0, a, b, idesc, (pass | s) != 0);
+      }
+    tc::mma_commit(&bar);
+  }
+  const bool ok = tc::mbar_wait(&bar, 0, status, 1u << 22);
+  tc::tc_fence_after();
+  if (ok) {
+    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    uint32_t r[32];
+    for (int c = 0; c < N; c += 32) {
+      tc::tmem_ld32(t0 + lane_base + c, r);
+      tc::tmem_ld_wait();
+      for (int i = 0; i < 32; ++i) D[(warp * 32 + (tid & 31)) * N + c + i] = __uint_as_float(r[i]);
+    }
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tc::tmem_dealloc(t0, 128);
+}
+
 }  // namespace ret
+
+extern "C" int retention_tc_probe_scale_d(int n, const void *A, const void *B, float *D,
+                                          unsigned *status, ret_stream_t stream) {
+  using namespace ret;
+  if (n < 0 || n > 15 || !A || !B || !D || !status) return RET_EINVAL;
+  const int smem = 33 * 1024;
+  if (cudaFuncSetAttribute(tc_probe_scale_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           smem) != cudaSuccess)
+    return RET_ECUDA;
+  tc_probe_scale_kernel<<<1, 128, smem, (cudaStream_t)stream>>>(
+      n, reinterpret_cast<const __nv_bfloat16 *>(A), reinterpret_cast<const __nv_bfloat16 *>(B),
+      D, status);
+  return cudaGetLastError() == cudaSuccess ? RET_OK : RET_ECUDA;
+}
 
 extern "C" int retention_tc_probe(int a_mode, int b_mode, int M, int N, int K, int a_lbo,
                                   int a_sbo, int b_lbo, int b_sbo, const void *A,

@@ -112,6 +112,7 @@ _SIGS = {
     "retention_kernel_name": (ctypes.c_char_p, [ctypes.c_int]),
     "retention_launch_count": (ctypes.c_longlong, []),
     "retention_tc_probe": (ctypes.c_int, [ctypes.c_int] * 9 + [_P, _P, _P, _P, _P]),
+    "retention_tc_probe_scale_d": (ctypes.c_int, [ctypes.c_int, _P, _P, _P, _P, _P]),
     "retention_kernel_timer_read": (ctypes.c_int, [ctypes.c_int,
                                                    ctypes.POINTER(ctypes.c_double),
                                                    ctypes.POINTER(ctypes.c_longlong),

@@ -212,3 +212,32 @@ def test_segments_through_the_abi(R, dtype, dk, dv, cuts):
     parts = [(S0, z0) if s < 0 else dS[s] for s, _ in terms]
     S_f, _ = R.state_combine(parts, [t for _, t in terms], gam, S_out=torch.empty_like(S0))
     assert np.max(np.abs(host(S_f) - S_ref)) / np.max(np.abs(S_ref)) < 1e-2
+
+
+@pytest.mark.gpu
+def test_state_pass_magnitude_jumps(R):
+    """The state kernel keeps its accumulator in units set by the data: a
+    run of all-zero values, then values 2^-20 smaller, then 2^20 larger (the
+    last jump needs more than the MMA's own 2^-15 accumulator scale, so the
+    kernel rescales on the CUDA cores) must still give the oracle's state."""
+    from tests.helpers import host, seeded
+    B, H, N, dk, dv = 1, 2, 64 * 40, 128, 128
+    q, q64 = seeded(717, "q", (B, H, N, dk), "bf16")
+    k, k64 = seeded(717, "k", (B, H, N, dk), "bf16")
+    v, v64 = seeded(717, "v", (B, H, N, dv), "bf16")
+    scale = np.ones(N)
+    scale[:640] = 0.0
+    scale[640:1280] = 2.0 ** -20
+    scale[1280:] = 2.0 ** 20
+    v = v * torch.from_numpy(scale).float().cuda()[None, None, :, None].bfloat16()
+    v64 = v64 * scale[None, None, :, None]
+    gam = [0.96875, 0.999]
+    p = oracle.Problem(B, H, N, dk, dv, gam, gn_eps=1e-6)
+    _, S_ref, z_ref = oracle.chunkwise(p, 64, q64, k64, v64)
+    R.lib.retention_kernel_timer_reset()
+    S, z = R.chunkwise_state(k, v, gam)
+    torch.cuda.synchronize()
+    assert "state_pass" in R.kernel_times()
+    got = host(S)
+    assert np.all(np.isfinite(got))
+    assert np.max(np.abs(got - S_ref)) / np.max(np.abs(S_ref)) < 1e-2

@@ -84,3 +84,24 @@ def test_m64_accumulator_lanes(R):
     D, ref = run_probe(R, 0, 0, 64, 64, 128)
     lanes = [m64_lane(r) for r in range(64)]
     assert close(D[lanes], ref)
+
+
+@pytest.mark.parametrize("n", [0, 1, 5, 15])
+def test_accumulator_scale_operand(R, n):
+    """tcgen05.mma's scale-input-d operand: D' = A B^T + D 2^-n, checked with
+    D = A B^T from a first chain, so D' = A B^T (1 + 2^-n)."""
+    g = torch.Generator().manual_seed(40 + n)
+    A = torch.randn(128, 64, generator=g).to(torch.bfloat16)
+    B = torch.randn(128, 64, generator=g).to(torch.bfloat16)
+    ref = (A.double() @ B.double().T).numpy() * (1.0 + 2.0 ** -n)
+    D = torch.zeros(128, 128, dtype=torch.float32, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    Ad, Bd = A.cuda(), B.cuda()
+    rc = R.lib.retention_tc_probe_scale_d(n, ctypes.c_void_p(Ad.data_ptr()),
+                                          ctypes.c_void_p(Bd.data_ptr()),
+                                          ctypes.c_void_p(D.data_ptr()),
+                                          ctypes.c_void_p(st.data_ptr()),
+                                          ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    torch.cuda.synchronize()
+    assert rc == 0 and int(st.item()) == 0
+    assert close(D.double().cpu().numpy(), ref)
