@@ -760,15 +760,32 @@ struct DecWs {
   size_t xn, q, k, v, g, y, m, h1, part, total;
 };
 
+// Decode-batch GEMM jobs stream their weights on CUDA cores for up to
+// kDecSkinnyRows rows; beyond, the tensor cores (128-row tiles, the missing
+// rows read as zeros) split over K do the same stream with less work per
+// weight byte, when the widths suit them.
+constexpr int kDecSkinnyRows = 4;
+
+static bool dec_use_tc(int B, int Ntot, int K) {
+  return B > kDecSkinnyRows && Ntot % 256 == 0 && K % 64 == 0;
+}
+
+// fp32 partials of one decode-batch GEMM job (either kernel's K slices).
+static size_t dec_job_partial_bytes(int B, int Ntot, int K) {
+  size_t tc = 0, sk = 0;
+  if (dec_use_tc(B, Ntot, K)) tc = (size_t)gemm_tc_split(B, Ntot, K) * B * Ntot * sizeof(float);
+  if (B <= 16) sk = gemm_skinny_partial_bytes(B, Ntot, K);
+  return tc > sk ? tc : sk;
+}
+
 static size_t dec_partial_bytes(const retnet_stack_desc *d) {
   const msr_desc &m = d->block.msr;
   const int B = m.B, dm = m.d_model, HK = m.H * m.d_k, HV = m.H * m.d_v, F = d->block.d_ffn;
-  if (B > 16) return 0;
   // the four input projections as one job, W_O, W1, W2, and each alone
-  const size_t c[7] = {gemm_skinny_partial_bytes(B, 2 * HK + 2 * HV, dm),
-                       gemm_skinny_partial_bytes(B, HK, dm), gemm_skinny_partial_bytes(B, HV, dm),
-                       gemm_skinny_partial_bytes(B, dm, HV), gemm_skinny_partial_bytes(B, F, dm),
-                       gemm_skinny_partial_bytes(B, dm, F), 0};
+  const size_t c[6] = {dec_job_partial_bytes(B, 2 * HK + 2 * HV, dm),
+                       dec_job_partial_bytes(B, HK, dm), dec_job_partial_bytes(B, HV, dm),
+                       dec_job_partial_bytes(B, dm, HV), dec_job_partial_bytes(B, F, dm),
+                       dec_job_partial_bytes(B, dm, F)};
   size_t mx = 0;
   for (size_t x : c) mx = x > mx ? x : mx;
   return mx;
@@ -834,24 +851,48 @@ static cudaError_t gemm_dec(const void *A, const void *Bm, void *C, int M, int N
   return gemm_any(A, Bm, C, M, N, K, status, st);
 }
 
-// Several decode-batch GEMMs of one A (same K) as one weight-streaming job,
-// with the reduce's epilogue (GELU, or a skip connection with R); false
-// when the job does not fit the kernel (the caller then runs them apart).
+// Several decode-batch GEMMs of one A (same K) as one job, with the
+// reduce's epilogue (GELU, or a skip connection with R): the
+// weight-streaming kernel for up to 16 rows, the tensor-core kernel split
+// over K beyond; false when the job fits neither (the caller then runs the
+// GEMMs apart).
 static bool skinny_job_fits(int M, int count, const void *const *Bs, const int *Ns) {
-  if (M < 1 || M > 16) return false;
+  if (M < 1) return false;
   for (int i = 0; i < count; ++i)
     if (Ns[i] < 8 || Ns[i] % 8 || !Bs[i] || reinterpret_cast<uintptr_t>(Bs[i]) % 16) return false;
   return true;
 }
 
+static bool dec_job_tc(const void *A, int M, int count, const void *const *Bs, const int *Ns,
+                       int K) {
+  int Ntot = 0;
+  for (int i = 0; i < count; ++i) {
+    if (!gemm_tc_supported(A, Bs[i], Bs[i], M, Ns[i], K)) return false;
+    Ntot += Ns[i];
+  }
+  return dec_use_tc(M, Ntot, K);
+}
+
+static bool dec_job_fits(const void *A, int M, int count, const void *const *Bs, const int *Ns,
+                         int K) {
+  if (!skinny_job_fits(M, count, Bs, Ns)) return false;
+  return dec_job_tc(A, M, count, Bs, Ns, K) || M <= 16;
+}
+
 static cudaError_t gemm_dec_job(const void *A, int count, const void *const *Bs, void *const *Cs,
                                 const int *Ns, int M, int K, int epi, const void *R, float *part,
-                                cudaStream_t st) {
+                                unsigned *status, cudaStream_t st) {
   SkinnyJob job;
   if (!skinny_job_init(job, count, Bs, Cs, Ns, epi, R)) return cudaErrorInvalidValue;
-  cudaError_t e = RET_TIMED_LAUNCH(kKGemmSkinny, st, launch_gemm_skinny_job(A, job, M, K, part, st));
+  if (!dec_job_tc(A, M, count, Bs, Ns, K)) {
+    cudaError_t e = RET_TIMED_LAUNCH(kKGemmSkinny, st, launch_gemm_skinny_job(A, job, M, K, part, st));
+    if (e != cudaSuccess) return e;
+    return RET_TIMED_LAUNCH(kKSkinnyReduce, st, launch_skinny_reduce_job(part, job, M, K, st));
+  }
+  const int split = gemm_tc_split(M, job.Ntot, K);
+  cudaError_t e = RET_TIMED_LAUNCH(kKGemmTc, st, launch_gemm_tc_partials(A, count, Bs, Ns, M, K, part, split, status, st));
   if (e != cudaSuccess) return e;
-  return RET_TIMED_LAUNCH(kKSkinnyReduce, st, launch_skinny_reduce_job(part, job, M, K, st));
+  return RET_TIMED_LAUNCH(kKSkinnyReduce, st, launch_skinny_reduce_split(part, job, M, split, st));
 }
 
 ret_status retnet_decode_step(const retnet_stack_desc *d, const retnet_layer_weights *layers,
@@ -907,10 +948,10 @@ ret_status retnet_decode_step(const retnet_stack_desc *d, const retnet_layer_wei
     const void *Win[4] = {L.WQ, L.WK, L.WV, L.WG};
     void *Cin[4] = {Q, K, V, G};
     const int Nin[4] = {HK, HK, HV, HV};
-    const bool fused = skinny_job_fits(B, 4, Win, Nin) && skinny_job_fits(B, 1, &L.WO, &dm) &&
-                       skinny_job_fits(B, 1, &L.W1, &F) && skinny_job_fits(B, 1, &L.W2, &dm);
+    const bool fused = dec_job_fits(Xn, B, 4, Win, Nin, dm) && dec_job_fits(Y, B, 1, &L.WO, &dm, HV) &&
+                       dec_job_fits(Xn, B, 1, &L.W1, &F, dm) && dec_job_fits(H1, B, 1, &L.W2, &dm, F);
     if (fused) {
-      RET_CUDA(gemm_dec_job(Xn, 4, Win, Cin, Nin, B, dm, kSkEpNone, nullptr, part, st));
+      RET_CUDA(gemm_dec_job(Xn, 4, Win, Cin, Nin, B, dm, kSkEpNone, nullptr, part, status, st));
     } else {
       RET_CUDA(gemm_dec(Xn, L.WQ, Q, B, HK, dm, part, status, st));
       RET_CUDA(gemm_dec(Xn, L.WK, K, B, HK, dm, part, status, st));
@@ -921,7 +962,7 @@ ret_status retnet_decode_step(const retnet_stack_desc *d, const retnet_layer_wei
     RET_CUDA(RET_TIMED_LAUNCH(kKGate, st, launch_swish_gate(Y, G, (long long)B * HV, st)));
     if (fused) {
       void *c = Mo;
-      RET_CUDA(gemm_dec_job(Y, 1, &L.WO, &c, &dm, B, HV, kSkEpResidual, X, part, st));
+      RET_CUDA(gemm_dec_job(Y, 1, &L.WO, &c, &dm, B, HV, kSkEpResidual, X, part, status, st));
     } else {
       RET_CUDA(gemm_dec(Y, L.WO, Mo, B, dm, HV, part, status, st));
       RET_CUDA(RET_TIMED_LAUNCH(kKResidual, st, launch_residual_add(Mo, X, (long long)B * dm, st)));
@@ -930,9 +971,9 @@ ret_status retnet_decode_step(const retnet_stack_desc *d, const retnet_layer_wei
     RET_CUDA(RET_TIMED_LAUNCH(kKLayerNorm, st, launch_layernorm(Mo, L.ln2_w, L.ln2_b, Xn, B, dm, d->block.ln_eps, st)));
     if (fused) {
       void *c = H1;
-      RET_CUDA(gemm_dec_job(Xn, 1, &L.W1, &c, &F, B, dm, kSkEpGelu, nullptr, part, st));
+      RET_CUDA(gemm_dec_job(Xn, 1, &L.W1, &c, &F, B, dm, kSkEpGelu, nullptr, part, status, st));
       c = X;
-      RET_CUDA(gemm_dec_job(H1, 1, &L.W2, &c, &dm, B, F, kSkEpResidual, Mo, part, st));
+      RET_CUDA(gemm_dec_job(H1, 1, &L.W2, &c, &dm, B, F, kSkEpResidual, Mo, part, status, st));
     } else {
       RET_CUDA(gemm_dec(Xn, L.W1, H1, B, F, dm, part, status, st));
       RET_CUDA(RET_TIMED_LAUNCH(kKGelu, st, launch_gelu(H1, (long long)B * F, st)));
@@ -943,11 +984,19 @@ ret_status retnet_decode_step(const retnet_stack_desc *d, const retnet_layer_wei
   return RET_OK;
 }
 
+// Few rows on the tensor cores: the K split only pays while the output
+// tiles alone leave most SMs idle.
+static bool gemm_wants_split(int M, int N, int K) {
+  return M > 16 && M <= 256 && N % 256 == 0 && K % 64 == 0 && gemm_tc_split(M, N, K) > 1;
+}
+
 size_t retention_gemm_workspace_size(int M, int N, int K) {
   if (M < 0 || N < 0 || K < 1) return 0;
   size_t need = kStatusBytes;
   if (M >= 1 && M <= 16 && N >= 8 && N % 8 == 0)
     need += align256(gemm_skinny_partial_bytes(M, N, K));
+  else if (gemm_wants_split(M, N, K))
+    need += align256(dec_job_partial_bytes(M, N, K));
   return need;
 }
 
@@ -961,10 +1010,18 @@ ret_status retention_gemm_bf16(const void *A, const void *Bm, void *C, int M, in
   if (rs != RET_OK) return rs;
   cudaStream_t st = (cudaStream_t)stream;
   unsigned *status = reinterpret_cast<unsigned *>(ws);
-  // Few rows with room for the split-K partials: the weight-streaming kernel.
+  // Few rows with room for the split-K partials: the weight-streaming kernel
+  // (up to 16 rows) or the tensor cores split over K (up to 256 rows).
   if (gemm_skinny_supported(A, Bm, C, M, N, K) &&
       ws_bytes >= retention_gemm_workspace_size(M, N, K)) {
     RET_CUDA(gemm_dec(A, Bm, C, M, N, K, at<float>(ws, kStatusBytes), status, st));
+    return RET_OK;
+  }
+  if (gemm_wants_split(M, N, K) && gemm_tc_supported(A, Bm, C, M, N, K) &&
+      ws_bytes >= retention_gemm_workspace_size(M, N, K)) {
+    void *c = C;
+    RET_CUDA(gemm_dec_job(A, 1, &Bm, &c, &N, M, K, kSkEpNone, nullptr, at<float>(ws, kStatusBytes),
+                          status, st));
     return RET_OK;
   }
   RET_CUDA(gemm_any(A, Bm, C, M, N, K, status, st));

@@ -143,6 +143,36 @@ skinny_reduce_kernel(const float *__restrict__ P, const SkinnyJob job, int M, in
   job.C[mat][o] = __float2bfloat16_rn(y);
 }
 
+// The same reduce for few slices (the tensor-core GEMM's K split): one
+// thread per (row, 8 adjacent columns) adds the slices in order.
+__global__ void __launch_bounds__(256)
+skinny_reduce_few_kernel(const float *__restrict__ P, const SkinnyJob job, int M, int split) {
+  const long long MN = (long long)M * job.Ntot;
+  const long long g = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (g * 8 >= MN) return;
+  const long long i0 = g * 8;
+  float v[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  for (int t = 0; t < split; ++t) {
+    const float4 *src = reinterpret_cast<const float4 *>(P + (long long)t * MN + i0);
+    const float4 x = src[0], y = src[1];
+    v[0] += x.x; v[1] += x.y; v[2] += x.z; v[3] += x.w;
+    v[4] += y.x; v[5] += y.y; v[6] += y.z; v[7] += y.w;
+  }
+  const int m = (int)(i0 / job.Ntot), n0 = (int)(i0 % job.Ntot);
+  int mat = 0;
+  while (mat + 1 < job.count && n0 >= job.col0[mat + 1]) ++mat;
+  const long long o = (long long)m * job.N[mat] + (n0 - job.col0[mat]);
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    float y = __bfloat162float(__float2bfloat16_rn(v[e]));
+    if (job.epi == kSkEpGelu)
+      y = 0.5f * y * (1.f + erff(y * 0.70710678118654752f));
+    else if (job.epi == kSkEpResidual)
+      y = y + __bfloat162float(job.R[o + e]);
+    job.C[mat][o + e] = __float2bfloat16_rn(y);
+  }
+}
+
 bool gemm_skinny_supported(const void *A, const void *Bm, const void *C, int M, int N, int K) {
   return M >= 1 && M <= 16 && N >= 8 && N % 8 == 0 && K >= 1 &&
          reinterpret_cast<uintptr_t>(Bm) % 16 == 0 && A && C;
@@ -225,9 +255,18 @@ cudaError_t launch_skinny_reduce_job(const float *partial, const SkinnyJob &job,
                                      cudaStream_t st) {
   int split = 1, rows = 1;
   skinny_plan(M, job.Ntot, K, split, rows);
-  const long long groups = (long long)M * job.Ntot / 8;  // one warp each
-  skinny_reduce_kernel<<<(unsigned)((groups * 32 + 255) / 256), 256, 0, st>>>(partial, job, M,
-                                                                             split);
+  return launch_skinny_reduce_split(partial, job, M, split, st);
+}
+
+cudaError_t launch_skinny_reduce_split(const float *partial, const SkinnyJob &job, int M,
+                                       int split, cudaStream_t st) {
+  const long long groups = (long long)M * job.Ntot / 8;
+  if (split <= 16)  // one thread per group
+    skinny_reduce_few_kernel<<<(unsigned)((groups + 255) / 256), 256, 0, st>>>(partial, job, M,
+                                                                              split);
+  else  // one warp per group
+    skinny_reduce_kernel<<<(unsigned)((groups * 32 + 255) / 256), 256, 0, st>>>(partial, job, M,
+                                                                               split);
   return cudaGetLastError();
 }
 

@@ -33,6 +33,7 @@ constexpr int kNumBars = 2 * kStages + 5;
 constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;
 constexpr uint32_t kSmem = kOffMisc + 16 + 1024;
 constexpr uint32_t kBudget = 1u << 24;
+constexpr int kGemmPlanSms = 152;  // the K split depends on the shape alone
 
 __device__ __forceinline__ bool gwait(uint64_t *bar, uint32_t parity, volatile int *abort_p,
                                       unsigned *status) {
@@ -52,10 +53,35 @@ __device__ __forceinline__ void gdrain(uint64_t *bar, uint32_t parity) {
 
 }  // namespace
 
-template <bool kGate>
+// One work item: a 128 x 256 output tile of one matrix of the job, over one
+// K slice.
+struct GemmItem {
+  int mat, m0, n0, kb0, kb1, ks;
+};
+
+__device__ __forceinline__ GemmItem gemm_item(const GemmJob &job, int t, int mtiles, int nk) {
+  const int ntiles = job.ntile0[job.count];
+  const int per = mtiles * ntiles;
+  GemmItem it;
+  it.ks = t / per;
+  const int r = t % per, mt = r / ntiles, nt = r % ntiles;
+  int mat = 0;
+  while (mat + 1 < job.count && nt >= job.ntile0[mat + 1]) ++mat;
+  it.mat = mat;
+  it.m0 = mt * BM;
+  it.n0 = (nt - job.ntile0[mat]) * BN;
+  const int nkb = (nk + job.ksplit - 1) / job.ksplit;
+  it.kb0 = it.ks * nkb;
+  it.kb1 = min(nk, it.kb0 + nkb);
+  return it;
+}
+
+// kMode 0: C = A B (bf16); 1: C <- swish(A B) (.) C; 2: fp32 partial
+// products of each K slice into P[ks][M][ldc] at the matrix's columns.
+template <int kMode>
 __global__ void __launch_bounds__(kNT, 1)
-gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-               __nv_bfloat16 *__restrict__ C, int M, int N, int K, unsigned *status) {
+gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ GemmJob job,
+               int M, int K, unsigned *status) {
   extern __shared__ uint8_t smraw[];
   uint8_t *sm = tc::smem_align1024(smraw);
   uint64_t *full = reinterpret_cast<uint64_t *>(sm + kOffBar);
@@ -68,7 +94,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   // M may be ragged: the last row tile's missing rows of A are outside the
   // tensor map and arrive as zeros; their rows of C are not stored.
-  const int tiles_n = N / BN, tiles = ((M + BM - 1) / BM) * tiles_n, nk = K / BK;
+  const int mtiles = (M + BM - 1) / BM, nk = K / BK;
+  const int tiles = mtiles * job.ntile0[job.count] * job.ksplit;
 
   if (tid == 0) {
     for (int i = 0; i < kStages; ++i) {
@@ -95,12 +122,20 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   if (warp == 0) {
     if (lane == 0) {
       tc::prefetch_tmap(&tmA);
-      tc::prefetch_tmap(&tmB);
+#pragma unroll
+      for (int i = 0; i < kGemmJobMax; ++i)
+        if (i < job.count) tc::prefetch_tmap(&job.tmB[i]);
       int it = 0;
       bool ok = true;
       for (int t = blockIdx.x; ok && t < tiles; t += gridDim.x) {
-        const int m0 = (t / tiles_n) * BM, n0 = (t % tiles_n) * BN;
-        for (int kb = 0; kb < nk; ++kb, ++it) {
+        const GemmItem w = gemm_item(job, t, mtiles, nk);
+        const int m0 = w.m0, n0 = w.n0;
+        // constant indices: each map's address stays the kernel parameter's own
+        const CUtensorMap *tmB = w.mat == 0   ? &job.tmB[0]
+                                 : w.mat == 1 ? &job.tmB[1]
+                                 : w.mat == 2 ? &job.tmB[2]
+                                              : &job.tmB[3];
+        for (int kb = w.kb0; kb < w.kb1; ++kb, ++it) {
           const int s = it % kStages;
           if (it >= kStages && !gwait(&empty[s], ((it / kStages) - 1) & 1, abort_p, status)) {
             ok = false;
@@ -111,7 +146,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
           tc::tma_load_2d(st, &tmA, &full[s], kb * BK, m0);
 #pragma unroll
           for (int j = 0; j < BN / 64; ++j)
-            tc::tma_load_2d(st + kABytes + j * 8192, &tmB, &full[s], n0 + j * 64, kb * BK);
+            tc::tma_load_2d(st + kABytes + j * 8192, tmB, &full[s], n0 + j * 64, kb * BK);
         }
       }
       for (int i = it > kStages ? it - kStages : 0; i < it; ++i)
@@ -128,7 +163,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         if (lt >= 2 && !gwait(&acc_empty[buf], ((lt >> 1) - 1) & 1, abort_p, status)) break;
         tc::tc_fence_after();
         const uint32_t d = tb + buf * BN;
-        for (int kb = 0; kb < nk; ++kb, ++it) {
+        const GemmItem w = gemm_item(job, t, mtiles, nk);
+        for (int kb = w.kb0; kb < w.kb1; ++kb, ++it) {
           const int s = it % kStages;
           if (!gwait(&full[s], (it / kStages) & 1, abort_p, status)) {
             ok = false;
@@ -140,7 +176,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
           for (int k = 0; k < BK / 16; ++k)
             tc::mma_ss(d, tc::smem_desc(sa + k * 32, 16, 1024, tc::kSw128),
                        tc::smem_desc(sb + k * 2048, 8192, 1024, tc::kSw128), idesc,
-                       (kb | k) != 0);
+                       (kb > w.kb0) || k != 0);
           tc::mma_commit(&empty[s]);
         }
         if (ok) tc::mma_commit(&acc_full[buf]);
@@ -169,16 +205,27 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       }
       if (!ok) break;
       tc::tc_fence_after();
-      const int m0 = (t / tiles_n) * BM, n0 = (t % tiles_n) * BN;
+      const GemmItem w = gemm_item(job, t, mtiles, nk);
+      const int m0 = w.m0, n0 = w.n0 + job.col0[w.mat];
       const bool live = m0 + row < M;  // the TMEM loads stay warp-wide
-      __nv_bfloat16 *crow = C + (long long)(live ? m0 + row : 0) * N + n0;
+      const long long orow = (long long)(live ? m0 + row : 0);
+      __nv_bfloat16 *crow = kMode == 2 ? nullptr : job.C + orow * job.ldc + n0;
+      float *prow = kMode == 2 ? job.P + ((long long)w.ks * M + orow) * job.ldc + n0 : nullptr;
       for (int g = 0; g < BN / 32; ++g) {
         uint32_t r[32];
         tc::tmem_ld32(tb + lb + buf * BN + g * 32, r);
         tc::tmem_ld_wait();
-        uint4 *dst = reinterpret_cast<uint4 *>(crow + g * 32);
         if (!live) continue;
-        if constexpr (kGate) {
+        if constexpr (kMode == 2) {
+          float4 *pd = reinterpret_cast<float4 *>(prow + g * 32);
+#pragma unroll
+          for (int v = 0; v < 8; ++v)
+            pd[v] = make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
+                                __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3]));
+          continue;
+        }
+        uint4 *dst = reinterpret_cast<uint4 *>(crow + g * 32);
+        if constexpr (kMode == 1) {
           // C <- swish(acc) (.) C: fast exponential and divide, a few ulp in
           // fp32 before the bf16 rounding; swish -> 0 as acc -> -inf.
           uint4 cur[4];
@@ -230,30 +277,78 @@ bool gemm_tc_supported(const void *A, const void *Bm, const void *C, int M, int 
   return tmap_available();
 }
 
-cudaError_t launch_gemm_tc(const void *A, const void *Bm, void *C, int M, int N, int K,
-                           unsigned *status, cudaStream_t st, bool gate) {
-  CUtensorMap ta, tbm;
-  const cuuint64_t da[2] = {(cuuint64_t)K, (cuuint64_t)M};
-  const cuuint64_t sa[1] = {(cuuint64_t)K * 2};
-  const cuuint32_t ba[2] = {BK, BM};
+static bool encode_b(CUtensorMap *tm, const void *Bm, int N, int K) {
   const cuuint64_t db[2] = {(cuuint64_t)N, (cuuint64_t)K};
   const cuuint64_t sb[1] = {(cuuint64_t)N * 2};
   const cuuint32_t bb[2] = {64, BK};
+  return tmap_encode(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, Bm, db, sb, bb,
+                     CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+template <int kMode>
+static cudaError_t launch_job(const void *A, const GemmJob &job, int M, int K, unsigned *status,
+                              cudaStream_t st) {
+  CUtensorMap ta;
+  const cuuint64_t da[2] = {(cuuint64_t)K, (cuuint64_t)M};
+  const cuuint64_t sa[1] = {(cuuint64_t)K * 2};
+  const cuuint32_t ba[2] = {BK, BM};
   if (!tmap_encode(&ta, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, A, da, sa, ba,
-                   CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !tmap_encode(&tbm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, Bm, db, sb, bb,
                    CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
-  auto kern = gate ? gemm_tc_kernel<true> : gemm_tc_kernel<false>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+  cudaError_t e =
+      cudaFuncSetAttribute(gemm_tc_kernel<kMode>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
   if (e != cudaSuccess) return e;
   int dev = 0, sms = 0;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  const int tiles = ((M + BM - 1) / BM) * (N / BN);
-  const int grid = tiles < sms ? tiles : sms;
-  kern<<<grid, kNT, kSmem, st>>>(ta, tbm, reinterpret_cast<__nv_bfloat16 *>(C), M, N, K, status);
+  const int items = ((M + BM - 1) / BM) * job.ntile0[job.count] * job.ksplit;
+  const int grid = items < sms ? items : sms;
+  gemm_tc_kernel<kMode><<<grid, kNT, kSmem, st>>>(ta, job, M, K, status);
   return cudaGetLastError();
+}
+
+cudaError_t launch_gemm_tc(const void *A, const void *Bm, void *C, int M, int N, int K,
+                           unsigned *status, cudaStream_t st, bool gate) {
+  GemmJob job;
+  if (!encode_b(&job.tmB[0], Bm, N, K)) return cudaErrorInvalidValue;
+  job.count = 1;
+  job.ntile0[1] = N / BN;
+  job.ldc = N;
+  job.ksplit = 1;
+  job.C = reinterpret_cast<__nv_bfloat16 *>(C);
+  return gate ? launch_job<1>(A, job, M, K, status, st) : launch_job<0>(A, job, M, K, status, st);
+}
+
+int gemm_tc_split(int M, int Ntot, int K) {
+  const int tiles = ((M + BM - 1) / BM) * (Ntot / BN), nk = K / BK;
+  int ks = (2 * kGemmPlanSms + tiles - 1) / tiles;  // about two items per SM
+  const int cap = K / (8 * (M > 0 ? M : 1));       // partials <= 1/4 of the weight bytes
+  ks = ks < cap ? ks : cap;
+  ks = ks < nk ? ks : nk;
+  if (ks < 1) ks = 1;
+  const int nkb = (nk + ks - 1) / ks;
+  return (nk + nkb - 1) / nkb;  // every slice non-empty
+}
+
+cudaError_t launch_gemm_tc_partials(const void *A, int count, const void *const *Bs,
+                                    const int *Ns, int M, int K, float *P, int ksplit,
+                                    unsigned *status, cudaStream_t st) {
+  if (count < 1 || count > kGemmJobMax || ksplit < 1) return cudaErrorInvalidValue;
+  GemmJob job;
+  job.count = count;
+  int col = 0, nt = 0;
+  for (int i = 0; i < count; ++i) {
+    if (!encode_b(&job.tmB[i], Bs[i], Ns[i], K)) return cudaErrorInvalidValue;
+    job.ntile0[i] = nt;
+    job.col0[i] = col;
+    nt += Ns[i] / BN;
+    col += Ns[i];
+  }
+  job.ntile0[count] = nt;
+  job.ldc = col;
+  job.ksplit = ksplit;
+  job.P = P;
+  return launch_job<2>(A, job, M, K, status, st);
 }
 
 }  // namespace ret

@@ -1,6 +1,7 @@
 // Internal launchers shared between the kernel files and the C ABI layer.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_fp16.h>
 
 #include "common.cuh"
@@ -104,6 +105,22 @@ bool gemm_tc_supported(const void *A, const void *Bm, const void *C, int M, int 
 // gate: C <- swish(A B) (.) C (bf16 C read and rewritten in the epilogue).
 cudaError_t launch_gemm_tc(const void *A, const void *Bm, void *C, int M, int N, int K,
                            unsigned *status, cudaStream_t st, bool gate = false);
+// Up to four B matrices of one A (same K), split over K: fp32 partials
+// P[ks][M][sum N_i] (matrix i at its column offset), added by the skinny
+// reduce (launch_skinny_reduce_split).  gemm_tc_split: the K split for a
+// shape (about two work items per SM, partials at most 1/4 of B's bytes).
+constexpr int kGemmJobMax = 4;
+struct GemmJob {
+  CUtensorMap tmB[kGemmJobMax];
+  int count = 0, ldc = 0, ksplit = 1;
+  int ntile0[kGemmJobMax + 1] = {}, col0[kGemmJobMax] = {};
+  __nv_bfloat16 *C = nullptr;
+  float *P = nullptr;
+};
+int gemm_tc_split(int M, int Ntot, int K);
+cudaError_t launch_gemm_tc_partials(const void *A, int count, const void *const *Bs,
+                                    const int *Ns, int M, int K, float *P, int ksplit,
+                                    unsigned *status, cudaStream_t st);
 
 // gemm_simt.cu: C[M,N] = A[M,K] B[K,N], bf16 in (row-major), fp32 accumulate.
 cudaError_t launch_gemm_bf16(const void *A, const void *Bm, void *C, int M, int N,
@@ -158,5 +175,8 @@ cudaError_t launch_gemm_skinny_job(const void *A, const SkinnyJob &job, int M, i
                                    float *partial, cudaStream_t st);
 cudaError_t launch_skinny_reduce_job(const float *partial, const SkinnyJob &job, int M, int K,
                                      cudaStream_t st);
+// The same reduce over `split` given slices (the tensor-core GEMM's partials).
+cudaError_t launch_skinny_reduce_split(const float *partial, const SkinnyJob &job, int M,
+                                       int split, cudaStream_t st);
 
 }  // namespace ret

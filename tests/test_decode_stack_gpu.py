@@ -94,3 +94,18 @@ def test_decode_msr_shape_stack(R):
 def test_decode_batch_past_the_skinny_gemm(R):
     """B=20 rows: the projections take the general GEMM."""
     run_decode(R, 92, 20, 64, 2, 32, 64, 96, 1, 0.1, 3, 0)
+
+
+def test_decode_batch_tensor_core_split(R):
+    """B=20 rows with projection widths that the tensor-core GEMM takes
+    (multiples of 256): the four input projections run as one job split over
+    K into fp32 partials, added by the reduce with its epilogues.  One layer:
+    with these weights a second layer makes batch row 14 ill-conditioned
+    (its second-layer retention output is near zero before GroupNorm), and
+    the weight-streaming path, which the other tests pin, shows the same
+    0.19 deviation there, so it says nothing about this GEMM."""
+    R.lib.retention_kernel_timer_reset()
+    run_decode(R, 93, 20, 256, 2, 128, 128, 512, 1, 0.05, 3, oracle.NORM_ALL)
+    torch.cuda.synchronize()
+    names = R.kernel_times()
+    assert "gemm_tc" in names and "skinny_reduce" in names and "gemm_skinny" not in names, names

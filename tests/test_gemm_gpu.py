@@ -17,10 +17,14 @@ def R():
 
 @pytest.mark.parametrize("M,N,K,tc", [(128, 256, 64, True), (384, 512, 192, True),
                                       (2048, 2048, 2048, True), (100, 200, 50, False),
-                                      (32, 512, 4096, True), (300, 256, 192, True)])
+                                      (32, 512, 4096, True), (300, 256, 192, True),
+                                      (20, 256, 4096, True), (128, 256, 4096, True),
+                                      (64, 1024, 2048, True)])
 def test_gemm_matches_fp32_product(R, M, N, K, tc):
     """Tensor-core shapes (including M not a multiple of the 128-row tile,
-    whose last tile is partly outside A and C) and a CUDA-core shape."""
+    whose last tile is partly outside A and C, and few-row shapes that the
+    tensor cores run split over K with fp32 partials added by a reduce) and a
+    CUDA-core shape."""
     g = torch.Generator(device="cuda").manual_seed(M + N + K)
     A = torch.randn(M, K, device="cuda", generator=g).bfloat16()
     B = (torch.randn(K, N, device="cuda", generator=g) * 0.05).bfloat16()
