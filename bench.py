@@ -414,7 +414,7 @@ def run_ours(args):
         extra["decode"] = bench_decode(args, R, dev, stream, hbm, world, max_over_ranks)
         extra["decode_stack"] = bench_decode_stack(args, R, dev, hbm, world, max_over_ranks)
         extra["msr_layer"] = bench_msr(args, R, dev, stream, tflops, world, max_over_ranks)
-        extra["backward"] = bench_backward(args, R, dev, world, max_over_ranks)
+        extra["backward"] = bench_backward(args, R, dev, tflops, hbm, world, max_over_ranks)
         extra["retnet_block"] = bench_block(args, R, dev, tflops, world, max_over_ranks)
 
     cpu = None
@@ -653,13 +653,18 @@ def flops_bwd_per_token_head(C):
     return 2 * (3 * (C + 1) / 2 * (DK + DV) + 6 * DK * DV)
 
 
-# fp32 CUDA-core peak: 152 SMs x 128 FP32 lanes x 2 flops (FMA) x 2.07 GHz.
-FP32_ALU_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
+# Bytes the backward must move per (token, head): q, k, v, dO read and
+# dq, dk, dv written, all bf16.
+BWD_BYTES_PER_TOKEN_HEAD = 2 * (DK + DK + DV + DV) + 2 * (DK + DK + DV)
 
 
-def bench_backward(args, R, dev, world, max_over_ranks):
+def bench_backward(args, R, dev, tflops, hbm, world, max_over_ranks):
     """Gradients of retention (no GroupNorm, no normalisations) at the
-    headline shape, bf16 inputs: dq, dk, dv from dO, fp32 on CUDA cores."""
+    headline shape, bf16 inputs: dq, dk, dv from dO, as five runs of the
+    forward tensor-core kernel (64-token chunks) and their operand passes.
+    At 64-token chunks the backward's arithmetic intensity (flops per byte
+    it must move) is above the GPU's ridge point, so the roofline is the
+    tensor cores' (fp16 operands, same dense rate as bf16)."""
     import torch
     from linear_recurrent_sequence_gb300 import synth
     gam = synth.head_gammas(H)
@@ -688,16 +693,18 @@ def bench_backward(args, R, dev, world, max_over_ranks):
     R.lib.retention_kernel_timer_enable(0)
     kt = {name: ms / max(n, 1) for name, (ms, n, t) in R.kernel_times().items()}
     ms = max_over_ranks(e0.elapsed_time(e1)) / reps
-    fl = flops_bwd_per_token_head(16) * H * N
+    fl = flops_bwd_per_token_head(64) * H * N
     achieved = fl / (ms * 1e-3) / 1e12
+    gbps = BWD_BYTES_PER_TOKEN_HEAD * H * N / (ms * 1e-3) / 1e9
     del q, k, v, dO, dq, dk_, dv_, ws
     torch.cuda.empty_cache()
     return {"tokens_per_s": world * N / (ms * 1e-3), "ms": ms,
             "kernel_ms": kt,
-            "roofline": {"bound": "alu", "achieved": achieved, "peak": FP32_ALU_TFLOPS,
-                         "unit": "TFLOP/s", "frac": achieved / FP32_ALU_TFLOPS,
-                         "note": "algorithmic flops at 16-token chunks; peak derived from "
-                                 "the unit counts and the maximum SM clock"}}
+            "roofline": {"bound": "tensor", "achieved": achieved, "peak": tflops,
+                         "unit": "TFLOP/s", "frac": achieved / tflops,
+                         "note": "algorithmic flops at 64-token chunks, of measured bf16 "
+                                 "burst peak"},
+            "GBps_algorithmic": gbps, "frac_hbm": gbps / hbm}
 
 
 def main():

@@ -179,6 +179,12 @@ ret_status retention_recurrent_step(const ret_desc *d, const void *q,
  * Requires gn_eps < 0 (no GroupNorm) and norm_flags without RET_NORM_RSUM:
  * RET_EUNSUPPORTED otherwise.  No output may overlap an input, except dS_in
  * and dS_out.  The chunk field does not change the result.
+ * bf16 inputs with d_k 128 or 256, d_v a multiple of 128 up to 1024 and
+ * every gamma^64 >= 2^-16 run on the tensor cores, as runs of the forward
+ * kernel on time-reversed operands (the adjoint of the recurrence is the
+ * recurrence in reversed time); their operands are rounded to bf16 / fp16
+ * as the forward rounds its own.  Everything else runs on CUDA cores in
+ * fp32.  The workspace size covers whichever path the descriptor takes.
  */
 size_t retention_backward_workspace_size(const ret_desc *d);
 ret_status retention_chunkwise_bwd(const ret_desc *d, const void *q, const void *k,

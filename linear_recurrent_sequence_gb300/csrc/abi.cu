@@ -398,6 +398,197 @@ ret_status state_impl(const ret_desc *d, const void *k, const void *v, const flo
   return RET_OK;
 }
 
+// ------------------------------------------------- tensor-core backward
+// The gradients as five runs of the forward tensor-core path (see
+// backward_tc.cu): dv and the state gradient from one run in reversed time,
+// dq' and dk' from runs over pieces of d_v (at most 256 wide, the forward's
+// score dimension).  bf16 inputs with d_k in {128, 256} and d_v a multiple
+// of 128 (at most 1024); other shapes and fp32 take the CUDA-core kernels.
+struct BwdTcWs {
+  int w = 0, nvc = 0;
+  size_t kr = 0, kr_rev = 0, qs_rev = 0, dos = 0, dos_rev = 0, v_rev = 0;
+  size_t ts = 0, tds = 0, sdv = 0, dvr = 0, o[kBwdFinishMax] = {}, total = 0;
+};
+
+bool bwd_tc_shape(const ret_desc *d) {
+  if (!(d->in_dtype == RET_BF16 && (d->d_k == 128 || d->d_k == 256) && d->d_v % 128 == 0 &&
+        d->d_v <= 1024 && d->N > 0 && (long long)d->B * d->H > 0 &&
+        (long long)d->B * d->H <= 65535))
+    return false;
+  // The forward's tensor-core range (gamma^64 >= 2^-16), which also keeps
+  // the 1/gamma of the reversed runs' entry states small.
+  for (int h = 0; h < d->H; ++h)
+    if (!(d->gamma[h] > 0.0 && std::log(d->gamma[h]) * 64.0 >= -16.0 * std::log(2.0) * 0.999))
+      return false;
+  return true;
+}
+
+// A forward run inside the backward: bf16 in, fp32 out, no rotation, no
+// normalisation, no GroupNorm, contiguous [B*H][N][d] operands unless the
+// caller sets other strides.
+void bwd_inner_desc(const ret_desc *d, int dk, int dv, ret_desc *r) {
+  retention_desc_init(r, d->B, d->H, d->N, dk, dv, d->gamma);
+  r->chunk = 64;
+  r->in_dtype = RET_BF16;
+  r->out_dtype = RET_F32;
+  r->rotate = 0;
+  r->norm_flags = 0;
+  r->gn_eps = -1.f;
+  r->pos0 = 0;
+}
+
+void contig(const ret_desc *d, int dim, int64_t s[3]) {
+  s[0] = (int64_t)d->H * d->N * dim;
+  s[1] = (int64_t)d->N * dim;
+  s[2] = dim;
+}
+
+BwdTcWs bwd_tc_ws(const ret_desc *d) {
+  BwdTcWs w;
+  w.w = d->d_v % 256 == 0 ? 256 : 128;
+  w.nvc = d->d_v / w.w;
+  ret_desc a, b;
+  bwd_inner_desc(d, d->d_k, d->d_v, &a);
+  bwd_inner_desc(d, w.w, d->d_k, &b);
+  const size_t ia = retention_workspace_size(&a), ib = retention_workspace_size(&b);
+  const size_t BH = (size_t)d->B * d->H, rows = BH * d->N;
+  const size_t sb = BH * d->d_k * d->d_v * sizeof(float);
+  size_t off = align256(ia > ib ? ia : ib);  // the inner runs' workspace, status word first
+  w.kr = off; off = align256(off + rows * d->d_k * 2);
+  w.kr_rev = off; off = align256(off + rows * d->d_k * 2);
+  w.qs_rev = off; off = align256(off + rows * d->d_k * 2);
+  w.dos = off;
+  if (d->out_dtype != RET_BF16) off = align256(off + rows * d->d_v * 2);
+  w.dos_rev = off; off = align256(off + rows * d->d_v * 2);
+  w.v_rev = off; off = align256(off + rows * d->d_v * 2);
+  w.ts = off; off = align256(off + sb);
+  w.tds = off; off = align256(off + sb);
+  w.sdv = off; off = align256(off + sb);
+  w.dvr = off; off = align256(off + rows * d->d_v * sizeof(float));
+  for (int j = 0; j < w.nvc; ++j) {
+    w.o[j] = off;
+    off = align256(off + rows * d->d_k * sizeof(float));
+  }
+  w.total = off;
+  return w;
+}
+
+ret_status bwd_tc_impl(const ret_desc *d, const KParams &p, const void *q, const void *k,
+                       const void *v, const float *S_in, const void *dO, const float *dS_out,
+                       void *dq, void *dk, void *dv, float *dS_in, void *ws, cudaStream_t st) {
+  const BwdTcWs w = bwd_tc_ws(d);
+  const int dkk = d->d_k, dvv = d->d_v, BH = d->B * d->H;
+  const bool scale = (d->norm_flags & (RET_NORM_SCALE | RET_NORM_DROW)) != 0;
+  const bool dO_bf16 = d->out_dtype == RET_BF16;
+  __nv_bfloat16 *kr = at<__nv_bfloat16>(ws, w.kr), *kr_rev = at<__nv_bfloat16>(ws, w.kr_rev);
+  __nv_bfloat16 *qs_rev = at<__nv_bfloat16>(ws, w.qs_rev), *dos = at<__nv_bfloat16>(ws, w.dos);
+  __nv_bfloat16 *dos_rev = at<__nv_bfloat16>(ws, w.dos_rev);
+  __nv_bfloat16 *v_rev = at<__nv_bfloat16>(ws, w.v_rev);
+  float *ts = at<float>(ws, w.ts), *tds = at<float>(ws, w.tds), *dvr = at<float>(ws, w.dvr);
+  const size_t inner_bytes = w.kr;
+  // Operands: k' forward and reversed, s q' reversed, dO reversed (and a
+  // bf16 copy when dO is fp32), v reversed.
+  BwdPrepJobs jobs;
+  jobs.count = 4;
+  BwdPrepJob *J = jobs.job;
+  J[0].src = k; J[0].d = dkk; J[0].rotate = p.rotate; J[0].fwd = kr; J[0].rev = kr_rev;
+  J[1].src = q; J[1].d = dkk; J[1].rotate = p.rotate; J[1].rowscale = scale; J[1].rev = qs_rev;
+  J[2].src = dO; J[2].d = dvv; J[2].bf16 = dO_bf16; J[2].fwd = dO_bf16 ? nullptr : dos;
+  J[2].rev = dos_rev;
+  J[3].src = v; J[3].d = dvv; J[3].rev = v_rev;
+  for (int i = 0; i < 3; ++i) {
+    J[0].s[i] = d->sk[i];
+    J[1].s[i] = d->sq[i];
+    J[2].s[i] = d->so[i];
+    J[3].s[i] = d->sv[i];
+  }
+  RET_CUDA(RET_TIMED_LAUNCH(kKBwdPrep, st, launch_bwd_prep(p, jobs, st)));
+  // Entry states, before dS_out (which dS_in may alias) is overwritten.
+  float *sdv = nullptr;
+  if (dS_out) {
+    CombineParts parts;  // dS_out / gamma
+    parts.count = 1;
+    parts.S[0] = dS_out;
+    parts.t[0] = -1;
+    sdv = at<float>(ws, w.sdv);
+    RET_CUDA(RET_TIMED_LAUNCH(kKStateCombine, st, launch_state_combine(p, parts, sdv, nullptr, st)));
+    RET_CUDA(RET_TIMED_LAUNCH(kKBwdPrep, st, launch_bwd_transpose(sdv, BH, dkk, dvv, w.w, tds, st)));
+  }
+  if (S_in) RET_CUDA(RET_TIMED_LAUNCH(kKBwdPrep, st, launch_bwd_transpose(S_in, BH, dkk, dvv, w.w, ts, st)));
+  // dv and U_0: the forward on (k', s q', dO) in reversed time.
+  {
+    ret_desc r;
+    bwd_inner_desc(d, dkk, dvv, &r);
+    ret_status rs = chunkwise_impl(&r, kr_rev, qs_rev, dos_rev, sdv, nullptr, dS_in, nullptr,
+                                   dvr, ws, inner_bytes, st);
+    if (rs != RET_OK) return rs;
+  }
+  BwdFinish F;
+  F.x[0] = dvr;
+  F.n_in = 1;
+  F.d = dvv;
+  F.reverse = 1;
+  for (int i = 0; i < 3; ++i) F.s[i] = d->sv[i];
+  F.out = dv;
+  RET_CUDA(RET_TIMED_LAUNCH(kKBwdFinish, st, launch_bwd_finish(p, F, st)));
+  if (dS_in) {  // dS_in = gamma U_0
+    CombineParts parts;
+    parts.count = 1;
+    parts.S[0] = dS_in;
+    parts.t[0] = 1;
+    RET_CUDA(RET_TIMED_LAUNCH(kKStateCombine, st, launch_state_combine(p, parts, dS_in, nullptr, st)));
+  }
+  // dq' / s: per piece of d_v, the forward on (dO, v, k') from S_in^T;
+  // dk': the forward on (v, dO, s q') in reversed time from (dS_out/gamma)^T.
+  for (int pass = 0; pass < 2; ++pass) {
+    BwdFinish G;
+    for (int j = 0; j < w.nvc; ++j) {
+      ret_desc r;
+      bwd_inner_desc(d, w.w, dkk, &r);
+      const void *Qp, *Kp, *Vp;
+      const float *Sp;
+      if (pass == 0) {
+        if (dO_bf16) {
+          for (int i = 0; i < 3; ++i) r.sq[i] = d->so[i];
+          Qp = reinterpret_cast<const __nv_bfloat16 *>(dO) + (size_t)j * w.w;
+        } else {
+          contig(d, dvv, r.sq);
+          Qp = dos + (size_t)j * w.w;
+        }
+        for (int i = 0; i < 3; ++i) r.sk[i] = d->sv[i];
+        Kp = reinterpret_cast<const __nv_bfloat16 *>(v) + (size_t)j * w.w;
+        Vp = kr;
+        Sp = S_in ? ts + (size_t)j * BH * w.w * dkk : nullptr;
+      } else {
+        contig(d, dvv, r.sq);
+        contig(d, dvv, r.sk);
+        Qp = v_rev + (size_t)j * w.w;
+        Kp = dos_rev + (size_t)j * w.w;
+        Vp = qs_rev;
+        Sp = dS_out ? tds + (size_t)j * BH * w.w * dkk : nullptr;
+      }
+      ret_status rs = chunkwise_impl(&r, Qp, Kp, Vp, Sp, nullptr, nullptr, nullptr,
+                                     at<float>(ws, w.o[j]), ws, inner_bytes, st);
+      if (rs != RET_OK) return rs;
+      G.x[j] = at<float>(ws, w.o[j]);
+    }
+    G.n_in = w.nvc;
+    G.d = dkk;
+    G.unrotate = p.rotate;
+    if (pass == 0) {
+      G.rowscale = scale;
+      for (int i = 0; i < 3; ++i) G.s[i] = d->sq[i];
+      G.out = dq;
+    } else {
+      G.reverse = 1;
+      for (int i = 0; i < 3; ++i) G.s[i] = d->sk[i];
+      G.out = dk;
+    }
+    RET_CUDA(RET_TIMED_LAUNCH(kKBwdFinish, st, launch_bwd_finish(p, G, st)));
+  }
+  return RET_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -548,7 +739,10 @@ ret_status retention_recurrent_step(const ret_desc *d, const void *q, const void
 
 size_t retention_backward_workspace_size(const ret_desc *d) {
   if (!desc_ok(d)) return 0;
-  return bwd_ws(d).total;
+  const size_t a = bwd_ws(d).total;
+  if (!bwd_tc_shape(d)) return a;
+  const size_t b = bwd_tc_ws(d).total;
+  return a > b ? a : b;
 }
 
 ret_status retention_chunkwise_bwd(const ret_desc *d, const void *q, const void *k,
@@ -575,6 +769,11 @@ ret_status retention_chunkwise_bwd(const ret_desc *d, const void *q, const void 
   }
   KParams p;
   make_params(d, ws, p);
+  if (bwd_tc_shape(d)) {
+    rs = check_ws(ws, ws_bytes, bwd_tc_ws(d).total);
+    if (rs != RET_OK) return rs;
+    return bwd_tc_impl(d, p, q, k, v, S_in, dO, dS_out, dq, dk, dv, dS_in, ws, st);
+  }
   float *Qr = at<float>(ws, w.qr), *Kr = at<float>(ws, w.kr);
   float *DQr = at<float>(ws, w.dq), *DKr = at<float>(ws, w.dk);
   RET_CUDA(RET_TIMED_LAUNCH(kKRotate, st, launch_rotate(p, q, p.sq, d->d_k, Qr, 0, nullptr, kScaleNone, st)));

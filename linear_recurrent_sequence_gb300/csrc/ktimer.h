@@ -28,6 +28,8 @@ enum KernelId {
   kKSkinnyReduce,
   kKStateCombine,
   kKStateSimt,
+  kKBwdPrep,
+  kKBwdFinish,
   kKernelCount
 };
 

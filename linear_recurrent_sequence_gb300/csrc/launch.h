@@ -140,6 +140,38 @@ cudaError_t launch_bwd_values(const KParams &p, const float *Qr, const float *Kr
 cudaError_t launch_unrotate(const KParams &p, const float *x, const long long s[3], void *out,
                             int out_bf16, cudaStream_t st);
 
+// backward_tc.cu: operands of the tensor-core backward's forward runs.
+// A prep job reads rows of src (strides s, bf16 or fp32, row width d, a
+// multiple of 8), optionally rotates them (+t theta) and scales them by the
+// first two normalisations' row factor, and writes bf16 rows to fwd[bh][t]
+// and/or rev[bh][N-1-t] (contiguous [B*H][N][d], 16-byte aligned).
+struct BwdPrepJob {
+  const void *src = nullptr;
+  long long s[3] = {};
+  int bf16 = 1, d = 0, rotate = 0, rowscale = 0, vec = 0;
+  __nv_bfloat16 *fwd = nullptr, *rev = nullptr;
+};
+constexpr int kBwdPrepMax = 4;
+struct BwdPrepJobs {
+  int count = 0;
+  BwdPrepJob job[kBwdPrepMax];
+};
+cudaError_t launch_bwd_prep(const KParams &p, BwdPrepJobs jobs, cudaStream_t st);
+// T_j[bh][e][a] = S[bh][a][j w + e]: the column blocks of width w transposed.
+cudaError_t launch_bwd_transpose(const float *S, int BH, int dk, int dv, int w, float *T,
+                                 cudaStream_t st);
+// out (strides s, dtype) at t = the sum of n_in fp32 [B*H][N][d] inputs at
+// row (reverse ? N-1-t : t), times the row factor when rowscale is set,
+// turned back by -t theta when unrotate is set.
+constexpr int kBwdFinishMax = 8;
+struct BwdFinish {
+  const float *x[kBwdFinishMax] = {};
+  int n_in = 0, d = 0, reverse = 0, rowscale = 0, unrotate = 0, out_bf16 = 1, vec = 0;
+  long long s[3] = {};
+  void *out = nullptr;
+};
+cudaError_t launch_bwd_finish(const KParams &p, BwdFinish F, cudaStream_t st);
+
 // block.cu: the RetNet block's LayerNorm (bf16 rows of d, fp32 gain and
 // bias), skip connection y <- y + r and in-place GELU (bf16, n values).
 cudaError_t launch_layernorm(const void *x, const float *w, const float *b, void *y, long long rows,
