@@ -411,11 +411,17 @@ def run_ours(args):
 
     extra = {}
     if not args.skip_extra:
-        extra["decode"] = bench_decode(args, R, dev, stream, hbm, world, max_over_ranks)
-        extra["decode_stack"] = bench_decode_stack(args, R, dev, hbm, world, max_over_ranks)
-        extra["msr_layer"] = bench_msr(args, R, dev, stream, tflops, world, max_over_ranks)
-        extra["backward"] = bench_backward(args, R, dev, tflops, hbm, world, max_over_ranks)
-        extra["retnet_block"] = bench_block(args, R, dev, tflops, world, max_over_ranks)
+        want = set(args.extra or EXTRAS)
+        if "decode" in want:
+            extra["decode"] = bench_decode(args, R, dev, stream, hbm, world, max_over_ranks)
+        if "decode_stack" in want:
+            extra["decode_stack"] = bench_decode_stack(args, R, dev, hbm, world, max_over_ranks)
+        if "msr_layer" in want:
+            extra["msr_layer"] = bench_msr(args, R, dev, stream, tflops, world, max_over_ranks)
+        if "backward" in want:
+            extra["backward"] = bench_backward(args, R, dev, tflops, hbm, world, max_over_ranks)
+        if "retnet_block" in want:
+            extra["retnet_block"] = bench_block(args, R, dev, tflops, world, max_over_ranks)
 
     cpu = None
     if rank == 0 and not args.skip_cpu:
@@ -435,6 +441,9 @@ def run_ours(args):
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
+
+
+EXTRAS = ("decode", "decode_stack", "msr_layer", "backward", "retnet_block")
 
 
 def bench_decode(args, R, dev, stream, hbm, world, max_over_ranks):
@@ -668,10 +677,11 @@ def bench_backward(args, R, dev, tflops, hbm, world, max_over_ranks):
     import torch
     from linear_recurrent_sequence_gb300 import synth
     gam = synth.head_gammas(H)
-    q = gen_bf16((1, H, N, DK), 4001, dev)
-    k = gen_bf16((1, H, N, DK), 4002, dev)
-    v = gen_bf16((1, H, N, DV), 4003, dev)
-    dO = gen_bf16((1, H, N, DV), 4004, dev)
+    Nb = args.bwd_tokens or N
+    q = gen_bf16((1, H, Nb, DK), 4001, dev)
+    k = gen_bf16((1, H, Nb, DK), 4002, dev)
+    v = gen_bf16((1, H, Nb, DV), 4003, dev)
+    dO = gen_bf16((1, H, Nb, DV), 4004, dev)
     dq, dk_, dv_ = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     d, _g = R.make_desc(q, k, v, dO, gam, gn_eps=None)
     ws = R.new_workspace(R.backward_workspace_size(d), dev)
@@ -681,25 +691,49 @@ def bench_backward(args, R, dev, tflops, hbm, world, max_over_ranks):
     f()
     f()
     torch.cuda.synchronize()
-    R.lib.retention_kernel_timer_reset()
-    R.lib.retention_kernel_timer_enable(1)
-    reps = 3
+    reps = 10
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    # Called from Python each time (host marshalling and launches included).
     e0.record()
     for _ in range(reps):
         f()
     e1.record()
     torch.cuda.synchronize()
-    R.lib.retention_kernel_timer_enable(0)
-    kt = {name: ms / max(n, 1) for name, (ms, n, t) in R.kernel_times().items()}
+    ms_eager = max_over_ranks(e0.elapsed_time(e1)) / reps
+    # Device time: the call's launches captured once in a CUDA graph.
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        f()
+    torch.cuda.current_stream().wait_stream(side)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        f()
+    graph.replay()
+    torch.cuda.synchronize()
+    e0.record()
+    for _ in range(reps):
+        graph.replay()
+    e1.record()
+    torch.cuda.synchronize()
     ms = max_over_ranks(e0.elapsed_time(e1)) / reps
-    fl = flops_bwd_per_token_head(64) * H * N
+    del graph
+    # Per-kernel times, from separate calls with the kernel timer on.
+    R.lib.retention_kernel_timer_reset()
+    R.lib.retention_kernel_timer_enable(1)
+    for _ in range(3):
+        f()
+    torch.cuda.synchronize()
+    R.lib.retention_kernel_timer_enable(0)
+    kt = {name: ms_k / max(n, 1) for name, (ms_k, n, t) in R.kernel_times().items()}
+    fl = flops_bwd_per_token_head(64) * H * Nb
     achieved = fl / (ms * 1e-3) / 1e12
-    gbps = BWD_BYTES_PER_TOKEN_HEAD * H * N / (ms * 1e-3) / 1e9
+    gbps = BWD_BYTES_PER_TOKEN_HEAD * H * Nb / (ms * 1e-3) / 1e9
     del q, k, v, dO, dq, dk_, dv_, ws
     torch.cuda.empty_cache()
-    return {"tokens_per_s": world * N / (ms * 1e-3), "ms": ms,
-            "kernel_ms": kt,
+    return {"tokens_per_s": world * Nb / (ms * 1e-3), "ms": ms, "tokens": Nb,
+            "ms_called_from_python": ms_eager, "timing": "CUDA graph of one call, 10 replays",
+            "kernel_ms_per_launch": kt,
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": tflops,
                          "unit": "TFLOP/s", "frac": achieved / tflops,
                          "note": "algorithmic flops at 64-token chunks, of measured bf16 "
@@ -721,7 +755,11 @@ def main():
     ap.add_argument("--stack-steps", type=int, default=16)
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--skip-extra", action="store_true")
+    ap.add_argument("--extra", nargs="*", choices=EXTRAS,
+                    help="which of the additional workloads to time (default: all)")
     ap.add_argument("--skip-cpu", action="store_true")
+    ap.add_argument("--bwd-tokens", type=int, default=0,
+                    help="sequence length of the backward workload (default: the headline N)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

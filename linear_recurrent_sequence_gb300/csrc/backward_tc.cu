@@ -84,6 +84,14 @@ __device__ __forceinline__ void stage_theta(const KParams &p, int pairs, ThetaSm
   __syncthreads();
 }
 
+// cos and sin of t theta for operands that are rounded to bf16 afterwards:
+// the reduced angle, then the hardware approximation, whose absolute error
+// (about 2^-21) is far below bf16's 2^-9.
+__device__ __forceinline__ void rot_cs_bf16(long long t, float th_hi, float th_lo, float &c,
+                                            float &s) {
+  __sincosf(rot_angle(t, th_hi, th_lo), &s, &c);
+}
+
 // Rotates the 4 pairs starting at pair j0 by +t theta (dir = 1) or back by
 // -t theta (dir = -1).
 __device__ __forceinline__ void rotate8(const ThetaSmem &th, long long t, int j0, float dir,
@@ -91,7 +99,7 @@ __device__ __forceinline__ void rotate8(const ThetaSmem &th, long long t, int j0
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     float cs, sn;
-    rot_cs(t, th.hi[j0 + i], th.lo[j0 + i], cs, sn);
+    rot_cs_bf16(t, th.hi[j0 + i], th.lo[j0 + i], cs, sn);
     sn *= dir;
     const float a = f[2 * i], c = f[2 * i + 1];
     f[2 * i] = a * cs - c * sn;
@@ -99,32 +107,46 @@ __device__ __forceinline__ void rotate8(const ThetaSmem &th, long long t, int j0
   }
 }
 
-// One CTA covers kBwdThreads * 8 / d rows of one (b, h) for job blockIdx.z:
-// row t of the source is read once and written to fwd[bh][t] and/or
-// rev[bh][N-1-t].
+// One CTA covers kBwdRowsPer * kBwdThreads * 8 / d rows of one (b, h) for
+// job blockIdx.z (each thread loads its rows before it works on them, for
+// more bytes in flight): row t of the source is read once and written to
+// fwd[bh][t] and/or rev[bh][N-1-t].
+constexpr int kBwdRowsPer = 2;
+
 __global__ void __launch_bounds__(kBwdThreads)
 bwd_prep_kernel(const __grid_constant__ KParams p, const __grid_constant__ BwdPrepJobs jobs) {
   __shared__ ThetaSmem th;
   const BwdPrepJob &J = jobs.job[blockIdx.z];
   const int per_row = J.d / kBwdVec, rows = kBwdThreads / per_row;
-  if (blockIdx.x * rows >= p.N) return;
+  const int t0 = blockIdx.x * rows * kBwdRowsPer;
+  if (t0 >= p.N) return;
   if (J.rotate) stage_theta(p, J.d / 2, th);
-  const int t = blockIdx.x * rows + threadIdx.x / per_row;
-  if (t >= p.N || threadIdx.x >= rows * per_row) return;
+  if (threadIdx.x >= rows * per_row) return;
   const int bh = blockIdx.y, b = bh / p.H, h = bh % p.H;
   const int c0 = (threadIdx.x % per_row) * kBwdVec;
-  float f[kBwdVec];
-  ld8(J.src, b * J.s[0] + h * J.s[1] + (long long)t * J.s[2] + c0, J.bf16, J.vec, f);
-  if (J.rotate) rotate8(th, p.pos0 + t, c0 / 2, 1.f, f);
-  if (J.rowscale) {
-    const float s = row_scale(p, h, p.pos0 + t + 1);
+  const int r0 = t0 + threadIdx.x / per_row;
+  float f[kBwdRowsPer][kBwdVec];
 #pragma unroll
-    for (int i = 0; i < kBwdVec; ++i) f[i] *= s;
+  for (int i = 0; i < kBwdRowsPer; ++i) {
+    const int t = r0 + i * rows;
+    if (t < p.N)
+      ld8(J.src, b * J.s[0] + h * J.s[1] + (long long)t * J.s[2] + c0, J.bf16, J.vec, f[i]);
   }
-  const uint4 u = pack8(f);
   const long long base = (long long)bh * p.N;
-  if (J.fwd) *reinterpret_cast<uint4 *>(J.fwd + (base + t) * J.d + c0) = u;
-  if (J.rev) *reinterpret_cast<uint4 *>(J.rev + (base + p.N - 1 - t) * J.d + c0) = u;
+#pragma unroll
+  for (int i = 0; i < kBwdRowsPer; ++i) {
+    const int t = r0 + i * rows;
+    if (t >= p.N) break;
+    if (J.rotate) rotate8(th, p.pos0 + t, c0 / 2, 1.f, f[i]);
+    if (J.rowscale) {
+      const float s = row_scale(p, h, p.pos0 + t + 1);
+#pragma unroll
+      for (int e = 0; e < kBwdVec; ++e) f[i][e] *= s;
+    }
+    const uint4 u = pack8(f[i]);
+    if (J.fwd) *reinterpret_cast<uint4 *>(J.fwd + (base + t) * J.d + c0) = u;
+    if (J.rev) *reinterpret_cast<uint4 *>(J.rev + (base + p.N - 1 - t) * J.d + c0) = u;
+  }
 }
 
 // T_j[bh][e][a] = S[bh][a][j*w + e] for the column blocks j of width w:
@@ -202,7 +224,7 @@ cudaError_t launch_bwd_prep(const KParams &p, BwdPrepJobs jobs, cudaStream_t st)
         (J.rev && (reinterpret_cast<uintptr_t>(J.rev) & 15)))
       return cudaErrorInvalidValue;
     J.vec = aligned16(J.src, J.s, J.bf16 ? 2 : 4);
-    const int rows = kBwdThreads / (J.d / kBwdVec);
+    const int rows = kBwdRowsPer * (kBwdThreads / (J.d / kBwdVec));
     const int x = (p.N + rows - 1) / rows;
     gx = x > gx ? x : gx;
   }

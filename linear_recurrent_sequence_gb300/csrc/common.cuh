@@ -57,19 +57,23 @@ __device__ __forceinline__ float rsum_scale(const KParams &p, float rowsum) {
   return (p.norm_flags & RET_NORM_RSUM) ? 1.f / fmaxf(fabsf(rowsum), 1.f) : 1.f;
 }
 
-// cos/sin of t * theta_j.  The product is kept as a float pair and reduced
-// modulo 2 pi with a two-part 2 pi (Cody-Waite), so the angle error stays
-// near 1e-6 rad for every position below 2^24.
-__device__ __forceinline__ void rot_cs(long long t, float th_hi, float th_lo,
-                                       float &c, float &s) {
+// t * theta_j reduced to [-pi, pi].  The product is kept as a float pair and
+// reduced modulo 2 pi with a two-part 2 pi (Cody-Waite), so the angle error
+// stays near 1e-6 rad for every position below 2^24.
+__device__ __forceinline__ float rot_angle(long long t, float th_hi, float th_lo) {
   const float tf = (float)t;
   const float p_hi = tf * th_hi;
   const float p_lo = fmaf(tf, th_hi, -p_hi) + tf * th_lo;
   const float k = rintf(p_hi * 0.159154943091895336f);
   float r = fmaf(-k, 6.28318548202514648f, p_hi);
   r = fmaf(-k, -1.74845553146951725e-07f, r);
-  r += p_lo;
-  sincosf(r, &s, &c);
+  return r + p_lo;
+}
+
+// cos/sin of t * theta_j.
+__device__ __forceinline__ void rot_cs(long long t, float th_hi, float th_lo,
+                                       float &c, float &s) {
+  sincosf(rot_angle(t, th_hi, th_lo), &s, &c);
 }
 
 // ---------------------------------------------------------------- memory
