@@ -420,6 +420,8 @@ def run_ours(args):
             extra["msr_layer"] = bench_msr(args, R, dev, stream, tflops, world, max_over_ranks)
         if "backward" in want:
             extra["backward"] = bench_backward(args, R, dev, tflops, hbm, world, max_over_ranks)
+        if "parallel" in want:
+            extra["parallel"] = bench_parallel(args, R, dev, tflops, world, max_over_ranks)
         if "retnet_block" in want:
             extra["retnet_block"] = bench_block(args, R, dev, tflops, world, max_over_ranks)
 
@@ -443,7 +445,7 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
-EXTRAS = ("decode", "decode_stack", "msr_layer", "backward", "retnet_block")
+EXTRAS = ("decode", "decode_stack", "msr_layer", "backward", "retnet_block", "parallel")
 
 
 def bench_decode(args, R, dev, stream, hbm, world, max_over_ranks):
@@ -653,6 +655,69 @@ def bench_block(args, R, dev, tflops, world, max_over_ranks):
             "frac_bf16_peak_if_all_gemm": gemm_flops / (ms * 1e-3) / 1e12 / tflops,
             "config": {"B": B, "N": Nm, "d_model": dm, "H": Hm, "d_k": dk, "d_v": dv,
                        "d_ffn": dff}}
+
+
+def bench_parallel(args, R, dev, tflops, world, max_over_ranks):
+    """The parallel form (Q K^T (.) D) V on the tensor cores at the chunkwise
+    training shape, B=4 H=8 N=2048 d_k=128 d_v=256, bf16 in and out, all
+    normalisations and GroupNorm.  Its work grows as N^2: the causal half of
+    the score matrix and of its product with V."""
+    import torch
+    from linear_recurrent_sequence_gb300 import synth
+    B, Hp, Np, dk, dv = 4, 8, 2048, 128, 256
+    gam = synth.head_gammas(Hp)
+    q = gen_bf16((B, Hp, Np, dk), 5001, dev)
+    k = gen_bf16((B, Hp, Np, dk), 5002, dev)
+    v = gen_bf16((B, Hp, Np, dv), 5003, dev)
+    o = torch.empty_like(v)
+    d, _g = R.make_desc(q, k, v, o, gam, norm_flags=R.NORM_ALL)
+    ws = R.new_workspace(R.workspace_size(d), dev)
+
+    def f():
+        R.parallel_fwd(q, k, v, gam, norm_flags=R.NORM_ALL, out=o, workspace=ws)
+    f()
+    f()
+    torch.cuda.synchronize()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        f()
+    torch.cuda.current_stream().wait_stream(side)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        f()
+    graph.replay()
+    torch.cuda.synchronize()
+    reps = 20
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        graph.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    ms = max_over_ranks(e0.elapsed_time(e1)) / reps
+    del graph
+    R.lib.retention_kernel_timer_reset()
+    R.lib.retention_kernel_timer_enable(1)
+    for _ in range(3):
+        f()
+    torch.cuda.synchronize()
+    R.lib.retention_kernel_timer_enable(0)
+    kt = {name: ms_k / max(n, 1) for name, (ms_k, n, t) in R.kernel_times().items()}
+    # Causal scores and their products with V: 2 (d_k + d_v) flops per pair.
+    pairs = B * Hp * Np * (Np + 1) / 2
+    fl = pairs * 2 * (dk + dv)
+    k_ms = kt.get("parallel_tc", ms)
+    del q, k, v, o, ws
+    torch.cuda.empty_cache()
+    return {"tokens_per_s": world * B * Np / (ms * 1e-3), "ms": ms,
+            "timing": "CUDA graph of one call, 20 replays", "kernel_ms_per_launch": kt,
+            "config": {"B": B, "H": Hp, "N": Np, "d_k": dk, "d_v": dv},
+            "roofline": {"bound": "tensor", "kernel": "parallel_tc",
+                         "achieved": fl / (k_ms * 1e-3) / 1e12, "peak": tflops,
+                         "unit": "TFLOP/s", "frac": fl / (k_ms * 1e-3) / 1e12 / tflops,
+                         "path_frac": fl / (ms * 1e-3) / 1e12 / tflops,
+                         "note": "causal-half flops; of measured bf16 burst peak"}}
 
 
 def flops_bwd_per_token_head(C):

@@ -121,6 +121,26 @@ SimtWs simt_ws(const ret_desc *d) {
   return w;
 }
 
+// Workspace of the parallel form on the tensor cores: status | Q' | K'
+// (fp16) | per-chunk records | raw rows (fp32) | row factors.
+struct ParTcWs {
+  size_t qp, kp, meta, oraw, f, total;
+};
+
+ParTcWs par_tc_ws(const ret_desc *d) {
+  ParTcWs w;
+  const size_t BH = (size_t)d->B * d->H, rows = BH * d->N;
+  const size_t nch = ((size_t)d->N + 63) / 64;
+  size_t off = kStatusBytes;
+  w.qp = off; off = align256(off + rows * d->d_k * 2);
+  w.kp = off; off = align256(off + rows * d->d_k * 2);
+  w.meta = off; off = align256(off + BH * nch * sizeof(ChunkMeta));
+  w.oraw = off; off = align256(off + rows * d->d_v * sizeof(float));
+  w.f = off; off = align256(off + rows * sizeof(float));
+  w.total = off;
+  return w;
+}
+
 // Workspace of the backward: status | Q' | K' | dQ' | dK' (fp32 rows).
 struct BwdWs {
   size_t qr, kr, dq, dk, total;
@@ -618,8 +638,8 @@ void retention_desc_init(ret_desc *d, int B, int H, int N, int d_k, int d_v,
 size_t retention_workspace_size(const ret_desc *d) {
   if (!desc_ok(d)) return 0;
   const ret_desc dt = tc_desc(d);
-  const size_t a = simt_ws(d).total, b = tc_ws(&dt).total;
-  return a > b ? a : b;
+  const size_t a = simt_ws(d).total, b = tc_ws(&dt).total, c = par_tc_ws(d).total;
+  return std::max(a, std::max(b, c));
 }
 
 ret_status retention_rotate(const ret_desc *d, const void *x, const int64_t sx[3], int dim,
@@ -650,12 +670,29 @@ ret_status retention_parallel_fwd(const ret_desc *d, const void *q, const void *
   const bool empty = (long long)d->B * d->H * d->N == 0;
   if (!empty && (!q || !k || !v || !o)) return RET_EINVAL;
   const SimtWs w = simt_ws(d);
-  ret_status rs = check_ws(ws, ws_bytes, w.total);
+  ret_status rs = check_ws(ws, ws_bytes, std::max(w.total, par_tc_ws(d).total));
   if (rs != RET_OK) return rs;
   if (empty) return RET_OK;
   cudaStream_t st = (cudaStream_t)stream;
   KParams p;
   make_params(d, ws, p);
+  // Tensor cores for bf16 inputs in the chunk path's operand range (its
+  // prologue writes the 64-token fp16 operands); CUDA cores otherwise.
+  ret_desc d64 = *d;
+  d64.chunk = 64;
+  KParams pt;
+  make_params(&d64, ws, pt);
+  if (pt.dk % 64 == 0 && chunk_tc_supported(pt, v, pt.sv)) {
+    const ParTcWs pw = par_tc_ws(d);
+    __half *Qp = at<__half>(ws, pw.qp), *Kp = at<__half>(ws, pw.kp);
+    ChunkMeta *meta = at<ChunkMeta>(ws, pw.meta);
+    float *Oraw = at<float>(ws, pw.oraw), *F = at<float>(ws, pw.f);
+    RET_CUDA(RET_TIMED_LAUNCH(kKRotate, st, launch_rotate_qk(pt, q, k, Qp, Kp, meta, nullptr, st)));
+    bool fused = false;
+    RET_CUDA(RET_TIMED_LAUNCH(kKParallelTc, st, launch_parallel_tc(pt, Qp, Kp, v, meta, Oraw, F, o, &fused, st)));
+    if (!fused) RET_CUDA(RET_TIMED_LAUNCH(kKGroupNorm, st, launch_groupnorm(pt, Oraw, F, o, st)));
+    return RET_OK;
+  }
   float *Qr = at<float>(ws, w.qr), *Kr = at<float>(ws, w.kr);
   float *Oraw = at<float>(ws, w.oraw), *F = at<float>(ws, w.f);
   RET_CUDA(RET_TIMED_LAUNCH(kKRotate, st, launch_rotate(p, q, p.sq, d->d_k, Qr, 0, nullptr, kScaleNone, st)));

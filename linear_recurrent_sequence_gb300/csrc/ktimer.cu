@@ -17,7 +17,7 @@ const char *kNames[kKernelCount] = {
     "gemm_simt", "chunk_tc", "gemm_tc", "state_pass", "swish_gate",
     "bwd_rows", "bwd_values", "unrotate",
     "layernorm", "residual_add", "gelu", "gemm_skinny", "skinny_reduce",
-    "state_combine", "state_simt", "bwd_prep", "bwd_finish"};
+    "state_combine", "state_simt", "bwd_prep", "bwd_finish", "parallel_tc"};
 
 struct Slot {
   std::vector<cudaEvent_t> start, stop;

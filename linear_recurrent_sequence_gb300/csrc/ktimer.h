@@ -30,6 +30,7 @@ enum KernelId {
   kKStateSimt,
   kKBwdPrep,
   kKBwdFinish,
+  kKParallelTc,
   kKernelCount
 };
 

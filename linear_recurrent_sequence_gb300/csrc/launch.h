@@ -140,6 +140,15 @@ cudaError_t launch_bwd_values(const KParams &p, const float *Qr, const float *Kr
 cudaError_t launch_unrotate(const KParams &p, const float *x, const long long s[3], void *out,
                             int out_bf16, cudaStream_t st);
 
+// parallel_tc.cu: the parallel form on the tensor cores.  Qp, Kp and meta
+// from launch_rotate_qk (64-token chunks).  d_v <= 256 (one CTA per row):
+// writes o itself (*fused = true).  Wider: writes the raw rows Oraw [B*H][N]
+// [d_v] and the row factors F [B*H][N] that launch_groupnorm turns into o.
+// d_k a multiple of 64 up to 256, d_v a multiple of 128 up to 1024.
+cudaError_t launch_parallel_tc(const KParams &p, const __half *Qp, const __half *Kp, const void *v,
+                               const ChunkMeta *meta, float *Oraw, float *F, void *o,
+                               bool *fused, cudaStream_t st);
+
 // backward_tc.cu: operands of the tensor-core backward's forward runs.
 // A prep job reads rows of src (strides s, bf16 or fp32, row width d, a
 // multiple of 8), optionally rotates them (+t theta) and scales them by the
