@@ -16,16 +16,21 @@
 //     the block is updated in registers, written back, and its share of q.S
 //     accumulated;
 //   * partial outputs are pushed into the owning CTA's shared memory
-//     (distributed shared memory stores, no remote loads) and summed there
-//     in a fixed order after one cluster barrier: deterministic, no atomics;
+//     (asynchronous distributed shared memory stores that count their bytes
+//     on the owner's mbarrier; no remote loads) and summed there in a fixed
+//     order once the owner has seen all the bytes it expects: deterministic,
+//     no atomics, and no cluster-wide barrier, whose release half would wait
+//     for this step's state stores to drain (with the state in L2 and more
+//     CTAs than SMs, plain stores and cluster barriers measured faster);
 //   * GroupNorm: each CTA reduces its own columns to a (mean, M2) pair, the
-//     pairs are pushed to every CTA of the cluster and merged there (Chan's
-//     pairwise update), which needs one more cluster barrier.  After it no
-//     CTA touches another's shared memory, so none has to wait at exit.
+//     pairs are pushed to every CTA of the cluster the same way and merged
+//     there (Chan's pairwise update).  Every CTA waits for all the bytes
+//     addressed to it, so none leaves while a peer may still write to it.
 #include <cooperative_groups.h>
 
 #include "common.cuh"
 #include "launch.h"
+#include "tc.cuh"
 
 namespace cg = cooperative_groups;
 
@@ -54,10 +59,21 @@ __device__ __forceinline__ void cluster_arrive_relaxed() {
 __device__ __forceinline__ void cluster_wait() {
   asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
 }
+
+// Bounded wait (acquire at cluster scope) for phase 0 of an exchange
+// barrier; each try suspends the thread for a while, so 2^20 tries are far
+// beyond any legitimate wait.  A wait that runs out records the timeout
+// and gives up.
+__device__ __noinline__ void xwait(uint64_t *bar, unsigned *status) {
+  for (unsigned i = 0; i < (1u << 20); ++i)
+    if (tc::mbar_try_wait_cluster(bar, 0)) return;
+  report(status, kDevTimeout);
+}
 }  // namespace
 
-// RB = rows of S a thread holds in registers at once.
-template <int RB>
+// RB = rows of S a thread holds in registers at once.  kAsyncX: the
+// exchanges count their bytes on mbarriers (else: cluster barriers).
+template <int RB, bool kAsyncX>
 __global__ void __launch_bounds__(NT)
 recurrent_step_kernel(KParams p, int KS, const void *__restrict__ q,
                       const void *__restrict__ k, const void *__restrict__ v,
@@ -65,7 +81,8 @@ recurrent_step_kernel(KParams p, int KS, const void *__restrict__ q,
   extern __shared__ __align__(16) float sm[];
   __shared__ float wsum[NT / 32];
   __shared__ float qz_in[KSMAX];     // partial q.z pushed by each CTA
-  __shared__ float2 st_in[KSMAX];    // (mean, M2) of each CTA's columns
+  __shared__ __align__(8) float2 st_in[KSMAX];  // (mean, M2) of each CTA's columns
+  __shared__ __align__(8) uint64_t xbar[2];  // bytes of [0] partials and q.z, [1] statistics
   cg::cluster_group cluster = cg::this_cluster();
   const int rank = (int)cluster.block_rank();
   const int bh = blockIdx.x / KS;
@@ -84,8 +101,20 @@ recurrent_step_kernel(KParams p, int KS, const void *__restrict__ q,
     for (int u = 0; u < RB; ++u)
       if (u < R) s[u] = Srow0[(long long)u * nvec + tid];
   }
+  // The exchange barriers, each expecting the bytes its CTA will receive:
+  // from every CTA of the cluster, its partial q.z and q.S for this CTA's
+  // columns, and (GroupNorm) its column statistics.
+  const bool gn = p.gn_eps >= 0.f;
+  if (kAsyncX && tid == 0) {
+    tc::mbar_init(&xbar[0], 1);
+    tc::mbar_init(&xbar[1], 1);
+    tc::fence_mbar_init();
+    tc::mbar_arrive_expect_tx(&xbar[0], (uint32_t)(KS * (span + 1) * 4));
+    if (gn) tc::mbar_arrive_expect_tx(&xbar[1], (uint32_t)(KS * 8));
+  }
   // Peers' shared memory may be written only once every CTA of the
-  // cluster runs: arrive now, wait just before the first push.
+  // cluster runs (and has set up its barriers): arrive now, wait just
+  // before the first push.
   cluster_arrive_relaxed();
 
   const float g = p.gam[h];
@@ -130,7 +159,12 @@ recurrent_step_kernel(KParams p, int KS, const void *__restrict__ q,
       }
 #pragma unroll
     for (int o2 = 16; o2 > 0; o2 >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o2);
-    if (tid < KS) cluster.map_shared_rank(qz_in, tid)[rank] = part;
+    if (tid < KS) {
+      if (kAsyncX)
+        tc::st_async_f32(&qz_in[rank], &xbar[0], (uint32_t)tid, part);
+      else
+        cluster.map_shared_rank(qz_in, tid)[rank] = part;
+    }
   }
 
   // Rows: S <- gamma S + k_a v ; acc += q_a S.  The first block is already
@@ -162,10 +196,16 @@ recurrent_step_kernel(KParams p, int KS, const void *__restrict__ q,
     }
     // Columns 4c..4c+3 belong to CTA e/span (span is a multiple of 4).
     const int e = 4 * c, dst = e / span;
-    float *box = cluster.map_shared_rank(inbox, dst);
-    *reinterpret_cast<float4 *>(box + rank * span + (e - dst * span)) = acc;
+    if (kAsyncX)
+      tc::st_async_v4(inbox + rank * span + (e - dst * span), &xbar[0], (uint32_t)dst, acc);
+    else
+      *reinterpret_cast<float4 *>(cluster.map_shared_rank(inbox, dst) + rank * span +
+                                  (e - dst * span)) = acc;
   }
-  cluster.sync();  // release the pushes above, acquire the peers'
+  if (kAsyncX)
+    xwait(&xbar[0], p.status);
+  else
+    cluster.sync();  // release the pushes above, acquire the peers'
 
   // Fixed-order sums of the KS partials for this CTA's columns
   // e0 + tid + NT*i (span = dv/KS <= 1024 columns, so i < 8).
@@ -197,8 +237,15 @@ recurrent_step_kernel(KParams p, int KS, const void *__restrict__ q,
     for (int i = 0; i < 8; ++i)
       if (tid + NT * i < span) lm2 = fmaf(x[i] - mloc, x[i] - mloc, lm2);
     const float m2loc = block_sum(lm2, wsum, tid);
-    if (tid < KS) cluster.map_shared_rank(st_in, tid)[rank] = make_float2(mloc, m2loc);
-    cluster.sync();
+    if (kAsyncX) {
+      if (tid < KS)
+        tc::st_async_v2(reinterpret_cast<float *>(&st_in[rank]), &xbar[1], (uint32_t)tid, mloc,
+                        m2loc);
+      xwait(&xbar[1], p.status);
+    } else {
+      if (tid < KS) cluster.map_shared_rank(st_in, tid)[rank] = make_float2(mloc, m2loc);
+      cluster.sync();
+    }
     float msum = 0.f;
     for (int r = 0; r < KS; ++r) msum += st_in[r].x;
     mu = msum / KS;
@@ -250,9 +297,17 @@ cudaError_t launch_recurrent_step(const KParams &p, const void *q, const void *k
   if (cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
     sms = 0;
+  //
+  // Exchange: counted asynchronous pushes except where the state fits in
+  // L2 with more CTAs than SMs (measured at B=1 / 8 / 32 / 128: 7.30 / 19.7
+  // / 85.6 / 316.7 us with them, 7.44 / 16.9 / 90 / 329 with cluster
+  // barriers, whose release half waits for the state stores to drain).
   if ((long long)p.B * p.H * KS <= sms)
-    return cudaLaunchKernelEx(&cfg, recurrent_step_kernel<32>, p, KS, q, k, v, S, z, o);
-  return cudaLaunchKernelEx(&cfg, recurrent_step_kernel<8>, p, KS, q, k, v, S, z, o);
+    return cudaLaunchKernelEx(&cfg, recurrent_step_kernel<32, true>, p, KS, q, k, v, S, z, o);
+  const double state_bytes = (double)p.B * p.H * p.dk * p.dv * 4.0;
+  if (state_bytes <= 96e6)
+    return cudaLaunchKernelEx(&cfg, recurrent_step_kernel<8, false>, p, KS, q, k, v, S, z, o);
+  return cudaLaunchKernelEx(&cfg, recurrent_step_kernel<8, true>, p, KS, q, k, v, S, z, o);
 }
 
 }  // namespace ret

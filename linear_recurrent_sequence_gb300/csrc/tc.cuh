@@ -98,6 +98,28 @@ __device__ __forceinline__ void st_async_v2(const float *local, uint64_t *bar, u
       : "memory");
 }
 
+// The same for one float (b32) and four floats (v4, 16-byte aligned).
+__device__ __forceinline__ void st_async_f32(const float *local, uint64_t *bar, uint32_t rank,
+                                             float a) {
+  uint32_t ra, rb;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(smem_u32(local)), "r"(rank));
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(rb) : "r"(smem_u32(bar)), "r"(rank));
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.f32 [%0], %1, [%2];" ::"r"(ra),
+               "f"(a), "r"(rb)
+               : "memory");
+}
+
+__device__ __forceinline__ void st_async_v4(const float *local, uint64_t *bar, uint32_t rank,
+                                            float4 v) {
+  uint32_t ra, rb;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(smem_u32(local)), "r"(rank));
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(rb) : "r"(smem_u32(bar)), "r"(rank));
+  asm volatile(
+      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(ra),
+      "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w), "r"(rb)
+      : "memory");
+}
+
 // Wait with acquire at cluster scope: the phase completed by st_async_v2's
 // transaction bytes from other CTAs of the cluster.
 __device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t *bar, uint32_t parity) {
