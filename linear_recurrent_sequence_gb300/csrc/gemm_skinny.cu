@@ -9,29 +9,52 @@
 //     each CTA keeps its K-slice of A in shared memory (fp32, MB rows) and
 //     writes an fp32 partial tile; a second kernel adds the partials in
 //     slice order (deterministic) and rounds to bf16;
-//   - eight rows of B per lane are loaded before they are used, to keep
-//     enough bytes in flight.
+//   - each thread keeps D - 1 rows of its columns of B in flight with
+//     asynchronous copies into its own slots of a shared-memory ring (no
+//     registers held by loads in flight; each thread reads back only what
+//     it copied, so its own copy-group waits order everything).
 #include "common.cuh"
 #include "launch.h"
+#include "tc.cuh"
 
 namespace ret {
 
 namespace {
 constexpr int kSkWarps = 8;
+constexpr int kSkThreads = kSkWarps * 32;
 constexpr int kSkCols = 256;                  // columns per warp (32 lanes x 8)
 constexpr int kSkCtaCols = kSkWarps * kSkCols;  // 2048
-constexpr int kSkUnroll = 8;                  // rows of B in flight per lane
 constexpr int kSkMaxSplit = 608;
 constexpr int kSkMaxRowsPerSlice = 512;       // K rows per CTA (A slice in shared memory)
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst),
+               "l"(reinterpret_cast<uint64_t>(src))
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
 }  // namespace
+
+// Ring depth (rows of B per thread, D - 1 of them in flight): about 190 KB
+// of copies in flight per SM at two CTAs per SM.
+template <int MB>
+__host__ __device__ constexpr int sk_depth() { return MB <= 4 ? 24 : 16; }
 
 // grid: x = column block of 2048 (over every matrix of the job), y = K
 // slice.  P: [split][M][Ntot] fp32, matrix i's columns at col0[i].
 template <int MB>
-__global__ void __launch_bounds__(kSkWarps * 32)
+__global__ void __launch_bounds__(kSkThreads)
 gemm_skinny_kernel(const __nv_bfloat16 *__restrict__ A, const SkinnyJob job,
                    float *__restrict__ P, int M, int K, int rows_per_slice) {
+  constexpr int D = sk_depth<MB>();
   __shared__ float As[kSkMaxRowsPerSlice][MB];
+  extern __shared__ __align__(16) uint4 ring[];  // [D][kSkThreads]
   const int k0 = blockIdx.y * rows_per_slice;
   const int kn = min(rows_per_slice, K - k0);
   for (int e = threadIdx.x; e < kn * MB; e += blockDim.x) {
@@ -45,43 +68,52 @@ gemm_skinny_kernel(const __nv_bfloat16 *__restrict__ A, const SkinnyJob job,
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n0 = ((int)blockIdx.x - job.blk0[mat]) * kSkCtaCols + warp * kSkCols + lane * 8;
   if (n0 >= N) return;  // N % 8 == 0: a lane's eight columns are all in or all out
-  float acc[MB][8];
+  float2 acc[MB][4];
 #pragma unroll
   for (int m = 0; m < MB; ++m)
 #pragma unroll
-    for (int c = 0; c < 8; ++c) acc[m][c] = 0.f;
-  const __nv_bfloat16 *bcol = job.B[mat] + (long long)k0 * N + n0;
-  for (int r0 = 0; r0 < kn; r0 += kSkUnroll) {
-    uint4 w[kSkUnroll];
+    for (int c = 0; c < 4; ++c) acc[m][c] = make_float2(0.f, 0.f);
+  const __nv_bfloat16 *brow = job.B[mat] + (long long)k0 * N + n0;
+  const uint32_t slot0 = tc::smem_u32(ring + threadIdx.x), sstride = kSkThreads * 16u;
+  // Rows 0 .. D-2 in flight, one copy group per row.
+  const __nv_bfloat16 *bnext = brow;
+#pragma unroll 1
+  for (int r = 0; r < D - 1; ++r, bnext += N) {
+    if (r < kn) cp_async16(slot0 + (uint32_t)r * sstride, bnext);
+    cp_async_commit();
+  }
+  int sl = 0, sn = D - 1;  // ring slots of rows r and r + D - 1
+#pragma unroll 1
+  for (int r = 0; r < kn; ++r, bnext += N) {
+    // Refill the slot of row r - 1 (read in the previous iteration) with
+    // row r + D - 1, then wait for row r (at most D - 1 groups pending).
+    if (r + D - 1 < kn) cp_async16(slot0 + (uint32_t)sn * sstride, bnext);
+    cp_async_commit();
+    cp_async_wait<D - 1>();
+    const uint4 w = ring[sl * kSkThreads + threadIdx.x];
+    sl = sl + 1 == D ? 0 : sl + 1;
+    sn = sn + 1 == D ? 0 : sn + 1;
+    const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
+    float2 b2[4];
 #pragma unroll
-    for (int u = 0; u < kSkUnroll; ++u)
-      w[u] = r0 + u < kn ? *reinterpret_cast<const uint4 *>(bcol + (long long)(r0 + u) * N)
-                         : make_uint4(0u, 0u, 0u, 0u);
+    for (int t = 0; t < 4; ++t)
+      b2[t] = make_float2(__uint_as_float(wv[t] << 16), __uint_as_float(wv[t] & 0xffff0000u));
 #pragma unroll
-    for (int u = 0; u < kSkUnroll; ++u) {
-      if (r0 + u >= kn) break;
-      const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&w[u]);
-      float b[8];
+    for (int m = 0; m < MB; ++m) {
+      const float a = As[r][m];
+      const float2 a2 = make_float2(a, a);
 #pragma unroll
-      for (int t = 0; t < 4; ++t) {
-        b[2 * t] = __low2float(h[t]);
-        b[2 * t + 1] = __high2float(h[t]);
-      }
-#pragma unroll
-      for (int m = 0; m < MB; ++m) {
-        const float a = As[r0 + u][m];
-#pragma unroll
-        for (int c = 0; c < 8; ++c) acc[m][c] = fmaf(a, b[c], acc[m][c]);
-      }
+      for (int t = 0; t < 4; ++t) acc[m][t] = tc::fma2(a2, b2[t], acc[m][t]);
     }
   }
+  cp_async_wait<0>();
   float *pt = P + (long long)blockIdx.y * M * job.Ntot + job.col0[mat] + n0;
 #pragma unroll
   for (int m = 0; m < MB; ++m) {
     if (m >= M) break;
     float4 *dst = reinterpret_cast<float4 *>(pt + (long long)m * job.Ntot);
-    dst[0] = make_float4(acc[m][0], acc[m][1], acc[m][2], acc[m][3]);
-    dst[1] = make_float4(acc[m][4], acc[m][5], acc[m][6], acc[m][7]);
+    dst[0] = make_float4(acc[m][0].x, acc[m][0].y, acc[m][1].x, acc[m][1].y);
+    dst[1] = make_float4(acc[m][2].x, acc[m][2].y, acc[m][3].x, acc[m][3].y);
   }
 }
 
@@ -178,9 +210,9 @@ bool gemm_skinny_supported(const void *A, const void *Bm, const void *C, int M, 
          reinterpret_cast<uintptr_t>(Bm) % 16 == 0 && A && C;
 }
 
-// Slices of K: about four CTAs per SM of a 152-SM GB300 (each CTA keeps
-// 32 KB of weight rows in flight, and the register budget allows four), at
-// least kSkUnroll rows and at most kSkMaxRowsPerSlice rows per slice, and
+// Slices of K: about two CTAs per SM of a 152-SM GB300 (the shared-memory
+// ring of each CTA holds its copies in flight), at least eight rows and at
+// most kSkMaxRowsPerSlice rows per slice, and
 // fp32 partials (split * M * N * 4 bytes) of at most 16 MB, which stay in
 // L2 between the two kernels.  The plan depends on the shape alone (not on
 // the device that happens to be current), so a workspace sized for a shape
@@ -189,12 +221,12 @@ constexpr int kSkPlanSms = 152;
 constexpr long long kSkMaxPartialBytes = 16LL << 20;
 static void skinny_plan(int M, int N, int K, int &split, int &rows) {
   const int colblocks = (N + kSkCtaCols - 1) / kSkCtaCols;
-  int s = (4 * kSkPlanSms + colblocks - 1) / colblocks;
+  int s = (2 * kSkPlanSms + colblocks - 1) / colblocks;
   s = s < kSkMaxSplit ? s : kSkMaxSplit;
   const long long per_slice = 4LL * (M > 0 ? M : 1) * N;
   const long long cap = kSkMaxPartialBytes / (per_slice > 0 ? per_slice : 1);
   s = s < cap ? s : (int)cap;
-  const int rmin = (K + kSkUnroll - 1) / kSkUnroll;  // slices of at least kSkUnroll rows
+  const int rmin = (K + 7) / 8;  // slices of at least eight rows
   s = s < rmin ? s : rmin;
   if (s < 1) s = 1;
   rows = (K + s - 1) / s;
@@ -231,24 +263,28 @@ bool skinny_job_init(SkinnyJob &job, int count, const void *const *Bs, void *con
   return (epi != kSkEpResidual || (count == 1 && R));
 }
 
+template <int MB>
+static cudaError_t launch_skinny_mb(dim3 grid, const __nv_bfloat16 *a, const SkinnyJob &job,
+                                    float *partial, int M, int K, int rows, cudaStream_t st) {
+  const int smem = sk_depth<MB>() * kSkThreads * 16;
+  cudaError_t e = cudaFuncSetAttribute(gemm_skinny_kernel<MB>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  gemm_skinny_kernel<MB><<<grid, kSkThreads, smem, st>>>(a, job, partial, M, K, rows);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_gemm_skinny_job(const void *A, const SkinnyJob &job, int M, int K,
                                    float *partial, cudaStream_t st) {
   int split = 1, rows = 1;
   skinny_plan(M, job.Ntot, K, split, rows);
   dim3 grid(job.blk0[job.count], split);
   const auto *a = reinterpret_cast<const __nv_bfloat16 *>(A);
-  const int threads = kSkWarps * 32;
-  if (M <= 1)
-    gemm_skinny_kernel<1><<<grid, threads, 0, st>>>(a, job, partial, M, K, rows);
-  else if (M <= 2)
-    gemm_skinny_kernel<2><<<grid, threads, 0, st>>>(a, job, partial, M, K, rows);
-  else if (M <= 4)
-    gemm_skinny_kernel<4><<<grid, threads, 0, st>>>(a, job, partial, M, K, rows);
-  else if (M <= 8)
-    gemm_skinny_kernel<8><<<grid, threads, 0, st>>>(a, job, partial, M, K, rows);
-  else
-    gemm_skinny_kernel<16><<<grid, threads, 0, st>>>(a, job, partial, M, K, rows);
-  return cudaGetLastError();
+  if (M <= 1) return launch_skinny_mb<1>(grid, a, job, partial, M, K, rows, st);
+  if (M <= 2) return launch_skinny_mb<2>(grid, a, job, partial, M, K, rows, st);
+  if (M <= 4) return launch_skinny_mb<4>(grid, a, job, partial, M, K, rows, st);
+  if (M <= 8) return launch_skinny_mb<8>(grid, a, job, partial, M, K, rows, st);
+  return launch_skinny_mb<16>(grid, a, job, partial, M, K, rows, st);
 }
 
 cudaError_t launch_skinny_reduce_job(const float *partial, const SkinnyJob &job, int M, int K,
