@@ -1194,8 +1194,8 @@ ret_status retnet_decode_step(const retnet_stack_desc *d, const retnet_layer_wei
       RET_CUDA(gemm_dec(Xn, L.WV, V, B, HV, dm, part, status, st));
       RET_CUDA(gemm_dec(Xn, L.WG, G, B, HV, dm, part, status, st));
     }
-    RET_CUDA(RET_TIMED_LAUNCH(kKRecurrent, st, launch_recurrent_step(p, Q, K, V, S[l], rsum ? z[l] : nullptr, Y, st)));
-    RET_CUDA(RET_TIMED_LAUNCH(kKGate, st, launch_swish_gate(Y, G, (long long)B * HV, st)));
+    // The retention step with the gate applied to its output.
+    RET_CUDA(RET_TIMED_LAUNCH(kKRecurrent, st, launch_recurrent_step(p, Q, K, V, S[l], rsum ? z[l] : nullptr, Y, st, G)));
     if (fused) {
       void *c = Mo;
       RET_CUDA(gemm_dec_job(Y, 1, &L.WO, &c, &dm, B, HV, kSkEpResidual, X, part, status, st));

@@ -57,31 +57,36 @@ gemm_skinny_kernel(const __nv_bfloat16 *__restrict__ A, const SkinnyJob job,
   extern __shared__ __align__(16) uint4 ring[];  // [D][kSkThreads]
   const int k0 = blockIdx.y * rows_per_slice;
   const int kn = min(rows_per_slice, K - k0);
-  for (int e = threadIdx.x; e < kn * MB; e += blockDim.x) {
-    const int r = e / MB, m = e % MB;
-    As[r][m] = m < M ? __bfloat162float(A[(long long)m * K + k0 + r]) : 0.f;
-  }
-  __syncthreads();
   int mat = 0;
   while (mat + 1 < job.count && (int)blockIdx.x >= job.blk0[mat + 1]) ++mat;
   const int N = job.N[mat];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n0 = ((int)blockIdx.x - job.blk0[mat]) * kSkCtaCols + warp * kSkCols + lane * 8;
-  if (n0 >= N) return;  // N % 8 == 0: a lane's eight columns are all in or all out
+  const bool live = n0 < N;  // N % 8 == 0: a lane's eight columns are all in or all out
+  const __nv_bfloat16 *brow = job.B[mat] + (long long)k0 * N + n0;
+  const uint32_t slot0 = tc::smem_u32(ring + threadIdx.x), sstride = kSkThreads * 16u;
+  // Rows 0 .. D-2 of B in flight first (one copy group per row): they do
+  // not depend on A, so staging A overlaps them.
+  const __nv_bfloat16 *bnext = brow;
+#pragma unroll 1
+  for (int r = 0; r < D - 1; ++r, bnext += N) {
+    if (live && r < kn) cp_async16(slot0 + (uint32_t)r * sstride, bnext);
+    cp_async_commit();
+  }
+  for (int e = threadIdx.x; e < kn * MB; e += blockDim.x) {
+    const int r = e / MB, m = e % MB;
+    As[r][m] = m < M ? __bfloat162float(A[(long long)m * K + k0 + r]) : 0.f;
+  }
+  __syncthreads();
+  if (!live) {
+    cp_async_wait<0>();
+    return;
+  }
   float2 acc[MB][4];
 #pragma unroll
   for (int m = 0; m < MB; ++m)
 #pragma unroll
     for (int c = 0; c < 4; ++c) acc[m][c] = make_float2(0.f, 0.f);
-  const __nv_bfloat16 *brow = job.B[mat] + (long long)k0 * N + n0;
-  const uint32_t slot0 = tc::smem_u32(ring + threadIdx.x), sstride = kSkThreads * 16u;
-  // Rows 0 .. D-2 in flight, one copy group per row.
-  const __nv_bfloat16 *bnext = brow;
-#pragma unroll 1
-  for (int r = 0; r < D - 1; ++r, bnext += N) {
-    if (r < kn) cp_async16(slot0 + (uint32_t)r * sstride, bnext);
-    cp_async_commit();
-  }
   int sl = 0, sn = D - 1;  // ring slots of rows r and r + D - 1
 #pragma unroll 1
   for (int r = 0; r < kn; ++r, bnext += N) {

@@ -94,10 +94,12 @@ cudaError_t launch_state_simt(const KParams &p, const float *Kr, const void *v,
                               const float *S_in, const float *z_in, float *S_out, float *z_out,
                               cudaStream_t st);
 
-// recurrent.cu: one decode step, state in place.
+// recurrent.cu: one decode step, state in place.  gate (optional, bf16
+// [B][H][d_v]): the output is multiplied by swish(gate) after its bf16
+// rounding, as the MSR layer's gate pass would.
 cudaError_t launch_recurrent_step(const KParams &p, const void *q, const void *k,
                                   const void *v, float *S, float *z, void *o,
-                                  cudaStream_t st);
+                                  cudaStream_t st, const void *gate = nullptr);
 
 // gemm_tc.cu: tensor-core C[M,N] = A[M,K] B[K,N] (bf16 row-major, fp32
 // accumulate); N % 256, K % 64 == 0 (any M >= 1) and 16-byte aligned pointers.

@@ -77,7 +77,8 @@ template <int RB, bool kAsyncX>
 __global__ void __launch_bounds__(NT)
 recurrent_step_kernel(KParams p, int KS, const void *__restrict__ q,
                       const void *__restrict__ k, const void *__restrict__ v,
-                      float *__restrict__ S, float *__restrict__ z, void *__restrict__ o) {
+                      float *__restrict__ S, float *__restrict__ z, void *__restrict__ o,
+                      const __nv_bfloat16 *__restrict__ gate) {
   extern __shared__ __align__(16) float sm[];
   __shared__ float wsum[NT / 32];
   __shared__ float qz_in[KSMAX];     // partial q.z pushed by each CTA
@@ -259,14 +260,25 @@ recurrent_step_kernel(KParams p, int KS, const void *__restrict__ q,
     inv = rsqrtf(m2 / dv + p.gn_eps);
   }
   const long long ob = b * p.so[0] + h * p.so[1] + e0;
+  // The MSR layer's gate, when given (bf16 [B][H][d_v]): the GroupNorm
+  // output rounded to bf16 as it would be stored, times swish(g) (fast
+  // exponential and divide, as the separate gate pass computes it).
+  const long long gb = ((long long)b * p.H + h) * dv + e0;
 #pragma unroll
   for (int i = 0; i < 8; ++i)
-    if (tid + NT * i < span) st_elem(o, ob + tid + NT * i, (x[i] - mu) * inv, p.out_bf16);
+    if (tid + NT * i < span) {
+      float y = (x[i] - mu) * inv;
+      if (gate) {
+        const float gi = __bfloat162float(gate[gb + tid + NT * i]);
+        y = __bfloat162float(__float2bfloat16_rn(y)) * __fdividef(gi, 1.f + __expf(-gi));
+      }
+      st_elem(o, ob + tid + NT * i, y, p.out_bf16);
+    }
 }
 
 cudaError_t launch_recurrent_step(const KParams &p, const void *q, const void *k,
                                   const void *v, float *S, float *z, void *o,
-                                  cudaStream_t st) {
+                                  cudaStream_t st, const void *gate) {
   if (p.B == 0 || p.H == 0) return cudaSuccess;
   // Cluster size: up to 8 CTAs per head, each keeping an even number of
   // rows and an equal share of the outputs, a multiple of 4 columns
@@ -302,12 +314,13 @@ cudaError_t launch_recurrent_step(const KParams &p, const void *q, const void *k
   // L2 with more CTAs than SMs (measured at B=1 / 8 / 32 / 128: 7.30 / 19.7
   // / 85.6 / 316.7 us with them, 7.44 / 16.9 / 90 / 329 with cluster
   // barriers, whose release half waits for the state stores to drain).
+  const __nv_bfloat16 *g = reinterpret_cast<const __nv_bfloat16 *>(gate);
   if ((long long)p.B * p.H * KS <= sms)
-    return cudaLaunchKernelEx(&cfg, recurrent_step_kernel<32, true>, p, KS, q, k, v, S, z, o);
+    return cudaLaunchKernelEx(&cfg, recurrent_step_kernel<32, true>, p, KS, q, k, v, S, z, o, g);
   const double state_bytes = (double)p.B * p.H * p.dk * p.dv * 4.0;
   if (state_bytes <= 96e6)
-    return cudaLaunchKernelEx(&cfg, recurrent_step_kernel<8, false>, p, KS, q, k, v, S, z, o);
-  return cudaLaunchKernelEx(&cfg, recurrent_step_kernel<8, true>, p, KS, q, k, v, S, z, o);
+    return cudaLaunchKernelEx(&cfg, recurrent_step_kernel<8, false>, p, KS, q, k, v, S, z, o, g);
+  return cudaLaunchKernelEx(&cfg, recurrent_step_kernel<8, true>, p, KS, q, k, v, S, z, o, g);
 }
 
 }  // namespace ret
