@@ -73,7 +73,13 @@ __device__ __noinline__ void xwait(uint64_t *bar, unsigned *status) {
 
 // RB = rows of S a thread holds in registers at once.  kAsyncX: the
 // exchanges count their bytes on mbarriers (else: cluster barriers).
-template <int RB, bool kAsyncX>
+// kFullRow (with kAsyncX): every CTA receives the partials of all d_v
+// columns and normalises the whole row itself, so the GroupNorm needs no
+// second exchange (a few microseconds less at small batches, where the
+// step is a chain of latencies).
+// kGate: the MSR gate is applied to the output (a separate instantiation,
+// so that the plain step keeps its register budget).
+template <int RB, bool kAsyncX, bool kFullRow, bool kGate>
 __global__ void __launch_bounds__(NT)
 recurrent_step_kernel(KParams p, int KS, const void *__restrict__ q,
                       const void *__restrict__ k, const void *__restrict__ v,
@@ -110,8 +116,8 @@ recurrent_step_kernel(KParams p, int KS, const void *__restrict__ q,
     tc::mbar_init(&xbar[0], 1);
     tc::mbar_init(&xbar[1], 1);
     tc::fence_mbar_init();
-    tc::mbar_arrive_expect_tx(&xbar[0], (uint32_t)(KS * (span + 1) * 4));
-    if (gn) tc::mbar_arrive_expect_tx(&xbar[1], (uint32_t)(KS * 8));
+    tc::mbar_arrive_expect_tx(&xbar[0], (uint32_t)(KS * ((kFullRow ? dv : span) + 1) * 4));
+    if (gn && !kFullRow) tc::mbar_arrive_expect_tx(&xbar[1], (uint32_t)(KS * 8));
   }
   // Peers' shared memory may be written only once every CTA of the
   // cluster runs (and has set up its barriers): arrive now, wait just
@@ -122,7 +128,7 @@ recurrent_step_kernel(KParams p, int KS, const void *__restrict__ q,
   float *qr = sm;             // [R]
   float *kr = qr + R;         // [R]
   float *vs = kr + R;         // [dv]
-  float *inbox = vs + dv;     // [KS][span]: partial q.S for this CTA's columns
+  float *inbox = vs + dv;     // [KS][span] (kFullRow: [KS][dv]): partial q.S
 
   // Rotated q, k rows of this CTA (positions: the token sits at pos0).
   const long long qb = b * p.sq[0] + h * p.sq[1];
@@ -197,7 +203,10 @@ recurrent_step_kernel(KParams p, int KS, const void *__restrict__ q,
     }
     // Columns 4c..4c+3 belong to CTA e/span (span is a multiple of 4).
     const int e = 4 * c, dst = e / span;
-    if (kAsyncX)
+    if (kFullRow) {
+      for (int r = 0; r < KS; ++r)
+        tc::st_async_v4(inbox + rank * dv + e, &xbar[0], (uint32_t)r, acc);
+    } else if (kAsyncX)
       tc::st_async_v4(inbox + rank * span + (e - dst * span), &xbar[0], (uint32_t)dst, acc);
     else
       *reinterpret_cast<float4 *>(cluster.map_shared_rank(inbox, dst) + rank * span +
@@ -215,6 +224,57 @@ recurrent_step_kernel(KParams p, int KS, const void *__restrict__ q,
   for (int r = 0; r < KS; ++r) qz += qz_in[r];
   const float sc = row_scale(p, h, p.pos0 + 1);
   const float f = sc * rsum_scale(p, sc * qz);
+  if (kFullRow) {
+    // The whole row: columns 4c..4c+3 for c = tid, tid + NT (d_v <= 1024).
+    float4 xs[2];
+    float lsum = 0.f;
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const int c = tid + NT * i;
+      xs[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (c < nvec) {
+        float4 a4 = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int r = 0; r < KS; ++r) {
+          const float4 t4 = *reinterpret_cast<const float4 *>(inbox + r * dv + 4 * c);
+          a4.x += t4.x; a4.y += t4.y; a4.z += t4.z; a4.w += t4.w;
+        }
+        xs[i] = make_float4(f * a4.x, f * a4.y, f * a4.z, f * a4.w);
+        lsum += (xs[i].x + xs[i].y) + (xs[i].z + xs[i].w);
+      }
+    }
+    float mu = 0.f, inv = 1.f;
+    if (gn) {
+      mu = block_sum(lsum, wsum, tid) / dv;
+      float lm2 = 0.f;
+#pragma unroll
+      for (int i = 0; i < 2; ++i)
+        if (tid + NT * i < nvec) {
+          lm2 = fmaf(xs[i].x - mu, xs[i].x - mu, lm2);
+          lm2 = fmaf(xs[i].y - mu, xs[i].y - mu, lm2);
+          lm2 = fmaf(xs[i].z - mu, xs[i].z - mu, lm2);
+          lm2 = fmaf(xs[i].w - mu, xs[i].w - mu, lm2);
+        }
+      inv = rsqrtf(block_sum(lm2, wsum, tid) / dv + p.gn_eps);
+    }
+    const long long ob = b * p.so[0] + h * p.so[1];
+    const long long gb = ((long long)b * p.H + h) * dv;
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const int c = tid + NT * i;
+      if (c >= nvec || 4 * c < e0 || 4 * c >= e0 + span) continue;
+      const float xv[4] = {xs[i].x, xs[i].y, xs[i].z, xs[i].w};
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        float y = (xv[u] - mu) * inv;
+        if (kGate) {
+          const float gi = __bfloat162float(gate[gb + 4 * c + u]);
+          y = __bfloat162float(__float2bfloat16_rn(y)) * __fdividef(gi, 1.f + __expf(-gi));
+        }
+        st_elem(o, ob + 4 * c + u, y, p.out_bf16);
+      }
+    }
+    return;
+  }
   float x[8];
   float lsum = 0.f;
 #pragma unroll
@@ -268,7 +328,7 @@ recurrent_step_kernel(KParams p, int KS, const void *__restrict__ q,
   for (int i = 0; i < 8; ++i)
     if (tid + NT * i < span) {
       float y = (x[i] - mu) * inv;
-      if (gate) {
+      if (kGate) {
         const float gi = __bfloat162float(gate[gb + tid + NT * i]);
         y = __bfloat162float(__float2bfloat16_rn(y)) * __fdividef(gi, 1.f + __expf(-gi));
       }
@@ -315,12 +375,18 @@ cudaError_t launch_recurrent_step(const KParams &p, const void *q, const void *k
   // / 85.6 / 316.7 us with them, 7.44 / 16.9 / 90 / 329 with cluster
   // barriers, whose release half waits for the state stores to drain).
   const __nv_bfloat16 *g = reinterpret_cast<const __nv_bfloat16 *>(gate);
-  if ((long long)p.B * p.H * KS <= sms)
-    return cudaLaunchKernelEx(&cfg, recurrent_step_kernel<32, true>, p, KS, q, k, v, S, z, o, g);
+  const bool gated = g != nullptr;
+  if ((long long)p.B * p.H * KS <= sms) {
+    cfg.dynamicSmemBytes = sizeof(float) * (2 * R + p.dv + (size_t)KS * p.dv);
+    return gated ? cudaLaunchKernelEx(&cfg, recurrent_step_kernel<32, true, true, true>, p, KS, q, k, v, S, z, o, g)
+                 : cudaLaunchKernelEx(&cfg, recurrent_step_kernel<32, true, true, false>, p, KS, q, k, v, S, z, o, g);
+  }
   const double state_bytes = (double)p.B * p.H * p.dk * p.dv * 4.0;
   if (state_bytes <= 96e6)
-    return cudaLaunchKernelEx(&cfg, recurrent_step_kernel<8, false>, p, KS, q, k, v, S, z, o, g);
-  return cudaLaunchKernelEx(&cfg, recurrent_step_kernel<8, true>, p, KS, q, k, v, S, z, o, g);
+    return gated ? cudaLaunchKernelEx(&cfg, recurrent_step_kernel<8, false, false, true>, p, KS, q, k, v, S, z, o, g)
+                 : cudaLaunchKernelEx(&cfg, recurrent_step_kernel<8, false, false, false>, p, KS, q, k, v, S, z, o, g);
+  return gated ? cudaLaunchKernelEx(&cfg, recurrent_step_kernel<8, true, false, true>, p, KS, q, k, v, S, z, o, g)
+               : cudaLaunchKernelEx(&cfg, recurrent_step_kernel<8, true, false, false>, p, KS, q, k, v, S, z, o, g);
 }
 
 }  // namespace ret
