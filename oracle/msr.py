@@ -10,9 +10,10 @@ piece: Gated Multi-Scale Retention"; m.sdkjxy.cn RetNet walkthrough,
 are numpy float64 matmuls (a library primitive); retention is the oracle's
 chunkwise form, whose equality with the parallel form the CPU tests pin.
 
-Parity unpinned beyond that: the pages print no worked MSR example, so the
-layer is checked for self-consistency only (the matmul steps against direct
-loops on small shapes, the retention step through the pinned forms).
+Pinned by a two-token example worked by hand from the definitions above
+(tests/golden/msr_two_tokens_hand.txt: projections, gate and output
+projection around the hand-worked retention example), with six planted
+mistakes that it catches, and by direct loops on a small shape.
 """
 from __future__ import annotations
 

@@ -243,6 +243,80 @@ def test_hand_derived_negative_row_sum():
             assert np.max(np.abs(got - exp)) < 1e-14, (name, chunk)
 
 
+_MSR_HAND = dict(
+    X=np.array([[[1.0, 0.0], [0.0, 1.0]]]),
+    WQ=np.array([[1.0, 0.0], [0.0, 1.0]]),
+    WK=np.array([[1.0, 0.0], [1.0, 1.0]]),
+    WV=np.array([[2.0, 1.0], [3.0, -1.0]]),
+    WG=np.array([[1.0, 2.0], [-1.0, 0.0]]),
+    WO=np.array([[1.0, -2.0], [3.0, 1.0]]),
+)
+
+
+def _msr_hand_pins(layer):
+    """The gated MSR layer on the two-token example worked by hand in
+    tests/golden/msr_two_tokens_hand.txt (GroupNorm off, no normalisations)."""
+    rows = _golden_rows("msr_two_tokens_hand.txt")
+    assert len(rows) == 2
+    m = _MSR_HAND
+    out = layer(m["X"], m["WQ"], m["WK"], m["WV"], m["WG"], m["WO"], H=1, dk=2, dv=2,
+                gamma=[0.5], chunk=1, norm_flags=0, gn_eps=-1.0)
+    for tok, expect in rows:
+        exp = np.array([eval(e, {"math": math}) for e in expect.split(";")])
+        assert np.max(np.abs(out[0, int(tok)] - exp)) < 1e-14, tok
+
+
+def test_msr_layer_hand_example():
+    from oracle.msr import msr_layer
+    _msr_hand_pins(msr_layer)
+
+
+def _msr_mutant(kind):
+    """The MSR layer with one plausible mistake planted (a copy of the
+    oracle's steps, changed in one place)."""
+    from oracle import msr as M
+
+    def layer(X, WQ, WK, WV, WG, WO, *, H, dk, dv, gamma, chunk, norm_flags, gn_eps):
+        B, N, _ = X.shape
+        Q, K, V, G = X @ WQ, X @ WK, X @ WV, X @ WG
+        if kind == "projections transposed":
+            Q, K = X @ WQ.T, X @ WK.T
+        if kind == "gate reads V":
+            G = V
+        q = Q.reshape(B, N, H, dk).transpose(0, 2, 1, 3)
+        k = K.reshape(B, N, H, dk).transpose(0, 2, 1, 3)
+        v = V.reshape(B, N, H, dv).transpose(0, 2, 1, 3)
+        if kind == "queries and keys swapped":
+            q, k = k, q
+        p = Problem(B, H, N, dk, dv, gamma, rotate=True, norm_flags=norm_flags, gn_eps=gn_eps)
+        o, _, _ = oracle.chunkwise(p, chunk, q, k, v)
+        Y = o.transpose(0, 2, 1, 3).reshape(B, N, H * dv)
+        gate = M.swish(G)
+        if kind == "sigmoid gate":
+            gate = 1.0 / (1.0 + np.exp(-G))
+        if kind == "gate after the output projection":
+            return (Y @ WO) * gate
+        if kind == "output projection transposed":
+            return (gate * Y) @ WO.T
+        return (gate * Y) @ WO
+    return layer
+
+
+MSR_MUTANTS = ["projections transposed", "gate reads V", "queries and keys swapped",
+               "sigmoid gate", "gate after the output projection", "output projection transposed"]
+
+
+@pytest.mark.parametrize("kind", MSR_MUTANTS)
+def test_msr_mutants_are_caught(kind):
+    with pytest.raises(AssertionError):
+        _msr_hand_pins(_msr_mutant(kind))
+
+
+def test_msr_mutant_harness_is_faithful():
+    """With no mistake planted the copy passes the same pins."""
+    _msr_hand_pins(_msr_mutant("none"))
+
+
 def test_hand_derived_groupnorm():
     for eps, xs, expect in _golden_rows("groupnorm_hand.txt"):
         x = np.array([float(t) for t in xs.split()])
