@@ -11,13 +11,17 @@ retnet_block) against what the mathematics fixes:
     connections alone); with W2 = 0 it is X + MSR(LN(X)), the pinned-by-parts
     MSR oracle; with W_O = 0 it is X + FFN(LN(X)) computed by direct loops.
 
-The pages print no worked block example: beyond these, the block's parity is
-pinned through its parts (m0nads.wordpress.com "A dubious successor to
-Transformer", "Overall architecture").
+  * a one-token block worked by hand from the definitions
+    (tests/golden/block_one_token_hand.txt), which four planted mistakes in
+    the block's composition fail (FFN on LN(X) instead of LN(Y), GELU after
+    W2, no second skip connection, the skips swapped for the LayerNorm
+    inputs).
 """
 import math
+import os
 
 import numpy as np
+import pytest
 
 from oracle.msr import gelu, layernorm, msr_layer, retnet_block
 
@@ -94,3 +98,65 @@ def test_block_reduces_to_its_parts():
             for o in range(d):
                 ref[b, n, o] = row[o] + sum(h[j] * W["W2"][j, o] for j in range(dff))
     assert np.max(np.abs(_block(X, F, ln, **KW) - ref)) < 1e-12
+
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+ONE = np.eye(2)
+
+
+def _hand_block_expect():
+    env = {"math": math}
+    out = {}
+    for line in open(os.path.join(GOLDEN, "block_one_token_hand.txt")):
+        line = line.strip()
+        if not line or line.startswith("#"):
+            continue
+        kind, name, expr = [c.strip() for c in line.split("|")]
+        val = eval(expr, env)
+        if kind == "let":
+            env[name] = val
+        else:
+            out[int(name)] = val
+    return np.array([out[0], out[1]])
+
+
+def _hand_block_pins(block):
+    X = np.array([[[1.0, -1.0]]])
+    u1, z1 = np.ones(2), np.zeros(2)
+    got = block(X, u1, z1, ONE, ONE, ONE, ONE, ONE, u1, z1, ONE, np.array([[1.0, 2.0], [0.0, 1.0]]),
+                H=1, dk=2, dv=2, gamma=[0.5], chunk=1, ln_eps=1e-5, norm_flags=0, gn_eps=-1.0)
+    assert np.max(np.abs(got[0, 0] - _hand_block_expect())) < 1e-14
+
+
+def test_block_hand_example():
+    _hand_block_pins(retnet_block)
+
+
+def _block_mutant(kind):
+    def block(X, ln1_w, ln1_b, WQ, WK, WV, WG, WO, ln2_w, ln2_b, W1, W2, *, H, dk, dv, gamma,
+              chunk, ln_eps, norm_flags, gn_eps):
+        M = msr_layer(layernorm(X, ln1_w, ln1_b, ln_eps), WQ, WK, WV, WG, WO, H=H, dk=dk, dv=dv,
+                      gamma=gamma, chunk=chunk, norm_flags=norm_flags, gn_eps=gn_eps)
+        Y = M + X
+        src = X if kind == "FFN on LN(X)" else Y
+        if kind == "GELU after W2":
+            F = gelu(layernorm(src, ln2_w, ln2_b, ln_eps) @ W1 @ W2)
+        else:
+            F = gelu(layernorm(src, ln2_w, ln2_b, ln_eps) @ W1) @ W2
+        if kind == "no second skip":
+            return F
+        if kind == "skips swapped":
+            return F + X
+        return F + Y
+    return block
+
+
+@pytest.mark.parametrize("kind", ["FFN on LN(X)", "GELU after W2", "no second skip",
+                                  "skips swapped"])
+def test_block_mutants_are_caught(kind):
+    with pytest.raises(AssertionError):
+        _hand_block_pins(_block_mutant(kind))
+
+
+def test_block_mutant_harness_is_faithful():
+    _hand_block_pins(_block_mutant("none"))
