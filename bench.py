@@ -291,7 +291,6 @@ def run_ours(args):
             step()
         barrier()
         R.lib.retention_kernel_timer_reset()
-        R.lib.retention_kernel_timer_enable(1)
         barrier()
         clk.mark_start()
         e0.record(stream)
@@ -300,9 +299,18 @@ def run_ours(args):
         e1.record(stream)
         barrier()
         clk.mark_end()
-    R.lib.retention_kernel_timer_enable(0)
     ms = max_over_ranks(e0.elapsed_time(e1))
     launches = int(R.lib.retention_launch_count())
+    # Per-kernel times: the same K steps again with a CUDA event pair around
+    # every launch (on its stream).  Kept out of the timed steps above,
+    # which the events would slow by about 4%.
+    R.lib.retention_kernel_timer_reset()
+    R.lib.retention_kernel_timer_enable(1)
+    barrier()
+    for _ in range(args.steps):
+        step()
+    barrier()
+    R.lib.retention_kernel_timer_enable(0)
     ktimes = R.kernel_times()
     value = job_throughput(world, N, args.steps, ms)
 
@@ -430,6 +438,9 @@ def run_ours(args):
             extra["parallel"] = bench_parallel(args, R, dev, tflops, world, max_over_ranks)
         if "retnet_block" in want:
             extra["retnet_block"] = bench_block(args, R, dev, tflops, world, max_over_ranks)
+        if "chunk_sizes" in want:
+            extra["chunk_sizes"] = bench_chunk_sizes(R, q, k, v, o, S, gam, ws, stream, hbm,
+                                                     world, max_over_ranks)
 
     cpu = None
     if rank == 0 and not args.skip_cpu:
@@ -451,7 +462,35 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
-EXTRAS = ("decode", "decode_stack", "msr_layer", "backward", "retnet_block", "parallel")
+EXTRAS = ("decode", "decode_stack", "msr_layer", "backward", "retnet_block", "parallel",
+          "chunk_sizes")
+
+
+def bench_chunk_sizes(R, q, k, v, o, S, gam, ws, stream, hbm, world, max_over_ranks):
+    """The headline step at chunk lengths 64, 128 and 256 (the workload's
+    sweep).  The tensor-core kernels work in 64-token chunks, so every
+    multiple of 64 runs the same kernels (the chunkwise form is one function
+    of the chunk length up to rounding); reported so the sweep is measured
+    rather than assumed."""
+    import torch
+    out = {}
+    for C in (64, 128, 256):
+        def f():
+            R.chunkwise_fwd(q, k, v, gam, chunk=C, norm_flags=R.NORM_ALL, out=o, S_out=S,
+                            workspace=ws, stream=stream)
+        for _ in range(3):
+            f()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(50):
+            f()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ms = max_over_ranks(e0.elapsed_time(e1)) / 50
+        out[f"C{C}"] = {"tokens_per_s": world * N / (ms * 1e-3), "ms_per_step": ms,
+                        "path_frac_hbm": BYTES_PER_TOKEN_HEAD * H * N / (ms * 1e-3) / 1e9 / hbm}
+    return out
 
 
 def bench_decode(args, R, dev, stream, hbm, world, max_over_ranks):
