@@ -131,6 +131,12 @@ ret_status retention_rotate(const ret_desc *d, const void *x, const int64_t sx[3
  * Parallel form [hwhale, Retention(X) = (Q K^T (.) D) V; ParallelRetention].
  * q,k: [B,H,N,d_k]; v, o: [B,H,N,d_v] via the descriptor's strides.
  * The call's tokens only (zero prior state); positions start at pos0.
+ * bf16 inputs with d_k a multiple of 64 up to 256, d_v a multiple of 128 up
+ * to 1024, v 16-byte aligned with strides a multiple of 8 elements and
+ * every gamma^64 >= 2^-16 run on the tensor cores (rotated q, k rounded to
+ * fp16 with power-of-two block scales, the decayed scores to bf16, fp32
+ * accumulation); everything else on CUDA cores in fp32.  The chunk field
+ * does not change the result.
  */
 ret_status retention_parallel_fwd(const ret_desc *d, const void *q,
                                   const void *k, const void *v, void *o,
