@@ -999,8 +999,10 @@ struct DecWs {
 // Decode-batch GEMM jobs stream their weights on CUDA cores for up to
 // kDecSkinnyRows rows; beyond, the tensor cores (128-row tiles, the missing
 // rows read as zeros) split over K do the same stream with less work per
-// weight byte, when the widths suit them.
-constexpr int kDecSkinnyRows = 4;
+// weight byte, when the widths suit them.  Measured per layer of the
+// 6.7B-scale stack: B=1 106 / 110 us (CUDA cores / tensor cores), B=2
+// 113 / 117, B=4 138 / 122, B=8 185 / 139.
+constexpr int kDecSkinnyRows = 2;
 
 static bool dec_use_tc(int B, int Ntot, int K) {
   return B > kDecSkinnyRows && Ntot % 256 == 0 && K % 64 == 0;
