@@ -1117,18 +1117,20 @@ static bool dec_job_fits(const void *A, int M, int count, const void *const *Bs,
   return dec_job_tc(A, M, count, Bs, Ns, K) || M <= 16;
 }
 
+// early_b: no kernel that may still run when this job starts writes its
+// weights (see launch_gemm_skinny_job).
 static cudaError_t gemm_dec_job(const void *A, int count, const void *const *Bs, void *const *Cs,
                                 const int *Ns, int M, int K, int epi, const void *R, float *part,
-                                unsigned *status, cudaStream_t st) {
+                                unsigned *status, cudaStream_t st, bool early_b = false) {
   SkinnyJob job;
   if (!skinny_job_init(job, count, Bs, Cs, Ns, epi, R)) return cudaErrorInvalidValue;
   if (!dec_job_tc(A, M, count, Bs, Ns, K)) {
-    cudaError_t e = RET_TIMED_LAUNCH(kKGemmSkinny, st, launch_gemm_skinny_job(A, job, M, K, part, st));
+    cudaError_t e = RET_TIMED_LAUNCH(kKGemmSkinny, st, launch_gemm_skinny_job(A, job, M, K, part, st, early_b));
     if (e != cudaSuccess) return e;
     return RET_TIMED_LAUNCH(kKSkinnyReduce, st, launch_skinny_reduce_job(part, job, M, K, st));
   }
   const int split = gemm_tc_split(M, job.Ntot, K);
-  cudaError_t e = RET_TIMED_LAUNCH(kKGemmTc, st, launch_gemm_tc_partials(A, count, Bs, Ns, M, K, part, split, status, st));
+  cudaError_t e = RET_TIMED_LAUNCH(kKGemmTc, st, launch_gemm_tc_partials(A, count, Bs, Ns, M, K, part, split, status, st, early_b));
   if (e != cudaSuccess) return e;
   return RET_TIMED_LAUNCH(kKSkinnyReduce, st, launch_skinny_reduce_split(part, job, M, split, st));
 }
@@ -1180,7 +1182,9 @@ ret_status retnet_decode_step(const retnet_stack_desc *d, const retnet_layer_wei
   for (int l = 0; l < d->n_layers; ++l) {
     const retnet_layer_weights &L = layers[l];
     // Y1 = MSR(LN1(X)) + X, the retention step on this layer's state.
-    RET_CUDA(RET_TIMED_LAUNCH(kKLayerNorm, st, launch_layernorm(X, L.ln1_w, L.ln1_b, Xn, B, dm, d->block.ln_eps, st)));
+    // The first kernel of the call starts once all earlier work is done, so
+    // the GEMMs after it may copy weights before their wait (early_b).
+    RET_CUDA(RET_TIMED_LAUNCH(kKLayerNorm, st, launch_layernorm(X, L.ln1_w, L.ln1_b, Xn, B, dm, d->block.ln_eps, st, l > 0)));
     // Few rows: the four projections of LN1(X) stream their weights in one
     // job, and the GELU and the skip connections ride on the reduces.
     const void *Win[4] = {L.WQ, L.WK, L.WV, L.WG};
@@ -1189,7 +1193,7 @@ ret_status retnet_decode_step(const retnet_stack_desc *d, const retnet_layer_wei
     const bool fused = dec_job_fits(Xn, B, 4, Win, Nin, dm) && dec_job_fits(Y, B, 1, &L.WO, &dm, HV) &&
                        dec_job_fits(Xn, B, 1, &L.W1, &F, dm) && dec_job_fits(H1, B, 1, &L.W2, &dm, F);
     if (fused) {
-      RET_CUDA(gemm_dec_job(Xn, 4, Win, Cin, Nin, B, dm, kSkEpNone, nullptr, part, status, st));
+      RET_CUDA(gemm_dec_job(Xn, 4, Win, Cin, Nin, B, dm, kSkEpNone, nullptr, part, status, st, true));
     } else {
       RET_CUDA(gemm_dec(Xn, L.WQ, Q, B, HK, dm, part, status, st));
       RET_CUDA(gemm_dec(Xn, L.WK, K, B, HK, dm, part, status, st));
@@ -1200,7 +1204,7 @@ ret_status retnet_decode_step(const retnet_stack_desc *d, const retnet_layer_wei
     RET_CUDA(RET_TIMED_LAUNCH(kKRecurrent, st, launch_recurrent_step(p, Q, K, V, S[l], rsum ? z[l] : nullptr, Y, st, G)));
     if (fused) {
       void *c = Mo;
-      RET_CUDA(gemm_dec_job(Y, 1, &L.WO, &c, &dm, B, HV, kSkEpResidual, X, part, status, st));
+      RET_CUDA(gemm_dec_job(Y, 1, &L.WO, &c, &dm, B, HV, kSkEpResidual, X, part, status, st, true));
     } else {
       RET_CUDA(gemm_dec(Y, L.WO, Mo, B, dm, HV, part, status, st));
       RET_CUDA(RET_TIMED_LAUNCH(kKResidual, st, launch_residual_add(Mo, X, (long long)B * dm, st)));
@@ -1209,9 +1213,9 @@ ret_status retnet_decode_step(const retnet_stack_desc *d, const retnet_layer_wei
     RET_CUDA(RET_TIMED_LAUNCH(kKLayerNorm, st, launch_layernorm(Mo, L.ln2_w, L.ln2_b, Xn, B, dm, d->block.ln_eps, st)));
     if (fused) {
       void *c = H1;
-      RET_CUDA(gemm_dec_job(Xn, 1, &L.W1, &c, &F, B, dm, kSkEpGelu, nullptr, part, status, st));
+      RET_CUDA(gemm_dec_job(Xn, 1, &L.W1, &c, &F, B, dm, kSkEpGelu, nullptr, part, status, st, true));
       c = X;
-      RET_CUDA(gemm_dec_job(H1, 1, &L.W2, &c, &dm, B, F, kSkEpResidual, Mo, part, status, st));
+      RET_CUDA(gemm_dec_job(H1, 1, &L.W2, &c, &dm, B, F, kSkEpResidual, Mo, part, status, st, true));
     } else {
       RET_CUDA(gemm_dec(Xn, L.W1, H1, B, F, dm, part, status, st));
       RET_CUDA(RET_TIMED_LAUNCH(kKGelu, st, launch_gelu(H1, (long long)B * F, st)));

@@ -45,6 +45,8 @@ layernorm_kernel(const __nv_bfloat16 *__restrict__ x, const float *__restrict__ 
                  const float *__restrict__ b, __nv_bfloat16 *__restrict__ y, int d, float eps) {
   extern __shared__ float row[];
   __shared__ float red[kLnThreads / 32];
+  pdl_launch_dependents();
+  pdl_wait();
   const long long base = (long long)blockIdx.x * d;
   float s = 0.f;
   for (int i = threadIdx.x; i < d; i += kLnThreads) {
@@ -76,6 +78,8 @@ template <int kOp>
 __global__ void __launch_bounds__(256)
 elementwise_kernel(__nv_bfloat16 *__restrict__ y, const __nv_bfloat16 *__restrict__ r,
                    long long n, int vec) {
+  pdl_launch_dependents();
+  pdl_wait();
   const long long nv = vec ? n / 8 : 0;
   const long long stride = (long long)gridDim.x * blockDim.x;
   for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < nv; i += stride) {
@@ -102,16 +106,15 @@ elementwise_kernel(__nv_bfloat16 *__restrict__ y, const __nv_bfloat16 *__restric
 }
 
 cudaError_t launch_layernorm(const void *x, const float *w, const float *b, void *y, long long rows,
-                             int d, float eps, cudaStream_t st) {
+                             int d, float eps, cudaStream_t st, bool pdl) {
   if (rows <= 0) return cudaSuccess;
   const size_t smem = sizeof(float) * (size_t)d;
   cudaError_t e = cudaFuncSetAttribute(layernorm_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  layernorm_kernel<<<(unsigned)rows, kLnThreads, smem, st>>>(
-      reinterpret_cast<const __nv_bfloat16 *>(x), w, b, reinterpret_cast<__nv_bfloat16 *>(y), d,
-      eps);
-  return cudaGetLastError();
+  return launch_k(layernorm_kernel, dim3((unsigned)rows), dim3(kLnThreads), smem, st, pdl,
+                  reinterpret_cast<const __nv_bfloat16 *>(x), w, b,
+                  reinterpret_cast<__nv_bfloat16 *>(y), d, eps);
 }
 
 static cudaError_t launch_elementwise(int op, void *y, const void *r, long long n,
@@ -125,11 +128,8 @@ static cudaError_t launch_elementwise(int op, void *y, const void *r, long long 
   if (blocks > cap) blocks = cap;
   auto *yp = reinterpret_cast<__nv_bfloat16 *>(y);
   auto *rp = reinterpret_cast<const __nv_bfloat16 *>(r);
-  if (op == 0)
-    elementwise_kernel<0><<<(unsigned)blocks, 256, 0, st>>>(yp, rp, n, vec);
-  else
-    elementwise_kernel<1><<<(unsigned)blocks, 256, 0, st>>>(yp, rp, n, vec);
-  return cudaGetLastError();
+  return launch_k(op == 0 ? elementwise_kernel<0> : elementwise_kernel<1>,
+                  dim3((unsigned)blocks), dim3(256), 0, st, true, yp, rp, n, vec);
 }
 
 cudaError_t launch_residual_add(void *y, const void *r, long long n, cudaStream_t st) {

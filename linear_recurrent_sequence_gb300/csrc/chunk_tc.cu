@@ -350,6 +350,9 @@ chunk_tc_kernel(const __grid_constant__ KParams p, const __grid_constant__ CUten
   cluster.sync();  // every CTA's barriers exist before any remote arrive
   tc::tc_fence_after();
   const uint32_t tb = *tbase_p;
+  // Launched with programmatic serialization: the setup above overlaps the
+  // kernel before this one; global memory only after it has completed.
+  pdl_wait();
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA and scores
@@ -415,6 +418,9 @@ chunk_tc_kernel(const __grid_constant__ KParams p, const __grid_constant__ CUten
           // No back-off: a sleep here (32 or 128 ns) measured slower.
         }
       }
+      // Every load and score is issued: the next kernel may be scheduled
+      // (it waits for this one to complete in its own pdl_wait).
+      pdl_launch_dependents();
       // Let every issued copy and MMA finish before the CTA can leave.
       // (Earlier stages were reused, so only the last two loads can be
       // outstanding.)
@@ -1050,13 +1056,15 @@ cudaError_t launch_chunk_tc(const KParams &p, const void *Qp, const void *Kp, co
   cfg.blockDim = dim3(kNT);
   cfg.dynamicSmemBytes = kSmemBytes;
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = a.NV;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, kern, p, tq, tk, tv, a);
 }
 

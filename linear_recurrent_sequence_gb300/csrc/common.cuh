@@ -93,4 +93,20 @@ __device__ __forceinline__ void report(unsigned *status, unsigned code) {
   if (status) atomicCAS(status, 0u, code);
 }
 
+// ---------------------------------------------------------------- launch order
+// Programmatic dependent launch.  A kernel launched with programmatic stream
+// serialization may start while the kernel before it on the stream still
+// runs: pdl_wait() blocks until every kernel it depends on has completed and
+// their memory operations are visible, so each such kernel calls it before
+// its first access to global memory that an earlier kernel may write or
+// read.  Since every kernel in such a chain waits before it touches shared
+// data, a kernel past its wait knows all earlier kernels complete.
+// pdl_launch_dependents() lets the next kernel be scheduled now (it takes
+// effect once every CTA has called it or exited).  Without programmatic
+// serialization both return at once.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 }  // namespace ret

@@ -51,7 +51,7 @@ __host__ __device__ constexpr int sk_depth() { return MB <= 4 ? 24 : 16; }
 template <int MB>
 __global__ void __launch_bounds__(kSkThreads)
 gemm_skinny_kernel(const __nv_bfloat16 *__restrict__ A, const SkinnyJob job,
-                   float *__restrict__ P, int M, int K, int rows_per_slice) {
+                   float *__restrict__ P, int M, int K, int rows_per_slice, int early_b) {
   constexpr int D = sk_depth<MB>();
   __shared__ float As[kSkMaxRowsPerSlice][MB];
   extern __shared__ __align__(16) uint4 ring[];  // [D][kSkThreads]
@@ -65,14 +65,17 @@ gemm_skinny_kernel(const __nv_bfloat16 *__restrict__ A, const SkinnyJob job,
   const bool live = n0 < N;  // N % 8 == 0: a lane's eight columns are all in or all out
   const __nv_bfloat16 *brow = job.B[mat] + (long long)k0 * N + n0;
   const uint32_t slot0 = tc::smem_u32(ring + threadIdx.x), sstride = kSkThreads * 16u;
+  if (!early_b) pdl_wait();
   // Rows 0 .. D-2 of B in flight first (one copy group per row): they do
-  // not depend on A, so staging A overlaps them.
+  // not depend on A, so staging A overlaps them (and, with early_b, the
+  // end of the kernel before this one).
   const __nv_bfloat16 *bnext = brow;
 #pragma unroll 1
   for (int r = 0; r < D - 1; ++r, bnext += N) {
     if (live && r < kn) cp_async16(slot0 + (uint32_t)r * sstride, bnext);
     cp_async_commit();
   }
+  if (early_b) pdl_wait();
   for (int e = threadIdx.x; e < kn * MB; e += blockDim.x) {
     const int r = e / MB, m = e % MB;
     As[r][m] = m < M ? __bfloat162float(A[(long long)m * K + k0 + r]) : 0.f;
@@ -80,6 +83,7 @@ gemm_skinny_kernel(const __nv_bfloat16 *__restrict__ A, const SkinnyJob job,
   __syncthreads();
   if (!live) {
     cp_async_wait<0>();
+    pdl_launch_dependents();
     return;
   }
   float2 acc[MB][4];
@@ -112,6 +116,9 @@ gemm_skinny_kernel(const __nv_bfloat16 *__restrict__ A, const SkinnyJob job,
     }
   }
   cp_async_wait<0>();
+  // The stream is read: the reduce may be scheduled (it waits for this
+  // kernel to complete before reading the partials).
+  pdl_launch_dependents();
   float *pt = P + (long long)blockIdx.y * M * job.Ntot + job.col0[mat] + n0;
 #pragma unroll
   for (int m = 0; m < MB; ++m) {
@@ -131,6 +138,8 @@ gemm_skinny_kernel(const __nv_bfloat16 *__restrict__ A, const SkinnyJob job,
 // depend on timing (the partials were just written and are read from L2).
 __global__ void __launch_bounds__(256)
 skinny_reduce_kernel(const float *__restrict__ P, const SkinnyJob job, int M, int split) {
+  pdl_launch_dependents();
+  pdl_wait();
   const long long MN = (long long)M * job.Ntot;
   const long long g = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;  // 8-column group
   const int lane = threadIdx.x & 31;
@@ -184,6 +193,8 @@ skinny_reduce_kernel(const float *__restrict__ P, const SkinnyJob job, int M, in
 // thread per (row, 8 adjacent columns) adds the slices in order.
 __global__ void __launch_bounds__(256)
 skinny_reduce_few_kernel(const float *__restrict__ P, const SkinnyJob job, int M, int split) {
+  pdl_launch_dependents();
+  pdl_wait();
   const long long MN = (long long)M * job.Ntot;
   const long long g = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   if (g * 8 >= MN) return;
@@ -270,26 +281,28 @@ bool skinny_job_init(SkinnyJob &job, int count, const void *const *Bs, void *con
 
 template <int MB>
 static cudaError_t launch_skinny_mb(dim3 grid, const __nv_bfloat16 *a, const SkinnyJob &job,
-                                    float *partial, int M, int K, int rows, cudaStream_t st) {
+                                    float *partial, int M, int K, int rows, int early_b,
+                                    cudaStream_t st) {
   const int smem = sk_depth<MB>() * kSkThreads * 16;
   cudaError_t e = cudaFuncSetAttribute(gemm_skinny_kernel<MB>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  gemm_skinny_kernel<MB><<<grid, kSkThreads, smem, st>>>(a, job, partial, M, K, rows);
-  return cudaGetLastError();
+  return launch_k(gemm_skinny_kernel<MB>, grid, dim3(kSkThreads), smem, st, true, a, job,
+                  partial, M, K, rows, early_b);
 }
 
 cudaError_t launch_gemm_skinny_job(const void *A, const SkinnyJob &job, int M, int K,
-                                   float *partial, cudaStream_t st) {
+                                   float *partial, cudaStream_t st, bool early_b) {
   int split = 1, rows = 1;
   skinny_plan(M, job.Ntot, K, split, rows);
   dim3 grid(job.blk0[job.count], split);
   const auto *a = reinterpret_cast<const __nv_bfloat16 *>(A);
-  if (M <= 1) return launch_skinny_mb<1>(grid, a, job, partial, M, K, rows, st);
-  if (M <= 2) return launch_skinny_mb<2>(grid, a, job, partial, M, K, rows, st);
-  if (M <= 4) return launch_skinny_mb<4>(grid, a, job, partial, M, K, rows, st);
-  if (M <= 8) return launch_skinny_mb<8>(grid, a, job, partial, M, K, rows, st);
-  return launch_skinny_mb<16>(grid, a, job, partial, M, K, rows, st);
+  const int eb = early_b ? 1 : 0;
+  if (M <= 1) return launch_skinny_mb<1>(grid, a, job, partial, M, K, rows, eb, st);
+  if (M <= 2) return launch_skinny_mb<2>(grid, a, job, partial, M, K, rows, eb, st);
+  if (M <= 4) return launch_skinny_mb<4>(grid, a, job, partial, M, K, rows, eb, st);
+  if (M <= 8) return launch_skinny_mb<8>(grid, a, job, partial, M, K, rows, eb, st);
+  return launch_skinny_mb<16>(grid, a, job, partial, M, K, rows, eb, st);
 }
 
 cudaError_t launch_skinny_reduce_job(const float *partial, const SkinnyJob &job, int M, int K,
@@ -303,12 +316,11 @@ cudaError_t launch_skinny_reduce_split(const float *partial, const SkinnyJob &jo
                                        int split, cudaStream_t st) {
   const long long groups = (long long)M * job.Ntot / 8;
   if (split <= 16)  // one thread per group
-    skinny_reduce_few_kernel<<<(unsigned)((groups + 255) / 256), 256, 0, st>>>(partial, job, M,
-                                                                              split);
-  else  // one warp per group
-    skinny_reduce_kernel<<<(unsigned)((groups * 32 + 255) / 256), 256, 0, st>>>(partial, job, M,
-                                                                               split);
-  return cudaGetLastError();
+    return launch_k(skinny_reduce_few_kernel, dim3((unsigned)((groups + 255) / 256)), dim3(256),
+                    0, st, true, partial, job, M, split);
+  // one warp per group
+  return launch_k(skinny_reduce_kernel, dim3((unsigned)((groups * 32 + 255) / 256)), dim3(256),
+                  0, st, true, partial, job, M, split);
 }
 
 // One matrix, no epilogue.

@@ -119,6 +119,27 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   tc::tc_fence_after();
   const uint32_t tb = *tbase_p;
 
+  // With early_b the producer sends the B tiles of the first stages before
+  // waiting for the kernel before this one; their A tiles follow the wait.
+  int pre = 0;
+  if (job.early_b && warp == 0 && lane == 0) {
+    for (int t = blockIdx.x; t < tiles && pre < kStages; t += gridDim.x) {
+      const GemmItem w = gemm_item(job, t, mtiles, nk);
+      const CUtensorMap *tmB = w.mat == 0   ? &job.tmB[0]
+                               : w.mat == 1 ? &job.tmB[1]
+                               : w.mat == 2 ? &job.tmB[2]
+                                            : &job.tmB[3];
+      for (int kb = w.kb0; kb < w.kb1 && pre < kStages; ++kb, ++pre) {
+        uint8_t *st = sm + pre * kStageBytes;
+        tc::mbar_arrive_expect_tx(&full[pre], kStageBytes);
+#pragma unroll
+        for (int j = 0; j < BN / 64; ++j)
+          tc::tma_load_2d(st + kABytes + j * 8192, tmB, &full[pre], w.n0 + j * 64, kb * BK);
+      }
+    }
+  }
+  pdl_wait();
+
   if (warp == 0) {
     if (lane == 0) {
       tc::prefetch_tmap(&tmA);
@@ -142,13 +163,18 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             break;
           }
           uint8_t *st = sm + s * kStageBytes;
-          tc::mbar_arrive_expect_tx(&full[s], kStageBytes);
+          if (it >= pre) tc::mbar_arrive_expect_tx(&full[s], kStageBytes);
           tc::tma_load_2d(st, &tmA, &full[s], kb * BK, m0);
+          if (it >= pre) {
 #pragma unroll
-          for (int j = 0; j < BN / 64; ++j)
-            tc::tma_load_2d(st + kABytes + j * 8192, tmB, &full[s], n0 + j * 64, kb * BK);
+            for (int j = 0; j < BN / 64; ++j)
+              tc::tma_load_2d(st + kABytes + j * 8192, tmB, &full[s], n0 + j * 64, kb * BK);
+          }
         }
       }
+      // Every load is issued: the next kernel may be scheduled (it waits
+      // for this one to complete before touching its results).
+      pdl_launch_dependents();
       for (int i = it > kStages ? it - kStages : 0; i < it; ++i)
         gdrain(&full[i % kStages], (i / kStages) & 1);
     }
@@ -303,8 +329,8 @@ static cudaError_t launch_job(const void *A, const GemmJob &job, int M, int K, u
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const int items = ((M + BM - 1) / BM) * job.ntile0[job.count] * job.ksplit;
   const int grid = items < sms ? items : sms;
-  gemm_tc_kernel<kMode><<<grid, kNT, kSmem, st>>>(ta, job, M, K, status);
-  return cudaGetLastError();
+  return launch_k(gemm_tc_kernel<kMode>, dim3(grid), dim3(kNT), kSmem, st, true, ta, job, M, K,
+                  status);
 }
 
 cudaError_t launch_gemm_tc(const void *A, const void *Bm, void *C, int M, int N, int K,
@@ -332,10 +358,11 @@ int gemm_tc_split(int M, int Ntot, int K) {
 
 cudaError_t launch_gemm_tc_partials(const void *A, int count, const void *const *Bs,
                                     const int *Ns, int M, int K, float *P, int ksplit,
-                                    unsigned *status, cudaStream_t st) {
+                                    unsigned *status, cudaStream_t st, bool early_b) {
   if (count < 1 || count > kGemmJobMax || ksplit < 1) return cudaErrorInvalidValue;
   GemmJob job;
   job.count = count;
+  job.early_b = early_b ? 1 : 0;
   int col = 0, nt = 0;
   for (int i = 0; i < count; ++i) {
     if (!encode_b(&job.tmB[i], Bs[i], Ns[i], K)) return cudaErrorInvalidValue;

@@ -4,9 +4,31 @@
 #include <cuda.h>
 #include <cuda_fp16.h>
 
+#include <utility>
+
 #include "common.cuh"
 
 namespace ret {
+
+// Launch with programmatic stream serialization when pdl is set: the kernel
+// may then start while the previous kernel on the stream still runs, so it
+// must call pdl_wait() before it touches global memory that an earlier
+// kernel may write or read (common.cuh).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_k(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                     bool pdl, Args &&...args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
 
 enum ScaleMode { kScaleNone = 0, kScaleArray = 1, kScaleXi = 2, kScaleZeta = 3 };
 
@@ -118,11 +140,12 @@ struct GemmJob {
   int ntile0[kGemmJobMax + 1] = {}, col0[kGemmJobMax] = {};
   __nv_bfloat16 *C = nullptr;
   float *P = nullptr;
+  int early_b = 0;  // B tiles of the first stages loaded before pdl_wait (as for the skinny job)
 };
 int gemm_tc_split(int M, int Ntot, int K);
 cudaError_t launch_gemm_tc_partials(const void *A, int count, const void *const *Bs,
                                     const int *Ns, int M, int K, float *P, int ksplit,
-                                    unsigned *status, cudaStream_t st);
+                                    unsigned *status, cudaStream_t st, bool early_b = false);
 
 // gemm_simt.cu: C[M,N] = A[M,K] B[K,N], bf16 in (row-major), fp32 accumulate.
 cudaError_t launch_gemm_bf16(const void *A, const void *Bm, void *C, int M, int N,
@@ -185,8 +208,11 @@ cudaError_t launch_bwd_finish(const KParams &p, BwdFinish F, cudaStream_t st);
 
 // block.cu: the RetNet block's LayerNorm (bf16 rows of d, fp32 gain and
 // bias), skip connection y <- y + r and in-place GELU (bf16, n values).
+// pdl = false: the kernel starts only once everything before it on the
+// stream is complete (the first kernel of a chain whose later kernels read
+// data before their pdl_wait, see launch_gemm_skinny_job).
 cudaError_t launch_layernorm(const void *x, const float *w, const float *b, void *y, long long rows,
-                             int d, float eps, cudaStream_t st);
+                             int d, float eps, cudaStream_t st, bool pdl = true);
 cudaError_t launch_residual_add(void *y, const void *r, long long n, cudaStream_t st);
 cudaError_t launch_gelu(void *y, long long n, cudaStream_t st);
 
@@ -214,8 +240,12 @@ struct SkinnyJob {
 };
 bool skinny_job_init(SkinnyJob &job, int count, const void *const *Bs, void *const *Cs,
                      const int *Ns, int epi, const void *R);
+// early_b: the first rows of the weights are copied before the kernel's
+// pdl_wait, overlapping the kernel before it.  Only for callers that know
+// no kernel that may still run writes the weights: every kernel launched
+// since the last launch without programmatic serialization.
 cudaError_t launch_gemm_skinny_job(const void *A, const SkinnyJob &job, int M, int K,
-                                   float *partial, cudaStream_t st);
+                                   float *partial, cudaStream_t st, bool early_b = false);
 cudaError_t launch_skinny_reduce_job(const float *partial, const SkinnyJob &job, int M, int K,
                                      cudaStream_t st);
 // The same reduce over `split` given slices (the tensor-core GEMM's partials).

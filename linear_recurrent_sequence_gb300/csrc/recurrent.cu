@@ -100,6 +100,9 @@ recurrent_step_kernel(KParams p, int KS, const void *__restrict__ q,
   const int tid = threadIdx.x;
   float4 *Srow0 = reinterpret_cast<float4 *>(S + ((long long)bh * dk + k0) * dv);
 
+  // Wait for the kernel before this one (the previous step's state stores)
+  // before any global access.
+  pdl_wait();
   // First block of S: rows 0..min(R,RB)-1 of column slice tid.  Nothing
   // these loads need depends on the inputs, so they go out first.
   float4 s[RB];
@@ -212,6 +215,9 @@ recurrent_step_kernel(KParams p, int KS, const void *__restrict__ q,
       *reinterpret_cast<float4 *>(cluster.map_shared_rank(inbox, dst) + rank * span +
                                   (e - dst * span)) = acc;
   }
+  // The state is written: the next kernel may be scheduled (it waits for
+  // this one to complete in its own pdl_wait).
+  pdl_launch_dependents();
   if (kAsyncX)
     xwait(&xbar[0], p.status);
   else
@@ -352,13 +358,17 @@ cudaError_t launch_recurrent_step(const KParams &p, const void *q, const void *k
   cfg.blockDim = dim3(NT);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = KS;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  // Programmatic serialization: the step's CTAs are placed while the kernel
+  // before it (usually the previous step) finishes, and wait in pdl_wait.
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   // Row block: with at most one CTA per SM (small batches) the step is
   // latency-bound and every thread keeps all its rows (<= 32) in flight at
   // once; with more CTAs than SMs it is bandwidth-bound, and 8 rows a thread
@@ -376,6 +386,11 @@ cudaError_t launch_recurrent_step(const KParams &p, const void *q, const void *k
   // barriers, whose release half waits for the state stores to drain).
   const __nv_bfloat16 *g = reinterpret_cast<const __nv_bfloat16 *>(gate);
   const bool gated = g != nullptr;
+  // Programmatic serialization only while the grid fits on the SMs (one CTA
+  // each): with more CTAs, the next step's early CTAs share SMs with this
+  // one's.  Measured at H=16, d_k=256, d_v=512: 6.40 vs 6.56 us per step at
+  // B=1 with it, 17.3 vs 16.8 at B=8.
+  if ((long long)p.B * p.H * KS > sms) cfg.numAttrs = 1;
   if ((long long)p.B * p.H * KS <= sms) {
     cfg.dynamicSmemBytes = sizeof(float) * (2 * R + p.dv + (size_t)KS * p.dv);
     return gated ? cudaLaunchKernelEx(&cfg, recurrent_step_kernel<32, true, true, true>, p, KS, q, k, v, S, z, o, g)

@@ -121,6 +121,7 @@ rotate_qk_kernel(const __grid_constant__ KParams p, const __grid_constant__ RotQ
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
+  pdl_wait();  // global memory only once the kernel before this one is complete
   auto issue = [&](int t, int buf) {
     int which, r;
     tile_of(a, t, which, r);
@@ -132,6 +133,7 @@ rotate_qk_kernel(const __grid_constant__ KParams p, const __grid_constant__ RotQ
   if (kTma && tid == 0 && (int)blockIdx.x < a.ntiles) issue(blockIdx.x, 0);
   int k = 0;
   for (int t = blockIdx.x; t < a.ntiles; t += gridDim.x, ++k) {
+    if (t + (int)gridDim.x >= a.ntiles) pdl_launch_dependents();  // this CTA's last tile
     int which, r;
     tile_of(a, t, which, r);
     const int bh = r / nch, c = r % nch;
@@ -307,15 +309,15 @@ cudaError_t launch_rotate_qk(const KParams &p, const void *q, const void *k, __h
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     const int grid = a.ntiles < 3 * sms ? a.ntiles : 3 * sms;
-    rotate_qk_kernel<true><<<grid, 256, smem, st>>>(p, a, tm[0], tm[1]);
-  } else {
-    cudaError_t e = cudaFuncSetAttribute(rotate_qk_kernel<false>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tile);
-    if (e != cudaSuccess) return e;
-    const int grid = a.ntiles < 6 * sms ? a.ntiles : 6 * sms;
-    rotate_qk_kernel<false><<<grid, 256, tile, st>>>(p, a, tm[0], tm[1]);
+    return launch_k(rotate_qk_kernel<true>, dim3(grid), dim3(256), smem, st, true, p, a, tm[0],
+                    tm[1]);
   }
-  return cudaGetLastError();
+  cudaError_t e = cudaFuncSetAttribute(rotate_qk_kernel<false>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tile);
+  if (e != cudaSuccess) return e;
+  const int grid = a.ntiles < 6 * sms ? a.ntiles : 6 * sms;
+  return launch_k(rotate_qk_kernel<false>, dim3(grid), dim3(256), tile, st, true, p, a, tm[0],
+                  tm[1]);
 }
 
 cudaError_t launch_rotate(const KParams &p, const void *x, const long long s[3], int d,

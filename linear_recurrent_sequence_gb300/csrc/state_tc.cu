@@ -123,6 +123,7 @@ state_tc_kernel(const __grid_constant__ KParams p, const __grid_constant__ CUten
   __syncthreads();
   tc::tc_fence_after();
   const uint32_t tb = *tbase_p;
+  pdl_wait();  // global memory only once the kernel before this one is complete
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA
@@ -148,6 +149,7 @@ state_tc_kernel(const __grid_constant__ KParams p, const __grid_constant__ CUten
                         &bars[FULL0 + s]);
         ++issued;
       }
+      pdl_launch_dependents();  // every load is issued
       for (int lc = issued > 2 ? issued - 2 : 0; lc < issued; ++lc)
         sdrain(&bars[FULL0 + (lc & 1)], (lc >> 1) & 1);
     }
@@ -337,9 +339,8 @@ cudaError_t launch_state_tc(const KParams &p, const void *Kp, const void *v,
       cudaFuncSetAttribute(state_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
   if (e != cudaSuccess) return e;
   const int grid = npieces * BH * (p.dv / kW);
-  state_tc_kernel<<<grid, kNT, kSmem, st>>>(p, tk, tv, meta, ksum, piece_len, Part, zPart,
-                                             need_z);
-  return cudaGetLastError();
+  return launch_k(state_tc_kernel, dim3(grid), dim3(kNT), kSmem, st, true, p, tk, tv, meta, ksum,
+                  piece_len, Part, zPart, need_z);
 }
 
 }  // namespace ret
