@@ -116,6 +116,8 @@ constexpr int kBwdRowsPer = 2;
 __global__ void __launch_bounds__(kBwdThreads)
 bwd_prep_kernel(const __grid_constant__ KParams p, const __grid_constant__ BwdPrepJobs jobs) {
   __shared__ ThetaSmem th;
+  pdl_wait();  // the kernel before this one is complete (programmatic launch)
+  pdl_launch_dependents();
   const BwdPrepJob &J = jobs.job[blockIdx.z];
   const int per_row = J.d / kBwdVec, rows = kBwdThreads / per_row;
   const int t0 = blockIdx.x * rows * kBwdRowsPer;
@@ -154,6 +156,8 @@ bwd_prep_kernel(const __grid_constant__ KParams p, const __grid_constant__ BwdPr
 __global__ void __launch_bounds__(256)
 bwd_transpose_kernel(const float *__restrict__ S, int BH, int dk, int dv, int w,
                      float *__restrict__ T) {
+  pdl_wait();  // the kernel before this one is complete (programmatic launch)
+  pdl_launch_dependents();
   const long long n = (long long)BH * dk * dv;
   for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n;
        i += (long long)gridDim.x * blockDim.x) {
@@ -172,6 +176,8 @@ bwd_transpose_kernel(const float *__restrict__ S, int BH, int dk, int dv, int w,
 __global__ void __launch_bounds__(kBwdThreads)
 bwd_finish_kernel(const __grid_constant__ KParams p, const __grid_constant__ BwdFinish F) {
   __shared__ ThetaSmem th;
+  pdl_wait();  // the kernel before this one is complete (programmatic launch)
+  pdl_launch_dependents();
   if (F.unrotate) stage_theta(p, F.d / 2, th);
   const int per_row = F.d / kBwdVec, rows = kBwdThreads / per_row;
   const int t = blockIdx.x * rows + threadIdx.x / per_row;
@@ -229,8 +235,7 @@ cudaError_t launch_bwd_prep(const KParams &p, BwdPrepJobs jobs, cudaStream_t st)
     gx = x > gx ? x : gx;
   }
   dim3 grid((unsigned)gx, (unsigned)(p.B * p.H), (unsigned)jobs.count);
-  bwd_prep_kernel<<<grid, kBwdThreads, 0, st>>>(p, jobs);
-  return cudaGetLastError();
+  return launch_k(bwd_prep_kernel, grid, dim3(kBwdThreads), 0, st, true, p, jobs);
 }
 
 cudaError_t launch_bwd_transpose(const float *S, int BH, int dk, int dv, int w, float *T,
@@ -239,8 +244,8 @@ cudaError_t launch_bwd_transpose(const float *S, int BH, int dk, int dv, int w, 
   if (n == 0) return cudaSuccess;
   long long blocks = (n + 255) / 256;
   if (blocks > 4096) blocks = 4096;
-  bwd_transpose_kernel<<<(unsigned)blocks, 256, 0, st>>>(S, BH, dk, dv, w, T);
-  return cudaGetLastError();
+  return launch_k(bwd_transpose_kernel, dim3((unsigned)blocks), dim3(256), 0, st, true, S, BH, dk,
+                  dv, w, T);
 }
 
 cudaError_t launch_bwd_finish(const KParams &p, BwdFinish F, cudaStream_t st) {
@@ -253,8 +258,7 @@ cudaError_t launch_bwd_finish(const KParams &p, BwdFinish F, cudaStream_t st) {
   F.vec = aligned16(F.out, F.s, F.out_bf16 ? 2 : 4);
   const int rows = kBwdThreads / (F.d / kBwdVec);
   dim3 grid((unsigned)((p.N + rows - 1) / rows), (unsigned)(p.B * p.H));
-  bwd_finish_kernel<<<grid, kBwdThreads, 0, st>>>(p, F);
-  return cudaGetLastError();
+  return launch_k(bwd_finish_kernel, grid, dim3(kBwdThreads), 0, st, true, p, F);
 }
 
 }  // namespace ret

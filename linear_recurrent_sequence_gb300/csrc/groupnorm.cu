@@ -15,6 +15,8 @@ constexpr int kGnMaxPerLane = 32;  // d_v <= 1024
 __global__ void __launch_bounds__(256)
 groupnorm_kernel(KParams p, const float *__restrict__ Oraw, const float *__restrict__ F,
                  void *__restrict__ o) {
+  pdl_wait();  // the kernel before this one is complete (programmatic launch)
+  pdl_launch_dependents();
   const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   const long long rows = (long long)p.B * p.H * p.N;
@@ -62,8 +64,7 @@ cudaError_t launch_groupnorm(const KParams &p, const float *Oraw, const float *F
   const long long rows = (long long)p.B * p.H * p.N;
   if (rows == 0) return cudaSuccess;
   const long long blocks = (rows * 32 + 255) / 256;
-  groupnorm_kernel<<<(unsigned)blocks, 256, 0, st>>>(p, Oraw, F, o);
-  return cudaGetLastError();
+  return launch_k(groupnorm_kernel, dim3((unsigned)blocks), dim3(256), 0, st, true, p, Oraw, F, o);
 }
 
 // The MSR layer's gate on the retention output, y <- y * swish(g), bf16
@@ -73,6 +74,8 @@ cudaError_t launch_groupnorm(const KParams &p, const float *Oraw, const float *F
 __global__ void __launch_bounds__(256)
 swish_gate_kernel(__nv_bfloat16 *__restrict__ y, const __nv_bfloat16 *__restrict__ g,
                   long long n, int vec) {
+  pdl_wait();  // the kernel before this one is complete (programmatic launch)
+  pdl_launch_dependents();
   const long long nv = vec ? n / 8 : 0;
   const long long stride = (long long)gridDim.x * blockDim.x;
   for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < nv; i += stride) {
@@ -109,10 +112,9 @@ cudaError_t launch_swish_gate(void *y, const void *g, long long n, cudaStream_t 
   const long long work = vec ? (n + 7) / 8 : n;
   long long blocks = (work + 255) / 256;
   if (blocks > 8LL * sms) blocks = 8LL * sms;
-  swish_gate_kernel<<<(unsigned)blocks, 256, 0, st>>>(reinterpret_cast<__nv_bfloat16 *>(y),
-                                                     reinterpret_cast<const __nv_bfloat16 *>(g),
-                                                     n, vec);
-  return cudaGetLastError();
+  return launch_k(swish_gate_kernel, dim3((unsigned)blocks), dim3(256), 0, st, true,
+                  reinterpret_cast<__nv_bfloat16 *>(y), reinterpret_cast<const __nv_bfloat16 *>(g),
+                  n, vec);
 }
 
 }  // namespace ret

@@ -159,6 +159,7 @@ parallel_tc_kernel(const __grid_constant__ KParams p, const __grid_constant__ CU
   tc::tc_fence_after();
   const uint32_t tb = *tbase_p;
   const uint32_t tO = tb + NSB * KT;  // O accumulator after the score buffers
+  pdl_wait();  // global memory only once the kernel before this one is complete
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA
@@ -205,6 +206,7 @@ parallel_tc_kernel(const __grid_constant__ KParams p, const __grid_constant__ CU
           if ((spin & 255u) == 255u && *abort_p) break;
         }
       }
+      pdl_launch_dependents();  // every load is issued
       // Every issued copy lands before the CTA can leave.
       par_drain(&bars[PB_FULLQ], 0);
       for (int u = tk > nst ? tk - nst : 0; u < tk; ++u)
@@ -551,9 +553,8 @@ cudaError_t launch_parallel_tc(const KParams &p, const __half *Qp, const __half 
   if (e != cudaSuccess) return e;
   const long long grid = (long long)((p.N + kPQ - 1) / kPQ) * BH * a.NVS;
   if (grid > 0x7fffffffLL) return cudaErrorInvalidValue;
-  kern<<<(unsigned)grid, kPThreads, smem, st>>>(p, tq, tk, tv, a);
   *fused = a.NVS == 1;
-  return cudaGetLastError();
+  return launch_k(kern, dim3((unsigned)grid), dim3(kPThreads), smem, st, true, p, tq, tk, tv, a);
 }
 
 }  // namespace ret

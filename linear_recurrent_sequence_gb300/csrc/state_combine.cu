@@ -27,6 +27,8 @@ __device__ __forceinline__ float part_weight(float lng, long long t) {
 __global__ void __launch_bounds__(256)
 state_combine_kernel(const CombineParts parts, const KParams p, float *__restrict__ out,
                      long long per_head, int is_z) {
+  pdl_wait();  // the kernel before this one is complete (programmatic launch)
+  pdl_launch_dependents();
   const long long n = (long long)p.B * p.H * per_head;
   for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n;
        i += (long long)gridDim.x * blockDim.x) {
@@ -53,8 +55,8 @@ cudaError_t launch_state_combine(const KParams &p, const CombineParts &parts, fl
     const long long per = which ? (long long)p.dk : (long long)p.dk * p.dv;
     const long long blocks = (BH * per + 255) / 256;
     const int grid = (int)(blocks < 8LL * sms ? blocks : 8LL * sms);
-    state_combine_kernel<<<grid, 256, 0, st>>>(parts, p, out, per, which);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_k(state_combine_kernel, dim3(grid), dim3(256), 0, st, true, parts, p,
+                             out, per, which);
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;
