@@ -38,6 +38,19 @@ int retention_tc_probe(int a_mode, int b_mode, int M, int N, int K, int a_lbo, i
 int retention_tc_probe_scale_d(int n, const void *A, const void *B, float *D,
                                unsigned *status, ret_stream_t stream);
 
+/*
+ * The CTA-pair MMA (PTX ISA, tcgen05.mma with .cta_group::2): the two CTAs
+ * of a cluster compute D = A * B^T for 256 rows, CTA r holding rows
+ * 128 r .. 128 r + 127 of A and columns N/2 r .. N/2 (r + 1) - 1 of B in
+ * its shared memory (K-major, 128-byte swizzled) and receiving its 128 rows
+ * of D in its TMEM; the even CTA issues the MMAs.  A: [256][K], B: [N][K]
+ * bf16 device; D: [256][N] fp32 device; tbase_out: two device words, the
+ * TMEM address each CTA's allocation returned.  N in {128, 256}, K in
+ * {64, 128}.  status as above.  Returns a ret_status value.
+ */
+int retention_tc_probe_pair(int N, int K, const void *A, const void *B, float *D,
+                            unsigned *tbase_out, unsigned *status, ret_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

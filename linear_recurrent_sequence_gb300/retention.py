@@ -113,6 +113,7 @@ _SIGS = {
     "retention_launch_count": (ctypes.c_longlong, []),
     "retention_tc_probe": (ctypes.c_int, [ctypes.c_int] * 9 + [_P, _P, _P, _P, _P]),
     "retention_tc_probe_scale_d": (ctypes.c_int, [ctypes.c_int, _P, _P, _P, _P, _P]),
+    "retention_tc_probe_pair": (ctypes.c_int, [ctypes.c_int, ctypes.c_int] + [_P] * 6),
     "retention_kernel_timer_read": (ctypes.c_int, [ctypes.c_int,
                                                    ctypes.POINTER(ctypes.c_double),
                                                    ctypes.POINTER(ctypes.c_longlong),

@@ -19,7 +19,8 @@ def R():
                                       (2048, 2048, 2048, True), (100, 200, 50, False),
                                       (32, 512, 4096, True), (300, 256, 192, True),
                                       (20, 256, 4096, True), (128, 256, 4096, True),
-                                      (64, 1024, 2048, True)])
+                                      (64, 1024, 2048, True), (1000, 768, 320, True),
+                                      (4096, 4096, 1024, True)])
 def test_gemm_matches_fp32_product(R, M, N, K, tc):
     """Tensor-core shapes (including M not a multiple of the 128-row tile,
     whose last tile is partly outside A and C, and few-row shapes that the

@@ -105,3 +105,30 @@ def test_accumulator_scale_operand(R, n):
     torch.cuda.synchronize()
     assert rc == 0 and int(st.item()) == 0
     assert close(D.double().cpu().numpy(), ref)
+
+
+@pytest.mark.parametrize("N,K", [(128, 64), (256, 128)])
+def test_cta_pair_mma(R, N, K):
+    """tcgen05.mma with .cta_group::2: the two CTAs of a cluster compute a
+    256-row product, each holding its 128 rows of A and half of B's columns
+    and receiving its rows of D in its own TMEM; their allocations return the
+    same TMEM address."""
+    g = torch.Generator().manual_seed(50 + N + K)
+    A = torch.randn(256, K, generator=g).to(torch.bfloat16)
+    B = torch.randn(N, K, generator=g).to(torch.bfloat16)
+    ref = (A.double() @ B.double().T).numpy()
+    D = torch.full((256, N), float("nan"), dtype=torch.float32, device="cuda")
+    tb = torch.full((2,), -1, dtype=torch.int32, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    Ad, Bd = A.cuda(), B.cuda()
+    rc = R.lib.retention_tc_probe_pair(N, K, ctypes.c_void_p(Ad.data_ptr()),
+                                       ctypes.c_void_p(Bd.data_ptr()),
+                                       ctypes.c_void_p(D.data_ptr()),
+                                       ctypes.c_void_p(tb.data_ptr()),
+                                       ctypes.c_void_p(st.data_ptr()),
+                                       ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    torch.cuda.synchronize()
+    assert rc == 0 and int(st.item()) == 0
+    t = tb.cpu().tolist()
+    assert t[0] == t[1], t
+    assert close(D.double().cpu().numpy(), ref)
