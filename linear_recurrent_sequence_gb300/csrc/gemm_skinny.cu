@@ -5,7 +5,8 @@
 //   - a warp owns 256 columns of B and reads each of its rows as one 512-byte
 //     run (16 bytes, eight columns, per lane); a CTA's eight warps own 2048
 //     adjacent columns;
-//   - K is split across CTAs (grid.y) so that about two CTAs run per SM;
+//   - K is split across CTAs (grid.y) so that about three CTAs (up to four
+//     rows) or two (more rows) run per SM;
 //     each CTA keeps its K-slice of A in shared memory (fp32, MB rows) and
 //     writes an fp32 partial tile; a second kernel adds the partials in
 //     slice order (deterministic) and rounds to bf16;
@@ -41,10 +42,13 @@ __device__ __forceinline__ void cp_async_wait() {
 }
 }  // namespace
 
-// Ring depth (rows of B per thread, D - 1 of them in flight): about 190 KB
-// of copies in flight per SM at two CTAs per SM.
+// Ring depth (rows of B per thread, D - 1 of them in flight): with three
+// CTAs per SM (up to four rows) about 180 KB of copies in flight per SM.
+// Measured per layer of the 6.7B-scale decode stack at B = 1 / 2 (CTAs per
+// SM x depth): 3 x 16 95.8 / 102.5 us, 2 x 24 97.9 / 104.8, 4 x 12
+// 95.6 / 104.6, 6 x 8 100.7 / 111.6, 1 x 48 108.1 / 119.0.
 template <int MB>
-__host__ __device__ constexpr int sk_depth() { return MB <= 4 ? 24 : 16; }
+__host__ __device__ constexpr int sk_depth() { return 16; }
 
 // grid: x = column block of 2048 (over every matrix of the job), y = K
 // slice.  P: [split][M][Ntot] fp32, matrix i's columns at col0[i].
@@ -226,8 +230,10 @@ bool gemm_skinny_supported(const void *A, const void *Bm, const void *C, int M, 
          reinterpret_cast<uintptr_t>(Bm) % 16 == 0 && A && C;
 }
 
-// Slices of K: about two CTAs per SM of a 152-SM GB300 (the shared-memory
-// ring of each CTA holds its copies in flight), at least eight rows and at
+// Slices of K: about three CTAs per SM of a 152-SM GB300 for up to four
+// rows, two beyond (the 16-row kernel's registers allow fewer; the
+// shared-memory ring of each CTA holds its copies in flight), at least
+// eight rows and at
 // most kSkMaxRowsPerSlice rows per slice, and
 // fp32 partials (split * M * N * 4 bytes) of at most 16 MB, which stay in
 // L2 between the two kernels.  The plan depends on the shape alone (not on
@@ -237,7 +243,8 @@ constexpr int kSkPlanSms = 152;
 constexpr long long kSkMaxPartialBytes = 16LL << 20;
 static void skinny_plan(int M, int N, int K, int &split, int &rows) {
   const int colblocks = (N + kSkCtaCols - 1) / kSkCtaCols;
-  int s = (2 * kSkPlanSms + colblocks - 1) / colblocks;
+  const int per_sm = M <= 4 ? 3 : 2;
+  int s = (per_sm * kSkPlanSms + colblocks - 1) / colblocks;
   s = s < kSkMaxSplit ? s : kSkMaxSplit;
   const long long per_slice = 4LL * (M > 0 ? M : 1) * N;
   const long long cap = kSkMaxPartialBytes / (per_slice > 0 ? per_slice : 1);
