@@ -462,6 +462,29 @@ def test_tc_chunk_shapes(R, B, H, N, dk, dv, flags):
     assert np.max(np.abs(host(z) - z_ref)) / np.max(np.abs(z_ref)) < 1e-2
 
 
+def test_max_heads_every_path(R):
+    """RET_MAX_HEADS (256) heads, so the last heads' constants (gamma and
+    its logarithm, the decay sums) reach every kernel: the chunkwise
+    tensor-core path over 130 tokens, one decode step that continues from
+    its state, and the parallel form of the same 130 tokens, each against
+    the oracle's chunkwise run over all 131 tokens."""
+    B, H, N, dk, dv = 1, 256, 130, 64, 128
+    (q, k, v), (q64, k64, v64) = inputs(2600, B, H, N + 1, dk, dv, "bf16")
+    gam = synth.head_gammas(H)
+    S = torch.empty(B, H, dk, dv, device="cuda")
+    z = torch.empty(B, H, dk, device="cuda")
+    o = R.chunkwise_fwd(q[:, :, :N], k[:, :, :N], v[:, :, :N], gam, chunk=64,
+                        norm_flags=R.NORM_ALL, S_out=S, z_out=z)
+    o_last = R.recurrent_step(q[:, :, N], k[:, :, N], v[:, :, N], S, gam, z=z, pos=N,
+                              norm_flags=R.NORM_ALL)
+    o_par = R.parallel_fwd(q[:, :, :N], k[:, :, :N], v[:, :, :N], gam, norm_flags=R.NORM_ALL)
+    p = oracle.Problem(B, H, N + 1, dk, dv, gam, norm_flags=oracle.NORM_ALL, gn_eps=1e-6)
+    ref, _, _ = oracle.chunkwise(p, 64, q64, k64, v64)
+    check_bf16(host(o), ref[:, :, :N], "256 heads, chunkwise")
+    check_bf16(host(o_last).reshape(B, H, 1, dv), ref[:, :, N:], "256 heads, decode step")
+    check_bf16(host(o_par), ref[:, :, :N], "256 heads, parallel form")
+
+
 def test_tc_chunk_state_in_strided_fp32_out(R):
     """Carried (S, z) in, [B,N,H,d] strided q/k/v/o, fp32 output, two calls
     that split the sequence (state passed through aliasing S_out = S_in)."""
