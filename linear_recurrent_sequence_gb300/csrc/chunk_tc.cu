@@ -233,15 +233,16 @@ __device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 
 enum StoreMode { kStoreAny = 0, kStoreBf16 = 1 };
 
 // Entry state of this CTA's value columns into the TMEM state columns at
-// `ts` (one warp, its 32 lanes): S_in, or for a later segment the decayed sum
-// of S_in and the pieces before it.  Returns the lane's max |S|.
+// `ts` (one warp, its 32 lanes), 32-row groups [g0, g1) of d_k: S_in, or for
+// a later segment the decayed sum of S_in and the pieces before it.  Returns
+// the lane's max |S| over those rows.
 __device__ __noinline__ float load_entry_state(const KParams &p, const TcArgs &a, uint32_t ts,
                                                int bh, long long vglob, int seg, int c0, int npc,
-                                               float lng) {
+                                               float lng, int g0, int g1) {
   const int DK = p.dk;
   const float w_in = seg > 0 ? gpow(lng, kC * c0) : 1.f;
   float m0 = 0.f;
-  for (int g = 0; g < DK / 32; ++g) {
+  for (int g = g0; g < g1; ++g) {
     uint32_t r[32];
 #pragma unroll
     for (int i = 0; i < 32; ++i) {
@@ -730,9 +731,20 @@ chunk_tc_kernel(const __grid_constant__ KParams p, const __grid_constant__ CUten
     // Entry state (S_in, or for a later segment the decayed sum of S_in and
     // the pieces before it) goes to the TMEM state columns; its max |S| is
     // the helper's first state bound.
+    // The first half of the entry state's rows here, the second half in the
+    // output group (idle until the first chunk's O^T): both halves are in
+    // TMEM, and the output group's bounds in OT (unused until then), after
+    // the two groups' join barrier.
     const bool has_state = a.S_in != nullptr || npc > 0;
-    const float m0 = has_state ? load_entry_state(p, a, tb + lb + kTS, bh, vglob, seg, c0, npc, lng)
-                               : 0.f;
+    float m0 = has_state ? load_entry_state(p, a, tb + lb + kTS, bh, vglob, seg, c0, npc, lng, 0,
+                                            DK / 64)
+                         : 0.f;
+    if (has_state) {
+      tc::tc_fence_before();
+      asm volatile("bar.sync 5, 256;" ::: "memory");
+      tc::tc_fence_after();
+      m0 = fmaxf(m0, OT[et]);
+    }
     {
       const float sb = grp_max(G, m0, rd, rslot, et);
       if (et == 0) {
@@ -838,6 +850,12 @@ chunk_tc_kernel(const __grid_constant__ KParams p, const __grid_constant__ CUten
     // pass, two passes.
     const int sq4 = et & 3, st0 = et >> 2;
     const float inv_nv = 1.f / (float)NV;
+    if (a.S_in != nullptr || npc > 0) {  // the second half of the entry state's rows
+      OT[et] = load_entry_state(p, a, tb + lb + kTS, bh, v0 + vrow, seg, c0, npc, lng, DK / 64,
+                                DK / 32);
+      tc::tc_fence_before();
+      asm volatile("bar.sync 5, 256;" ::: "memory");
+    }
     bool ok = true;
     for (int lc = 0; lc < ncl && ok; ++lc) {
       const int s = lc & 1, c = c0 + lc;
