@@ -89,6 +89,19 @@ def test_short_sequences(R, N):
     check_bf16(host(o), oracle.parallel(p, q64, k64, v64), f"parallel tensor cores, N={N}")
 
 
+def test_dk_192(R):
+    """d_k = 192 (a multiple of 64 that is not a power of two), ragged N,
+    all normalisations."""
+    B, H, N, dk, dv = 1, 2, 300, 192, 256
+    q, q64 = seeded(3110, "q", (B, H, N, dk), "bf16")
+    k, k64 = seeded(3110, "k", (B, H, N, dk), "bf16")
+    v, v64 = seeded(3110, "v", (B, H, N, dv), "bf16")
+    gam = [0.95, 0.999]
+    o = run_parallel(R, q, k, v, gam, norm_flags=R.NORM_ALL, out_dtype=torch.float32)
+    p = oracle.Problem(B, H, N, dk, dv, gam, norm_flags=oracle.NORM_ALL, gn_eps=1e-6)
+    check_bf16(host(o), oracle.parallel(p, q64, k64, v64), "parallel tensor cores, d_k=192")
+
+
 def test_negative_row_sums_without_groupnorm(R):
     """k = -q: most rows' sums of R fall below -1, so the third
     normalisation divides by |sum R| (hwhale.com/article/285883, R_nm /

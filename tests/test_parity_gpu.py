@@ -462,6 +462,30 @@ def test_tc_chunk_shapes(R, B, H, N, dk, dv, flags):
     assert np.max(np.abs(host(z) - z_ref)) / np.max(np.abs(z_ref)) < 1e-2
 
 
+@pytest.mark.parametrize("N", [1, 63, 65])
+def test_tc_chunk_path_at_chunk_edges(R, N):
+    """The tensor-core chunk path at the shortest sequences (one token; one
+    token short of and one past a 64-token chunk), all normalisations, a
+    carried (S, z) in and out."""
+    B, H, dk, dv = 1, 2, 128, 256
+    (q, k, v), (q64, k64, v64) = inputs(2700 + N, B, H, N, dk, dv, "bf16")
+    gam = [0.96875, 0.999]
+    S0, S064 = seeded(2750, "S", (B, H, dk, dv), "f32")
+    z0, z064 = seeded(2750, "z", (B, H, dk), "f32")
+    S = torch.empty_like(S0)
+    z = torch.empty_like(z0)
+    R.lib.retention_kernel_timer_reset()
+    o = R.chunkwise_fwd(q, k, v, gam, chunk=64, norm_flags=R.NORM_ALL, pos0=40, S_in=S0, z_in=z0,
+                        S_out=S, z_out=z)
+    torch.cuda.synchronize()
+    assert "chunk_tc" in R.kernel_times()
+    p = oracle.Problem(B, H, N, dk, dv, gam, pos0=40, norm_flags=oracle.NORM_ALL, gn_eps=1e-6)
+    ref, S_ref, z_ref = oracle.chunkwise(p, 64, q64, k64, v64, S064, z064)
+    check_bf16(host(o), ref, f"tc chunk path N={N}")
+    assert np.max(np.abs(host(S) - S_ref)) / np.max(np.abs(S_ref)) < 1e-2
+    assert np.max(np.abs(host(z) - z_ref)) / np.max(np.abs(z_ref)) < 1e-2
+
+
 def test_max_heads_every_path(R):
     """RET_MAX_HEADS (256) heads, so the last heads' constants (gamma and
     its logarithm, the decay sums) reach every kernel: the chunkwise
