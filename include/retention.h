@@ -343,8 +343,14 @@ ret_status retnet_block_fwd(const retnet_block_desc *d, const void *X, const flo
  * S[l] and z[l] is updated in place and must not overlap X, the workspace
  * or each other (RET_EINVAL where a state overlaps X or the workspace).
  * Weights are only read and may be shared between layers.
- * Projections with up to 16 rows (B <= 16) stream the weights with split-K
- * partial sums added in a fixed order. */
+ * Projections stream the weights with split-K partial sums added in a fixed
+ * order: up to two rows on CUDA cores, more rows on the tensor cores where
+ * the widths are multiples of 256 (else CUDA cores, up to 16 rows).  The
+ * call's first kernel starts only once all earlier work on the stream is
+ * complete; the projection kernels after it start reading their weights
+ * before the kernel before them has finished, so weights written on the
+ * stream before the call are seen, while weights written concurrently on
+ * another stream are not allowed. */
 typedef struct {
   retnet_block_desc block;
   int n_layers;
