@@ -151,7 +151,16 @@ def _check(status, where):
 
 
 def _ptr(t):
-    return None if t is None else ctypes.c_void_p(t.data_ptr())
+    """Device address of a tensor for the C ABI.  Only CUDA tensors on the
+    current device are accepted: any other address would reach a kernel."""
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError(f"expected a CUDA tensor, got one on {t.device}")
+    if t.device.index != torch.cuda.current_device():
+        raise ValueError(f"tensor on {t.device}, but the current device is "
+                         f"cuda:{torch.cuda.current_device()} (use torch.cuda.device)")
+    return ctypes.c_void_p(t.data_ptr())
 
 
 def _stream(stream):

@@ -247,3 +247,15 @@ def test_decode_stack_rejects_overlapping_buffers(R):
     assert call(X, ws) == 1
     S[1] = base + sbytes
     assert call(ws + 512, ws) == 1  # X inside the workspace
+
+
+def test_binding_rejects_host_tensors(R):
+    """A tensor that is not on the current CUDA device never reaches a kernel:
+    the binding raises before the library is called."""
+    import torch
+    from linear_recurrent_sequence_gb300 import retention
+    q = torch.zeros(1, 1, 4, 8, dtype=torch.bfloat16)
+    out = torch.empty(1, 1, 4, 8, dtype=torch.bfloat16)
+    ws = torch.zeros(256, dtype=torch.uint8)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        retention.chunkwise_fwd(q, q, q, [0.9], out=out, workspace=ws)
